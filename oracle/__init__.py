@@ -1,0 +1,193 @@
+"""Float64 CPU oracle for batched draft-token verification (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+import this package.  The product path (the CUDA library and its binding) never
+does.  The arithmetic lives in ``spec_oracle.c`` (plain loops, float64); this
+module compiles it with gcc and marshals numpy arrays to it.
+
+Functions and the passages they follow:
+
+* :func:`verify_sample` -- rejection-sampling verification: "EAGLE-3
+  speculative decoding review", sections "Speculative Decoding" (step 3, Accept
+  or Reject) and "Does Using a Small Model's Answer Reduce Quality?" (eqs.
+  A(x), p_residual); "EAGLE math", section "Vanilla speculative decoding";
+  "Speculative decoding" wiki, section "The mechanism".
+* :func:`verify_greedy` -- greedy verification: review page, "Does Using a
+  Small Model's Answer Reduce Quality?" (greedy bullets).
+* :func:`verify_tree_greedy` -- draft-tree greedy walk: review page, "EAGLE-2"
+  and "The Complete EAGLE-3 Inference Process" (steps 3-4); "EAGLE math",
+  "EAGLE-2: dynamic draft trees".
+* :func:`expected_tokens`, :func:`speedup_model` -- "EAGLE math", sections
+  "Vanilla speculative decoding" (E formula) and "The speedup math, worked".
+
+Every function is pinned by tests against values that do not come from the
+oracle itself (the worked example printed on the "EAGLE math" page, exact
+enumeration of the emitted-token law, chi-square tests, the expected-length
+closed form, brute-force tree search).  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libspecoracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERRORS = {0: "ok", 1: "invalid argument", 2: "non-finite logit", 3: "token out of range",
+          4: "malformed tree", 5: "out of memory"}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared library next to its source."""
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+                       check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    D = ctypes.c_double
+    lib.oracle_verify_sample.argtypes = [P, P, I, P, P, P, D, I, I, I,
+                                         P, P, P, P, P, P, P, P]
+    lib.oracle_verify_sample.restype = I
+    lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P]
+    lib.oracle_verify_greedy.restype = I
+    lib.oracle_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P]
+    lib.oracle_verify_tree_greedy.restype = I
+    lib.oracle_expected_tokens.argtypes = [D, I]
+    lib.oracle_expected_tokens.restype = D
+    lib.oracle_speedup_model.argtypes = [D, I, D]
+    lib.oracle_speedup_model.restype = D
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def load_variant(lib_path):
+    """Bind another compiled copy of the oracle source (used by the tests that
+    plant mistakes in the oracle to show the pins catch them)."""
+    return _bind(ctypes.CDLL(lib_path))
+
+
+def _dtype_code(dtype: str) -> int:
+    return {"f32": 0, "bf16": 1}[dtype]
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logits(a, dtype):
+    want = np.uint16 if dtype == "bf16" else np.float32
+    return np.ascontiguousarray(a, dtype=want)
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc):
+    if rc != 0:
+        raise OracleError(f"oracle error {rc}: {ERRORS.get(rc, '?')}")
+
+
+def verify_sample(target, draft, tokens, u_accept, u_sample, temperature, dtype="f32", lib=None):
+    """Sampling verification over a batch.  Returns a dict of numpy arrays.
+
+    target [B, k+1, V], draft [B, k, V] (float32, or uint16 bf16 bits);
+    tokens int32 [B, k]; u_accept float32 [B, k]; u_sample float32 [B].
+    """
+    lib = lib or _load()
+    target = _logits(target, dtype)
+    B, k1, V = target.shape
+    k = k1 - 1
+    draft = _logits(draft if draft is not None else np.zeros((B, 0, V)), dtype)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, k)
+    u_accept = np.ascontiguousarray(u_accept, dtype=np.float32).reshape(B, k)
+    u_sample = np.ascontiguousarray(u_sample, dtype=np.float32).reshape(B)
+    out = dict(
+        accepted_len=np.zeros(B, np.int32),
+        out_tokens=np.zeros((B, k + 1), np.int32),
+        p=np.zeros((B, k), np.float64),
+        q=np.zeros((B, k), np.float64),
+        resid_mass=np.zeros(B, np.float64),
+        acc_margin=np.zeros(B, np.float64),
+        cdf_margin=np.zeros(B, np.float64),
+        fallback=np.zeros(B, np.int32),
+    )
+    rc = lib.oracle_verify_sample(
+        _ptr(target), _ptr(draft), _dtype_code(dtype), _ptr(tokens), _ptr(u_accept),
+        _ptr(u_sample), float(temperature), B, k, V,
+        _ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out["p"]), _ptr(out["q"]),
+        _ptr(out["resid_mass"]), _ptr(out["acc_margin"]), _ptr(out["cdf_margin"]),
+        _ptr(out["fallback"]))
+    _check(rc)
+    return out
+
+
+def verify_greedy(target, tokens, dtype="f32", lib=None):
+    lib = lib or _load()
+    target = _logits(target, dtype)
+    B, k1, V = target.shape
+    k = k1 - 1
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, k)
+    out = dict(accepted_len=np.zeros(B, np.int32),
+               out_tokens=np.zeros((B, k + 1), np.int32),
+               argmax=np.zeros((B, k + 1), np.int32))
+    rc = lib.oracle_verify_greedy(_ptr(target), _dtype_code(dtype), _ptr(tokens), B, k, V,
+                                  _ptr(out["accepted_len"]), _ptr(out["out_tokens"]),
+                                  _ptr(out["argmax"]))
+    _check(rc)
+    return out
+
+
+def verify_tree_greedy(target, tokens, parents, max_depth, dtype="bf16", lib=None):
+    lib = lib or _load()
+    target = _logits(target, dtype)
+    B, N, V = target.shape
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, N)
+    parents = np.ascontiguousarray(parents, dtype=np.int32).reshape(B, N)
+    W = max_depth + 1
+    out = dict(accepted_len=np.zeros(B, np.int32),
+               path_nodes=np.zeros((B, W), np.int32),
+               out_tokens=np.zeros((B, W), np.int32))
+    rc = lib.oracle_verify_tree_greedy(_ptr(target), _dtype_code(dtype), _ptr(tokens),
+                                       _ptr(parents), B, N, V, int(max_depth),
+                                       _ptr(out["accepted_len"]), _ptr(out["path_nodes"]),
+                                       _ptr(out["out_tokens"]))
+    _check(rc)
+    return out
+
+
+def expected_tokens(alpha: float, gamma: int, lib=None) -> float:
+    return (lib or _load()).oracle_expected_tokens(float(alpha), int(gamma))
+
+
+def speedup_model(alpha: float, gamma: int, c: float, lib=None) -> float:
+    return (lib or _load()).oracle_speedup_model(float(alpha), int(gamma), float(c))
+
+
+def sample_flags(res: dict, window: float = 1e-6) -> np.ndarray:
+    """Rows whose outcome sits within ``window`` of an acceptance threshold or
+    of a CDF boundary (oracle float64 values); such rows may legitimately
+    differ between two correct implementations."""
+    return (res["acc_margin"] < window) | (res["cdf_margin"] < window)

@@ -1,0 +1,358 @@
+/*
+ * spec_oracle.c -- plain, slow, float64 CPU oracle for batched draft-token
+ * verification in speculative decoding.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg load this file.  It shares no code, header,
+ * table or helper with the CUDA library; it is the written-out definition the
+ * CUDA path is checked against.
+ *
+ * Sources (web pages; section names as they appear on each page):
+ *   [REVIEW]  "EAGLE-3 speculative decoding review" (6unoyunr.github.io)
+ *   [MATH]    "EAGLE math" (aicassindra.com, transformer_math/tm_eagle_math)
+ *   [WIKI]    "Speculative decoding" (addictedtoai.net wiki)
+ *
+ * Readings where the pages are silent (the CUDA path follows the same ones):
+ *   R1 temperature: p = softmax(z_target / T), q = softmax(z_draft / T), one T
+ *      for both rows (the pages never define T).
+ *   R2 row alignment: target row i and draft row i both score draft position
+ *      i; target row k is the bonus row.
+ *   R3 accept iff u * q(x) < p(x) with u in [0,1): the strict form of
+ *      "accept with probability min(1, p/q)"; q = 0 accepts iff p > 0, and a
+ *      uniform exactly on the threshold rejects.
+ *   R4 u_accept[b,i] decides position i only; u_sample[b] is consumed once,
+ *      by the residual draw after a rejection or else by the bonus draw.
+ *   R5 inverse CDF in vocabulary order over unnormalised weights: token =
+ *      smallest j with u * R < C_j (C_j inclusive prefix sum, R the total);
+ *      if rounding leaves no such j, the last j with positive weight.
+ *   R6 residual mass R = 0 after a rejection (impossible in exact arithmetic)
+ *      falls back to sampling p of the rejected row; flagged per sequence.
+ *   R7 greedy argmax on raw logits, lowest index among ties; T is unused.
+ *   R8 tree: node 0 is the root (last committed token), parents[v] < v;
+ *      accepted nodes are those whose every edge root->v matches the parent
+ *      row's argmax; the deepest accepted node wins, ties to the lowest node
+ *      index; the bonus token is the argmax of the winner's own row.
+ *   Non-finite logits are outside the method's domain (rejected here).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_OK 0
+#define OR_ERR_ARG 1
+#define OR_ERR_NONFINITE 2
+#define OR_ERR_TOKEN 3
+#define OR_ERR_TREE 4
+#define OR_ERR_NOMEM 5
+
+#define OR_F32 0
+#define OR_BF16 1
+
+/* One stored logit as float64: fp32 as is, bf16 widened by a 16-bit shift. */
+static double logit_at(const void* base, int dtype, size_t idx) {
+  if (dtype == OR_F32) return (double)((const float*)base)[idx];
+  uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* softmax of one row at temperature T, float64, max-subtracted.
+ * [REVIEW] "EAGLE: Predict Features, Not Tokens" (z -> softmax -> p);
+ * [MATH] "EAGLE's move" (p = softmax(LM_head(f'))).  R1 for T. */
+static int softmax_row(const void* base, int dtype, size_t off, int V, double T,
+                       double* out) {
+  double m = -INFINITY;
+  for (int j = 0; j < V; ++j) {
+    double x = logit_at(base, dtype, off + (size_t)j);
+    if (!isfinite(x)) return OR_ERR_NONFINITE;
+    x = x / T;
+    if (x > m) m = x;
+  }
+  double s = 0.0;
+  for (int j = 0; j < V; ++j) {
+    out[j] = exp(logit_at(base, dtype, off + (size_t)j) / T - m);
+    s += out[j];
+  }
+  for (int j = 0; j < V; ++j) out[j] /= s;
+  return OR_OK;
+}
+
+/* Inverse CDF over unnormalised weights w[0..V) (R5).  Also reports the
+ * distance of u*R to the two cumulative values bracketing the choice,
+ * divided by R (the "CDF boundary margin"). */
+static int inverse_cdf(const double* w, int V, double u, double* total_out,
+                       double* margin_out) {
+  double R = 0.0;
+  for (int j = 0; j < V; ++j) R += w[j];
+  double t = u * R;
+  double c = 0.0, prev = 0.0;
+  int tok = -1;
+  for (int j = 0; j < V; ++j) {
+    prev = c;
+    c += w[j];
+    if (t < c) { tok = j; break; }
+  }
+  if (tok < 0) { /* rounding left no j: last j with positive weight */
+    for (int j = V - 1; j >= 0; --j)
+      if (w[j] > 0.0) { tok = j; break; }
+    c = R;
+    prev = R;
+  }
+  double m1 = fabs(t - c), m0 = fabs(t - prev);
+  *total_out = R;
+  *margin_out = (R > 0.0) ? fmin(m0, m1) / R : 0.0;
+  return tok;
+}
+
+/*
+ * Sampling verification, one call over B sequences.
+ *
+ * Follows [REVIEW] "Speculative Decoding" step 3 "Accept or Reject" (left to
+ * right, discard after the first rejection, resample the rejected position,
+ * take one extra target token when all are accepted) and "Does Using a Small
+ * Model's Answer Reduce Quality?" (eq. A(x) = min(1, p(x)/q(x)); eq.
+ * p_residual(x) = norm(max(0, p(x) - q(x))));  [MATH] "Vanilla speculative
+ * decoding" (accept w.p. min(1, p/q), resample from (p - q)_+, the +1 bonus
+ * token);  [WIKI] "The mechanism" (normalized residual max(0, p - q)).
+ *
+ * Layouts: target [B, k+1, V], draft [B, k, V] (fp32 or bf16 bits), tokens
+ * int32 [B, k], u_accept float [B, k], u_sample float [B].
+ * Outputs: accepted_len [B] (n in [0, k]); out_tokens [B, k+1] (x_0..x_{n-1},
+ * then the resampled or bonus token, rest -1); p_out, q_out [B, k] float64 for
+ * every position; resid_mass [B] (R of the rejected row, 0 when all accepted).
+ * Diagnostics: acc_margin [B] = min over decided positions i <= n of
+ * |u_i - p_i/q_i| (infinite where the decision is forced); cdf_margin [B];
+ * fallback [B] = 1 where R6 applied.  Any diagnostic pointer may be NULL.
+ */
+int oracle_verify_sample(const void* target, const void* draft, int dtype,
+                         const int32_t* tokens, const float* u_accept,
+                         const float* u_sample, double temperature, int B, int k,
+                         int V, int32_t* accepted_len, int32_t* out_tokens,
+                         double* p_out, double* q_out, double* resid_mass,
+                         double* acc_margin, double* cdf_margin,
+                         int32_t* fallback) {
+  if (B < 0 || k < 0 || V < 1 || !(temperature > 0.0) || !isfinite(temperature))
+    return OR_ERR_ARG;
+  if (dtype != OR_F32 && dtype != OR_BF16) return OR_ERR_ARG;
+  double* pt = (double*)malloc(sizeof(double) * (size_t)(k + 1) * (size_t)V);
+  double* pd = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * (size_t)V);
+  double* r = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!pt || !pd || !r) { free(pt); free(pd); free(r); return OR_ERR_NOMEM; }
+  int rc = OR_OK;
+  for (int b = 0; b < B && rc == OR_OK; ++b) {
+    /* probabilities of every row of this sequence */
+    for (int i = 0; i <= k && rc == OR_OK; ++i)
+      rc = softmax_row(target, dtype, ((size_t)b * (size_t)(k + 1) + (size_t)i) * (size_t)V,
+                       V, temperature, pt + (size_t)i * V);
+    for (int i = 0; i < k && rc == OR_OK; ++i)
+      rc = softmax_row(draft, dtype, ((size_t)b * (size_t)k + (size_t)i) * (size_t)V, V,
+                       temperature, pd + (size_t)i * V);
+    if (rc != OR_OK) break;
+    for (int i = 0; i < k; ++i) {
+      int32_t x = tokens[(size_t)b * k + i];
+      if (x < 0 || x >= V) { rc = OR_ERR_TOKEN; break; }
+    }
+    if (rc != OR_OK) break;
+
+    /* accept test left to right, stop at the first rejection */
+    int n = k;
+    double amarg = INFINITY;
+    for (int i = 0; i < k; ++i) {
+      int32_t x = tokens[(size_t)b * k + i];
+      double p = pt[(size_t)i * V + x];
+      double q = pd[(size_t)i * V + x];
+      if (p_out) p_out[(size_t)b * k + i] = p;
+      if (q_out) q_out[(size_t)b * k + i] = q;
+    }
+    for (int i = 0; i < k; ++i) {
+      int32_t x = tokens[(size_t)b * k + i];
+      double p = pt[(size_t)i * V + x];
+      double q = pd[(size_t)i * V + x];
+      double u = (double)u_accept[(size_t)b * k + i];
+      if (q > 0.0 && p > 0.0) amarg = fmin(amarg, fabs(u - p / q));
+      if (!(u * q < p)) { n = i; break; }
+    }
+
+    /* residual (after a rejection) or bonus (all accepted) distribution */
+    int fb = 0;
+    double R = 0.0, cmarg = 0.0;
+    int tok;
+    if (n < k) {
+      for (int j = 0; j < V; ++j) {
+        double d = pt[(size_t)n * V + j] - pd[(size_t)n * V + j];
+        r[j] = d > 0.0 ? d : 0.0;
+      }
+      double tot = 0.0;
+      for (int j = 0; j < V; ++j) tot += r[j];
+      if (!(tot > 0.0)) { /* R6 */
+        fb = 1;
+        memcpy(r, pt + (size_t)n * V, sizeof(double) * (size_t)V);
+      }
+      tok = inverse_cdf(r, V, (double)u_sample[b], &R, &cmarg);
+      if (fb) R = 0.0;
+    } else {
+      tok = inverse_cdf(pt + (size_t)k * V, V, (double)u_sample[b], &R, &cmarg);
+      R = 0.0;
+    }
+
+    accepted_len[b] = n;
+    for (int i = 0; i <= k; ++i) {
+      int32_t v = -1;
+      if (i < n) v = tokens[(size_t)b * k + i];
+      else if (i == n) v = tok;
+      out_tokens[(size_t)b * (k + 1) + i] = v;
+    }
+    if (resid_mass) resid_mass[b] = R;
+    if (acc_margin) acc_margin[b] = amarg;
+    if (cdf_margin) cdf_margin[b] = cmarg;
+    if (fallback) fallback[b] = fb;
+  }
+  free(pt);
+  free(pd);
+  free(r);
+  return rc;
+}
+
+/* Lowest index of the largest raw logit of one row (R7). */
+static int argmax_row(const void* base, int dtype, size_t off, int V, int* err) {
+  int best = 0;
+  double bv = logit_at(base, dtype, off);
+  if (!isfinite(bv)) *err = 1;
+  for (int j = 1; j < V; ++j) {
+    double z = logit_at(base, dtype, off + (size_t)j);
+    if (!isfinite(z)) *err = 1;
+    if (z > bv) { bv = z; best = j; }
+  }
+  return best;
+}
+
+/*
+ * Greedy verification.  [REVIEW] "Does Using a Small Model's Answer Reduce
+ * Quality?" (greedy: accept if the proposal equals the target's argmax,
+ * otherwise use the target token and discard the rest) and "The Complete
+ * EAGLE-3 Inference Process" step 4 (accept the longest prefix matching target
+ * choices).  target [B, k+1, V]; tokens [B, k].  Outputs accepted_len [B],
+ * out_tokens [B, k+1] (x_0..x_{n-1}, argmax of row n, rest -1) and, if not
+ * NULL, argmax_out [B, k+1] (argmax of every target row).
+ */
+int oracle_verify_greedy(const void* target, int dtype, const int32_t* tokens, int B,
+                         int k, int V, int32_t* accepted_len, int32_t* out_tokens,
+                         int32_t* argmax_out) {
+  if (B < 0 || k < 0 || V < 1) return OR_ERR_ARG;
+  if (dtype != OR_F32 && dtype != OR_BF16) return OR_ERR_ARG;
+  int32_t* g = (int32_t*)malloc(sizeof(int32_t) * (size_t)(k + 1));
+  if (!g) return OR_ERR_NOMEM;
+  for (int b = 0; b < B; ++b) {
+    int err = 0;
+    for (int i = 0; i <= k; ++i)
+      g[i] = argmax_row(target, dtype, ((size_t)b * (k + 1) + i) * (size_t)V, V, &err);
+    if (err) { free(g); return OR_ERR_NONFINITE; }
+    int n = k;
+    for (int i = 0; i < k; ++i) {
+      int32_t x = tokens[(size_t)b * k + i];
+      if (x < 0 || x >= V) { free(g); return OR_ERR_TOKEN; }
+      if (x != g[i]) { n = i; break; }
+    }
+    accepted_len[b] = n;
+    for (int i = 0; i <= k; ++i) {
+      int32_t v = -1;
+      if (i < n) v = tokens[(size_t)b * k + i];
+      else if (i == n) v = g[n];
+      out_tokens[(size_t)b * (k + 1) + i] = v;
+      if (argmax_out) argmax_out[(size_t)b * (k + 1) + i] = g[i];
+    }
+  }
+  free(g);
+  return OR_OK;
+}
+
+/*
+ * Draft-tree greedy verification (EAGLE-2 style trees).  [REVIEW] "EAGLE-2:
+ * Does Every Context Need the Same Draft Tree?" (each node sees only the
+ * shared prefix and its own ancestors), "The Complete EAGLE-3 Inference
+ * Process" steps 3-4 (verify the tree in one pass; greedy accepts the longest
+ * prefix matching target choices); [MATH] "EAGLE-2: dynamic draft trees".
+ * Readings R7, R8.
+ *
+ * target [B, N, V]: row v is the target's next-token logits after the path
+ * root..v.  node_tokens [B, N] (node 0 ignored), parents [B, N] (parents[0]
+ * = -1, 0 <= parents[v] < v, depth(v) <= max_depth).
+ * Outputs: accepted_len [B] = depth of the chosen node; path_nodes
+ * [B, max_depth+1] = 0, ..., v* then -1; out_tokens [B, max_depth+1] = tokens
+ * of path nodes 1..depth, then the bonus token, then -1.
+ */
+int oracle_verify_tree_greedy(const void* target, int dtype, const int32_t* node_tokens,
+                              const int32_t* parents, int B, int N, int V, int max_depth,
+                              int32_t* accepted_len, int32_t* path_nodes,
+                              int32_t* out_tokens) {
+  if (B < 0 || N < 1 || V < 1 || max_depth < 0) return OR_ERR_ARG;
+  if (dtype != OR_F32 && dtype != OR_BF16) return OR_ERR_ARG;
+  int32_t* g = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+  int32_t* depth = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+  int32_t* ok = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+  if (!g || !depth || !ok) { free(g); free(depth); free(ok); return OR_ERR_NOMEM; }
+  int rc = OR_OK;
+  const int W = max_depth + 1;
+  for (int b = 0; b < B && rc == OR_OK; ++b) {
+    const int32_t* par = parents + (size_t)b * N;
+    const int32_t* tok = node_tokens + (size_t)b * N;
+    int err = 0;
+    for (int v = 0; v < N; ++v)
+      g[v] = argmax_row(target, dtype, ((size_t)b * N + v) * (size_t)V, V, &err);
+    if (err) { rc = OR_ERR_NONFINITE; break; }
+    if (par[0] != -1) { rc = OR_ERR_TREE; break; }
+    depth[0] = 0;
+    ok[0] = 1;
+    for (int v = 1; v < N; ++v) {
+      int p = par[v];
+      if (p < 0 || p >= v) { rc = OR_ERR_TREE; break; }
+      if (tok[v] < 0 || tok[v] >= V) { rc = OR_ERR_TOKEN; break; }
+      depth[v] = depth[p] + 1;
+      if (depth[v] > max_depth) { rc = OR_ERR_TREE; break; }
+      /* v is accepted iff its parent is and its token is the parent's choice */
+      ok[v] = ok[p] && (tok[v] == g[p]);
+    }
+    if (rc != OR_OK) break;
+    int best = 0;
+    for (int v = 1; v < N; ++v)
+      if (ok[v] && depth[v] > depth[best]) best = v; /* strict: lowest index on ties */
+    int d = depth[best];
+    accepted_len[b] = d;
+    for (int i = 0; i < W; ++i) {
+      path_nodes[(size_t)b * W + i] = -1;
+      out_tokens[(size_t)b * W + i] = -1;
+    }
+    int cur = best;
+    for (int i = d; i >= 0; --i) {
+      path_nodes[(size_t)b * W + i] = cur;
+      if (i >= 1) out_tokens[(size_t)b * W + i - 1] = tok[cur];
+      cur = par[cur];
+    }
+    out_tokens[(size_t)b * W + d] = g[best];
+  }
+  free(g);
+  free(depth);
+  free(ok);
+  return rc;
+}
+
+/* Expected tokens per verification pass with per-token acceptance alpha and
+ * gamma drafts: the geometric sum 1 + alpha + ... + alpha^gamma, i.e.
+ * (1 - alpha^(gamma+1)) / (1 - alpha).  [MATH] "Vanilla speculative decoding"
+ * (E formula; the +1 is the bonus token). */
+double oracle_expected_tokens(double alpha, int gamma) {
+  double e = 0.0, a = 1.0;
+  for (int i = 0; i <= gamma; ++i) {
+    e += a;
+    a *= alpha;
+  }
+  return e;
+}
+
+/* Wall-clock speedup model E / (1 + gamma * c), c = draft-step / target-pass
+ * cost.  [MATH] "The speedup math, worked". */
+double oracle_speedup_model(double alpha, int gamma, double c) {
+  return oracle_expected_tokens(alpha, gamma) / (1.0 + (double)gamma * c);
+}

@@ -1,0 +1,98 @@
+"""Plant plausible mistakes in copies of the oracle source and check that the
+pins in test_oracle_pins.py catch every one of them.
+
+Each mutant is a one-line change of ``oracle/spec_oracle.c`` (a dropped term,
+a wrong sign or index, a transposed operand, a flipped tie-break), compiled
+into a temporary library on the CPU.  The committed oracle itself is never
+modified.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "spec_oracle.c")
+
+MUTANTS = {
+    "residual_sign": ("double d = pt[(size_t)n * V + j] - pd[(size_t)n * V + j];",
+                      "double d = pd[(size_t)n * V + j] - pt[(size_t)n * V + j];"),
+    "accept_transposed": ("if (!(u * q < p)) { n = i; break; }",
+                          "if (!(u * p < q)) { n = i; break; }"),
+    "accept_non_strict": ("if (!(u * q < p)) { n = i; break; }",
+                          "if (!(u * q <= p)) { n = i; break; }"),
+    "residual_wrong_row": ("double d = pt[(size_t)n * V + j] - pd[(size_t)n * V + j];",
+                           "double d = pt[(size_t)(n + 1) * V + j] - pd[(size_t)n * V + j];"),
+    "bonus_wrong_row": ("tok = inverse_cdf(pt + (size_t)k * V,",
+                        "tok = inverse_cdf(pt + (size_t)(k > 0 ? k - 1 : 0) * V,"),
+    "temperature_dropped": ("out[j] = exp(logit_at(base, dtype, off + (size_t)j) / T - m);",
+                            "out[j] = exp(logit_at(base, dtype, off + (size_t)j) - m / T);"),
+    "cdf_unnormalised_u": ("double t = u * R;", "double t = u;"),
+    "argmax_last_tie": ("if (z > bv) { bv = z; best = j; }", "if (z >= bv) { bv = z; best = j; }"),
+    "tree_last_tie": ("if (ok[v] && depth[v] > depth[best]) best = v;",
+                      "if (ok[v] && depth[v] >= depth[best]) best = v;"),
+    "tree_ignores_ancestors": ("ok[v] = ok[p] && (tok[v] == g[p]);", "ok[v] = (tok[v] == g[p]);"),
+    "tree_bonus_from_parent": ("out_tokens[(size_t)b * W + d] = g[best];",
+                               "out_tokens[(size_t)b * W + d] = g[best > 0 ? par[best] : 0];"),
+    "greedy_emits_draft": ("else if (i == n) v = g[n];",
+                           "else if (i == n) v = (n < k) ? tokens[(size_t)b * k + n] : g[n];"),
+    "expected_tokens_short": ("for (int i = 0; i <= gamma; ++i) {", "for (int i = 0; i < gamma; ++i) {"),
+}
+
+
+class _Variant:
+    """Same API as the oracle module, bound to a mutated library."""
+
+    OracleError = oracle.OracleError
+
+    def __init__(self, lib):
+        self.lib = lib
+
+    def verify_sample(self, *a, **kw):
+        return oracle.verify_sample(*a, lib=self.lib, **kw)
+
+    def verify_greedy(self, *a, **kw):
+        return oracle.verify_greedy(*a, lib=self.lib, **kw)
+
+    def verify_tree_greedy(self, *a, **kw):
+        return oracle.verify_tree_greedy(*a, lib=self.lib, **kw)
+
+    def expected_tokens(self, *a, **kw):
+        return oracle.expected_tokens(*a, lib=self.lib, **kw)
+
+    def speedup_model(self, *a, **kw):
+        return oracle.speedup_model(*a, lib=self.lib, **kw)
+
+
+def _pin_checks(o):
+    yield lambda: pins.test_worked_example_expected_tokens_and_speedup(o)
+    yield lambda: pins.test_emission_law_equals_target_first_position(o, 1, 8, 0.7)
+    yield lambda: pins.test_emission_law_equals_target_later_position(o, 4)
+    yield lambda: pins.test_bonus_token_law_is_last_target_row(o, 3)
+    yield lambda: pins.test_zero_probability_cases(o)
+    yield lambda: pins.test_greedy_equals_argmax_decoding(o, "f32", 5)
+    yield lambda: pins.test_tree_bruteforce(o, 1)
+    yield lambda: pins.test_star_tree(o)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique/found"
+    mutated = tmp_path / f"mut_{name}.c"
+    mutated.write_text(src.replace(old, new))
+    lib_path = tmp_path / f"libmut_{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(lib_path),
+                    str(mutated), "-lm"], check=True)
+    o = _Variant(oracle.load_variant(str(lib_path)))
+    caught = []
+    for check in _pin_checks(o):
+        try:
+            check()
+        except (AssertionError, oracle.OracleError) as e:  # the pin fired
+            caught.append(type(e).__name__)
+            break
+    assert caught, f"mutant {name} survived every pin"

@@ -1,0 +1,431 @@
+"""Pins of the float64 oracle against facts that do not come from the oracle.
+
+* the worked example printed on the "EAGLE math" page (golden fixture);
+* exact enumeration of the first emitted token's law, obtained from the
+  oracle's own decisions by bisection over float32 uniforms, against
+  softmax(target/T) ("EAGLE-3 speculative decoding review", section "Does Using
+  a Small Model's Answer Reduce Quality?": accepted mass min(p,q) plus the
+  normalised residual recovers p);
+* chi-square goodness of fit of emitted tokens against p at every reached
+  position (review page, "Interpreting 'No Quality Loss' Precisely":
+  sampling keeps the target distribution);
+* the expected-tokens law E = (1 - alpha^(gamma+1)) / (1 - alpha) ("EAGLE
+  math", "Vanilla speculative decoding") by Monte Carlo;
+* greedy verification equals target-only argmax decoding (review page,
+  greedy bullets);
+* brute-force top-down search of tiny draft trees; the chain tree reduces to
+  greedy verification; the star tree to "any child equal to the root argmax".
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+from speculative_decoding_verification_56_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+F32_ONE_BITS = int(np.float32(1.0).view(np.uint32))
+
+
+def f32_from_bits(b):
+    return float(np.uint32(b).view(np.float32))
+
+
+def smallest_u_where(pred):
+    """Smallest float32 u in [0, 1) with pred(u) True (pred monotone False->True);
+    returns 1.0 when pred is False on all of [0, 1)."""
+    lo, hi = 0, F32_ONE_BITS  # invariant: pred false below lo, answer in [lo, hi]
+    if pred(0.0):
+        return 0.0
+    lo = 1
+    while lo < hi:
+        mid = (lo + hi) // 2
+        if pred(f32_from_bits(mid)):
+            hi = mid
+        else:
+            lo = mid + 1
+    return f32_from_bits(lo)  # == 1.0 when never true
+
+
+# ---------------------------------------------------------------------------
+# worked example printed on the page
+# ---------------------------------------------------------------------------
+
+def test_worked_example_expected_tokens_and_speedup(oracle_mod):
+    g = json.load(open(os.path.join(GOLDEN, "eagle_math_worked_example.json")))
+    half = 0.5 * 10 ** (-g["printed_decimals"])
+    for case in g["cases"]:
+        e = oracle_mod.expected_tokens(case["alpha"], g["gamma"])
+        s = oracle_mod.speedup_model(case["alpha"], g["gamma"], g["c"])
+        assert abs(e - case["E"]) <= half + 1e-12, (case, e)
+        assert abs(s - case["speedup"]) <= half + 1e-12, (case, s)
+
+
+@pytest.mark.parametrize("alpha", [0.0, 0.3, 0.7, 0.95, 1.0])
+@pytest.mark.parametrize("gamma", [0, 1, 4, 7])
+def test_expected_tokens_closed_form(oracle_mod, alpha, gamma):
+    closed = gamma + 1.0 if alpha == 1.0 else (1 - alpha ** (gamma + 1)) / (1 - alpha)
+    assert oracle_mod.expected_tokens(alpha, gamma) == pytest.approx(closed, rel=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# exact enumeration of the emitted-token law
+# ---------------------------------------------------------------------------
+
+def _call(oracle_mod, zt, zd, T, toks, ua, us):
+    B = 1
+    k = zd.shape[0]
+    return oracle_mod.verify_sample(zt.reshape(B, k + 1, -1), zd.reshape(B, k, -1),
+                                    np.array(toks, np.int32).reshape(B, k),
+                                    np.array(ua, np.float32).reshape(B, k),
+                                    np.array([us], np.float32), T, dtype="f32")
+
+
+def _emission_law_at(oracle_mod, zt, zd, T, pos):
+    """Law of the token emitted at position ``pos`` given that the first ``pos``
+    drafts were accepted, measured from the oracle's decisions."""
+    k, V = zd.shape
+    q = special.softmax(zd[pos].astype(np.float64) / T)
+    base_tok = [0] * k
+    base_ua = [0.0] * k            # u = 0 accepts every earlier position (p > 0)
+    # P(accept | x) as the measure of the accepting uniforms
+    p_acc = np.zeros(V)
+    for x in range(V):
+        toks = list(base_tok)
+        toks[pos] = x
+
+        def rejected(u, toks=toks):
+            ua = list(base_ua)
+            ua[pos] = u
+            return _call(oracle_mod, zt, zd, T, toks, ua, 0.5)["accepted_len"][0] == pos
+        p_acc[x] = smallest_u_where(rejected)
+    # residual law: reject at pos with the draft whose p/q is smallest
+    p = special.softmax(zt[pos].astype(np.float64) / T)
+    xr = int(np.argmin(p / q))
+    toks = list(base_tok)
+    toks[pos] = xr
+    ua = list(base_ua)
+    ua[pos] = float(np.nextafter(np.float32(1.0), np.float32(0.0)))
+    assert _call(oracle_mod, zt, zd, T, toks, ua, 0.5)["accepted_len"][0] == pos
+    cdf = np.zeros(V)
+    for j in range(V):
+        cdf[j] = smallest_u_where(
+            lambda u: _call(oracle_mod, zt, zd, T, toks, ua, u)["out_tokens"][0, pos] > j)
+    p_res = np.diff(np.concatenate([[0.0], cdf]))
+    emit = q * p_acc + (1.0 - np.dot(q, p_acc)) * p_res
+    return emit, p
+
+
+@pytest.mark.parametrize("seed,V,T", [(0, 5, 1.0), (1, 8, 0.7), (2, 16, 1.3), (3, 6, 0.5)])
+def test_emission_law_equals_target_first_position(oracle_mod, seed, V, T):
+    rng = np.random.default_rng(seed)
+    zt = (rng.standard_normal((2, V)) * 1.5).astype(np.float32)
+    zd = (zt[:1] + rng.standard_normal((1, V))).astype(np.float32)
+    emit, p = _emission_law_at(oracle_mod, zt, zd, T, 0)
+    assert np.abs(emit - p).max() < 2e-6 * V, (emit, p)
+
+
+@pytest.mark.parametrize("seed", [4, 5])
+def test_emission_law_equals_target_later_position(oracle_mod, seed):
+    """Position 1 must use target row 1 and draft row 1 (row alignment)."""
+    V, T = 7, 0.9
+    rng = np.random.default_rng(seed)
+    zt = (rng.standard_normal((3, V)) * 2.0).astype(np.float32)
+    zd = (zt[:2] + rng.standard_normal((2, V)) * 0.8).astype(np.float32)
+    emit, p = _emission_law_at(oracle_mod, zt, zd, T, 1)
+    assert np.abs(emit - p).max() < 2e-6 * V
+    # and it is not the law of any other row
+    for other in (0, 2):
+        po = special.softmax(zt[other].astype(np.float64) / T)
+        assert np.abs(emit - po).max() > 1e-3
+
+
+@pytest.mark.parametrize("k", [1, 3])
+def test_bonus_token_law_is_last_target_row(oracle_mod, k):
+    V, T = 9, 1.1
+    rng = np.random.default_rng(10 + k)
+    zt = (rng.standard_normal((k + 1, V)) * 2.0).astype(np.float32)
+    zd = (zt[:k] + rng.standard_normal((k, V))).astype(np.float32)
+    toks, ua = [0] * k, [0.0] * k
+    assert _call(oracle_mod, zt, zd, T, toks, ua, 0.5)["accepted_len"][0] == k
+    cdf = np.array([smallest_u_where(
+        lambda u: _call(oracle_mod, zt, zd, T, toks, ua, u)["out_tokens"][0, k] > j)
+        for j in range(V)])
+    law = np.diff(np.concatenate([[0.0], cdf]))
+    p = special.softmax(zt[k].astype(np.float64) / T)
+    assert np.abs(law - p).max() < 2e-6 * V
+
+
+# ---------------------------------------------------------------------------
+# chi-square over many seeded trials
+# ---------------------------------------------------------------------------
+
+def _trials(B, zt_row, zd_row, rng):
+    zt = np.broadcast_to(zt_row, (B,) + zt_row.shape).copy()
+    zd = np.broadcast_to(zd_row, (B,) + zd_row.shape).copy()
+    return zt, zd
+
+
+def _chisq_pvalue(samples, probs):
+    V = probs.size
+    obs = np.bincount(samples, minlength=V).astype(np.float64)
+    exp = probs * samples.size
+    keep = exp > 5
+    obs_k = np.append(obs[keep], obs[~keep].sum())
+    exp_k = np.append(exp[keep], exp[~keep].sum())
+    if exp_k[-1] == 0:
+        obs_k, exp_k = obs_k[:-1], exp_k[:-1]
+    return stats.chisquare(obs_k, exp_k).pvalue
+
+
+@pytest.mark.parametrize("seed,T,dtype", [(0, 1.0, "f32"), (1, 0.8, "bf16")])
+def test_chisquare_every_position(oracle_mod, seed, T, dtype):
+    B, k, V = 200_000, 3, 8
+    rng = np.random.default_rng(seed)
+    zt_row = (rng.standard_normal((k + 1, V)) * 1.5).astype(np.float32)
+    zd_row = (zt_row[:k] + rng.standard_normal((k, V)) * 0.9).astype(np.float32)
+    if dtype == "bf16":
+        zt_row = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(zt_row))
+        zd_row = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(zd_row))
+    zt, zd = _trials(B, zt_row, zd_row, rng)
+    qs = [special.softmax(zd_row[i].astype(np.float64) / T) for i in range(k)]
+    toks = np.stack([rng.choice(V, size=B, p=qs[i]) for i in range(k)], axis=1).astype(np.int32)
+    ua = synth.uniforms_f32(rng, (B, k))
+    us = synth.uniforms_f32(rng, (B,))
+    if dtype == "bf16":
+        zt_s, zd_s = synth.f32_to_bf16_bits(zt), synth.f32_to_bf16_bits(zd)
+    else:
+        zt_s, zd_s = zt, zd
+    res = oracle_mod.verify_sample(zt_s, zd_s, toks, ua, us, T, dtype=dtype)
+    n = res["accepted_len"]
+    for j in range(k + 1):
+        reached = n >= j
+        emitted = res["out_tokens"][reached, j]
+        p = special.softmax(zt_row[j].astype(np.float64) / T)
+        pv = _chisq_pvalue(emitted, p)
+        assert pv > 1e-3, (j, pv)
+    # a wrong law is detected by the same statistic
+    p_wrong = special.softmax(zd_row[0].astype(np.float64) / T)
+    assert _chisq_pvalue(res["out_tokens"][:, 0], p_wrong) < 1e-6
+
+
+def test_chisquare_k0_is_plain_sampling(oracle_mod):
+    B, V, T = 100_000, 10, 1.0
+    rng = np.random.default_rng(7)
+    row = (rng.standard_normal((1, V)) * 2).astype(np.float32)
+    zt = np.broadcast_to(row, (B, 1, V)).copy()
+    res = oracle_mod.verify_sample(zt, np.zeros((B, 0, V), np.float32), np.zeros((B, 0), np.int32),
+                                   np.zeros((B, 0), np.float32), synth.uniforms_f32(rng, (B,)), T)
+    assert (res["accepted_len"] == 0).all()
+    assert _chisq_pvalue(res["out_tokens"][:, 0], special.softmax(row[0].astype(np.float64))) > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# expected tokens per pass
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("alpha_target", [0.7, 0.8, 0.9])
+def test_expected_tokens_monte_carlo(oracle_mod, alpha_target):
+    B, k = 200_000, 4
+    a = 0.35
+    b = a + (1.0 - alpha_target)           # |a - b| = 1 - alpha
+    zt_row = np.array([0.0, np.log((1 - a) / a)], np.float32)
+    zd_row = np.array([0.0, np.log((1 - b) / b)], np.float32)
+    p = special.softmax(zt_row.astype(np.float64))
+    q = special.softmax(zd_row.astype(np.float64))
+    alpha = np.minimum(p, q).sum()          # exact per-row acceptance of these logits
+    assert abs(alpha - alpha_target) < 1e-6
+    rng = np.random.default_rng(int(alpha_target * 100))
+    zt = np.broadcast_to(zt_row, (B, k + 1, 2)).copy()
+    zd = np.broadcast_to(zd_row, (B, k, 2)).copy()
+    toks = (rng.random((B, k)) >= q[0]).astype(np.int32)
+    res = oracle_mod.verify_sample(zt, zd, toks, synth.uniforms_f32(rng, (B, k)),
+                                   synth.uniforms_f32(rng, (B,)), 1.0)
+    emitted = res["accepted_len"].astype(np.float64) + 1.0
+    E = (1 - alpha ** (k + 1)) / (1 - alpha)
+    se = emitted.std() / np.sqrt(B)
+    assert abs(emitted.mean() - E) < 5 * se, (emitted.mean(), E, se)
+    # per-position acceptance is alpha: P(n >= i) = alpha^i
+    for i in range(1, k + 1):
+        frac = (res["accepted_len"] >= i).mean()
+        assert abs(frac - alpha ** i) < 5 * np.sqrt(alpha ** i * (1 - alpha ** i) / B)
+
+
+# ---------------------------------------------------------------------------
+# boundary cases of the acceptance rule
+# ---------------------------------------------------------------------------
+
+def test_identical_rows_accept_everything(oracle_mod):
+    c = synth.make_chain_case(B=20, k=4, V=50, seed=3)
+    ua = np.full((20, 4), np.nextafter(np.float32(1), np.float32(0)), np.float32)
+    res = oracle_mod.verify_sample(c.target, c.target[:, :4], c.tokens, ua, c.u_sample, 1.0)
+    assert (res["accepted_len"] == 4).all()
+    assert (res["resid_mass"] == 0).all()
+    assert np.allclose(res["p"], res["q"])
+
+
+def test_zero_probability_cases(oracle_mod):
+    V = 6
+    zt = np.zeros((1, 3, V), np.float32)
+    zd = np.zeros((1, 2, V), np.float32)
+    zt[0, 0, 2] = -5000.0     # p(2) underflows to 0 at position 0
+    zd[0, 1, 4] = -5000.0     # q(4) underflows to 0 at position 1
+    # position 0: p = 0 rejects even with u = 0 (0 * q < 0 is false)
+    r = oracle_mod.verify_sample(zt, zd, np.array([[2, 4]]), np.array([[0.0, 0.5]], np.float32),
+                                 np.array([0.3], np.float32), 1.0)
+    assert r["accepted_len"][0] == 0 and r["p"][0, 0] == 0.0
+    assert r["out_tokens"][0, 0] != 2 and r["out_tokens"][0, 1] == -1
+    # position 1: q = 0 accepts for any u (p > 0)
+    r = oracle_mod.verify_sample(zt, zd, np.array([[0, 4]]),
+                                 np.array([[0.0, np.nextafter(np.float32(1), np.float32(0))]],
+                                          np.float32), np.array([0.3], np.float32), 1.0)
+    assert r["accepted_len"][0] == 2 and r["q"][0, 1] == 0.0
+
+
+def test_residual_zero_falls_back_to_target_row(oracle_mod):
+    V = 5
+    zt = np.zeros((1, 2, V), np.float32)
+    zt[0, 0] = [0.0, 1.0, -5000.0, 0.5, 0.2]
+    zd = zt[:, :1].copy()                      # identical rows, token has p = q = 0
+    us = np.array([0.8], np.float32)
+    r = oracle_mod.verify_sample(zt, zd, np.array([[2]]), np.array([[0.0]], np.float32), us, 1.0)
+    assert r["accepted_len"][0] == 0 and r["fallback"][0] == 1 and r["resid_mass"][0] == 0
+    p = special.softmax(zt[0, 0].astype(np.float64))
+    expect = int(np.searchsorted(np.cumsum(p), 0.8 * p.sum(), side="right"))
+    assert r["out_tokens"][0, 0] == expect
+
+
+def test_invalid_inputs_raise(oracle_mod):
+    c = synth.make_chain_case(B=2, k=2, V=10, seed=1)
+    bad = c.tokens.copy()
+    bad[1, 1] = 10
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.verify_sample(c.target, c.draft, bad, c.u_accept, c.u_sample, 1.0)
+    t = c.target.copy()
+    t[0, 0, 3] = np.inf
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.verify_sample(t, c.draft, c.tokens, c.u_accept, c.u_sample, 1.0)
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.verify_greedy(t, c.tokens)
+
+
+# ---------------------------------------------------------------------------
+# greedy == target-only argmax decoding
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("k", [0, 1, 5])
+def test_greedy_equals_argmax_decoding(oracle_mod, dtype, k):
+    B, V = 300, 23
+    rng = np.random.default_rng(k)
+    # small integer logits: many ties, lowest index must win
+    zt = rng.integers(-3, 4, size=(B, k + 1, V)).astype(np.float32)
+    g = np.argmax(zt, axis=-1)                         # library argmax: first maximum
+    toks = np.where(rng.random((B, k)) < 0.75, g[:, :k],
+                    rng.integers(0, V, size=(B, k))).astype(np.int32)
+    stored = synth.f32_to_bf16_bits(zt) if dtype == "bf16" else zt
+    res = oracle_mod.verify_greedy(stored, toks, dtype=dtype)
+    for b in range(B):
+        n = 0
+        while n < k and toks[b, n] == g[b, n]:
+            n += 1
+        assert res["accepted_len"][b] == n
+        expect = list(g[b, :n + 1]) + [-1] * (k - n)
+        assert list(res["out_tokens"][b]) == expect
+    assert (res["argmax"] == g).all()
+
+
+# ---------------------------------------------------------------------------
+# draft trees: brute-force top-down search
+# ---------------------------------------------------------------------------
+
+def _tree_bruteforce(rows, tok, par):
+    """Follow target greedy decoding down the tree from the root, exploring
+    every child whose token equals the current row's argmax."""
+    N = len(par)
+    children = [[] for _ in range(N)]
+    for v in range(1, N):
+        children[par[v]].append(v)
+    best = (0, 0)           # (depth, node)
+    stack = [(0, 0)]
+    while stack:
+        v, d = stack.pop()
+        if d > best[0] or (d == best[0] and v < best[1]):
+            best = (d, v)
+        g = int(np.argmax(rows[v]))
+        for c in children[v]:
+            if tok[c] == g:
+                stack.append((c, d + 1))
+    d, v = best
+    path = [v]
+    while path[-1] != 0:
+        path.append(par[path[-1]])
+    path = path[::-1]
+    return d, path, [tok[x] for x in path[1:]] + [int(np.argmax(rows[v]))]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_tree_bruteforce(oracle_mod, seed):
+    rng = np.random.default_rng(seed)
+    B, V, max_depth = 40, 6, 5
+    N = int(rng.integers(1, 13))
+    zt = rng.integers(-2, 3, size=(B, N, V)).astype(np.float32)
+    par = np.stack([synth.make_tree_parents(rng, N, max_depth, 3) for _ in range(B)])
+    g = np.argmax(zt, axis=-1)
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    for b in range(B):
+        for v in range(1, N):
+            if rng.random() < 0.7:
+                tok[b, v] = g[b, par[b, v]]
+    res = oracle_mod.verify_tree_greedy(zt, tok, par, max_depth, dtype="f32")
+    W = max_depth + 1
+    for b in range(B):
+        d, path, toks = _tree_bruteforce(zt[b], tok[b], par[b])
+        assert res["accepted_len"][b] == d
+        assert list(res["path_nodes"][b]) == path + [-1] * (W - len(path))
+        assert list(res["out_tokens"][b]) == toks + [-1] * (W - len(toks))
+
+
+def test_chain_tree_reduces_to_greedy(oracle_mod):
+    c = synth.make_chain_case(B=50, k=6, V=30, seed=9, greedy_force=0.8)
+    k = c.k
+    par = np.tile(np.arange(-1, k, dtype=np.int32), (c.B, 1))     # parent[v] = v - 1
+    tok = np.concatenate([np.zeros((c.B, 1), np.int32), c.tokens], axis=1)
+    tr = oracle_mod.verify_tree_greedy(c.target, tok, par, k, dtype="f32")
+    gr = oracle_mod.verify_greedy(c.target, c.tokens, dtype="f32")
+    assert (tr["accepted_len"] == gr["accepted_len"]).all()
+    assert (tr["out_tokens"] == gr["out_tokens"]).all()
+
+
+def test_star_tree(oracle_mod):
+    B, N, V = 60, 9, 7
+    rng = np.random.default_rng(2)
+    zt = rng.standard_normal((B, N, V)).astype(np.float32)
+    par = np.zeros((B, N), np.int32)
+    par[:, 0] = -1
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    res = oracle_mod.verify_tree_greedy(zt, tok, par, 1, dtype="f32")
+    g0 = np.argmax(zt[:, 0], axis=-1)
+    for b in range(B):
+        hits = [v for v in range(1, N) if tok[b, v] == g0[b]]
+        if hits:
+            v = hits[0]
+            assert res["accepted_len"][b] == 1
+            assert list(res["path_nodes"][b]) == [0, v]
+            assert list(res["out_tokens"][b]) == [g0[b], int(np.argmax(zt[b, v]))]
+        else:
+            assert res["accepted_len"][b] == 0
+            assert list(res["out_tokens"][b]) == [g0[b], -1]
+
+
+def test_malformed_trees_raise(oracle_mod):
+    zt = np.zeros((1, 4, 5), np.float32)
+    tok = np.zeros((1, 4), np.int32)
+    for par in ([-1, 0, 2, 1], [-1, 0, 1, 5], [0, 0, 1, 2], [-1, -1, 0, 1]):
+        with pytest.raises(oracle_mod.OracleError):
+            oracle_mod.verify_tree_greedy(zt, tok, np.array([par], np.int32), 5, dtype="f32")
+    with pytest.raises(oracle_mod.OracleError):   # depth 3 > max_depth 2
+        oracle_mod.verify_tree_greedy(zt, tok, np.array([[-1, 0, 1, 2]], np.int32), 2, dtype="f32")
