@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""Throughput of batched draft-token verification on one GB300.
+
+One step = one pass of the whole verification path over one batch:
+  1. spec_verify_sample      B=64 sequences, k=4 drafts, V=128256, bf16, T=1.0
+  2. spec_verify_greedy      same logits shape, 70% of drafts forced to argmax
+  3. spec_verify_tree_greedy 16 trees of 60 nodes, depth <= 6, V=128256, bf16
+Metric: verified draft positions per second (B*k + B*k + B*(N-1) = 1456 per
+step) and the achieved HBM bandwidth on the logits the method must read.
+
+Inputs are generated once on the host (seeded) and copied to 4 device sets used
+in rotation; every tree call reads 246 MB (> the 129 MB L2) between two uses of
+any set, so every read comes from HBM.  `value` is timed with CUDA events on the
+launching stream with inputs resident in HBM; `e2e` repeats the step through the
+same public API with inputs copied from pinned host memory and results copied
+back inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank verifies its own batches (sequences are independent:
+no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("verified draft positions/sec and achieved HBM GB/s (% of GB300 peak) "
+          "at B=64,k=4,V=128k")
+UNIT = "positions/s"
+NSETS = 4
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["speculative_decoding_verification_56_gb300/csrc/sv_device.cuh",
+                  "speculative_decoding_verification_56_gb300/csrc/sv_kernels.cuh",
+                  "speculative_decoding_verification_56_gb300/csrc/spec_verify.cu"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the oracle CPU baseline (0 disables it)")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def workload(seed):
+    from speculative_decoding_verification_56_gb300 import synth
+    samp = synth.zipf128k(seed=seed)
+    greedy = synth.greedy_variant(samp, 0.7)
+    tree = synth.tree(seed=seed)
+    return samp, greedy, tree
+
+
+def positions(samp, greedy, tree):
+    return samp.B * samp.k + greedy.B * greedy.k + tree.B * (tree.N - 1)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel):
+    """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, or
+    None when the summary is missing or the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel \
+                and parts[1] == cur:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) taken while timing."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[1]), float(parts[2]), parts[5:9]))
+            except Exception:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        use = inside if inside else rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for n, v in zip(names, r[3]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(use),
+                "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import speculative_decoding_verification_56_gb300 as sv
+    from speculative_decoding_verification_56_gb300 import build
+
+    build.build_library()
+    lib = sv.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    samp, greedy, tree = workload(args.seed + 1000 * rank)
+    pos_step = positions(samp, greedy, tree)
+    eb = samp.elem_bytes
+    B, k, V = samp.B, samp.k, samp.V
+    Bt, N, Vt = tree.B, tree.N, tree.V
+
+    # pinned host copies (e2e) and NSETS device sets (rotation)
+    def pinned(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t.pin_memory()
+
+    h = dict(t=pinned(samp.target.view(np.int16)), d=pinned(samp.draft.view(np.int16)),
+             tok=pinned(samp.tokens), ua=pinned(samp.u_accept), us=pinned(samp.u_sample),
+             gtok=pinned(greedy.tokens), tt=pinned(tree.target.view(np.int16)),
+             ttok=pinned(tree.tokens), tpar=pinned(tree.parents))
+    sets = []
+    for _ in range(NSETS):
+        sets.append({key: val.to(dev, non_blocking=False) for key, val in h.items()})
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    outs = dict(n=torch.empty(B, **i32), tok=torch.empty(B, k + 1, **i32),
+                p=torch.empty(B, k, **f32), q=torch.empty(B, k, **f32), R=torch.empty(B, **f32),
+                gn=torch.empty(B, **i32), gtok=torch.empty(B, k + 1, **i32),
+                tn=torch.empty(Bt, **i32), tpath=torch.empty(Bt, tree.max_depth + 1, **i32),
+                ttok=torch.empty(Bt, tree.max_depth + 1, **i32))
+    ws_bytes = max(sv.spec_verify_workspace_bytes(sv.SPEC_MODE_SAMPLE, B, k, V, 1),
+                   sv.spec_verify_workspace_bytes(sv.SPEC_MODE_GREEDY, B, k, V, 1),
+                   sv.spec_verify_workspace_bytes(sv.SPEC_MODE_TREE_GREEDY, Bt, N, Vt, 1))
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    O = {key: v.data_ptr() for key, v in outs.items()}
+    wsp = ws.data_ptr()
+    T = float(samp.temperature)
+
+    def call_sample(s):
+        st = lib.spec_verify_sample(s["t"].data_ptr(), s["d"].data_ptr(), 1, s["tok"].data_ptr(),
+                                    s["ua"].data_ptr(), s["us"].data_ptr(), T, B, k, V, O["n"],
+                                    O["tok"], O["p"], O["q"], O["R"], wsp, ws_bytes, sp)
+        assert st == 0, st
+
+    def call_greedy(s):
+        st = lib.spec_verify_greedy(s["t"].data_ptr(), 1, s["gtok"].data_ptr(), B, k, V,
+                                    O["gn"], O["gtok"], wsp, ws_bytes, sp)
+        assert st == 0, st
+
+    def call_tree(s):
+        st = lib.spec_verify_tree_greedy(s["tt"].data_ptr(), 1, s["ttok"].data_ptr(),
+                                         s["tpar"].data_ptr(), Bt, N, Vt, tree.max_depth,
+                                         O["tn"], O["tpath"], O["ttok"], wsp, ws_bytes, sp)
+        assert st == 0, st
+
+    # pointer tuples precomputed so the host loop stays far ahead of the GPU
+    def step(i, ev=None):
+        sa, sg, st_ = sets[(2 * i) % NSETS], sets[(2 * i + 1) % NSETS], sets[i % NSETS]
+        if ev is not None:
+            ev[0].record(stream)
+        call_sample(sa)
+        if ev is not None:
+            ev[1].record(stream)
+        call_greedy(sg)
+        if ev is not None:
+            ev[2].record(stream)
+        call_tree(st_)
+        if ev is not None:
+            ev[3].record(stream)
+
+    # second-pass bytes depend on each set's accept outcomes (same data in all sets)
+    with torch.cuda.stream(stream):
+        call_sample(sets[0])
+    stream.synchronize()
+    n_acc = outs["n"].cpu().numpy()
+    pass2_rows = int(np.where(n_acc < k, 2, 1).sum())
+    bytes_sample = (B * (2 * k + 1) + pass2_rows) * V * eb
+    bytes_greedy = B * (k + 1) * V * eb
+    bytes_tree = Bt * N * Vt * eb
+    bytes_step = bytes_sample + bytes_greedy + bytes_tree
+
+    for i in range(args.warmup):
+        step(i)
+    stream.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = sv.spec_verify_launch_count()
+    t_wall0 = time.time()
+    for i in range(K):
+        step(i, evs[i])
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    launches = sv.spec_verify_launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop(t_wall0, t_wall1) if clocks else None
+
+    total_ms = evs[0][0].elapsed_time(evs[-1][3])
+    per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+                    for e in evs])
+    mean_ms = per.mean(axis=0)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / K
+    value = world * K * pos_step / (total_ms / 1e3)
+
+    # ---- e2e through the public API: pinned host in, results back each step ----
+    E = args.e2e_steps
+    out_host = {key: torch.empty(v.shape, dtype=v.dtype).pin_memory() for key, v in outs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s = sets[0]
+        for warm in (True, False):
+            if not warm:
+                e0.record(stream)
+            for i in range(2 if warm else E):
+                for key in h:
+                    s[key].copy_(h[key], non_blocking=True)
+                sv.spec_verify_sample(s["t"].view(torch.bfloat16).view(B, k + 1, V),
+                                      s["d"].view(torch.bfloat16).view(B, k, V), s["tok"],
+                                      s["ua"], s["us"], T, outs["n"], outs["tok"], outs["p"],
+                                      outs["q"], outs["R"], ws, stream)
+                sv.spec_verify_greedy(s["t"].view(torch.bfloat16).view(B, k + 1, V), s["gtok"],
+                                      outs["gn"], outs["gtok"], ws, stream)
+                sv.spec_verify_tree_greedy(s["tt"].view(torch.bfloat16).view(Bt, N, Vt),
+                                           s["ttok"], s["tpar"], tree.max_depth, outs["tn"],
+                                           outs["tpath"], outs["ttok"], ws, stream)
+                for key in outs:
+                    out_host[key].copy_(outs[key], non_blocking=True)
+            if not warm:
+                e1.record(stream)
+            stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_value = world * E * pos_step / (e2e_ms / 1e3)
+
+    # ---- roofline of the dominant kernel ----
+    names = ["sample (stats + draw kernels)", "argmax_verify_kernel (greedy)",
+             "argmax_verify_kernel (tree)"]
+    byts = [bytes_sample, bytes_greedy, bytes_tree]
+    peak, peak_kind = measured_peak()
+    dom = int(np.argmax(mean_ms))
+    dom_name = ["sample_stats_kernel+sample_draw_kernel", "argmax_verify_kernel",
+                "argmax_verify_kernel"][dom]
+    achieved = byts[dom] / (mean_ms[dom] / 1e3) / 1e9
+    traffic = recorded_traffic(["sample", "greedy", "tree"][dom])
+    breakdown = {}
+    for j, nm in enumerate(names):
+        gbs = byts[j] / (mean_ms[j] / 1e3) / 1e9
+        breakdown[["sample", "greedy", "tree"][j]] = {
+            "kernels": nm, "ms": round(float(mean_ms[j]), 5),
+            "algorithmic_bytes": int(byts[j]), "gb_s": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4)}
+    step_gbs = bytes_step / (ms_step / 1e3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Zipf-biased Gaussian logits; random draft trees)",
+        "config": {"workload": "sample+greedy B=64 k=4 V=128256 bf16 T=1.0; "
+                               "tree greedy B=16 N=60 depth<=6 V=128256 bf16",
+                   "positions_per_step": pos_step, "algorithmic_bytes_per_step": bytes_step,
+                   "l2": f"{NSETS} rotating input sets; every set is reused only after a "
+                         "246 MB tree read (> 129 MB L2)",
+                   "parallelism": f"replicas x{world} (sequences shard, no collective)"},
+        "hbm_gbs": round(step_gbs, 1), "hbm_frac_of_peak": round(step_gbs / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": traffic, "algorithmic_bytes_per_launch": int(byts[dom])},
+        "breakdown": breakdown,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": E},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        result["cpu_baseline"] = cpu_baseline(samp, greedy, tree, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def cpu_baseline(samp, greedy, tree, budget_s):
+    """The float64 oracle as it stands, single-threaded, on whole steps of the
+    same workload until the budget is spent."""
+    import oracle
+    oracle.build()
+    pos = positions(samp, greedy, tree)
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        oracle.verify_sample(samp.target, samp.draft, samp.tokens, samp.u_accept, samp.u_sample,
+                             samp.temperature, dtype=samp.dtype)
+        oracle.verify_greedy(greedy.target, greedy.tokens, dtype=greedy.dtype)
+        oracle.verify_tree_greedy(tree.target, tree.tokens, tree.parents, tree.max_depth,
+                                  dtype=tree.dtype)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(steps * pos / el, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{steps} whole step(s) of the same workload (sample+greedy 64 seqs, "
+                      f"16 trees) in {el:.1f} s, single thread, float64 C oracle"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    samp, greedy, tree = workload(args.seed)
+    # one step = one sequence (or tree) of one mode, cycling through the modes
+    units = [("sample", samp.k), ("greedy", greedy.k), ("tree", tree.N - 1)]
+
+    def ref_step(i):
+        mode, _ = units[i % 3]
+        if mode == "sample":
+            b = (i // 3) % samp.B
+            s = slice(b, b + 1)
+            oracle.verify_sample(samp.target[s], samp.draft[s], samp.tokens[s], samp.u_accept[s],
+                                 samp.u_sample[s], samp.temperature, dtype=samp.dtype)
+        elif mode == "greedy":
+            b = (i // 3) % greedy.B
+            s = slice(b, b + 1)
+            oracle.verify_greedy(greedy.target[s], greedy.tokens[s], dtype=greedy.dtype)
+        else:
+            b = (i // 3) % tree.B
+            s = slice(b, b + 1)
+            oracle.verify_tree_greedy(tree.target[s], tree.tokens[s], tree.parents[s],
+                                      tree.max_depth, dtype=tree.dtype)
+        return units[i % 3][1]
+
+    for i in range(args.warmup):
+        ref_step(i)
+    pos = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        pos += ref_step(i)
+    el = time.perf_counter() - t0
+    value = pos / el
+    out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(el * 1e3 / max(args.steps, 1), 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference",
+           "config": {"workload": "sample+greedy B=64 k=4 V=128256 bf16 T=1.0; "
+                                  "tree greedy B=16 N=60 depth<=6 V=128256 bf16",
+                      "reference": "float64 CPU oracle (the method written out from the "
+                                   "pages); one sequence or tree per step, cycling modes"},
+           "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1,
+                            "kind": "oracle",
+                            "sample": "one sequence (sample, greedy) or one tree per step"},
+           "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify: batched draft-token verification
+ * for speculative decoding on one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (sources are web pages, cited by title and section):
+ *   [REVIEW] "EAGLE-3 speculative decoding review" (6unoyunr.github.io)
+ *   [MATH]   "EAGLE math" (aicassindra.com, tm_eagle_math)
+ *   [WIKI]   "Speculative decoding" (addictedtoai.net wiki)
+ *
+ * Conventions shared by every entry point
+ *   - All array arguments are DEVICE pointers (cudaMalloc / torch CUDA
+ *     memory), row-major and contiguous.  The caller owns all memory; the
+ *     library allocates nothing and keeps no state across calls except the
+ *     launch counter read by spec_verify_launch_count().
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on that stream and returns; it
+ *     never synchronises.  Outputs are valid once the stream reaches them.
+ *   - Logits are fp32 (SPEC_DTYPE_F32) or bf16 (SPEC_DTYPE_BF16, raw 16-bit
+ *     patterns).  Logit pointers must be aligned to the element size; rows
+ *     whose byte length is a multiple of 16 starting at a 16-byte aligned base
+ *     take the vectorised path, others a scalar path with identical results.
+ *   - Logits must be finite with |logit / T| < 2^23; other values give
+ *     unspecified (but memory-safe) outputs.
+ *   - `workspace`: device scratch of at least spec_verify_workspace_bytes()
+ *     bytes, 256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE (e.g.
+ *     cudaMemsetAsync).  Every call returns the workspace's synchronisation
+ *     counters to zero, so one workspace serves any later call of any shape.
+ *     Two calls that share a workspace must not run concurrently (issue them
+ *     on one stream, or order them with events).
+ *   - Errors found on the host (NULL pointer, bad size, bad temperature,
+ *     misalignment, workspace too small) return before anything is enqueued.
+ *     A failed kernel launch returns SPEC_ERR_CUDA.  Bad DEVICE data (a token
+ *     id outside [0, V), a malformed tree) is never trapped: the kernels clamp
+ *     every access, treat the item as not matching, and set a bit of the
+ *     workspace's flag word (spec_verify_read_flags).
+ *   - B = 0 is a no-op that returns SPEC_OK.
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_VERIFY_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define SPEC_API __attribute__((visibility("default")))
+#else
+#define SPEC_API
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1, /* NULL pointer, size out of range, T <= 0 or NaN */
+  SPEC_ERR_ALIGNMENT = 2,   /* pointer not aligned as documented */
+  SPEC_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than required */
+  SPEC_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+} spec_status_t;
+
+typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
+
+typedef enum {
+  SPEC_MODE_SAMPLE = 0,
+  SPEC_MODE_GREEDY = 1,
+  SPEC_MODE_TREE_GREEDY = 2
+} spec_mode_t;
+
+/* Bits of the workspace flag word (sticky until read with clear != 0). */
+#define SPEC_FLAG_TOKEN_RANGE 1u       /* a draft/node token was outside [0, V) */
+#define SPEC_FLAG_BAD_PARENT 2u        /* parents[v] outside [0, v) for some v >= 1 */
+#define SPEC_FLAG_DEPTH 4u             /* a node deeper than max_depth */
+#define SPEC_FLAG_RESIDUAL_FALLBACK 8u /* residual mass was 0 after a rejection;
+                                          that position was sampled from p */
+
+/* Limits checked on the host. */
+#define SPEC_MAX_V (1 << 26)
+#define SPEC_MAX_K 1024
+#define SPEC_MAX_TREE_NODES 65536
+#define SPEC_MAX_TREE_DEPTH 1024
+/* Rows of one call plus 2*B must not exceed this (synchronisation counters). */
+#define SPEC_MAX_COUNTERS 262144
+
+/*
+ * Bytes of workspace needed by one call.  mode: spec_mode_t; k_or_N: k draft
+ * tokens (chain modes) or N tree nodes (tree mode).  Returns 0 for arguments
+ * outside the limits above.
+ */
+SPEC_API size_t spec_verify_workspace_bytes(int mode, int B, int k_or_N, int V, int dtype);
+
+/*
+ * Rejection-sampling verification of B chains of k draft tokens.
+ *
+ * Computes, per sequence b ([REVIEW] "Speculative Decoding" step 3 "Accept or
+ * Reject"; "Does Using a Small Model's Answer Reduce Quality?", eqs. A(x) and
+ * p_residual; [MATH] "Vanilla speculative decoding"; [WIKI] "The mechanism"):
+ *   p_i = softmax(target[b,i,:] / T),  q_i = softmax(draft[b,i,:] / T)
+ *   accept draft i iff u_accept[b,i] * q_i(x_i) < p_i(x_i)  (strict; left to
+ *   right); n = index of the first rejection, or k if none;
+ *   if n < k: token ~ norm(max(0, p_n - q_n)) by inverse CDF with u_sample[b]
+ *   else:     bonus token ~ p_k by inverse CDF with u_sample[b].
+ * Inverse CDF: the smallest vocabulary index j with u * R < C_j, C_j the
+ * inclusive prefix sum of the weights and R their total.
+ *
+ *   target_logits [B, k+1, V]  row i scores draft position i; row k = bonus row
+ *   draft_logits  [B, k, V]    row i = the distribution draft i was drawn from
+ *   draft_tokens  int32 [B, k]
+ *   u_accept      float [B, k] in [0, 1);   u_sample float [B] in [0, 1)
+ *   temperature   > 0, finite; the same T scales target and draft rows
+ * Outputs (device, written in full):
+ *   accepted_len  int32 [B]       n in [0, k]
+ *   out_tokens    int32 [B, k+1]  x_0..x_{n-1}, the resampled/bonus token, then -1
+ *   p_out, q_out  float [B, k]    p_i(x_i), q_i(x_i) for EVERY i (also i > n)
+ *   resid_mass    float [B]       R = sum_j max(0, p_n - q_n) when n < k, else 0
+ * With k = 0, draft_logits, draft_tokens, u_accept, p_out and q_out may be
+ * NULL and the call samples one token from softmax(target[b,0,:] / T).
+ * Launches two kernels (softmax statistics + accept test; residual/bonus draw).
+ */
+SPEC_API spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
+                                 int dtype, const int32_t* draft_tokens,
+                                 const float* u_accept, const float* u_sample,
+                                 float temperature, int B, int k, int V,
+                                 int32_t* accepted_len, int32_t* out_tokens,
+                                 float* p_out, float* q_out, float* resid_mass,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Greedy verification ([REVIEW] "Does Using a Small Model's Answer Reduce
+ * Quality?", greedy bullets): g_i = argmax_j target[b,i,j] on raw logits,
+ * lowest index among ties; n = first i < k with draft_tokens[b,i] != g_i, or
+ * k; emits x_0..x_{n-1}, g_n.  Temperature plays no part.
+ *   target_logits [B, k+1, V]; draft_tokens int32 [B, k] (NULL allowed if k = 0)
+ *   accepted_len  int32 [B];   out_tokens int32 [B, k+1] (unused slots -1)
+ * One kernel launch.
+ */
+SPEC_API spec_status_t spec_verify_greedy(const void* target_logits, int dtype,
+                                 const int32_t* draft_tokens, int B, int k, int V,
+                                 int32_t* accepted_len, int32_t* out_tokens,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Draft-tree greedy verification (EAGLE-2 style trees; [REVIEW] "EAGLE-2",
+ * "The Complete EAGLE-3 Inference Process" steps 3-4; [MATH] "EAGLE-2:
+ * dynamic draft trees").  Node 0 is the root (the last committed token); row v
+ * of target_logits is the target's next-token logits after the path root..v.
+ * Node v >= 1 is accepted iff every node w on the path root..v has
+ * node_tokens[w] == argmax(target row of parent(w)).  The deepest accepted
+ * node v* wins (lowest node index among equally deep ones); the bonus token
+ * is argmax(target row v*).
+ *   target_logits [B, N, V]
+ *   node_tokens   int32 [B, N]   (node 0's entry is ignored)
+ *   parents       int32 [B, N]   parents[b,0] ignored; 0 <= parents[b,v] < v
+ *   max_depth     depth limit of the trees, 0..SPEC_MAX_TREE_DEPTH
+ * Outputs:
+ *   accepted_len  int32 [B]                depth of v*
+ *   path_nodes    int32 [B, max_depth+1]   0, ..., v*, then -1
+ *   out_tokens    int32 [B, max_depth+1]   tokens of path nodes 1..depth, the
+ *                                          bonus token, then -1
+ * One kernel launch.
+ */
+SPEC_API spec_status_t spec_verify_tree_greedy(const void* target_logits, int dtype,
+                                      const int32_t* node_tokens, const int32_t* parents,
+                                      int B, int N, int V, int max_depth,
+                                      int32_t* accepted_len, int32_t* path_nodes,
+                                      int32_t* out_tokens, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/*
+ * Copy the workspace's flag word to *host_flags (synchronises `stream`); with
+ * clear != 0 the word is then reset to 0 on the stream.
+ */
+SPEC_API spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_flags, int clear,
+                                     void* stream);
+
+/* Number of kernels this library has launched in this process. */
+SPEC_API uint64_t spec_verify_launch_count(void);
+
+/* Static description of a status code. */
+SPEC_API const char* spec_status_string(int status);
+
+/* SPEC_VERIFY_ABI_VERSION of the loaded library. */
+SPEC_API int spec_verify_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H_ */

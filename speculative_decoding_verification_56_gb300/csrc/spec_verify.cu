@@ -1,0 +1,313 @@
+// spec_verify.cu -- C ABI of libspecverify (declared in include/spec_verify.h):
+// host-side argument checks, workspace layout and kernel launches.
+//
+// Workspace layout (all offsets 256-byte aligned):
+//   [0, 256)                 header; word 0 = sticky device flag bits
+//   [256, 256 + 4*MAXC)      synchronisation counters, zero between calls
+//   [256 + 4*MAXC, ...)      per-call scratch records (any content on entry)
+// Counters live at fixed offsets, so a workspace zero-filled once stays valid
+// for calls of any shape: each call's last-arriving CTAs reset what they used.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "spec_verify.h"
+#include "sv_kernels.cuh"
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr size_t kAlign = 256;
+constexpr size_t kHeaderBytes = 256;
+constexpr size_t kCounterBytes = (size_t)SPEC_MAX_COUNTERS * sizeof(unsigned);
+constexpr size_t kDataOffset = kHeaderBytes + kCounterBytes;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int elem_bytes(int dtype) { return dtype == SPEC_DTYPE_BF16 ? 2 : 4; }
+int chunk_elems(int dtype) {
+  return dtype == SPEC_DTYPE_BF16 ? sv::BF16::kChunk : sv::F32::kChunk;
+}
+
+struct Layout {
+  size_t bytes = 0;
+  int rows = 0, nchunks = 0;
+  size_t off_part = 0, off_rows = 0, off_sel = 0, off_csum = 0;  // sample
+  size_t off_arg = 0;                                            // greedy / tree
+};
+
+// Returns false for arguments outside the documented limits.
+bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return false;
+  if (B < 0 || V < 1 || V > SPEC_MAX_V) return false;
+  const int C = (V + chunk_elems(dtype) - 1) / chunk_elems(dtype);
+  long long rows;
+  if (mode == SPEC_MODE_SAMPLE) {
+    if (kN < 0 || kN > SPEC_MAX_K) return false;
+    rows = (long long)B * (2LL * kN + 1);
+  } else if (mode == SPEC_MODE_GREEDY) {
+    if (kN < 0 || kN > SPEC_MAX_K) return false;
+    rows = (long long)B * (kN + 1LL);
+  } else if (mode == SPEC_MODE_TREE_GREEDY) {
+    if (kN < 1 || kN > SPEC_MAX_TREE_NODES) return false;
+    rows = (long long)B * kN;
+  } else {
+    return false;
+  }
+  if (rows + 2LL * B > SPEC_MAX_COUNTERS) return false;
+  if (rows * C > 0x7FFFFFFFLL) return false;
+  L->rows = (int)rows;
+  L->nchunks = C;
+  size_t off = kDataOffset;
+  if (mode == SPEC_MODE_SAMPLE) {
+    L->off_part = off;
+    off = align_up(off + (size_t)rows * C * sizeof(sv::SoftmaxPartial));
+    L->off_rows = off;
+    off = align_up(off + (size_t)rows * sizeof(sv::RowStats));
+    L->off_sel = off;
+    off = align_up(off + (size_t)B * sizeof(int32_t));
+    L->off_csum = off;
+    off = align_up(off + (size_t)B * C * sizeof(double));
+  } else {
+    L->off_part = off;
+    off = align_up(off + (size_t)rows * C * sizeof(sv::ArgPartial));
+    L->off_arg = off;
+    off = align_up(off + (size_t)rows * sizeof(int32_t));
+  }
+  L->bytes = off;
+  return true;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// 16-byte vector path: base aligned and every row a whole number of vectors.
+bool vec_ok(const void* p, int V, int dtype) {
+  return aligned(p, 16) && ((size_t)V * elem_bytes(dtype)) % 16 == 0;
+}
+
+template <typename KernelT, typename ParamT>
+spec_status_t launch(KernelT kernel, int grid, const ParamT& prm, void* stream, bool pdl) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(sv::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return SPEC_OK;
+}
+
+template <typename E, bool kVec>
+spec_status_t run_sample(const sv::SampleParams& prm, int rows, void* stream) {
+  spec_status_t st =
+      launch(sv::sample_stats_kernel<E, kVec>, rows * prm.nchunks, prm, stream, false);
+  if (st != SPEC_OK) return st;
+  return launch(sv::sample_draw_kernel<E, kVec>, prm.B * prm.nchunks, prm, stream, true);
+}
+
+template <typename E, bool kVec>
+spec_status_t run_argmax(const sv::ArgmaxParams& prm, int rows, void* stream) {
+  return launch(sv::argmax_verify_kernel<E, kVec>, rows * prm.nchunks, prm, stream, false);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_verify_workspace_bytes(int mode, int B, int k_or_N, int V, int dtype) {
+  Layout L;
+  if (!make_layout(mode, B, k_or_N, V, dtype, &L)) return 0;
+  return L.bytes;
+}
+
+spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits, int dtype,
+                                 const int32_t* draft_tokens, const float* u_accept,
+                                 const float* u_sample, float temperature, int B, int k, int V,
+                                 int32_t* accepted_len, int32_t* out_tokens, float* p_out,
+                                 float* q_out, float* resid_mass, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || k < 0 || k > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(SPEC_MODE_SAMPLE, B, k, V, dtype, &L)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !u_sample || !accepted_len || !out_tokens || !resid_mass)
+    return SPEC_ERR_INVALID_ARG;
+  if (k > 0 && (!draft_logits || !draft_tokens || !u_accept || !p_out || !q_out))
+    return SPEC_ERR_INVALID_ARG;
+  const int eb = elem_bytes(dtype);
+  if (!aligned(target_logits, eb) || (k > 0 && !aligned(draft_logits, eb)))
+    return SPEC_ERR_ALIGNMENT;
+  if (!aligned(accepted_len, 4) || !aligned(out_tokens, 4) || !aligned(u_sample, 4) ||
+      !aligned(resid_mass, 4) ||
+      (k > 0 && (!aligned(draft_tokens, 4) || !aligned(u_accept, 4) || !aligned(p_out, 4) ||
+                 !aligned(q_out, 4))))
+    return SPEC_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
+
+  char* ws = static_cast<char*>(workspace);
+  unsigned* counters = reinterpret_cast<unsigned*>(ws + kHeaderBytes);
+  sv::SampleParams prm;
+  prm.target = target_logits;
+  prm.draft = draft_logits;
+  prm.tokens = draft_tokens;
+  prm.u_accept = u_accept;
+  prm.u_sample = u_sample;
+  prm.scale = (float)(1.4426950408889634 / (double)temperature);
+  prm.B = B;
+  prm.k = k;
+  prm.V = V;
+  prm.nchunks = L.nchunks;
+  prm.accepted_len = accepted_len;
+  prm.out_tokens = out_tokens;
+  prm.p_out = p_out;
+  prm.q_out = q_out;
+  prm.resid_mass = resid_mass;
+  prm.flags = reinterpret_cast<unsigned*>(ws);
+  prm.row_cnt = counters;
+  prm.seq_cnt = counters + L.rows;
+  prm.draw_cnt = counters + L.rows + B;
+  prm.part = reinterpret_cast<sv::SoftmaxPartial*>(ws + L.off_part);
+  prm.rows = reinterpret_cast<sv::RowStats*>(ws + L.off_rows);
+  prm.sel = reinterpret_cast<int32_t*>(ws + L.off_sel);
+  prm.csum = reinterpret_cast<double*>(ws + L.off_csum);
+
+  const bool vec = vec_ok(target_logits, V, dtype) && (k == 0 || vec_ok(draft_logits, V, dtype));
+  if (dtype == SPEC_DTYPE_BF16)
+    return vec ? run_sample<sv::BF16, true>(prm, L.rows, stream)
+               : run_sample<sv::BF16, false>(prm, L.rows, stream);
+  return vec ? run_sample<sv::F32, true>(prm, L.rows, stream)
+             : run_sample<sv::F32, false>(prm, L.rows, stream);
+}
+
+static spec_status_t argmax_common(sv::ArgmaxParams& prm, const Layout& L, void* workspace,
+                                   int dtype, void* stream) {
+  char* ws = static_cast<char*>(workspace);
+  unsigned* counters = reinterpret_cast<unsigned*>(ws + kHeaderBytes);
+  prm.flags = reinterpret_cast<unsigned*>(ws);
+  prm.row_cnt = counters;
+  prm.seq_cnt = counters + L.rows;
+  prm.part = reinterpret_cast<sv::ArgPartial*>(ws + L.off_part);
+  prm.rowarg = reinterpret_cast<int32_t*>(ws + L.off_arg);
+  prm.nchunks = L.nchunks;
+  const bool vec = vec_ok(prm.target, prm.V, dtype);
+  if (dtype == SPEC_DTYPE_BF16)
+    return vec ? run_argmax<sv::BF16, true>(prm, L.rows, stream)
+               : run_argmax<sv::BF16, false>(prm, L.rows, stream);
+  return vec ? run_argmax<sv::F32, true>(prm, L.rows, stream)
+             : run_argmax<sv::F32, false>(prm, L.rows, stream);
+}
+
+spec_status_t spec_verify_greedy(const void* target_logits, int dtype,
+                                 const int32_t* draft_tokens, int B, int k, int V,
+                                 int32_t* accepted_len, int32_t* out_tokens, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || k < 0 || k > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(SPEC_MODE_GREEDY, B, k, V, dtype, &L)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !accepted_len || !out_tokens || (k > 0 && !draft_tokens))
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned(target_logits, elem_bytes(dtype)) || !aligned(accepted_len, 4) ||
+      !aligned(out_tokens, 4) || (k > 0 && !aligned(draft_tokens, 4)))
+    return SPEC_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
+  sv::ArgmaxParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  prm.target = target_logits;
+  prm.tokens = draft_tokens;
+  prm.parents = nullptr;
+  prm.B = B;
+  prm.rows_per_seq = k + 1;
+  prm.V = V;
+  prm.tree = 0;
+  prm.max_depth = 0;
+  prm.accepted_len = accepted_len;
+  prm.out_tokens = out_tokens;
+  prm.path_nodes = nullptr;
+  return argmax_common(prm, L, workspace, dtype, stream);
+}
+
+spec_status_t spec_verify_tree_greedy(const void* target_logits, int dtype,
+                                      const int32_t* node_tokens, const int32_t* parents, int B,
+                                      int N, int V, int max_depth, int32_t* accepted_len,
+                                      int32_t* path_nodes, int32_t* out_tokens, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V)
+    return SPEC_ERR_INVALID_ARG;
+  if (max_depth < 0 || max_depth > SPEC_MAX_TREE_DEPTH) return SPEC_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(SPEC_MODE_TREE_GREEDY, B, N, V, dtype, &L)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !node_tokens || !parents || !accepted_len || !path_nodes || !out_tokens)
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned(target_logits, elem_bytes(dtype)) || !aligned(node_tokens, 4) ||
+      !aligned(parents, 4) || !aligned(accepted_len, 4) || !aligned(path_nodes, 4) ||
+      !aligned(out_tokens, 4))
+    return SPEC_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
+  sv::ArgmaxParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  prm.target = target_logits;
+  prm.tokens = node_tokens;
+  prm.parents = parents;
+  prm.B = B;
+  prm.rows_per_seq = N;
+  prm.V = V;
+  prm.tree = 1;
+  prm.max_depth = max_depth;
+  prm.accepted_len = accepted_len;
+  prm.out_tokens = out_tokens;
+  prm.path_nodes = path_nodes;
+  return argmax_common(prm, L, workspace, dtype, stream);
+}
+
+spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_flags, int clear,
+                                     void* stream) {
+  if (!workspace || !host_flags) return SPEC_ERR_INVALID_ARG;
+  if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(host_flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (clear && cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+uint64_t spec_verify_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* spec_status_string(int status) {
+  switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_ALIGNMENT: return "misaligned pointer";
+    case SPEC_ERR_WORKSPACE: return "workspace missing or too small";
+    case SPEC_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int spec_verify_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
+
+}  // extern "C"

@@ -206,8 +206,7 @@ def make_chain_case(*, B, k, V, dtype=DTYPE_F32, temperature=1.0, recipe="gauss"
     """Generic chain case.
 
     Draft tokens are exact samples of softmax(draft/T) (Gumbel-max).  With
-    ``greedy_force=f`` each draft token is replaced, with probability f, by the
-    lowest-index argmax of the same position's target row (greedy workloads).
+    ``greedy_force=f`` the tokens are those of :func:`greedy_variant`.
     """
     rng = np.random.default_rng(seed)
     target, draft = make_chain_logits(rng, B, k, V, dtype, recipe, target_sigma,
@@ -217,19 +216,38 @@ def make_chain_case(*, B, k, V, dtype=DTYPE_F32, temperature=1.0, recipe="gauss"
         zd_f = logits_as_f32(draft, dtype)
         tokens = gumbel_max_tokens(rng, zd_f, temperature).astype(np.int32)
         del zd_f
-        if greedy_force is not None:
-            zt_f = logits_as_f32(target[:, :k, :], dtype)
-            amax = np.argmax(zt_f, axis=-1).astype(np.int32)
-            force = rng.random((B, k)) < greedy_force
-            tokens = np.where(force, amax, tokens).astype(np.int32)
     urng = np.random.default_rng(seed + 1)
     u_accept = uniforms_f32(urng, (B, k))
     u_sample = uniforms_f32(urng, (B,))
-    return ChainInputs(name=name, B=B, k=k, V=V, dtype=dtype,
+    case = ChainInputs(name=name, B=B, k=k, V=V, dtype=dtype,
                        temperature=float(temperature), target=target,
                        draft=draft if with_draft else None, tokens=tokens,
                        u_accept=u_accept, u_sample=u_sample,
                        meta=dict(recipe=recipe, seed=seed))
+    if greedy_force is not None:
+        case = greedy_variant(case, greedy_force)
+        if not with_draft:
+            case.draft = None
+    return case
+
+
+def greedy_variant(case: ChainInputs, force: float) -> ChainInputs:
+    """Same logits; each draft token replaced, with probability ``force``, by
+    the lowest-index argmax of the same position's target row (seed + 2)."""
+    rng = np.random.default_rng(case.meta.get("seed", 0) + 2)
+    k = case.k
+    tokens = case.tokens.copy()
+    if k > 0:
+        zt_f = logits_as_f32(case.target[:, :k, :], case.dtype)
+        amax = np.argmax(zt_f, axis=-1).astype(np.int32)
+        del zt_f
+        forced = rng.random((case.B, k)) < force
+        tokens = np.where(forced, amax, tokens).astype(np.int32)
+    meta = dict(case.meta, greedy_force=force)
+    return ChainInputs(name=case.name + " greedy", B=case.B, k=k, V=case.V, dtype=case.dtype,
+                       temperature=case.temperature, target=case.target, draft=case.draft,
+                       tokens=tokens, u_accept=case.u_accept, u_sample=case.u_sample,
+                       meta=meta)
 
 
 def make_tree_parents(rng, N, max_depth=6, max_children=4):

@@ -1,0 +1,78 @@
+"""Comparison rules between the CUDA path and the float64 oracle.
+
+Tolerances (the method's outputs are decisions plus a few probabilities):
+
+* accepted lengths and emitted tokens: bit-exact for greedy and tree modes;
+  bit-exact for sampling except on rows the oracle flags (a uniform within
+  1e-6 of an acceptance threshold p/q, or u*R within 1e-6*R of the CDF value
+  at the chosen token or the one before it).  Flagged rows must be at most
+  1e-4 of the rows compared (or none when fewer than 10^4 rows are compared).
+* p(x_i), q(x_i): within 1e-5 relative of the oracle's float64 value (plus
+  1e-37 absolute, below which float32 outputs lose relative precision).
+* residual mass R: within 1e-5 relative or 1e-7 absolute, whichever is
+  looser (fp32 p - q cancellation bounds R's absolute error near 1e-7).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+FLAG_WINDOW = 1e-6
+PQ_RTOL = 1e-5
+PQ_ATOL = 1e-37
+R_RTOL = 1e-5
+R_ATOL = 1e-7
+MAX_FLAG_FRACTION = 1e-4
+
+
+def flagged_rows(orc: dict) -> np.ndarray:
+    return (orc["acc_margin"] < FLAG_WINDOW) | (orc["cdf_margin"] < FLAG_WINDOW)
+
+
+def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None):
+    """Assert sampling parity.  ``gpu`` holds numpy copies of the CUDA outputs
+    (accepted_len, out_tokens, p, q, resid_mass); ``orc`` the oracle's result
+    for the same rows.  ``rows`` selects which GPU rows ``orc`` covers.
+    Returns a summary dict."""
+    sel = slice(None) if rows is None else rows
+    g_n = np.asarray(gpu["accepted_len"])[sel]
+    g_tok = np.asarray(gpu["out_tokens"])[sel]
+    g_p = np.asarray(gpu["p"], dtype=np.float64)[sel]
+    g_q = np.asarray(gpu["q"], dtype=np.float64)[sel]
+    g_R = np.asarray(gpu["resid_mass"], dtype=np.float64)[sel]
+    n_rows = g_n.shape[0]
+    flags = flagged_rows(orc)
+    nflag = int(flags.sum())
+    if allow_flags is None:
+        allow_flags = int(MAX_FLAG_FRACTION * n_rows)
+    assert nflag <= allow_flags, f"{nflag} flagged rows of {n_rows}"
+    ok = ~flags
+    bad_n = np.nonzero(ok & (g_n != orc["accepted_len"]))[0]
+    assert bad_n.size == 0, f"accepted_len differs on unflagged rows {bad_n[:10]}: " \
+        f"gpu {g_n[bad_n[:10]]} oracle {orc['accepted_len'][bad_n[:10]]}"
+    bad_t = np.nonzero(ok & (g_tok != orc["out_tokens"]).any(axis=1))[0]
+    assert bad_t.size == 0, f"out_tokens differ on unflagged rows {bad_t[:10]}: " \
+        f"gpu {g_tok[bad_t[:3]]} oracle {orc['out_tokens'][bad_t[:3]]}"
+    for name, gv, ov in (("p", g_p, orc["p"]), ("q", g_q, orc["q"])):
+        err = np.abs(gv - ov)
+        lim = PQ_RTOL * np.abs(ov) + PQ_ATOL
+        worst = np.unravel_index(np.argmax(err - lim), err.shape) if err.size else None
+        assert (err <= lim).all(), f"{name} out of tolerance at {worst}: gpu {gv[worst]} " \
+            f"oracle {ov[worst]}"
+    errR = np.abs(g_R - orc["resid_mass"])
+    limR = np.maximum(R_RTOL * np.abs(orc["resid_mass"]), R_ATOL)
+    badR = np.nonzero(ok & (errR > limR))[0]
+    assert badR.size == 0, f"resid_mass out of tolerance rows {badR[:10]}: " \
+        f"gpu {g_R[badR[:5]]} oracle {orc['resid_mass'][badR[:5]]}"
+    relp = np.abs(g_p - orc["p"]) / np.maximum(np.abs(orc["p"]), 1e-300)
+    return dict(rows=n_rows, flagged=nflag, max_rel_p=float(relp.max()) if relp.size else 0.0,
+                mean_accepted=float(g_n.mean()) if n_rows else 0.0)
+
+
+def compare_exact(gpu: dict, orc: dict, keys, rows=None):
+    sel = slice(None) if rows is None else rows
+    for k in keys:
+        g = np.asarray(gpu[k])[sel]
+        o = np.asarray(orc[k])
+        bad = np.nonzero((g != o).reshape(g.shape[0], -1).any(axis=1))[0]
+        assert bad.size == 0, f"{k} differs at rows {bad[:10]}: gpu {g[bad[:3]]} " \
+            f"oracle {o[bad[:3]]}"

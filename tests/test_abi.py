@@ -1,0 +1,139 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every symbol the
+header declares, and rejects bad host arguments before touching the GPU.
+
+No test here launches a kernel: every call below fails host validation (or is
+the B = 0 no-op), which the library performs before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_56_gb300 as sv
+from speculative_decoding_verification_56_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+FAKE = 0x10000          # 64 KiB-aligned fake device address, never dereferenced
+MISALIGNED = FAKE + 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return sv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"SPEC_API\s+[\w\s\*]+?\b(spec_\w+)\s*\(", text)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("spec_verify_sample", "spec_verify_greedy", "spec_verify_tree_greedy",
+              "spec_verify_workspace_bytes", "spec_verify_read_flags",
+              "spec_verify_launch_count", "spec_status_string", "spec_verify_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(sv.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(raw, n), n
+
+
+def test_abi_version_and_status_strings(lib):
+    assert sv.spec_verify_abi_version() == 1
+    assert sv.spec_status_string(0) == "ok"
+    assert "workspace" in sv.spec_status_string(3)
+    assert sv.spec_verify_launch_count() >= 0
+
+
+def test_workspace_bytes(lib):
+    ws = sv.spec_verify_workspace_bytes
+    a = ws(sv.SPEC_MODE_SAMPLE, 64, 4, 128256, sv.SPEC_DTYPE_BF16)
+    b = ws(sv.SPEC_MODE_SAMPLE, 128, 4, 128256, sv.SPEC_DTYPE_BF16)
+    assert 0 < a < b and a % 256 == 0
+    assert ws(sv.SPEC_MODE_GREEDY, 64, 4, 128256, sv.SPEC_DTYPE_BF16) > 0
+    assert ws(sv.SPEC_MODE_TREE_GREEDY, 16, 60, 128256, sv.SPEC_DTYPE_BF16) > 0
+    assert ws(sv.SPEC_MODE_SAMPLE, 1, 4, 0, sv.SPEC_DTYPE_F32) == 0            # V < 1
+    assert ws(sv.SPEC_MODE_SAMPLE, 1, 4, 10, 7) == 0                            # dtype
+    assert ws(sv.SPEC_MODE_TREE_GREEDY, 1, 0, 10, 0) == 0                       # N < 1
+    assert ws(sv.SPEC_MODE_SAMPLE, 200000, 4, 10, 0) == 0                       # counters
+    assert ws(9, 1, 1, 10, 0) == 0
+
+
+def _sample(lib, **over):
+    a = dict(target=FAKE, draft=FAKE, dtype=0, tokens=FAKE, ua=FAKE, us=FAKE, T=1.0, B=2, k=3,
+             V=64, acc=FAKE, out=FAKE, p=FAKE, q=FAKE, R=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(over)
+    return lib.spec_verify_sample(a["target"], a["draft"], a["dtype"], a["tokens"], a["ua"],
+                                  a["us"], a["T"], a["B"], a["k"], a["V"], a["acc"], a["out"],
+                                  a["p"], a["q"], a["R"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(T=0.0), 1), (dict(T=-1.0), 1), (dict(T=float("nan")), 1), (dict(T=float("inf")), 1),
+    (dict(k=-1), 1), (dict(V=0), 1), (dict(dtype=5), 1), (dict(B=-1), 1),
+    (dict(k=2000), 1),
+    (dict(target=None), 1), (dict(draft=None), 1), (dict(tokens=None), 1), (dict(us=None), 1),
+    (dict(acc=None), 1), (dict(p=None), 1), (dict(R=None), 1),
+    (dict(target=MISALIGNED), 2), (dict(out=MISALIGNED), 2), (dict(dtype=1, draft=FAKE + 1), 2),
+    (dict(ws=None), 3), (dict(wsb=1024), 3), (dict(ws=FAKE + 16), 2),
+    (dict(B=0), 0),
+])
+def test_sample_host_validation(lib, over, status):
+    assert _sample(lib, **over) == status
+
+
+def test_sample_k0_allows_null_draft_arguments(lib):
+    # passes the NULL checks and then fails on the workspace size, before CUDA
+    assert _sample(lib, k=0, draft=None, tokens=None, ua=None, p=None, q=None, wsb=16) == 3
+
+
+def test_greedy_and_tree_host_validation(lib):
+    g = lib.spec_verify_greedy
+    assert g(None, 1, FAKE, 4, 3, 100, FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert g(FAKE, 1, None, 4, 3, 100, FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert g(FAKE, 1, FAKE, 4, 3, 100, FAKE, FAKE, FAKE, 10, None) == 3
+    assert g(FAKE + 1, 1, FAKE, 4, 3, 100, FAKE, FAKE, FAKE, 1 << 30, None) == 2
+    assert g(FAKE, 1, FAKE, 0, 3, 100, FAKE, FAKE, FAKE, 0, None) == 0
+    t = lib.spec_verify_tree_greedy
+    args = [FAKE, 1, FAKE, FAKE, 4, 60, 1000, 6, FAKE, FAKE, FAKE, FAKE, 10, None]
+    assert t(*args) == 3
+    bad = list(args); bad[5] = 0
+    assert t(*bad) == 1
+    bad = list(args); bad[7] = -1
+    assert t(*bad) == 1
+    bad = list(args); bad[7] = 5000
+    assert t(*bad) == 1
+    bad = list(args); bad[3] = None
+    assert t(*bad) == 1
+    bad = list(args); bad[3] = FAKE + 2
+    assert t(*bad) == 2
+
+
+def test_read_flags_validation(lib):
+    v = ctypes.c_uint32(0)
+    assert lib.spec_verify_read_flags(None, ctypes.byref(v), 0, None) == 1
+    assert lib.spec_verify_read_flags(FAKE + 8, ctypes.byref(v), 0, None) == 2
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(sv, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        sv.load_library(str(tmp_path / "nope.so"))
+
+
+def test_product_path_never_touches_the_oracle():
+    pkg = os.path.dirname(sv.__file__)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", text, re.M), f
+                assert "spec_oracle" not in text, f
+                assert "libspecoracle" not in text, f
