@@ -6,7 +6,13 @@ Tolerances (the method's outputs are decisions plus a few probabilities):
   bit-exact for sampling except on rows the oracle flags (a uniform within
   1e-6 of an acceptance threshold p/q, or u*R within 1e-6*R of the CDF value
   at the chosen token or the one before it).  Flagged rows must be at most
-  1e-4 of the rows compared (or none when fewer than 10^4 rows are compared).
+  1e-4 of the rows compared when the vocabulary is small.  With V >= 16384 the
+  CDF of a residual or bonus row has thousands of boundaries closer together
+  than the window: a row is flagged with probability close to
+  sum_j min(r_j / R, 2e-6), about 1.3% per row on the V=128256 Zipf workload
+  (5 of 384 rows over seeds 0-5, counted by the oracle alone).  No
+  implementation can meet 1e-4 there, so large-V comparisons allow 5% of rows
+  (at least one) and report the count.
 * p(x_i), q(x_i): within 1e-5 relative of the oracle's float64 value (plus
   1e-37 absolute, below which float32 outputs lose relative precision).
 * residual mass R: within 1e-5 relative or 1e-7 absolute, whichever is
@@ -22,13 +28,21 @@ PQ_ATOL = 1e-37
 R_RTOL = 1e-5
 R_ATOL = 1e-7
 MAX_FLAG_FRACTION = 1e-4
+LARGE_V = 16384
+LARGE_V_FLAG_FRACTION = 0.05
+
+
+def flag_allowance(n_rows: int, V: int) -> int:
+    if V >= LARGE_V:
+        return max(1, int(np.ceil(LARGE_V_FLAG_FRACTION * n_rows)))
+    return int(MAX_FLAG_FRACTION * n_rows)
 
 
 def flagged_rows(orc: dict) -> np.ndarray:
     return (orc["acc_margin"] < FLAG_WINDOW) | (orc["cdf_margin"] < FLAG_WINDOW)
 
 
-def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None):
+def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None, V=None):
     """Assert sampling parity.  ``gpu`` holds numpy copies of the CUDA outputs
     (accepted_len, out_tokens, p, q, resid_mass); ``orc`` the oracle's result
     for the same rows.  ``rows`` selects which GPU rows ``orc`` covers.
@@ -43,7 +57,7 @@ def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None):
     flags = flagged_rows(orc)
     nflag = int(flags.sum())
     if allow_flags is None:
-        allow_flags = int(MAX_FLAG_FRACTION * n_rows)
+        allow_flags = flag_allowance(n_rows, V if V is not None else 0)
     assert nflag <= allow_flags, f"{nflag} flagged rows of {n_rows}"
     ok = ~flags
     bad_n = np.nonzero(ok & (g_n != orc["accepted_len"]))[0]
@@ -64,7 +78,10 @@ def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None):
     assert badR.size == 0, f"resid_mass out of tolerance rows {badR[:10]}: " \
         f"gpu {g_R[badR[:5]]} oracle {orc['resid_mass'][badR[:5]]}"
     relp = np.abs(g_p - orc["p"]) / np.maximum(np.abs(orc["p"]), 1e-300)
-    return dict(rows=n_rows, flagged=nflag, max_rel_p=float(relp.max()) if relp.size else 0.0,
+    flag_mismatch = int((flags & ((g_n != orc["accepted_len"]) |
+                                  (g_tok != orc["out_tokens"]).any(axis=1))).sum())
+    return dict(rows=n_rows, flagged=nflag, flagged_mismatch=flag_mismatch,
+                max_rel_p=float(relp.max()) if relp.size else 0.0,
                 mean_accepted=float(g_n.mean()) if n_rows else 0.0)
 
 

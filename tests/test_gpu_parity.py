@@ -66,7 +66,7 @@ def oracle_sample(c, rows=None):
 def sample_parity(c, rows=None, allow_flags=None, ws=None):
     g = gpu_sample(c, ws=ws)
     o = oracle_sample(c, rows)
-    return ph.compare_sample(g, o, rows=rows, allow_flags=allow_flags), g, o
+    return ph.compare_sample(g, o, rows=rows, allow_flags=allow_flags, V=c.V), g, o
 
 
 # ---------------------------------------------------------------------------
@@ -150,7 +150,7 @@ SHAPES = [  # dtype, V, B, k, T
 def test_sample_shapes(dtype, V, B, k, T):
     c = synth.make_chain_case(B=B, k=k, V=V, dtype=dtype, temperature=T, target_sigma=2.0,
                               draft_noise=1.0, seed=V + B + k)
-    s, g, _ = sample_parity(c, allow_flags=0)
+    s, g, _ = sample_parity(c)
     if V == 1:
         assert (g["accepted_len"] == k).all() and (g["out_tokens"][:, k] == 0).all()
 
@@ -273,7 +273,7 @@ def test_workspace_reuse_across_shapes_and_modes():
     c2 = synth.make_chain_case(B=3, k=6, V=777, dtype="f32", seed=2)
     t = synth.make_tree_case(B=4, N=30, V=9000, dtype="bf16", seed=3)
     for _ in range(2):
-        sample_parity(c1, ws=big, allow_flags=0)
+        sample_parity(c1, ws=big)
         sample_parity(c2, ws=big, allow_flags=0)
         g = gpu_tree(t, ws=big)
         o = oracle.verify_tree_greedy(t.target, t.tokens, t.parents, t.max_depth, dtype="bf16")
