@@ -22,11 +22,13 @@
  *   - Logits must be finite with |logit / T| < 2^23; other values give
  *     unspecified (but memory-safe) outputs.
  *   - `workspace`: device scratch of at least spec_verify_workspace_bytes()
- *     bytes, 256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE (e.g.
- *     cudaMemsetAsync).  Every call returns the workspace's synchronisation
- *     counters to zero, so one workspace serves any later call of any shape.
- *     Two calls that share a workspace must not run concurrently (issue them
- *     on one stream, or order them with events).
+ *     bytes, 256-byte aligned.  Its contents on entry do not matter: every
+ *     record a kernel reads is written earlier in the same call, so one
+ *     workspace serves calls of any shape.  Its first 4 bytes hold the sticky
+ *     flag word (see spec_verify_read_flags): zero the workspace once, or
+ *     read the flags with clear != 0, before relying on them.  Two calls that
+ *     share a workspace must not run concurrently (issue them on one stream,
+ *     or order them with events).
  *   - Errors found on the host (NULL pointer, bad size, bad temperature,
  *     misalignment, workspace too small) return before anything is enqueued.
  *     A failed kernel launch returns SPEC_ERR_CUDA.  Bad DEVICE data (a token
@@ -75,19 +77,20 @@ typedef enum {
 #define SPEC_FLAG_DEPTH 4u             /* a node deeper than max_depth */
 #define SPEC_FLAG_RESIDUAL_FALLBACK 8u /* residual mass was 0 after a rejection;
                                           that position was sampled from p */
+#define SPEC_FLAG_TIMEOUT 16u          /* a kernel gave up waiting for its own
+                                          bulk copies (outputs of that call are
+                                          unspecified); never expected */
 
 /* Limits checked on the host. */
 #define SPEC_MAX_V (1 << 26)
-#define SPEC_MAX_K 1024
+#define SPEC_MAX_K 256
 #define SPEC_MAX_TREE_NODES 65536
 #define SPEC_MAX_TREE_DEPTH 1024
-/* Rows of one call plus 2*B must not exceed this (synchronisation counters). */
-#define SPEC_MAX_COUNTERS 262144
 
 /*
  * Bytes of workspace needed by one call.  mode: spec_mode_t; k_or_N: k draft
  * tokens (chain modes) or N tree nodes (tree mode).  Returns 0 for arguments
- * outside the limits above.
+ * outside the limits above or whose scratch index space exceeds 2^31 records.
  */
 SPEC_API size_t spec_verify_workspace_bytes(int mode, int B, int k_or_N, int V, int dtype);
 
@@ -117,7 +120,8 @@ SPEC_API size_t spec_verify_workspace_bytes(int mode, int B, int k_or_N, int V, 
  *   resid_mass    float [B]       R = sum_j max(0, p_n - q_n) when n < k, else 0
  * With k = 0, draft_logits, draft_tokens, u_accept, p_out and q_out may be
  * NULL and the call samples one token from softmax(target[b,0,:] / T).
- * Launches two kernels (softmax statistics + accept test; residual/bonus draw).
+ * Launches three kernels: softmax statistics; row merge + accept test +
+ * residual/bonus prefix sums; the inverse-CDF walk.
  */
 SPEC_API spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
                                  int dtype, const int32_t* draft_tokens,
@@ -134,7 +138,7 @@ SPEC_API spec_status_t spec_verify_sample(const void* target_logits, const void*
  * k; emits x_0..x_{n-1}, g_n.  Temperature plays no part.
  *   target_logits [B, k+1, V]; draft_tokens int32 [B, k] (NULL allowed if k = 0)
  *   accepted_len  int32 [B];   out_tokens int32 [B, k+1] (unused slots -1)
- * One kernel launch.
+ * Launches two kernels (argmax partials; row merge + accept).
  */
 SPEC_API spec_status_t spec_verify_greedy(const void* target_logits, int dtype,
                                  const int32_t* draft_tokens, int B, int k, int V,
@@ -159,7 +163,7 @@ SPEC_API spec_status_t spec_verify_greedy(const void* target_logits, int dtype,
  *   path_nodes    int32 [B, max_depth+1]   0, ..., v*, then -1
  *   out_tokens    int32 [B, max_depth+1]   tokens of path nodes 1..depth, the
  *                                          bonus token, then -1
- * One kernel launch.
+ * Launches two kernels (argmax partials; row merge + tree walk).
  */
 SPEC_API spec_status_t spec_verify_tree_greedy(const void* target_logits, int dtype,
                                       const int32_t* node_tokens, const int32_t* parents,

@@ -39,6 +39,7 @@ SPEC_FLAG_TOKEN_RANGE = 1
 SPEC_FLAG_BAD_PARENT = 2
 SPEC_FLAG_DEPTH = 4
 SPEC_FLAG_RESIDUAL_FALLBACK = 8
+SPEC_FLAG_TIMEOUT = 16
 
 _lock = threading.Lock()
 _lib = None
@@ -160,7 +161,7 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, u_accept, u_sa
     draft_tokens int32 [B, k]; u_accept float32 [B, k]; u_sample float32 [B].
     Outputs (preallocated CUDA tensors): accepted_len int32 [B], out_tokens
     int32 [B, k+1], p_out/q_out float32 [B, k], resid_mass float32 [B].
-    workspace: uint8 CUDA tensor, zero-filled before first use.
+    workspace: uint8 CUDA tensor of at least spec_verify_workspace_bytes() bytes.
     """
     torch = _torch()
     B, k1, V = target_logits.shape

@@ -2,15 +2,16 @@
 // host-side argument checks, workspace layout and kernel launches.
 //
 // Workspace layout (all offsets 256-byte aligned):
-//   [0, 256)                 header; word 0 = sticky device flag bits
-//   [256, 256 + 4*MAXC)      synchronisation counters, zero between calls
-//   [256 + 4*MAXC, ...)      per-call scratch records (any content on entry)
-// Counters live at fixed offsets, so a workspace zero-filled once stays valid
-// for calls of any shape: each call's last-arriving CTAs reset what they used.
+//   [0, 256)     header; word 0 = sticky device flag bits
+//   [256, ...)   per-call scratch records; every record a kernel reads was
+//                written earlier in the same call, so the contents on entry
+//                do not matter and calls of any shape can share a workspace.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -23,8 +24,7 @@ std::atomic<uint64_t> g_launches{0};
 
 constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 256;
-constexpr size_t kCounterBytes = (size_t)SPEC_MAX_COUNTERS * sizeof(unsigned);
-constexpr size_t kDataOffset = kHeaderBytes + kCounterBytes;
+constexpr size_t kDataOffset = kHeaderBytes;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -36,7 +36,8 @@ int chunk_elems(int dtype) {
 struct Layout {
   size_t bytes = 0;
   int rows = 0, nchunks = 0;
-  size_t off_part = 0, off_rows = 0, off_sel = 0, off_csum = 0;  // sample
+  size_t off_part = 0, off_desc = 0, off_csum = 0, off_csum_p = 0;  // sample
+  size_t off_gsum = 0, off_gsum_p = 0;
   size_t off_arg = 0;                                            // greedy / tree
 };
 
@@ -58,23 +59,27 @@ bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
   } else {
     return false;
   }
-  if (rows + 2LL * B > SPEC_MAX_COUNTERS) return false;
-  if (rows * C > 0x7FFFFFFFLL) return false;
+  if (rows * C * sv::kWarps > 0x7FFFFFFFLL) return false;
   L->rows = (int)rows;
   L->nchunks = C;
   size_t off = kDataOffset;
   if (mode == SPEC_MODE_SAMPLE) {
     L->off_part = off;
-    off = align_up(off + (size_t)rows * C * sizeof(sv::SoftmaxPartial));
-    L->off_rows = off;
-    off = align_up(off + (size_t)rows * sizeof(sv::RowStats));
-    L->off_sel = off;
-    off = align_up(off + (size_t)B * sizeof(int32_t));
+    off = align_up(off + (size_t)rows * C * sv::kWarps * sizeof(sv::SoftmaxPartial));
+    L->off_desc = off;
+    off = align_up(off + (size_t)B * sizeof(sv::DrawDesc));
+    const size_t bc = (size_t)B * C;
     L->off_csum = off;
-    off = align_up(off + (size_t)B * C * sizeof(double));
+    off = align_up(off + bc * sizeof(sv::FSum));
+    L->off_csum_p = off;
+    off = align_up(off + bc * sizeof(sv::FSum));
+    L->off_gsum = off;
+    off = align_up(off + bc * sv::kVecPerChunk * sizeof(float));
+    L->off_gsum_p = off;
+    off = align_up(off + bc * sv::kVecPerChunk * sizeof(float));
   } else {
     L->off_part = off;
-    off = align_up(off + (size_t)rows * C * sizeof(sv::ArgPartial));
+    off = align_up(off + (size_t)rows * C * sv::kWarps * sizeof(sv::ArgPartial));
     L->off_arg = off;
     off = align_up(off + (size_t)rows * sizeof(int32_t));
   }
@@ -90,12 +95,13 @@ bool vec_ok(const void* p, int V, int dtype) {
 }
 
 template <typename KernelT, typename ParamT>
-spec_status_t launch(KernelT kernel, int grid, const ParamT& prm, void* stream, bool pdl) {
+spec_status_t launch(KernelT kernel, int grid, size_t smem, const ParamT& prm, void* stream,
+                     bool pdl) {
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(sv::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
   if (pdl) {
@@ -110,17 +116,73 @@ spec_status_t launch(KernelT kernel, int grid, const ParamT& prm, void* stream, 
   return SPEC_OK;
 }
 
-template <typename E, bool kVec>
-spec_status_t run_sample(const sv::SampleParams& prm, int rows, void* stream) {
-  spec_status_t st =
-      launch(sv::sample_stats_kernel<E, kVec>, rows * prm.nchunks, prm, stream, false);
-  if (st != SPEC_OK) return st;
-  return launch(sv::sample_draw_kernel<E, kVec>, prm.B * prm.nchunks, prm, stream, true);
+// Per-device launch shape of a persistent streaming kernel: the shared-memory
+// opt-in is set once per device, the grid is SMs x resident CTAs per SM.
+constexpr int kMaxDevices = 64;
+constexpr size_t kStreamSmem = (size_t)sv::kStages * sv::kChunkBytes;
+std::mutex g_shape_mu;
+
+template <auto kernel>
+spec_status_t persistent_grid(int items, int* grid) {
+  static int cached[kMaxDevices] = {0};  // one table per kernel instantiation
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_shape_mu);
+  if (cached[dev] == 0) {
+    int sms = 0, per_sm = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStreamSmem) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, sv::kThreads,
+                                                      kStreamSmem) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    cached[dev] = std::max(1, sms * std::max(1, per_sm));
+  }
+  *grid = std::min(items, cached[dev]);
+  return SPEC_OK;
 }
 
-template <typename E, bool kVec>
-spec_status_t run_argmax(const sv::ArgmaxParams& prm, int rows, void* stream) {
-  return launch(sv::argmax_verify_kernel<E, kVec>, rows * prm.nchunks, prm, stream, false);
+template <typename E>
+spec_status_t run_sample(sv::SampleParams prm, int rows, bool vec, void* stream) {
+  prm.items = rows * prm.nchunks;
+  spec_status_t st;
+  if (vec) {
+    int grid = 0;
+    st = persistent_grid<sv::stream_stats_kernel<E>>(prm.items, &grid);
+    if (st != SPEC_OK) return st;
+    st = launch(sv::stream_stats_kernel<E>, grid, kStreamSmem, prm, stream, false);
+  } else {
+    st = launch(sv::chunk_stats_kernel<E, false>, prm.items, 0, prm, stream, false);
+  }
+  if (st != SPEC_OK) return st;
+  const int resolve_grid = (prm.B + sv::kWarps - 1) / sv::kWarps;
+  if (vec) {
+    st = launch(sv::draw_kernel<E, true>, prm.B * prm.nchunks, 0, prm, stream, true);
+    if (st != SPEC_OK) return st;
+    return launch(sv::draw_resolve_kernel<E, true>, resolve_grid, 0, prm, stream, true);
+  }
+  st = launch(sv::draw_kernel<E, false>, prm.B * prm.nchunks, 0, prm, stream, true);
+  if (st != SPEC_OK) return st;
+  return launch(sv::draw_resolve_kernel<E, false>, resolve_grid, 0, prm, stream, true);
+}
+
+template <typename E>
+spec_status_t run_argmax(sv::ArgmaxParams prm, int rows, bool vec, void* stream) {
+  prm.items = rows * prm.nchunks;
+  if (vec) {
+    int grid = 0;
+    spec_status_t st = persistent_grid<sv::stream_argmax_kernel<E>>(prm.items, &grid);
+    if (st != SPEC_OK) return st;
+    st = launch(sv::stream_argmax_kernel<E>, grid, kStreamSmem, prm, stream, false);
+    if (st != SPEC_OK) return st;
+  } else {
+    const spec_status_t st =
+        launch(sv::chunk_argmax_kernel<E, false>, prm.items, 0, prm, stream, false);
+    if (st != SPEC_OK) return st;
+  }
+  return launch(sv::argmax_resolve_kernel, prm.B, 0, prm, stream, true);
 }
 
 }  // namespace
@@ -161,7 +223,6 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
 
   char* ws = static_cast<char*>(workspace);
-  unsigned* counters = reinterpret_cast<unsigned*>(ws + kHeaderBytes);
   sv::SampleParams prm;
   prm.target = target_logits;
   prm.draft = draft_logits;
@@ -179,38 +240,28 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   prm.q_out = q_out;
   prm.resid_mass = resid_mass;
   prm.flags = reinterpret_cast<unsigned*>(ws);
-  prm.row_cnt = counters;
-  prm.seq_cnt = counters + L.rows;
-  prm.draw_cnt = counters + L.rows + B;
   prm.part = reinterpret_cast<sv::SoftmaxPartial*>(ws + L.off_part);
-  prm.rows = reinterpret_cast<sv::RowStats*>(ws + L.off_rows);
-  prm.sel = reinterpret_cast<int32_t*>(ws + L.off_sel);
-  prm.csum = reinterpret_cast<double*>(ws + L.off_csum);
+  prm.desc = reinterpret_cast<sv::DrawDesc*>(ws + L.off_desc);
+  prm.csum = reinterpret_cast<sv::FSum*>(ws + L.off_csum);
+  prm.csum_p = reinterpret_cast<sv::FSum*>(ws + L.off_csum_p);
+  prm.gsum = reinterpret_cast<float*>(ws + L.off_gsum);
+  prm.gsum_p = reinterpret_cast<float*>(ws + L.off_gsum_p);
 
   const bool vec = vec_ok(target_logits, V, dtype) && (k == 0 || vec_ok(draft_logits, V, dtype));
-  if (dtype == SPEC_DTYPE_BF16)
-    return vec ? run_sample<sv::BF16, true>(prm, L.rows, stream)
-               : run_sample<sv::BF16, false>(prm, L.rows, stream);
-  return vec ? run_sample<sv::F32, true>(prm, L.rows, stream)
-             : run_sample<sv::F32, false>(prm, L.rows, stream);
+  if (dtype == SPEC_DTYPE_BF16) return run_sample<sv::BF16>(prm, L.rows, vec, stream);
+  return run_sample<sv::F32>(prm, L.rows, vec, stream);
 }
 
 static spec_status_t argmax_common(sv::ArgmaxParams& prm, const Layout& L, void* workspace,
                                    int dtype, void* stream) {
   char* ws = static_cast<char*>(workspace);
-  unsigned* counters = reinterpret_cast<unsigned*>(ws + kHeaderBytes);
   prm.flags = reinterpret_cast<unsigned*>(ws);
-  prm.row_cnt = counters;
-  prm.seq_cnt = counters + L.rows;
   prm.part = reinterpret_cast<sv::ArgPartial*>(ws + L.off_part);
   prm.rowarg = reinterpret_cast<int32_t*>(ws + L.off_arg);
   prm.nchunks = L.nchunks;
   const bool vec = vec_ok(prm.target, prm.V, dtype);
-  if (dtype == SPEC_DTYPE_BF16)
-    return vec ? run_argmax<sv::BF16, true>(prm, L.rows, stream)
-               : run_argmax<sv::BF16, false>(prm, L.rows, stream);
-  return vec ? run_argmax<sv::F32, true>(prm, L.rows, stream)
-             : run_argmax<sv::F32, false>(prm, L.rows, stream);
+  if (dtype == SPEC_DTYPE_BF16) return run_argmax<sv::BF16>(prm, L.rows, vec, stream);
+  return run_argmax<sv::F32>(prm, L.rows, vec, stream);
 }
 
 spec_status_t spec_verify_greedy(const void* target_logits, int dtype,

@@ -1,11 +1,11 @@
 // sv_device.cuh -- device helpers shared by the verification kernels.
 //
-// Layout model: every logits row is cut into chunks of kChunk elements (16 KB
-// of logits).  One CTA of kThreads threads handles one (row, chunk) item: each
-// thread owns kVecPerThread 16-byte vectors, vector index vi = q * kThreads +
-// tid, so a warp's loads are 512 contiguous bytes.  Cross-CTA hand-off uses the
-// "last CTA to arrive finishes the row" pattern with an atomic counter, never a
-// wait, so no kernel here spins on another CTA.
+// Layout model: every logits row is cut into chunks of kChunk elements (32 KB
+// of logits).  A chunk is 2048 16-byte vectors; in a CTA of kThreads threads,
+// thread t owns vectors vi = q * kThreads + t (q < kVecPerThread), so each
+// warp touches 512 contiguous bytes per q.  Cross-CTA hand-off uses the "last
+// CTA to arrive finishes the row" pattern with an atomic counter: no kernel
+// waits on another CTA.  The only waits are on this CTA's own bulk copies.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -13,42 +13,47 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVecPerThread = 4;
-constexpr int kGroupsPerChunk = kThreads * kVecPerThread;  // 1024 vectors = groups
-constexpr int kRefEmpty = -(1 << 30);                      // reference of an empty slice
+constexpr int kVecPerChunk = kThreads * kVecPerThread;  // 2048 vectors = 32 KB
+constexpr int kChunkBytes = kVecPerChunk * 16;
+constexpr int kStages = 3;                              // bulk-copy ring depth per CTA
+constexpr int kRefEmpty = -(1 << 30);                   // reference of an empty slice
+constexpr uint64_t kWaitLimitNs = 200000000ull;         // 0.2 s per bulk-copy wait
 
-// Element storage traits: 16-byte vectors hold kEPV elements.
+// Flag bits (mirrors include/spec_verify.h).
+constexpr unsigned kFlagTokenRange = 1u;
+constexpr unsigned kFlagBadParent = 2u;
+constexpr unsigned kFlagDepth = 4u;
+constexpr unsigned kFlagResidualFallback = 8u;
+constexpr unsigned kFlagTimeout = 16u;
+
+// Element storage traits: 16-byte vectors hold kEPV elements; kNegInf is a
+// vector of -inf used to pad past the end of a row.
 struct F32 {
   using storage = float;
   static constexpr int kEPV = 4;
-  static constexpr int kChunk = kThreads * kVecPerThread * kEPV;  // 4096
+  static constexpr int kChunk = kVecPerChunk * kEPV;  // 8192
+  static constexpr uint32_t kNegInfWord = 0xFF800000u;
   static __device__ __forceinline__ float load1(const storage* p) { return __ldg(p); }
-  static __device__ __forceinline__ void unpack(const uint4& v, float (&z)[kEPV]) {
-    z[0] = __uint_as_float(v.x);
-    z[1] = __uint_as_float(v.y);
-    z[2] = __uint_as_float(v.z);
-    z[3] = __uint_as_float(v.w);
+  static __device__ __forceinline__ float elem(const uint4& v, int e) {
+    const uint32_t w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+    return __uint_as_float(w);
   }
 };
 
 struct BF16 {
   using storage = uint16_t;
   static constexpr int kEPV = 8;
-  static constexpr int kChunk = kThreads * kVecPerThread * kEPV;  // 8192
+  static constexpr int kChunk = kVecPerChunk * kEPV;  // 16384
+  static constexpr uint32_t kNegInfWord = 0xFF80FF80u;
   static __device__ __forceinline__ float load1(const storage* p) {
     return __uint_as_float(((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
   }
-  static __device__ __forceinline__ void unpack(const uint4& v, float (&z)[kEPV]) {
-    z[0] = __uint_as_float(v.x << 16);
-    z[1] = __uint_as_float(v.x & 0xFFFF0000u);
-    z[2] = __uint_as_float(v.y << 16);
-    z[3] = __uint_as_float(v.y & 0xFFFF0000u);
-    z[4] = __uint_as_float(v.z << 16);
-    z[5] = __uint_as_float(v.z & 0xFFFF0000u);
-    z[6] = __uint_as_float(v.w << 16);
-    z[7] = __uint_as_float(v.w & 0xFFFF0000u);
+  static __device__ __forceinline__ float elem(const uint4& v, int e) {
+    const uint32_t w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
   }
 };
 
@@ -61,43 +66,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
-// One chunk of one row, held in registers: z[q][e] is element
-// j0 + (q * kThreads + tid) * kEPV + e; slots past the row end hold -inf.
-template <typename E, bool kVec>
-__device__ __forceinline__ void load_chunk(const typename E::storage* __restrict__ row, int j0,
-                                           int j1, float (&z)[kVecPerThread][E::kEPV]) {
-  const int tid = threadIdx.x;
-  if constexpr (kVec) {
-    const int nvec = (j1 - j0) / E::kEPV;  // rows are whole vectors on this path
-    uint4 raw[kVecPerThread];
-#pragma unroll
-    for (int q = 0; q < kVecPerThread; ++q) {
-      const int vi = q * kThreads + tid;
-      if (vi < nvec)
-        raw[q] = ldg_stream(row + j0 + vi * E::kEPV);
-      else
-        raw[q] = make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int q = 0; q < kVecPerThread; ++q) {
-      const int vi = q * kThreads + tid;
-      E::unpack(raw[q], z[q]);
-      if (vi >= nvec) {
-#pragma unroll
-        for (int e = 0; e < E::kEPV; ++e) z[q][e] = -INFINITY;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < kVecPerThread; ++q) {
-      const int base = j0 + (q * kThreads + tid) * E::kEPV;
-#pragma unroll
-      for (int e = 0; e < E::kEPV; ++e)
-        z[q][e] = (base + e < j1) ? E::load1(row + base + e) : -INFINITY;
-    }
-  }
-}
-
 // 2^x on the special-function unit (flush-to-zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -105,7 +73,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Exact 2^d for an integer d <= 0 (0 below the float normal range).
+// Exact 2^d for an integer d <= 0 (0 below the normal range).
 __device__ __forceinline__ float pow2i_f(int d) {
   return d < -126 ? 0.0f : __int_as_float((d + 127) << 23);
 }
@@ -153,10 +121,11 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
-// Error-free accumulation of positive float terms: (hi, lo) with hi + lo the
-// running sum to about 2^-48 relative (Knuth's two-sum).
+// Error-free accumulation of non-negative float terms: hi + lo is the running
+// sum to about 2^-48 relative (Knuth's two-sum).
 struct FSum {
-  float hi = 0.0f, lo = 0.0f;
+  float hi, lo;  // plain aggregate (usable in __shared__ storage); start from zero()
+  static __device__ __forceinline__ FSum zero() { return FSum{0.0f, 0.0f}; }
   __device__ __forceinline__ void add(float b) {
     const float s = __fadd_rn(hi, b);
     const float bb = __fsub_rn(s, hi);
@@ -165,29 +134,224 @@ struct FSum {
     lo = __fadd_rn(lo, err);
   }
   __device__ __forceinline__ double value() const { return (double)hi + (double)lo; }
+  __device__ __forceinline__ void scale(float f) {  // exact for powers of two
+    hi *= f;
+    lo *= f;
+  }
 };
 
-// Release this CTA's global writes, count its arrival, and tell whether it
-// arrived last (then acquire the other arrivals' writes and reset the counter).
-// Called by every thread of the CTA.
-__device__ __forceinline__ bool arrive_last(unsigned* counter, unsigned expected, int* s_flag) {
-  __threadfence();
+// a + b for double-float values (two-sum of the high parts, then a fast
+// renormalisation); about 2^-44 relative, float-pipe arithmetic only.
+__device__ __forceinline__ FSum df_add(const FSum& a, const FSum& b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  const float bb = __fsub_rn(s, a.hi);
+  float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  FSum r;
+  r.hi = __fadd_rn(s, e);
+  r.lo = __fsub_rn(e, __fsub_rn(r.hi, s));
+  return r;
+}
+
+__device__ __forceinline__ FSum warp_sum_df(FSum v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    FSum y;
+    y.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+    y.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+    v = df_add(v, y);
+  }
+  return v;
+}
+
+// Normalised double-float (|lo| <= half an ulp of hi), so that values compare
+// lexicographically.
+__device__ __forceinline__ FSum df_norm(const FSum& a) {
+  FSum r;
+  r.hi = __fadd_rn(a.hi, a.lo);
+  r.lo = __fsub_rn(a.lo, __fsub_rn(r.hi, a.hi));
+  return r;
+}
+// a < b for normalised double-floats.
+__device__ __forceinline__ bool df_less(const FSum& a, const FSum& b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+// u * a for a float u >= 0 and a double-float a (two-product via FMA).
+__device__ __forceinline__ FSum df_mul_f(float u, const FSum& a) {
+  const float p = __fmul_rn(u, a.hi);
+  float e = __fmaf_rn(u, a.hi, -p);
+  e = __fmaf_rn(u, a.lo, e);
+  FSum r;
+  r.hi = __fadd_rn(p, e);
+  r.lo = __fsub_rn(e, __fsub_rn(r.hi, p));
+  return r;
+}
+__device__ __forceinline__ FSum df_from(float x) { return FSum{x, 0.0f}; }
+
+// Inclusive warp scan of double-float values in lane order.
+__device__ __forceinline__ FSum warp_scan_df(FSum v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    FSum y;
+    y.hi = __shfl_up_sync(0xffffffffu, v.hi, o);
+    y.lo = __shfl_up_sync(0xffffffffu, v.lo, o);
+    if (lane >= o) v = df_add(y, v);
+  }
+  return v;
+}
+
+// Add `n` arrivals to `counter` after this CTA's global writes, and tell
+// whether they completed it (old + n == expected).  The bar.sync orders every
+// thread's writes before thread 0's release fence and atomic (fences are
+// cumulative); the completing CTA's thread 0 fences again (acquire) before
+// the bar.sync that releases its other threads to read what the others wrote
+// (through L2, with ld.cg).  The completing CTA resets the counter, so every
+// call leaves its counters at zero.  Called by every thread of the CTA.
+__device__ __forceinline__ bool arrive_last(unsigned* counter, unsigned n, unsigned expected,
+                                            int* s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(counter, 1u);
-    const bool last = (old == expected - 1u);
+    __threadfence();
+    const unsigned old = atomicAdd(counter, n);
+    const bool last = (old + n == expected);
     if (last) {
       __threadfence();
-      *counter = 0u;  // every call leaves its counters at zero
+      *counter = 0u;
     }
     *s_flag = last ? 1 : 0;
   }
   __syncthreads();
-  const bool last = *s_flag != 0;
-  if (last) __threadfence();
-  return last;
+  return *s_flag != 0;
 }
 
 __device__ __forceinline__ void set_flag(unsigned* flags, unsigned bit) { atomicOr(flags, bit); }
+
+// Packed pairs of floats (f32x2) for the FMA pipe's two-wide instructions.
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Largest of the elements of 4 vectors, as float.
+template <typename E>
+__device__ __forceinline__ float vec4_max(const uint4 (&raw)[4]);
+
+template <>
+__device__ __forceinline__ float vec4_max<F32>(const uint4 (&raw)[4]) {
+  float m[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    m[q] = fmaxf(fmaxf(__uint_as_float(raw[q].x), __uint_as_float(raw[q].y)),
+                 fmaxf(__uint_as_float(raw[q].z), __uint_as_float(raw[q].w)));
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+template <>
+__device__ __forceinline__ float vec4_max<BF16>(const uint4 (&raw)[4]) {
+  uint32_t m[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) m[q] = bmax2(bmax2(raw[q].x, raw[q].y), bmax2(raw[q].z, raw[q].w));
+  const uint32_t w = bmax2(bmax2(m[0], m[1]), bmax2(m[2], m[3]));
+  return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// ---------------------------------------------------------------------------
+// Bulk asynchronous copies (global -> shared) completed on an mbarrier.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make barrier initialisation visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Test a barrier phase; the thread may sleep up to ~1 ms in the instruction
+// while the phase is incomplete (woken when it completes), so waiting warps
+// do not spin through the issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for a barrier phase; give up after kWaitLimitNs (returns false).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (unsigned it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
 
 }  // namespace sv

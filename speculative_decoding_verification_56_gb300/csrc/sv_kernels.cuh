@@ -3,23 +3,28 @@
 // Sampling verification ("EAGLE-3 speculative decoding review", sections
 // "Speculative Decoding" step 3 and "Does Using a Small Model's Answer Reduce
 // Quality?"; "EAGLE math", "Vanilla speculative decoding"):
-//   sample_stats_kernel   pass 1: one streaming read of all 2k+1 rows of every
-//                         sequence; per-chunk softmax partials, per-row merge,
-//                         p(x_i)/q(x_i), accept test and first rejection.
-//   sample_draw_kernel    pass 2: re-reads only the selected row (pair) of each
-//                         sequence: residual max(0, p - q) after a rejection,
-//                         else p of the bonus row; chunk sums, then the last
-//                         CTA of the sequence draws the token by inverse CDF.
+//   stats    one streaming read of all 2k+1 rows of every sequence: softmax
+//            partials per row segment, per-row merge, p(x_i) and q(x_i), the
+//            accept test and the first rejection (warp ballot).
+//   draw     re-reads only the selected row (pair) of each sequence: residual
+//            max(0, p - q) after a rejection, else p of the bonus row; chunk
+//            sums, then the last CTA of the sequence draws the token by
+//            inverse CDF.
 // Greedy and tree verification ("Does Using a Small Model's Answer Reduce
 // Quality?" greedy bullets; "EAGLE-2"; "The Complete EAGLE-3 Inference
 // Process" step 4):
-//   argmax_verify_kernel  one streaming read of every target row; per-chunk
-//                         argmax, per-row merge, then the last CTA of each
-//                         sequence (tree) resolves the accepted prefix (path).
+//   argmax   one streaming read of every target row: argmax per row segment,
+//            per-row merge, then the last CTA of each sequence (tree) resolves
+//            the accepted prefix (path).
+//
+// Two loaders feed the same per-thread arithmetic: a persistent kernel that
+// streams contiguous ranges of 32 KB chunks through a ring of bulk async
+// copies (rows whose bytes are a multiple of 16 at a 16-byte aligned base),
+// and a one-CTA-per-chunk kernel with plain loads for any other row size.
 //
 // Softmax arithmetic: with s = log2(e) / T, p_j = 2^(z_j s - R) / S where R
-// is an integer reference >= max_j z_j s.  Integer references make every
-// rescaling between threads, chunks and rows an exact power of two.
+// is an integer >= max_j z_j s.  Integer references make every rescaling
+// between threads, segments and rows an exact power of two.
 #pragma once
 
 #include "sv_device.cuh"
@@ -29,30 +34,45 @@ namespace sv {
 // ---------------------------------------------------------------------------
 // Workspace records
 // ---------------------------------------------------------------------------
-struct SoftmaxPartial {  // one (row, chunk)
+// Segment records: a segment is a run of consecutive chunks of one row handled
+// by one CTA.  Each WARP of that CTA writes its own record for the segment in
+// slot (row, first chunk, warp) with nch = the segment's chunk count, and
+// nch = 0 in the slots (row, other chunks of the segment, warp); so every slot
+// is written on every call and no CTA barrier is needed to publish a result.
+struct SoftmaxPartial {
   int ref;
-  int pad;
-  double sum;  // sum of 2^(z s - ref) over the chunk
-};
-struct RowStats {  // one row after the merge
-  int ref;       // integer reference R of the row
-  float inv_sum; // 1 / S rounded to float
-  double sum;    // S = sum_j 2^(z_j s - R)
-  double prob;   // p (or q) of the row's draft token, float64
+  int nch;
+  float hi, lo;  // double-float sum of 2^(z s - ref) over the warp's elements
 };
 struct ArgPartial {
   float val;
   int idx;
+  int nch;
+  int pad;
+};
+struct RowStats {  // one row after the merge
+  int ref;         // integer reference R of the row
+  float inv_sum;   // 1 / S rounded to float
+  double sum;      // unused
+  double prob;     // p (or q) of the row's draft token, float64
+};
+
+// What the draw needs of sequence b: the selected position n and the
+// normalisers of its target (and, after a rejection, draft) row.
+struct DrawDesc {
+  int n;
+  float nref_t, inv_t, nref_d, inv_d;
+  int pad[3];
 };
 
 struct SampleParams {
-  const void* target;   // [B, k+1, V]
-  const void* draft;    // [B, k, V]
+  const void* target;  // [B, k+1, V]
+  const void* draft;   // [B, k, V]
   const int32_t* tokens;
   const float* u_accept;
   const float* u_sample;
-  float scale;          // log2(e) / T
-  int B, k, V, nchunks;
+  float scale;  // log2(e) / T
+  int B, k, V, nchunks, items;
   int32_t* accepted_len;
   int32_t* out_tokens;
   float* p_out;
@@ -60,13 +80,30 @@ struct SampleParams {
   float* resid_mass;
   // workspace
   unsigned* flags;
-  unsigned* row_cnt;    // [B*(2k+1)]
-  unsigned* seq_cnt;    // [B]
-  unsigned* draw_cnt;   // [B]
-  SoftmaxPartial* part; // [B*(2k+1)*nchunks]
-  RowStats* rows;       // [B*(2k+1)]
-  int32_t* sel;         // [B]
-  double* csum;         // [B*nchunks]
+  SoftmaxPartial* part;  // [B*(2k+1) * nchunks * kWarps]
+  DrawDesc* desc;        // [B]
+  // draw prefix structure per (sequence, chunk): group sums and chunk
+  // totals; the _p arrays hold p-only weights of a rejected row (used when
+  // its residual mass rounds to zero)
+  float* gsum;     // [B*nchunks*kVecPerChunk]
+  float* gsum_p;   // [B*nchunks*kVecPerChunk]
+  FSum* csum;      // [B*nchunks]
+  FSum* csum_p;    // [B*nchunks]
+};
+
+struct ArgmaxParams {
+  const void* target;      // [B, rows_per_seq, V]
+  const int32_t* tokens;   // chain: [B, k]; tree: [B, N]
+  const int32_t* parents;  // tree only: [B, N]
+  int B, rows_per_seq, V, nchunks, items;
+  int tree;       // 0 = chain greedy (rows_per_seq = k+1), 1 = tree (rows_per_seq = N)
+  int max_depth;  // tree only
+  int32_t* accepted_len;
+  int32_t* out_tokens;  // chain: [B, k+1]; tree: [B, max_depth+1]
+  int32_t* path_nodes;  // tree: [B, max_depth+1]
+  unsigned* flags;
+  ArgPartial* part;   // [B*rows_per_seq * nchunks * kWarps]
+  int32_t* rowarg;    // [B*rows_per_seq]
 };
 
 // Row r of sequence b: r in [0, k] is target row r, r in [k+1, 2k] is draft
@@ -80,455 +117,371 @@ __device__ __forceinline__ const typename E::storage* seq_row_ptr(const SamplePa
   return reinterpret_cast<const S*>(p.draft) + ((size_t)b * p.k + (r - p.k - 1)) * (size_t)p.V;
 }
 
-// ---------------------------------------------------------------------------
-// Pass 1: softmax statistics, accept test, first rejection
-// ---------------------------------------------------------------------------
+// A 16-byte vector of elements j..j+kEPV-1 of a row; on the plain-load path
+// elements at or past j1 read as -inf.
 template <typename E, bool kVec>
-__global__ void __launch_bounds__(kThreads) sample_stats_kernel(const SampleParams p) {
-  __shared__ int s_ref[kWarps];
-  __shared__ float s_sum[kWarps];
-  __shared__ int s_flag;
-
-  const int rows_per_seq = 2 * p.k + 1;
-  const int item = blockIdx.x;
-  const int row = item / p.nchunks;  // global row id b * (2k+1) + r
-  const int c = item - row * p.nchunks;
-  const int b = row / rows_per_seq;
-  const int r = row - b * rows_per_seq;
-  const int j0 = c * E::kChunk;
-  const int j1 = min(p.V, j0 + E::kChunk);
-  const typename E::storage* rp = seq_row_ptr<E>(p, b, r);
-
-  float z[kVecPerThread][E::kEPV];
-  load_chunk<E, kVec>(rp, j0, j1, z);
-
-  // the dependent draw kernel may start its launch now
-  asm volatile("griddepcontrol.launch_dependents;");
-
-  float m = -INFINITY;
+__device__ __forceinline__ uint4 fetch_vec(const typename E::storage* row, int j, int j1) {
+  if constexpr (kVec) {
+    return ldg_stream(row + j);
+  } else {
+    uint32_t w[4];
+    if constexpr (E::kEPV == 4) {
 #pragma unroll
-  for (int q = 0; q < kVecPerThread; ++q)
+      for (int e = 0; e < 4; ++e)
+        w[e] = (j + e < j1) ? __float_as_uint(E::load1(row + j + e)) : 0xFF800000u;
+    } else {
 #pragma unroll
-    for (int e = 0; e < E::kEPV; ++e) m = fmaxf(m, z[q][e]);
-  const int ref = exp_ref(m, p.scale);
-  const float nref = -(float)ref;
-  float acc = 0.0f;
-#pragma unroll
-  for (int q = 0; q < kVecPerThread; ++q) {
-    float t[E::kEPV];
-#pragma unroll
-    for (int e = 0; e < E::kEPV; ++e) t[e] = ex2(__fmaf_rn(z[q][e], p.scale, nref));
-    // pairwise sum of the vector
-#pragma unroll
-    for (int w = E::kEPV / 2; w > 0; w >>= 1)
-#pragma unroll
-      for (int e = 0; e < w; ++e) t[e] = __fadd_rn(t[e], t[e + w]);
-    acc = __fadd_rn(acc, t[0]);
-  }
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int wref = warp_max_i(ref);
-  if (lane == 0) s_ref[warp] = wref;
-  __syncthreads();
-  int bref = s_ref[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) bref = max(bref, s_ref[w]);
-  float wsum = warp_sum_f(acc * pow2i_f(ref - bref));
-  if (lane == 0) s_sum[warp] = wsum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double tot = 0.0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) tot += (double)s_sum[w];
-    SoftmaxPartial sp;
-    sp.ref = bref;
-    sp.pad = 0;
-    sp.sum = tot;
-    p.part[item] = sp;
-  }
-
-  if (!arrive_last(&p.row_cnt[row], (unsigned)p.nchunks, &s_flag)) return;
-
-  // ---- this CTA finishes the row: merge the chunk partials (fixed order) ----
-  if (warp == 0) {
-    int lref = kRefEmpty;
-    for (int cc = lane; cc < p.nchunks; cc += 32)
-      lref = max(lref, __ldcg(&p.part[(size_t)row * p.nchunks + cc].ref));
-    const int R = warp_max_i(lref);
-    double lsum = 0.0;
-    for (int cc = lane; cc < p.nchunks; cc += 32) {
-      const SoftmaxPartial* pp = &p.part[(size_t)row * p.nchunks + cc];
-      lsum += __ldcg(&pp->sum) * pow2i_d(__ldcg(&pp->ref) - R);
-    }
-    const double S = warp_sum_d(lsum);
-    if (lane == 0) {
-      double prob = 0.0;
-      if (r != p.k) {  // rows with a draft token: target r < k, draft r > k
-        const int i = (r < p.k) ? r : r - p.k - 1;
-        const int x = p.tokens[(size_t)b * p.k + i];
-        if (x >= 0 && x < p.V) {
-          const float zx = E::load1(rp + x);
-          const float xs = __fmaf_rn(zx, p.scale, -(float)R);
-          prob = exp2((double)xs) / S;
-        } else {
-          set_flag(p.flags, 1u);
-        }
-      }
-      RowStats rs;
-      rs.ref = R;
-      rs.inv_sum = (float)(1.0 / S);
-      rs.sum = S;
-      rs.prob = prob;
-      p.rows[row] = rs;
-    }
-  }
-
-  if (!arrive_last(&p.seq_cnt[b], (unsigned)rows_per_seq, &s_flag)) return;
-
-  // ---- this CTA finishes the sequence: accept test left to right ----
-  if (threadIdx.x == 0) {
-    const size_t rb = (size_t)b * rows_per_seq;
-    int n = p.k;
-    for (int i = 0; i < p.k; ++i) {
-      const double pi = __ldcg(&p.rows[rb + i].prob);
-      const double qi = __ldcg(&p.rows[rb + p.k + 1 + i].prob);
-      p.p_out[(size_t)b * p.k + i] = (float)pi;
-      p.q_out[(size_t)b * p.k + i] = (float)qi;
-      if (n == p.k) {
-        const double u = (double)p.u_accept[(size_t)b * p.k + i];
-        if (!(u * qi < pi)) n = i;
+      for (int h = 0; h < 4; ++h) {
+        const int j0 = j + 2 * h;
+        const uint32_t lo = (j0 < j1) ? (uint32_t)reinterpret_cast<const uint16_t*>(row)[j0]
+                                      : 0xFF80u;
+        const uint32_t hi = (j0 + 1 < j1)
+                                ? (uint32_t)reinterpret_cast<const uint16_t*>(row)[j0 + 1]
+                                : 0xFF80u;
+        w[h] = lo | (hi << 16);
       }
     }
-    p.accepted_len[b] = n;
-    for (int i = 0; i <= p.k; ++i)
-      p.out_tokens[(size_t)b * (p.k + 1) + i] = (i < n) ? p.tokens[(size_t)b * p.k + i] : -1;
-    p.sel[b] = n;
+    return make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
 // ---------------------------------------------------------------------------
-// Pass 2: residual / bonus draw by inverse CDF
+// Per-thread arithmetic on one chunk (raw vectors in registers)
 // ---------------------------------------------------------------------------
-struct DrawRows {
-  const void* t;  // target row
-  const void* d;  // draft row (nullptr: weights are p of the target row)
-  float nref_t, inv_t, nref_d, inv_d;
+struct StatsState {  // running softmax partial of one thread over one segment
+  int ref = kRefEmpty;
+  FSum acc = FSum::zero();
 };
 
-// Weight of one element; explicit round-to-nearest intrinsics keep every
-// evaluation bit-identical (no contraction differences between call sites).
-__device__ __forceinline__ float draw_weight(float zt, float zd, float s, const DrawRows& w,
-                                             bool resid) {
-  const float pt = __fmul_rn(ex2(__fmaf_rn(zt, s, w.nref_t)), w.inv_t);
-  if (!resid) return pt;
-  const float pd = __fmul_rn(ex2(__fmaf_rn(zd, s, w.nref_d)), w.inv_d);
-  return fmaxf(__fsub_rn(pt, pd), 0.0f);
-}
-
-// Sequential float sum of one vector's weights (the "group sum").
-template <typename E, bool kVec>
-__device__ __forceinline__ void chunk_group_sums(const DrawRows& w, bool resid, float s, int j0,
-                                                 int j1, float (&g)[kVecPerThread]) {
-  using S = typename E::storage;
-  float zt[kVecPerThread][E::kEPV];
-  float zd[kVecPerThread][E::kEPV];
-  load_chunk<E, kVec>(reinterpret_cast<const S*>(w.t), j0, j1, zt);
-  if (resid) load_chunk<E, kVec>(reinterpret_cast<const S*>(w.d), j0, j1, zd);
-#pragma unroll
-  for (int q = 0; q < kVecPerThread; ++q) {
-    float a = 0.0f;
-#pragma unroll
-    for (int e = 0; e < E::kEPV; ++e)
-      a = __fadd_rn(a, draw_weight(zt[q][e], resid ? zd[q][e] : 0.0f, s, w, resid));
-    g[q] = a;
-  }
-}
-
-// Lane-level two-sum over 32 consecutive groups held in shared memory, then an
-// inclusive warp scan in float64.  Lane l owns [excl_l, inc_l) with excl_l
-// taken from lane l-1's inclusive value, so the lanes tile [0, inc_31).
-__device__ __forceinline__ double lane_scan(const float* s_g, int lane, double* excl) {
-  FSum acc;
-#pragma unroll 8
-  for (int g = 0; g < 32; ++g) acc.add(s_g[lane * 32 + g]);
-  double inc = acc.value();
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
-  }
-  const double prev = __shfl_up_sync(0xffffffffu, inc, 1);
-  *excl = lane == 0 ? 0.0 : prev;
-  return inc;
-}
-
+// Element pairs of a 16-byte vector as f32x2 values: bf16 words split into
+// (low, high) halves, fp32 vectors into (x, y) and (z, w).
 template <typename E>
-__device__ __forceinline__ DrawRows draw_rows(const SampleParams& p, int b, int n, bool resid) {
-  using S = typename E::storage;
-  const int rows_per_seq = 2 * p.k + 1;
-  const size_t rb = (size_t)b * rows_per_seq;
-  DrawRows w;
-  const RowStats rt = p.rows[rb + n];
-  w.t = reinterpret_cast<const S*>(p.target) + ((size_t)b * (p.k + 1) + n) * (size_t)p.V;
-  w.nref_t = -(float)rt.ref;
-  w.inv_t = rt.inv_sum;
-  w.d = nullptr;
-  w.nref_d = 0.0f;
-  w.inv_d = 0.0f;
-  if (resid) {
-    const RowStats rd = p.rows[rb + p.k + 1 + n];
-    w.d = reinterpret_cast<const S*>(p.draft) + ((size_t)b * p.k + n) * (size_t)p.V;
-    w.nref_d = -(float)rd.ref;
-    w.inv_d = rd.inv_sum;
-  }
-  return w;
-}
-
-// Sum of one chunk's weights, computed the same way the final scan walks them.
-template <typename E, bool kVec>
-__device__ double chunk_total(const DrawRows& w, bool resid, float s, int j0, int j1, float* s_g,
-                              double* s_tot) {
-  float g[kVecPerThread];
-  chunk_group_sums<E, kVec>(w, resid, s, j0, j1, g);
+__device__ __forceinline__ void vec_pairs(const uint4& v, unsigned long long (&pr)[E::kEPV / 2]);
+template <>
+__device__ __forceinline__ void vec_pairs<BF16>(const uint4& v, unsigned long long (&pr)[4]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int q = 0; q < kVecPerThread; ++q) s_g[q * kThreads + threadIdx.x] = g[q];
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    double excl;
-    const double inc = lane_scan(s_g, threadIdx.x, &excl);
-    if (threadIdx.x == 31) *s_tot = inc;
-  }
-  __syncthreads();
-  const double t = *s_tot;
-  __syncthreads();
-  return t;
+  for (int h = 0; h < 4; ++h)
+    pr[h] = f2pack(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
+}
+template <>
+__device__ __forceinline__ void vec_pairs<F32>(const uint4& v, unsigned long long (&pr)[2]) {
+  pr[0] = f2pack(__uint_as_float(v.x), __uint_as_float(v.y));
+  pr[1] = f2pack(__uint_as_float(v.z), __uint_as_float(v.w));
 }
 
-template <typename E, bool kVec>
-__global__ void __launch_bounds__(kThreads) sample_draw_kernel(const SampleParams p) {
-  __shared__ float s_g[kGroupsPerChunk];
-  __shared__ double s_tot;
-  __shared__ int s_flag;
-  __shared__ int s_tok;
-
-  // wait for the stats kernel's results (programmatic dependent launch)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  const int item = blockIdx.x;
-  const int b = item / p.nchunks;
-  const int c = item - b * p.nchunks;
-  const int n = p.sel[b];
-  bool resid = n < p.k;
-  DrawRows w = draw_rows<E>(p, b, n, resid);
-
-  {
-    const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
-    const double t = chunk_total<E, kVec>(w, resid, p.scale, j0, j1, s_g, &s_tot);
-    if (threadIdx.x == 0) p.csum[item] = t;
+// Add this chunk's 2^(z s - ref) terms to the thread's running sum.  Scale and
+// shift run two-wide (fma.f32x2), sums pairwise two-wide (add.f32x2), the
+// exponentials on the special-function unit; one two-sum per chunk.
+template <typename E>
+__device__ __forceinline__ void stats_chunk(const uint4 (&raw)[kVecPerThread], float s,
+                                            StatsState& st) {
+  // past-the-end vectors hold -inf: they raise no maximum and add 2^-inf = 0
+  const int r = exp_ref(vec4_max<E>(raw), s);
+  if (r > st.ref) {  // exact rescale of the running sum by 2^(old - new)
+    st.acc.scale(pow2i_f(st.ref - r));
+    st.ref = r;
   }
-
-  if (!arrive_last(&p.draw_cnt[b], (unsigned)p.nchunks, &s_flag)) return;
-
-  // ---- last CTA of sequence b: locate the chunk, then the token ----
-  double* cs = p.csum + (size_t)b * p.nchunks;
-  double total = 0.0;
-  if (threadIdx.x == 0) {
-    for (int cc = 0; cc < p.nchunks; ++cc) total += __ldcg(&cs[cc]);
-    s_tot = total;
-  }
-  __syncthreads();
-  total = s_tot;
-  __syncthreads();
-  bool fallback = false;
-  if (resid && !(total > 0.0)) {
-    // residual mass vanished in rounding: sample p of the rejected row instead
-    fallback = true;
-    resid = false;
-    w.d = nullptr;
-    total = 0.0;
-    for (int cc = 0; cc < p.nchunks; ++cc) {
-      const int j0 = cc * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
-      const double t = chunk_total<E, kVec>(w, false, p.scale, j0, j1, s_g, &s_tot);
-      if (threadIdx.x == 0) {
-        cs[cc] = t;
-        total += t;
-      }
-    }
-    if (threadIdx.x == 0) {
-      s_tot = total;
-      set_flag(p.flags, 8u);
-    }
-    __syncthreads();
-    total = s_tot;
-    __syncthreads();
-  }
-
-  const double target = (double)p.u_sample[b] * total;
-  // chunk holding the target: first chunk whose inclusive prefix exceeds it
-  if (threadIdx.x == 0) {
-    double cum = 0.0, base = 0.0;
-    int cstar = -1, lastpos = 0;
-    for (int cc = 0; cc < p.nchunks; ++cc) {
-      const double v = __ldcg(&cs[cc]);
-      if (v > 0.0) lastpos = cc;
-      if (cstar < 0 && target < cum + v) {
-        cstar = cc;
-        base = cum;
-      }
-      cum += v;
-    }
-    if (cstar < 0) {  // rounding: last chunk with positive mass
-      cstar = lastpos;
-      base = cum - __ldcg(&cs[lastpos]);
-    }
-    s_flag = cstar;
-    s_tot = base;
-  }
-  __syncthreads();
-  const int cstar = s_flag;
-  const double base = s_tot;
-  __syncthreads();
-
-  const int j0 = cstar * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
-  float g[kVecPerThread];
-  chunk_group_sums<E, kVec>(w, resid, p.scale, j0, j1, g);
+  const float nref = -(float)st.ref;
+  const unsigned long long s2 = f2pack(s, s), n2 = f2pack(nref, nref);
+  constexpr int kP = E::kEPV / 2;
+  unsigned long long vs[kVecPerThread];
 #pragma unroll
-  for (int q = 0; q < kVecPerThread; ++q) s_g[q * kThreads + threadIdx.x] = g[q];
-  if (threadIdx.x == 0) s_tok = -1;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    using S = typename E::storage;
-    const int lane = threadIdx.x;
-    double excl;
-    const double inc = lane_scan(s_g, lane, &excl);
-    // the lane whose range [base+excl, base+inc) holds the target walks it;
-    // if rounding left the target outside every range, the last lane with
-    // positive mass takes its last positive element
-    const bool mine = target >= base + excl && target < base + inc;
-    const unsigned own = __ballot_sync(0xffffffffu, mine);
-    const unsigned pos = __ballot_sync(0xffffffffu, inc > excl);
-    const int owner = own ? (__ffs(own) - 1) : (pos ? (31 - __clz(pos)) : 0);
-    const bool exact = own != 0;
-    if (lane == owner) {
-      FSum acc;
-      int tok = -1, lastg = -1;
-      for (int gi = 0; gi < 32; ++gi) {
-        const int vi = lane * 32 + gi;
-        const float gs = s_g[vi];
-        if (!(gs > 0.0f)) continue;
-        lastg = gi;
-        FSum nxt = acc;
-        nxt.add(gs);
-        if (exact && target < base + excl + nxt.value()) {
-          // the target lies in this vector: walk its elements in order
-          const double before = base + excl + acc.value();
-          const int e0 = j0 + vi * E::kEPV;
-          float part = 0.0f;
-          int lastpos = -1;
-          for (int e = 0; e < E::kEPV && e0 + e < j1; ++e) {
-            const float zt = E::load1(reinterpret_cast<const S*>(w.t) + e0 + e);
-            const float zd = resid ? E::load1(reinterpret_cast<const S*>(w.d) + e0 + e) : 0.0f;
-            const float we = draw_weight(zt, zd, p.scale, w, resid);
-            part = __fadd_rn(part, we);
-            if (we > 0.0f) lastpos = e0 + e;
-            if (target < before + (double)part) {
-              tok = e0 + e;
-              break;
-            }
-          }
-          if (tok < 0) tok = lastpos;  // rounding inside the vector
-          break;
-        }
-        acc = nxt;
-      }
-      if (tok < 0 && lastg >= 0) {  // rounding: last positive element of the lane
-        const int e0 = j0 + (lane * 32 + lastg) * E::kEPV;
-        for (int e = 0; e < E::kEPV && e0 + e < j1; ++e) {
-          const float zt = E::load1(reinterpret_cast<const S*>(w.t) + e0 + e);
-          const float zd = resid ? E::load1(reinterpret_cast<const S*>(w.d) + e0 + e) : 0.0f;
-          if (draw_weight(zt, zd, p.scale, w, resid) > 0.0f) tok = e0 + e;
-        }
-      }
-      s_tok = tok;
+  for (int q = 0; q < kVecPerThread; ++q) {
+    unsigned long long pr[kP];
+    vec_pairs<E>(raw[q], pr);
+#pragma unroll
+    for (int h = 0; h < kP; ++h) {
+      float x0, x1;
+      f2unpack(fma2(pr[h], s2, n2), x0, x1);
+      pr[h] = f2pack(ex2(x0), ex2(x1));
     }
+#pragma unroll
+    for (int w = kP / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int h = 0; h < w; ++h) pr[h] = add2(pr[h], pr[h + w]);
+    vs[q] = pr[0];
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int tok = s_tok;
-    if (tok < 0) tok = j0;  // unreachable with finite inputs
-    p.out_tokens[(size_t)b * (p.k + 1) + n] = tok;
-    p.resid_mass[b] = (n < p.k && !fallback) ? (float)total : 0.0f;
-  }
+  float a0, a1;
+  f2unpack(add2(add2(vs[0], vs[1]), add2(vs[2], vs[3])), a0, a1);
+  st.acc.add(__fadd_rn(a0, a1));
 }
 
-// ---------------------------------------------------------------------------
-// Greedy and tree verification: argmax of every target row
-// ---------------------------------------------------------------------------
-struct ArgmaxParams {
-  const void* target;  // [B, rows_per_seq, V]
-  const int32_t* tokens;   // chain: [B, k]; tree: [B, N]
-  const int32_t* parents;  // tree only: [B, N]
-  int B, rows_per_seq, V, nchunks;
-  int tree;       // 0 = chain greedy (rows_per_seq = k+1), 1 = tree (rows_per_seq = N)
-  int max_depth;  // tree only
-  int32_t* accepted_len;
-  int32_t* out_tokens;  // chain: [B, k+1]; tree: [B, max_depth+1]
-  int32_t* path_nodes;  // tree: [B, max_depth+1]
-  unsigned* flags;
-  unsigned* row_cnt;  // [B*rows_per_seq]
-  unsigned* seq_cnt;  // [B]
-  ArgPartial* part;   // [B*rows_per_seq*nchunks]
-  int32_t* rowarg;    // [B*rows_per_seq]
+struct ArgState {
+  float v = -INFINITY;
+  int i = 0x7FFFFFFF;
 };
 
-// Chain resolve ("accept while the draft equals the target argmax").
+// The thread's running (max, lowest index) over its elements; the index is
+// searched only when this chunk raises the thread's maximum.
+template <typename E>
+__device__ __forceinline__ void argmax_chunk(const uint4 (&raw)[kVecPerThread], int j0,
+                                             ArgState& st) {
+  const float m = vec4_max<E>(raw);
+  if (m > st.v) {
+    int idx = 0x7FFFFFFF;
+#pragma unroll
+    for (int q = kVecPerThread - 1; q >= 0; --q)
+#pragma unroll
+      for (int e = E::kEPV - 1; e >= 0; --e)
+        if (E::elem(raw[q], e) == m) idx = j0 + (q * kThreads + (int)threadIdx.x) * E::kEPV + e;
+    st.v = m;
+    st.i = idx;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Segment records (per warp, no barrier)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void emit_stats_warp(const SampleParams& p, const StatsState& st,
+                                                int row, int c_first, int c_last) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wref = warp_max_i(st.ref);
+  FSum mine = st.acc;
+  mine.scale(pow2i_f(st.ref - wref));
+  const FSum wsum = warp_sum_df(mine);
+  const int n = c_last - c_first + 1;
+  for (int i = lane; i < n; i += 32) {
+    SoftmaxPartial sp;
+    sp.ref = wref;
+    sp.nch = i == 0 ? n : 0;
+    sp.hi = i == 0 ? wsum.hi : 0.0f;
+    sp.lo = i == 0 ? wsum.lo : 0.0f;
+    p.part[((size_t)row * p.nchunks + c_first + i) * kWarps + warp] = sp;
+  }
+}
+
+__device__ __forceinline__ void emit_arg_warp(const ArgmaxParams& p, const ArgState& st, int row,
+                                              int c_first, int c_last) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float v = st.v;
+  int i = st.i;
+  warp_argmax(v, i);
+  const int n = c_last - c_first + 1;
+  for (int t = lane; t < n; t += 32) {
+    ArgPartial ap;
+    ap.val = v;
+    ap.idx = i;
+    ap.nch = t == 0 ? n : 0;
+    ap.pad = 0;
+    p.part[((size_t)row * p.nchunks + c_first + t) * kWarps + warp] = ap;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Row and sequence finalisation (one warp per row / sequence / tree)
+// ---------------------------------------------------------------------------
+// 2^x / S as float64 for x <= 1 and S >= 1/2: the float mantissa
+// 2^frac(x) / S times the exact power of two 2^floor(x), so probabilities far
+// below the float range keep their value (float-pipe arithmetic except the
+// final exact scaling).
+__device__ __forceinline__ double exp2_over(float x, float S) {
+  const float n = floorf(x);
+  return pow2i_d((int)n) * (double)__fdiv_rn(ex2(__fsub_rn(x, n)), S);
+}
+
+// Merge one row's segment records (one warp).  Loads are issued four per
+// lane before use, so a row of up to 128 records costs one round trip.
+template <typename E>
+__device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out) {
+  const int lane = threadIdx.x & 31;
+  const int rows_per_seq = 2 * p.k + 1;
+  const int b = row / rows_per_seq, r = row - b * rows_per_seq;
+  const SoftmaxPartial* pr = p.part + (size_t)row * p.nchunks * kWarps;
+  const int nrec = p.nchunks * kWarps;
+  // the token's logit is fetched alongside the records
+  float zx = 0.0f;
+  int x = -1;
+  if (r != p.k && lane == 0) {  // rows with a draft token: target r < k, draft r > k
+    const int i = (r < p.k) ? r : r - p.k - 1;
+    x = p.tokens[(size_t)b * p.k + i];
+    if (x >= 0 && x < p.V) zx = E::load1(seq_row_ptr<E>(p, b, r) + x);
+  }
+  // one pass: running (reference, double-float sum), rescaled exactly when
+  // a record's reference is larger
+  int lref = kRefEmpty;
+  FSum acc = FSum::zero();
+  for (int base = lane; base < nrec; base += 128) {
+    int4 rec[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      rec[u] = (base + 32 * u < nrec) ? __ldcg(reinterpret_cast<const int4*>(pr + base + 32 * u))
+                                      : make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (rec[u].y > 0) {
+        if (rec[u].x > lref) {
+          acc.scale(pow2i_f(lref - rec[u].x));
+          lref = rec[u].x;
+        }
+        FSum v;
+        v.hi = __int_as_float(rec[u].z);
+        v.lo = __int_as_float(rec[u].w);
+        v.scale(pow2i_f(rec[u].x - lref));
+        acc = df_add(acc, v);
+      }
+    }
+  }
+  const int R = warp_max_i(lref);
+  acc.scale(pow2i_f(lref - R));
+  const FSum S = df_norm(warp_sum_df(acc));
+  if (lane == 0) {
+    double prob = 0.0;
+    if (r != p.k) {
+      if (x >= 0 && x < p.V)
+        prob = exp2_over(__fmaf_rn(zx, p.scale, -(float)R), S.hi);
+      else
+        set_flag(p.flags, kFlagTokenRange);
+    }
+    RowStats rs;
+    rs.ref = R;
+    rs.inv_sum = __frcp_rn(S.hi);
+    rs.sum = 0.0;
+    rs.prob = prob;
+    *out = rs;
+  }
+}
+
+// Accept test left to right and first rejection of sequence b (one warp),
+// from the sequence's merged rows `rs` (index r of rows_per_seq).  Returns the
+// draw descriptor; with `write`, also stores the call's outputs for b (all
+// but the drawn token) and the descriptor.
+__device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, const RowStats* rs,
+                                       bool write) {
+  const int lane = threadIdx.x & 31;
+  const int k = p.k;
+  int n = k;
+  for (int i0 = 0; i0 < k; i0 += 32) {
+    const int i = i0 + lane;
+    bool rej = false;
+    if (i < k) {
+      const double pi = rs[i].prob;
+      const double qi = rs[k + 1 + i].prob;
+      if (write) {
+        p.p_out[(size_t)b * k + i] = (float)pi;
+        p.q_out[(size_t)b * k + i] = (float)qi;
+      }
+      const double u = (double)p.u_accept[(size_t)b * k + i];
+      rej = !(u * qi < pi);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, rej);
+    if (n == k && m) n = i0 + __ffs(m) - 1;
+  }
+  DrawDesc d;
+  d.n = n;
+  d.nref_t = -(float)rs[n].ref;
+  d.inv_t = rs[n].inv_sum;
+  d.nref_d = n < k ? -(float)rs[k + 1 + n].ref : 0.0f;
+  d.inv_d = n < k ? rs[k + 1 + n].inv_sum : 0.0f;
+  d.pad[0] = d.pad[1] = d.pad[2] = 0;
+  if (write) {
+    for (int i = lane; i <= k; i += 32)
+      p.out_tokens[(size_t)b * (k + 1) + i] = (i < n) ? p.tokens[(size_t)b * k + i] : -1;
+    if (lane == 0) {
+      p.accepted_len[b] = n;
+      p.desc[b] = d;
+    }
+  }
+  return d;
+}
+
+// Merge the argmax records of rows r0, r0+stride, r0+2*stride, r0+3*stride
+// of sequence b (one warp; rows past `nrows` are skipped).  All loads of a
+// pass are issued before any is used.  Returns the lane-uniform argmaxes.
+__device__ void finalize_arg_rows4(const ArgmaxParams& p, int b, int r0, int stride, int nrows,
+                                   int (&g)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int nrec = p.nchunks * kWarps;
+  float v[4];
+  int i[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    v[u] = -INFINITY;
+    i[u] = 0x7FFFFFFF;
+  }
+  for (int base = lane; base < nrec; base += 128) {
+    int4 rec[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u * stride;
+      const ArgPartial* pr = p.part + ((size_t)b * p.rows_per_seq + r) * nrec;
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        rec[u][t] = (r < nrows && base + 32 * t < nrec)
+                        ? __ldcg(reinterpret_cast<const int4*>(pr + base + 32 * t))
+                        : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (rec[u][t].z > 0 && better(__int_as_float(rec[u][t].x), rec[u][t].y, v[u], i[u])) {
+          v[u] = __int_as_float(rec[u][t].x);
+          i[u] = rec[u][t].y;
+        }
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    warp_argmax(v[u], i[u]);
+    g[u] = (i[u] >= 0 && i[u] < p.V) ? i[u] : 0;
+    const int r = r0 + u * stride;
+    if (lane == 0 && r < nrows) p.rowarg[(size_t)b * p.rows_per_seq + r] = g[u];
+  }
+}
+
+// Chain resolve: accept while the draft equals the target argmax (one warp).
 __device__ void resolve_chain(const ArgmaxParams& p, int b) {
-  if (threadIdx.x != 0) return;
+  const int lane = threadIdx.x & 31;
   const int k = p.rows_per_seq - 1;
   const int32_t* g = p.rowarg + (size_t)b * p.rows_per_seq;
   int n = k;
-  for (int i = 0; i < k; ++i) {
-    const int x = p.tokens[(size_t)b * k + i];
-    if (x < 0 || x >= p.V) set_flag(p.flags, 1u);
-    if (x != __ldcg(&g[i])) {
-      n = i;
-      break;
+  bool bad = false;
+  for (int i0 = 0; i0 < k; i0 += 32) {
+    const int i = i0 + lane;
+    bool miss = false;
+    if (i < k) {
+      const int x = p.tokens[(size_t)b * k + i];
+      bad |= (x < 0 || x >= p.V);
+      miss = x != __ldcg(&g[i]);
     }
+    const unsigned m = __ballot_sync(0xffffffffu, miss);
+    if (n == k && m) n = i0 + __ffs(m) - 1;
   }
-  p.accepted_len[b] = n;
-  for (int i = 0; i <= k; ++i) {
+  if (bad) set_flag(p.flags, kFlagTokenRange);
+  for (int i = lane; i <= k; i += 32) {
     int v = -1;
     if (i < n) v = p.tokens[(size_t)b * k + i];
     else if (i == n) v = __ldcg(&g[n]);
     p.out_tokens[(size_t)b * (k + 1) + i] = v;
   }
+  if (lane == 0) p.accepted_len[b] = n;
 }
 
-// Tree resolve: one thread per node walks to the root (at most max_depth + 1
-// hops), then a block max over (depth, -node) picks the winner.
-__device__ void resolve_tree(const ArgmaxParams& p, int b, unsigned long long* s_key) {
+// Tree resolve (one warp): every node walks to the root (at most max_depth + 1
+// hops); a warp max over (depth, -node) picks the deepest accepted node with
+// the lowest index.
+__device__ void resolve_tree(const ArgmaxParams& p, int b, const int32_t* par,
+                             const int32_t* tok, const int32_t* g) {
+  const int lane = threadIdx.x & 31;
   const int N = p.rows_per_seq;
-  const int32_t* par = p.parents + (size_t)b * N;
-  const int32_t* tok = p.tokens + (size_t)b * N;
-  const int32_t* g = p.rowarg + (size_t)b * N;
   const int W = p.max_depth + 1;
-  unsigned long long best = 0xFFFFFFFFull;  // root: depth 0, node 0
+  unsigned long long best = 0xFFFFFFFFull;  // the root: depth 0, node 0
   unsigned bad = 0;
-  for (int v = 1 + threadIdx.x; v < N; v += kThreads) {
+  for (int v = 1 + lane; v < N; v += 32) {
     int cur = v, d = 0;
     bool ok = true;
     while (cur != 0) {
       const int pa = par[cur];
       if (pa < 0 || pa >= cur) {
-        bad |= 2u;
+        bad |= kFlagBadParent;
         ok = false;
         break;
       }
       const int tv = tok[cur];
-      if (tv < 0 || tv >= p.V) bad |= 1u;
-      if (tv != __ldcg(&g[pa])) ok = false;
+      if (tv < 0 || tv >= p.V) bad |= kFlagTokenRange;
+      if (tv != g[pa]) ok = false;
       if (++d > p.max_depth) {
-        bad |= 4u;
+        bad |= kFlagDepth;
         ok = false;
         break;
       }
@@ -541,30 +494,18 @@ __device__ void resolve_tree(const ArgmaxParams& p, int b, unsigned long long* s
     }
   }
   if (bad) set_flag(p.flags, bad);
-  // block max
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
     best = y > best ? y : best;
   }
-  if ((threadIdx.x & 31) == 0) s_key[threadIdx.x >> 5] = best;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned long long k = s_key[0];
-    for (int w = 1; w < kWarps; ++w) k = s_key[w] > k ? s_key[w] : k;
-    s_key[0] = k;
+  const int depth = (int)(best >> 32);
+  const int vstar = (int)(0xFFFFFFFFu - (unsigned)(best & 0xFFFFFFFFull));
+  for (int i = depth + 1 + lane; i < W; i += 32) {
+    p.path_nodes[(size_t)b * W + i] = -1;
+    p.out_tokens[(size_t)b * W + i] = -1;
   }
-  __syncthreads();
-  const unsigned long long key = s_key[0];
-  const int depth = (int)(key >> 32);
-  const int vstar = (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull));
-  for (int i = threadIdx.x; i < W; i += kThreads) {
-    if (i > depth) {
-      p.path_nodes[(size_t)b * W + i] = -1;
-      p.out_tokens[(size_t)b * W + i] = -1;
-    }
-  }
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     p.accepted_len[b] = depth;
     int cur = vstar;
     for (int i = depth; i >= 0; --i) {
@@ -572,83 +513,607 @@ __device__ void resolve_tree(const ArgmaxParams& p, int b, unsigned long long* s
       if (i >= 1) p.out_tokens[(size_t)b * W + i - 1] = tok[cur];
       cur = (i >= 1) ? par[cur] : 0;
     }
-    p.out_tokens[(size_t)b * W + depth] = __ldcg(&g[vstar]);
+    p.out_tokens[(size_t)b * W + depth] = g[vstar];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Resolve kernels (launched after the streaming kernel, programmatic
+// dependent launch): one CTA per sequence or tree merges its rows' records,
+// one warp per row, then one warp resolves the sequence.  No atomics.
+// ---------------------------------------------------------------------------
+// Trees up to this many nodes are walked on shared-memory copies of their
+// parents, tokens and row argmaxes; larger ones read global memory.
+constexpr int kTreeSmemNodes = 2048;
+
+__global__ void __launch_bounds__(kThreads) argmax_resolve_kernel(const ArgmaxParams p) {
+  __shared__ int32_t s_par[kTreeSmemNodes], s_tok[kTreeSmemNodes], s_g[kTreeSmemNodes];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x;
+  const int N = p.rows_per_seq;
+  const bool in_smem = p.tree && N <= kTreeSmemNodes;
+  if (in_smem) {  // independent loads, issued before the merges
+    for (int v = threadIdx.x; v < N; v += kThreads) {
+      s_par[v] = p.parents[(size_t)b * N + v];
+      s_tok[v] = p.tokens[(size_t)b * N + v];
+    }
+  }
+  for (int r0 = threadIdx.x >> 5; r0 < N; r0 += 4 * kWarps) {
+    int g[4];
+    finalize_arg_rows4(p, b, r0, kWarps, N, g);
+    if (in_smem && (threadIdx.x & 31) == 0)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (r0 + u * kWarps < N) s_g[r0 + u * kWarps] = g[u];
+  }
+  __threadfence_block();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    if (!p.tree)
+      resolve_chain(p, b);
+    else if (in_smem)
+      resolve_tree(p, b, s_par, s_tok, s_g);
+    else
+      resolve_tree(p, b, p.parents + (size_t)b * N, p.tokens + (size_t)b * N,
+                   p.rowarg + (size_t)b * N);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Loader 1: persistent CTAs streaming chunk ranges through bulk async copies
+// ---------------------------------------------------------------------------
+// CTA g owns items [items*g/G, items*(g+1)/G) (item = row * nchunks + chunk).
+// Thread 0 keeps kStages chunk copies in flight.  A slot is released (its
+// "empty" barrier, one arrival per warp) as soon as every warp has copied it
+// into registers, and thread 0 refills it before computing on its own copy.
+// The loop has no CTA-wide barrier.  Every wait is bounded: a wait that runs
+// out sets kFlagTimeout, the CTA keeps its control flow but stops copying and
+// computing, and it drains the copies still in flight before it exits.
+struct Ring {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  int abort;
+};
+
+__device__ __forceinline__ void item_range(int items, int& i0, int& i1) {
+  const long long G = gridDim.x, g = blockIdx.x;
+  i0 = (int)((long long)items * g / G);
+  i1 = (int)((long long)items * (g + 1) / G);
+}
+
+// Thread 0 initialises the barriers and issues the first kStages copies
+// before the CTA barrier, so the first bytes are in flight at once.
+template <typename IssueFn>
+__device__ __forceinline__ int ring_init(Ring& ring, int i0, int i1, IssueFn issue) {
+  int issued = i0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ring.full[s], 1);
+      mbar_init(&ring.empty[s], kWarps);
+    }
+    ring.abort = 0;
+    mbar_init_fence();
+    for (; issued < i1 && issued < i0 + kStages; ++issued) issue(issued, issued - i0);
+  }
+  __syncthreads();
+  return issued;
+}
+
+// Thread 0, at the end: wait (bounded) for the copies issued into each slot.
+__device__ __noinline__ void ring_drain(Ring& ring, int i0, int issued) {
+  for (int j = max(i0, issued - kStages); j < issued; ++j)
+    mbar_wait_bounded(&ring.full[(j - i0) % kStages], (unsigned)(((j - i0) / kStages) & 1));
+}
+
+// Wait for the item in `slot` (phase parity `par`), copy this thread's
+// vectors to registers (past-the-end vectors read as -inf) and release the
+// slot.  Returns false once the CTA has aborted.
+template <typename E>
+__device__ __forceinline__ bool ring_take(Ring& ring, const uint8_t* stage_mem, int slot,
+                                          unsigned par, int nvec, unsigned* flags,
+                                          uint4 (&raw)[kVecPerThread]) {
+  bool ok = *(volatile int*)&ring.abort == 0;
+  if (ok && !mbar_wait_bounded(&ring.full[slot], par)) {
+    ok = false;
+    ring.abort = 1;
+    set_flag(flags, kFlagTimeout);
+  }
+  const uint8_t* sm = stage_mem + (size_t)slot * kChunkBytes + threadIdx.x * 16;
+  const uint4 ninf = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+#pragma unroll
+  for (int q = 0; q < kVecPerThread; ++q) {
+    const int vi = q * kThreads + (int)threadIdx.x;
+    raw[q] = (ok && vi < nvec) ? lds128(sm + q * kThreads * 16) : ninf;
+  }
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&ring.empty[slot]);
+  return ok;
+}
+
+// Thread 0: once every warp has released `slot` (phase parity `par`), reuse
+// it for item `nxt` (if any).  Returns the new count of issued items.
+template <typename IssueFn>
+__device__ __forceinline__ int ring_refill(Ring& ring, int slot, unsigned par, int nxt, int i1,
+                                           int issued, unsigned* flags, IssueFn issue) {
+  if (nxt >= i1 || *(volatile int*)&ring.abort) return issued;
+  if (!mbar_wait_bounded(&ring.empty[slot], par)) {
+    ring.abort = 1;
+    set_flag(flags, kFlagTimeout);
+    return issued;
+  }
+  issue(nxt, slot);
+  return nxt + 1;
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleParams p) {
+  extern __shared__ __align__(128) uint8_t stage_mem[];
+  __shared__ Ring ring;
+  using S = typename E::storage;
+
+  int i0, i1;
+  item_range(p.items, i0, i1);
+  // the dependent draw kernel may begin launching; it waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (i0 >= i1) return;
+  const int C = p.nchunks;
+  const int rows_per_seq = 2 * p.k + 1;
+
+  auto issue = [&](int item, int slot) {
+    const int row = item / C, c = item - (item / C) * C;
+    const int b = row / rows_per_seq, r = row - b * rows_per_seq;
+    const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+    const unsigned bytes = (unsigned)(j1 - j0) * (unsigned)sizeof(S);
+    mbar_expect_tx(&ring.full[slot], bytes);
+    bulk_g2s(stage_mem + (size_t)slot * kChunkBytes, seq_row_ptr<E>(p, b, r) + j0, bytes,
+             &ring.full[slot]);
+  };
+
+  int issued = ring_init(ring, i0, i1, issue);
+
+  StatsState st;
+  int row = i0 / C, c = i0 - row * C, c_first = c;
+  int slot = 0;
+  unsigned par = 0;
+  for (int it = i0; it < i1; ++it) {
+    const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+    uint4 raw[kVecPerThread];
+    const bool ok = ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw);
+    if (threadIdx.x == 0)
+      issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
+    if (ok) stats_chunk<E>(raw, p.scale, st);
+    const bool row_end = (c + 1 == C);
+    if (row_end || it + 1 == i1) {
+      emit_stats_warp(p, st, row, c_first, c);
+      st = StatsState();
+      c_first = 0;
+    }
+    if (row_end) {
+      c = 0;
+      ++row;
+    } else {
+      ++c;
+    }
+    if (++slot == kStages) {
+      slot = 0;
+      par ^= 1u;
+    }
+  }
+  if (threadIdx.x == 0) ring_drain(ring, i0, issued);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const ArgmaxParams p) {
+  extern __shared__ __align__(128) uint8_t stage_mem[];
+  __shared__ Ring ring;
+  using S = typename E::storage;
+
+  int i0, i1;
+  item_range(p.items, i0, i1);
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (i0 >= i1) return;
+  const int C = p.nchunks;
+
+  auto issue = [&](int item, int slot) {
+    const int row = item / C, c = item - (item / C) * C;
+    const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+    const unsigned bytes = (unsigned)(j1 - j0) * (unsigned)sizeof(S);
+    mbar_expect_tx(&ring.full[slot], bytes);
+    bulk_g2s(stage_mem + (size_t)slot * kChunkBytes,
+             reinterpret_cast<const S*>(p.target) + (size_t)row * p.V + j0, bytes,
+             &ring.full[slot]);
+  };
+
+  int issued = ring_init(ring, i0, i1, issue);
+
+  ArgState st;
+  int row = i0 / C, c = i0 - row * C, c_first = c;
+  int slot = 0;
+  unsigned par = 0;
+  for (int it = i0; it < i1; ++it) {
+    const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+    uint4 raw[kVecPerThread];
+    const bool ok = ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw);
+    if (threadIdx.x == 0)
+      issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
+    if (ok) argmax_chunk<E>(raw, j0, st);
+    const bool row_end = (c + 1 == C);
+    if (row_end || it + 1 == i1) {
+      emit_arg_warp(p, st, row, c_first, c);
+      st = ArgState();
+      c_first = 0;
+    }
+    if (row_end) {
+      c = 0;
+      ++row;
+    } else {
+      ++c;
+    }
+    if (++slot == kStages) {
+      slot = 0;
+      par ^= 1u;
+    }
+  }
+  if (threadIdx.x == 0) ring_drain(ring, i0, issued);
+}
+
+// ---------------------------------------------------------------------------
+// Loader 2: one CTA per chunk with plain loads (any row size)
+// ---------------------------------------------------------------------------
+template <typename E, bool kVec>
+__device__ __forceinline__ void load_chunk_regs(const typename E::storage* row, int j0, int j1,
+                                                uint4 (&raw)[kVecPerThread]) {
+  const int nvec = (j1 - j0 + E::kEPV - 1) / E::kEPV;
+  const uint4 ninf = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+#pragma unroll
+  for (int q = 0; q < kVecPerThread; ++q) {
+    const int vi = q * kThreads + (int)threadIdx.x;
+    raw[q] = vi < nvec ? fetch_vec<E, kVec>(row, j0 + vi * E::kEPV, j1) : ninf;
   }
 }
 
 template <typename E, bool kVec>
-__global__ void __launch_bounds__(kThreads) argmax_verify_kernel(const ArgmaxParams p) {
-  __shared__ float s_v[kWarps];
-  __shared__ int s_i[kWarps];
-  __shared__ int s_flag;
-  __shared__ unsigned long long s_key[kWarps];
+__global__ void __launch_bounds__(kThreads) chunk_stats_kernel(const SampleParams p) {
+  const int rows_per_seq = 2 * p.k + 1;
+  const int item = blockIdx.x;
+  const int row = item / p.nchunks, c = item - row * p.nchunks;
+  const int b = row / rows_per_seq, r = row - b * rows_per_seq;
+  const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+  uint4 raw[kVecPerThread];
+  load_chunk_regs<E, kVec>(seq_row_ptr<E>(p, b, r), j0, j1, raw);
+  asm volatile("griddepcontrol.launch_dependents;");
+  StatsState st;
+  stats_chunk<E>(raw, p.scale, st);
+  emit_stats_warp(p, st, row, c, c);
+}
+
+template <typename E, bool kVec>
+__global__ void __launch_bounds__(kThreads) chunk_argmax_kernel(const ArgmaxParams p) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int item = blockIdx.x;
+  const int row = item / p.nchunks, c = item - row * p.nchunks;
+  const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+  uint4 raw[kVecPerThread];
+  load_chunk_regs<E, kVec>(
+      reinterpret_cast<const typename E::storage*>(p.target) + (size_t)row * p.V, j0, j1, raw);
+  ArgState st;
+  argmax_chunk<E>(raw, j0, st);
+  emit_arg_warp(p, st, row, c, c);
+}
+
+// ---------------------------------------------------------------------------
+// Draw: residual / bonus inverse CDF
+// ---------------------------------------------------------------------------
+// Prefix structure of one chunk of draw weights, in vector (element) order:
+//   group  g[vi]  sequential float sum of vector vi's weights (2048 groups)
+//   quad   Q      double-float sum of groups 4Q..4Q+3, added to zero in order
+//   lane   l      double-float sum of quads 16l..16l+15, added in order
+//   chunk         inclusive double-float warp scan of the 32 lane values
+// draw_kernel builds it per chunk (group sums kept in the workspace, chunk
+// totals too); draw_resolve_kernel recomputes the lane and quad levels of the
+// chosen chunk with the same arithmetic and walks down to the token.
+struct DrawRows {
+  const void* t;  // target row
+  const void* d;  // draft row (residual only)
+  float nref_t, inv_t, nref_d, inv_d;
+};
+
+template <typename E>
+__device__ __forceinline__ DrawRows draw_rows(const SampleParams& p, int b, const DrawDesc& d) {
+  using S = typename E::storage;
+  DrawRows w;
+  w.t = reinterpret_cast<const S*>(p.target) + ((size_t)b * (p.k + 1) + d.n) * (size_t)p.V;
+  w.d = d.n < p.k
+            ? reinterpret_cast<const S*>(p.draft) + ((size_t)b * p.k + d.n) * (size_t)p.V
+            : nullptr;
+  w.nref_t = d.nref_t;
+  w.inv_t = d.inv_t;
+  w.nref_d = d.nref_d;
+  w.inv_d = d.inv_d;
+  return w;
+}
+
+// p of one target element, and the residual max(0, p - q) with the draft
+// element; explicit round-to-nearest intrinsics keep every evaluation
+// bit-identical wherever it is computed.
+__device__ __forceinline__ float draw_p(float zt, float s, const DrawRows& w) {
+  return __fmul_rn(ex2(__fmaf_rn(zt, s, w.nref_t)), w.inv_t);
+}
+__device__ __forceinline__ float draw_r(float pt, float zd, float s, const DrawRows& w) {
+  const float pd = __fmul_rn(ex2(__fmaf_rn(zd, s, w.nref_d)), w.inv_d);
+  return fmaxf(__fsub_rn(pt, pd), 0.0f);
+}
+// Weight of one element: the residual after a rejection, else p.
+__device__ __forceinline__ float draw_weight(float zt, float zd, float s, const DrawRows& w,
+                                             bool resid) {
+  const float pt = draw_p(zt, s, w);
+  return resid ? draw_r(pt, zd, s, w) : pt;
+}
+
+__device__ __forceinline__ FSum quad_sum(const float4& v) {
+  FSum a = FSum::zero();
+  a.add(v.x);
+  a.add(v.y);
+  a.add(v.z);
+  a.add(v.w);
+  return a;
+}
+
+// Chunk total from a group array (warp-collective, every lane gets it).
+__device__ __forceinline__ FSum chunk_total_warp(const float* g) {
+  const int lane = threadIdx.x & 31;
+  FSum acc = FSum::zero();
+  for (int qd = 0; qd < 16; ++qd)
+    acc = df_add(acc, quad_sum(*reinterpret_cast<const float4*>(g + (lane * 16 + qd) * 4)));
+  const FSum inc = warp_scan_df(acc);
+  FSum tot;
+  tot.hi = __shfl_sync(0xffffffffu, inc.hi, 31);
+  tot.lo = __shfl_sync(0xffffffffu, inc.lo, 31);
+  return tot;
+}
+
+// The sequences's rows are merged by every draw CTA of the sequence (one warp
+// per row), into shared memory, followed by the accept test: the CTA of chunk
+// 0 writes the outputs.  Limits: 2k+1 <= kMaxSeqRows.
+constexpr int kMaxSeqRows = 2 * 256 + 1;
+
+template <typename E, bool kVec>
+__global__ void __launch_bounds__(kThreads) draw_kernel(const SampleParams p) {
+  using St = typename E::storage;
+  __shared__ __align__(16) float s_g[kVecPerChunk];
+  __shared__ __align__(16) float s_gp[kVecPerChunk];
+  __shared__ RowStats s_rows[kMaxSeqRows];
+  __shared__ DrawDesc s_desc;
+
+  // wait for the statistics kernel's records (programmatic dependent launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
 
   const int item = blockIdx.x;
-  const int row = item / p.nchunks;
-  const int c = item - row * p.nchunks;
-  const int b = row / p.rows_per_seq;
-  const int j0 = c * E::kChunk;
-  const int j1 = min(p.V, j0 + E::kChunk);
-  const typename E::storage* rp =
-      reinterpret_cast<const typename E::storage*>(p.target) + (size_t)row * p.V;
-
-  float z[kVecPerThread][E::kEPV];
-  load_chunk<E, kVec>(rp, j0, j1, z);
-  float bv = -INFINITY;
-  int bi = 0x7FFFFFFF;
-#pragma unroll
-  for (int q = 0; q < kVecPerThread; ++q)
-#pragma unroll
-    for (int e = 0; e < E::kEPV; ++e)
-      if (z[q][e] > bv) {  // ascending index within the thread: strict keeps the lowest
-        bv = z[q][e];
-        bi = j0 + (q * kThreads + threadIdx.x) * E::kEPV + e;
-      }
-  warp_argmax(bv, bi);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) {
-    s_v[warp] = bv;
-    s_i[warp] = bi;
+  const int b = item / p.nchunks;
+  const int c = item - b * p.nchunks;
+  const int rows_per_seq = 2 * p.k + 1;
+  for (int r = threadIdx.x >> 5; r < rows_per_seq; r += kWarps)
+    finalize_stats_row<E>(p, b * rows_per_seq + r, &s_rows[r]);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const DrawDesc dd = resolve_sample_seq(p, b, s_rows, c == 0);
+    if (threadIdx.x == 0) s_desc = dd;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float v = s_v[0];
-    int i = s_i[0];
-    for (int w = 1; w < kWarps; ++w)
-      if (better(s_v[w], s_i[w], v, i)) {
-        v = s_v[w];
-        i = s_i[w];
-      }
-    ArgPartial ap;
-    ap.val = v;
-    ap.idx = i;
-    p.part[item] = ap;
+  const DrawDesc d = s_desc;
+  const bool resid = d.n < p.k;
+  const DrawRows w = draw_rows<E>(p, b, d);
+  const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+  const int nvec = (j1 - j0 + E::kEPV - 1) / E::kEPV;
+  const size_t gofs = (size_t)item * kVecPerChunk;
+
+  uint4 vt[kVecPerThread], vd[kVecPerThread];
+#pragma unroll
+  for (int q = 0; q < kVecPerThread; ++q) {
+    const int vi = q * kThreads + (int)threadIdx.x;
+    const int j = j0 + vi * E::kEPV;
+    vt[q] = vi < nvec ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1)
+                      : make_uint4(0, 0, 0, 0);
+    vd[q] = (resid && vi < nvec) ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
+                                 : make_uint4(0, 0, 0, 0);
   }
-
-  if (!arrive_last(&p.row_cnt[row], (unsigned)p.nchunks, &s_flag)) return;
-
-  if (warp == 0) {
-    float v = -INFINITY;
-    int i = 0x7FFFFFFF;
-    for (int cc = lane; cc < p.nchunks; cc += 32) {
-      const ArgPartial* pp = &p.part[(size_t)row * p.nchunks + cc];
-      const float v2 = __ldcg(&pp->val);
-      const int i2 = __ldcg(&pp->idx);
-      if (better(v2, i2, v, i)) {
-        v = v2;
-        i = i2;
+#pragma unroll
+  for (int q = 0; q < kVecPerThread; ++q) {
+    const int vi = q * kThreads + (int)threadIdx.x;
+    float g = 0.0f, gp = 0.0f;
+    if (vi < nvec) {
+#pragma unroll
+      for (int e = 0; e < E::kEPV; ++e) {
+        const float pt = draw_p(E::elem(vt[q], e), p.scale, w);
+        gp = __fadd_rn(gp, pt);
+        g = __fadd_rn(g, resid ? draw_r(pt, E::elem(vd[q], e), p.scale, w) : pt);
       }
     }
-    warp_argmax(v, i);
-    if (lane == 0) p.rowarg[row] = (i >= 0 && i < p.V) ? i : 0;
+    s_g[vi] = g;
+    p.gsum[gofs + vi] = g;
+    if (resid) {
+      s_gp[vi] = gp;
+      p.gsum_p[gofs + vi] = gp;
+    }
   }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const FSum t = chunk_total_warp(s_g);
+    if (threadIdx.x == 0) p.csum[item] = t;
+  } else if (resid && threadIdx.x < 64) {
+    const FSum t = chunk_total_warp(s_gp);
+    if (threadIdx.x == 32) p.csum_p[item] = t;
+  }
+}
 
-  if (!arrive_last(&p.seq_cnt[b], (unsigned)p.rows_per_seq, &s_flag)) return;
+// Inclusive double-float scan of the chunk totals by one warp; with a target,
+// also finds the first chunk whose inclusive prefix exceeds it (else the last
+// chunk with positive mass) and that chunk's exclusive prefix.  Returns the
+// (normalised) total.
+__device__ __forceinline__ FSum chunk_prefix(const FSum* cs, int C, const FSum* target,
+                                             int* cstar, FSum* base) {
+  const int lane = threadIdx.x & 31;
+  FSum carry = FSum::zero();
+  int found = -1, lastpos = -1;
+  FSum fbase = FSum::zero(), lbase = FSum::zero();
+  for (int c0 = 0; c0 < C; c0 += 32) {
+    const int c = c0 + lane;
+    FSum v = FSum::zero();
+    if (c < C) {
+      const float2 t = __ldcg(reinterpret_cast<const float2*>(cs + c));
+      v.hi = t.x;
+      v.lo = t.y;
+    }
+    const FSum inc = df_norm(df_add(carry, warp_scan_df(v)));
+    FSum excl;
+    excl.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
+    excl.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
+    if (lane == 0) excl = carry;
+    if (target) {
+      const unsigned hit = __ballot_sync(0xffffffffu, c < C && df_less(*target, inc));
+      if (found < 0 && hit) {
+        const int L = __ffs(hit) - 1;
+        found = c0 + L;
+        fbase.hi = __shfl_sync(0xffffffffu, excl.hi, L);
+        fbase.lo = __shfl_sync(0xffffffffu, excl.lo, L);
+      }
+      const unsigned pos = __ballot_sync(0xffffffffu, c < C && v.hi > 0.0f);
+      if (pos) {
+        const int L = 31 - __clz(pos);
+        lastpos = c0 + L;
+        lbase.hi = __shfl_sync(0xffffffffu, excl.hi, L);
+        lbase.lo = __shfl_sync(0xffffffffu, excl.lo, L);
+      }
+    }
+    carry.hi = __shfl_sync(0xffffffffu, inc.hi, 31);
+    carry.lo = __shfl_sync(0xffffffffu, inc.lo, 31);
+  }
+  if (target) {
+    if (found < 0) {
+      found = lastpos < 0 ? 0 : lastpos;
+      fbase = lastpos < 0 ? FSum::zero() : lbase;
+    }
+    *cstar = found;
+    *base = fbase;
+  }
+  return carry;
+}
 
-  if (p.tree)
-    resolve_tree(p, b, s_key);
-  else
-    resolve_chain(p, b);
+// One warp per sequence walks the prefix structure down to the token: chunk,
+// lane (16 quads), quad, vector, element.  Where rounding leaves the target
+// just past a level's end, the last position with positive weight is taken
+// (such a target lies within ~1e-15 of a boundary).
+template <typename E, bool kVec>
+__global__ void __launch_bounds__(kThreads) draw_resolve_kernel(const SampleParams p) {
+  using St = typename E::storage;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (b >= p.B) return;
+  const int C = p.nchunks;
+  const DrawDesc d = p.desc[b];
+  const DrawRows w = draw_rows<E>(p, b, d);
+  bool resid = d.n < p.k;
+  const FSum* cs = p.csum + (size_t)b * C;
+  const float* gs = p.gsum + (size_t)b * C * kVecPerChunk;
+  int cstar = 0;
+  FSum base = FSum::zero();
+  FSum total = chunk_prefix(cs, C, nullptr, &cstar, &base);
+  bool fallback = false;
+  if (resid && !(total.hi > 0.0f)) {
+    // the residual mass vanished in rounding: sample p of the rejected row
+    fallback = true;
+    resid = false;
+    cs = p.csum_p + (size_t)b * C;
+    gs = p.gsum_p + (size_t)b * C * kVecPerChunk;
+    total = chunk_prefix(cs, C, nullptr, &cstar, &base);
+    if (lane == 0) set_flag(p.flags, kFlagResidualFallback);
+  }
+  const FSum target = df_mul_f(p.u_sample[b], total);
+  chunk_prefix(cs, C, &target, &cstar, &base);
+  const int j0 = cstar * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+
+  // lane level: this lane's 16 quads (64 groups) of the chosen chunk
+  const float* gch = gs + (size_t)cstar * kVecPerChunk;
+  float4 g4[16];
+#pragma unroll
+  for (int qd = 0; qd < 16; ++qd)
+    g4[qd] = __ldcg(reinterpret_cast<const float4*>(gch + (lane * 16 + qd) * 4));
+  FSum acc = FSum::zero();
+#pragma unroll
+  for (int qd = 0; qd < 16; ++qd) acc = df_add(acc, quad_sum(g4[qd]));
+  const FSum inc = warp_scan_df(acc);
+  FSum exc;
+  exc.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
+  exc.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
+  if (lane == 0) exc = FSum::zero();
+  const unsigned hit = __ballot_sync(0xffffffffu, df_less(target, df_norm(df_add(base, inc))));
+  const unsigned pos = __ballot_sync(0xffffffffu, acc.hi > 0.0f);
+  const bool exact = hit != 0;
+  const int L = exact ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+
+  int tok = -1;
+  if (lane == L) {
+    FSum run = df_add(base, exc);
+    int lastv = -1;
+    for (int qd = 0; qd < 16 && tok < 0; ++qd) {
+      const FSum qs = quad_sum(g4[qd]);
+      const FSum nxt = df_add(run, qs);
+      const float gv[4] = {g4[qd].x, g4[qd].y, g4[qd].z, g4[qd].w};
+      if (exact && df_less(target, df_norm(nxt))) {
+        // the target lies in this quad: walk its groups, then the elements
+        FSum r2 = run;
+        for (int i = 0; i < 4 && tok < 0; ++i) {
+          if (!(gv[i] > 0.0f)) continue;
+          const int vi = (lane * 16 + qd) * 4 + i;
+          lastv = vi;
+          const FSum n2 = df_add(r2, df_from(gv[i]));
+          if (df_less(target, df_norm(n2))) {
+            const int j = j0 + vi * E::kEPV;
+            const uint4 vt = fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1);
+            const uint4 vd = resid
+                                 ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
+                                 : make_uint4(0, 0, 0, 0);
+            float part = 0.0f;
+            int lastpos = -1;
+#pragma unroll
+            for (int e = 0; e < E::kEPV; ++e) {
+              const float we =
+                  draw_weight(E::elem(vt, e), resid ? E::elem(vd, e) : 0.0f, p.scale, w, resid);
+              part = __fadd_rn(part, we);
+              if (we > 0.0f && j + e < j1) lastpos = j + e;
+              if (tok < 0 && we > 0.0f && df_less(target, df_norm(df_add(r2, df_from(part)))))
+                tok = j + e;
+            }
+            if (tok < 0) tok = lastpos;  // rounding inside the vector
+          }
+          r2 = n2;
+        }
+        break;
+      }
+      for (int i = 0; i < 4; ++i)
+        if (gv[i] > 0.0f) lastv = (lane * 16 + qd) * 4 + i;
+      run = nxt;
+    }
+    if (tok < 0 && lastv >= 0) {  // rounding: last positive element seen
+      const int j = j0 + lastv * E::kEPV;
+      const uint4 vt = fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1);
+      const uint4 vd = resid ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int e = 0; e < E::kEPV; ++e)
+        if (j + e < j1 &&
+            draw_weight(E::elem(vt, e), resid ? E::elem(vd, e) : 0.0f, p.scale, w, resid) > 0.0f)
+          tok = j + e;
+    }
+  }
+  tok = __shfl_sync(0xffffffffu, tok, L);
+  if (lane == 0) {
+    if (tok < 0 || tok >= p.V) tok = min(j0, p.V - 1);  // unreachable with finite inputs
+    p.out_tokens[(size_t)b * (p.k + 1) + d.n] = tok;
+    p.resid_mass[b] = (d.n < p.k && !fallback) ? __fadd_rn(total.hi, total.lo) : 0.0f;
+  }
 }
 
 }  // namespace sv

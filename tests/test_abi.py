@@ -62,7 +62,7 @@ def test_workspace_bytes(lib):
     assert ws(sv.SPEC_MODE_SAMPLE, 1, 4, 0, sv.SPEC_DTYPE_F32) == 0            # V < 1
     assert ws(sv.SPEC_MODE_SAMPLE, 1, 4, 10, 7) == 0                            # dtype
     assert ws(sv.SPEC_MODE_TREE_GREEDY, 1, 0, 10, 0) == 0                       # N < 1
-    assert ws(sv.SPEC_MODE_SAMPLE, 200000, 4, 10, 0) == 0                       # counters
+    assert ws(sv.SPEC_MODE_SAMPLE, 1 << 20, 1024, 1 << 26, 1) == 0              # index space
     assert ws(9, 1, 1, 10, 0) == 0
 
 

@@ -281,8 +281,9 @@ def test_workspace_reuse_across_shapes_and_modes():
         gg = gpu_greedy(c1, ws=big)
         og = oracle.verify_greedy(c1.target, c1.tokens, dtype="bf16")
         ph.compare_exact(gg, og, ["accepted_len", "out_tokens"])
-    # the counters are back at zero after every call
-    assert int(big[256:256 + 4 * 262144].view(torch.int32).abs().sum()) == 0
+    # garbage left in the workspace by other shapes does not leak into results
+    big[256:].fill_(0xA5)
+    sample_parity(c2, ws=big, allow_flags=0)
 
 
 def test_deterministic_and_side_stream():
@@ -299,6 +300,6 @@ def test_launch_count():
     c = synth.make_chain_case(B=2, k=2, V=100, dtype="f32", seed=0)
     n0 = sv.spec_verify_launch_count()
     gpu_sample(c)
-    assert sv.spec_verify_launch_count() - n0 == 2
-    gpu_greedy(c)
     assert sv.spec_verify_launch_count() - n0 == 3
+    gpu_greedy(c)
+    assert sv.spec_verify_launch_count() - n0 == 5
