@@ -60,7 +60,9 @@ typedef enum {
   SPEC_ERR_INVALID_ARG = 1, /* NULL pointer, size out of range, T <= 0 or NaN */
   SPEC_ERR_ALIGNMENT = 2,   /* pointer not aligned as documented */
   SPEC_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than required */
-  SPEC_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+  SPEC_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  SPEC_ERR_TOO_LARGE = 5    /* the call needs more scratch than the fixed
+                               array of spec_verify_greedy_noalloc holds */
 } spec_status_t;
 
 typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
@@ -181,6 +183,37 @@ SPEC_API spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_fl
 
 /* Number of kernels this library has launched in this process. */
 SPEC_API uint64_t spec_verify_launch_count(void);
+
+/*
+ * Greedy verification without any allocation (no counterpart in the pages:
+ * this is a deployment convenience, not part of the method).
+ *
+ * Same computation, arguments and outputs as spec_verify_greedy, minus the
+ * workspace: its scratch is a fixed array of SPEC_NOALLOC_SCRATCH_BYTES in
+ * the library's own device memory, resident on every GPU that loads the
+ * library until the process exits.  It is for callers that cannot allocate
+ * device memory at the point of the call: for example a plugin inside a
+ * serving framework that owns every device allocation, or a decode loop that
+ * must not allocate once it is running.  The library itself calls no
+ * cudaMalloc, cudaFree or other allocating routine on this path.
+ *
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture begins on the device.
+ *   - Calls whose scratch would exceed SPEC_NOALLOC_SCRATCH_BYTES return
+ *     SPEC_ERR_TOO_LARGE before anything is enqueued (B=64 sequences of k=4
+ *     drafts over V=128256 bf16 need about 0.66 MB).
+ *   - Every call uses the same array, which keeps what the previous call left
+ *     there.  Nothing the kernels read needs to start at zero; the flag word is
+ *     cleared on entry and device-side input errors are not reported.  Calls
+ *     that overlap on the GPU (different streams without ordering, or
+ *     concurrent host threads) race on the array: serialise them.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (4u << 20)
+SPEC_API spec_status_t spec_verify_greedy_noalloc(const void* target_logits, int dtype,
+                                                  const int32_t* draft_tokens, int B, int k, int V,
+                                                  int32_t* accepted_len, int32_t* out_tokens,
+                                                  void* stream);
 
 /* Static description of a status code. */
 SPEC_API const char* spec_status_string(int status);

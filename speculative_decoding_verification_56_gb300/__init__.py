@@ -30,6 +30,8 @@ SPEC_ERR_INVALID_ARG = 1
 SPEC_ERR_ALIGNMENT = 2
 SPEC_ERR_WORKSPACE = 3
 SPEC_ERR_CUDA = 4
+SPEC_ERR_TOO_LARGE = 5
+SPEC_NOALLOC_SCRATCH_BYTES = 4 << 20
 SPEC_DTYPE_F32 = 0
 SPEC_DTYPE_BF16 = 1
 SPEC_MODE_SAMPLE = 0
@@ -71,6 +73,8 @@ def load_library(path: str = LIB_PATH):
         lib.spec_verify_greedy.restype = I
         lib.spec_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, Z, P]
         lib.spec_verify_tree_greedy.restype = I
+        lib.spec_verify_greedy_noalloc.argtypes = [P, I, P, I, I, I, P, P, P]
+        lib.spec_verify_greedy_noalloc.restype = I
         lib.spec_verify_read_flags.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I, P]
         lib.spec_verify_read_flags.restype = I
         lib.spec_verify_launch_count.argtypes = []
@@ -200,6 +204,22 @@ def spec_verify_greedy(target_logits, draft_tokens, accepted_len, out_tokens, wo
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream_ptr(stream))
     _check(st, "spec_verify_greedy")
+
+
+def spec_verify_greedy_noalloc(target_logits, draft_tokens, accepted_len, out_tokens,
+                               stream=None):
+    """Greedy verification on the library's fixed device scratch (C ABI
+    ``spec_verify_greedy_noalloc``): for callers that cannot allocate device
+    memory when they verify.  Calls sharing the scratch must not overlap."""
+    torch = _torch()
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    st = load_library().spec_verify_greedy_noalloc(
+        _dev(target_logits, "target_logits"), _dtype_code(target_logits),
+        _dev(draft_tokens, "draft_tokens", torch.int32, optional=k == 0), B, k, V,
+        _dev(accepted_len, "accepted_len", torch.int32),
+        _dev(out_tokens, "out_tokens", torch.int32), _stream_ptr(stream))
+    _check(st, "spec_verify_greedy_noalloc")
 
 
 def spec_verify_tree_greedy(target_logits, node_tokens, parents, max_depth, accepted_len,

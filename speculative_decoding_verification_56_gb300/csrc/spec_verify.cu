@@ -185,6 +185,28 @@ spec_status_t run_argmax(sv::ArgmaxParams prm, int rows, bool vec, void* stream)
   return launch(sv::argmax_resolve_kernel, prm.B, 0, prm, stream, true);
 }
 
+// Scratch of spec_verify_greedy_noalloc: a fixed array in the library's own
+// device memory (one copy per device that loads the library).  Host code may
+// not use the symbol as an address; its device address is looked up once per
+// device with cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_addr[kMaxDevices] = {nullptr};
+std::mutex g_noalloc_mu;
+
+spec_status_t noalloc_scratch(void** addr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return SPEC_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -346,6 +368,30 @@ spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_flags, int 
   return SPEC_OK;
 }
 
+spec_status_t spec_verify_greedy_noalloc(const void* target_logits, int dtype,
+                                         const int32_t* draft_tokens, int B, int k, int V,
+                                         int32_t* accepted_len, int32_t* out_tokens, void* stream) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || k < 0 || k > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(SPEC_MODE_GREEDY, B, k, V, dtype, &L)) return SPEC_ERR_INVALID_ARG;
+  if (L.bytes > (size_t)SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_ERR_TOO_LARGE;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !accepted_len || !out_tokens || (k > 0 && !draft_tokens))
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned(target_logits, elem_bytes(dtype)) || !aligned(accepted_len, 4) ||
+      !aligned(out_tokens, 4) || (k > 0 && !aligned(draft_tokens, 4)))
+    return SPEC_ERR_ALIGNMENT;
+  void* scratch = nullptr;
+  const spec_status_t st = noalloc_scratch(&scratch);
+  if (st != SPEC_OK) return st;
+  // the flag word starts clear on every call (nothing else needs zeroing)
+  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), (cudaStream_t)stream) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return spec_verify_greedy(target_logits, dtype, draft_tokens, B, k, V, accepted_len, out_tokens,
+                            scratch, (size_t)SPEC_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 uint64_t spec_verify_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* spec_status_string(int status) {
@@ -355,6 +401,7 @@ const char* spec_status_string(int status) {
     case SPEC_ERR_ALIGNMENT: return "misaligned pointer";
     case SPEC_ERR_WORKSPACE: return "workspace missing or too small";
     case SPEC_ERR_CUDA: return "CUDA error";
+    case SPEC_ERR_TOO_LARGE: return "call exceeds the fixed no-allocation scratch";
     default: return "unknown status";
   }
 }

@@ -116,6 +116,14 @@ def test_greedy_and_tree_host_validation(lib):
     assert t(*bad) == 2
 
 
+def test_noalloc_host_validation(lib):
+    f = lib.spec_verify_greedy_noalloc
+    assert f(None, 1, FAKE, 4, 3, 100, FAKE, FAKE, None) == 1
+    assert f(FAKE, 9, FAKE, 4, 3, 100, FAKE, FAKE, None) == 1
+    assert f(FAKE, 1, FAKE, 0, 3, 100, FAKE, FAKE, None) == 0          # B = 0: no work
+    assert f(FAKE, 1, FAKE, 4096, 8, 1 << 20, FAKE, FAKE, None) == 5   # beyond the scratch
+
+
 def test_read_flags_validation(lib):
     v = ctypes.c_uint32(0)
     assert lib.spec_verify_read_flags(None, ctypes.byref(v), 0, None) == 1
