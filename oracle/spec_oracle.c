@@ -114,8 +114,9 @@ static int inverse_cdf(const double* w, int V, double u, double* total_out,
  * take one extra target token when all are accepted) and "Does Using a Small
  * Model's Answer Reduce Quality?" (eq. A(x) = min(1, p(x)/q(x)); eq.
  * p_residual(x) = norm(max(0, p(x) - q(x))));  [MATH] "Vanilla speculative
- * decoding" (accept w.p. min(1, p/q), resample from (p - q)_+, the +1 bonus
- * token);  [WIKI] "The mechanism" (normalized residual max(0, p - q)).
+ * decoding" (acceptance ratio, resampling from the positive part of p - q, the
+ * extra target token in the expected count);  [WIKI] "The mechanism" (the
+ * resample draws from the renormalised positive part of p - q).
  *
  * Layouts: target [B, k+1, V], draft [B, k, V] (fp32 or bf16 bits), tokens
  * int32 [B, k], u_accept float [B, k], u_sample float [B].
@@ -232,7 +233,7 @@ static int argmax_row(const void* base, int dtype, size_t off, int V, int* err) 
  * Greedy verification.  [REVIEW] "Does Using a Small Model's Answer Reduce
  * Quality?" (greedy: accept if the proposal equals the target's argmax,
  * otherwise use the target token and discard the rest) and "The Complete
- * EAGLE-3 Inference Process" step 4 (accept the longest prefix matching target
+ * EAGLE-3 Inference Process" step 4 (keep the longest prefix that agrees with the target's
  * choices).  target [B, k+1, V]; tokens [B, k].  Outputs accepted_len [B],
  * out_tokens [B, k+1] (x_0..x_{n-1}, argmax of row n, rest -1) and, if not
  * NULL, argmax_out [B, k+1] (argmax of every target row).
