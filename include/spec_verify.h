@@ -122,8 +122,10 @@ SPEC_API size_t spec_verify_workspace_bytes(int mode, int B, int k_or_N, int V, 
  *   resid_mass    float [B]       R = sum_j max(0, p_n - q_n) when n < k, else 0
  * With k = 0, draft_logits, draft_tokens, u_accept, p_out and q_out may be
  * NULL and the call samples one token from softmax(target[b,0,:] / T).
- * Launches three kernels: softmax statistics; row merge + accept test +
- * residual/bonus prefix sums; the inverse-CDF walk.
+ * Launches two kernels: the softmax statistics, then one thread-block cluster
+ * per sequence for row merge, accept test, residual/bonus prefix sums and the
+ * inverse-CDF walk (three kernels when a row spans more than 16 32-KB chunks:
+ * V > 262144 bf16 or 131072 fp32).
  */
 SPEC_API spec_status_t spec_verify_sample(const void* target_logits, const void* draft_logits,
                                  int dtype, const int32_t* draft_tokens,
@@ -180,6 +182,15 @@ SPEC_API spec_status_t spec_verify_tree_greedy(const void* target_logits, int dt
  */
 SPEC_API spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_flags, int clear,
                                      void* stream);
+
+/*
+ * Self-test of the two 2^x evaluations the kernels use (no counterpart in the
+ * pages): y_fma[i] = the FMA-pipe polynomial (Cody-Waite reduction, degree-5
+ * minimax; relative error below 2e-7 for -126 <= x <= 0.5), y_sfu[i] = the
+ * special-function unit's ex2.approx.ftz.  x, y_fma, y_sfu: device float [n].
+ */
+SPEC_API spec_status_t spec_verify_selftest_exp2(const float* x, float* y_fma, float* y_sfu,
+                                                 int n, void* stream);
 
 /* Number of kernels this library has launched in this process. */
 SPEC_API uint64_t spec_verify_launch_count(void);

@@ -75,6 +75,8 @@ def load_library(path: str = LIB_PATH):
         lib.spec_verify_tree_greedy.restype = I
         lib.spec_verify_greedy_noalloc.argtypes = [P, I, P, I, I, I, P, P, P]
         lib.spec_verify_greedy_noalloc.restype = I
+        lib.spec_verify_selftest_exp2.argtypes = [P, P, P, I, P]
+        lib.spec_verify_selftest_exp2.restype = I
         lib.spec_verify_read_flags.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I, P]
         lib.spec_verify_read_flags.restype = I
         lib.spec_verify_launch_count.argtypes = []

@@ -59,13 +59,13 @@ bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
   } else {
     return false;
   }
-  if (rows * C * sv::kWarps > 0x7FFFFFFFLL) return false;
+  if (rows * C > 0x7FFFFFFFLL || (long long)B * C * sv::kVecPerChunk > 0x7FFFFFFFLL) return false;
   L->rows = (int)rows;
   L->nchunks = C;
   size_t off = kDataOffset;
   if (mode == SPEC_MODE_SAMPLE) {
     L->off_part = off;
-    off = align_up(off + (size_t)rows * C * sv::kWarps * sizeof(sv::SoftmaxPartial));
+    off = align_up(off + (size_t)rows * C * sizeof(sv::SoftmaxPartial));
     L->off_desc = off;
     off = align_up(off + (size_t)B * sizeof(sv::DrawDesc));
     const size_t bc = (size_t)B * C;
@@ -79,7 +79,7 @@ bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
     off = align_up(off + bc * sv::kVecPerChunk * sizeof(float));
   } else {
     L->off_part = off;
-    off = align_up(off + (size_t)rows * C * sv::kWarps * sizeof(sv::ArgPartial));
+    off = align_up(off + (size_t)rows * C * sizeof(sv::ArgPartial));
     L->off_arg = off;
     off = align_up(off + (size_t)rows * sizeof(int32_t));
   }
@@ -96,20 +96,29 @@ bool vec_ok(const void* p, int V, int dtype) {
 
 template <typename KernelT, typename ParamT>
 spec_status_t launch(KernelT kernel, int grid, size_t smem, const ParamT& prm, void* stream,
-                     bool pdl) {
+                     bool pdl, int cluster = 1) {
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(sv::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
   if (pdl) {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
   }
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -144,6 +153,36 @@ spec_status_t persistent_grid(int items, int* grid) {
   return SPEC_OK;
 }
 
+// Dynamic shared-memory opt-in for a kernel, once per device.
+template <auto kernel>
+spec_status_t ensure_smem(size_t bytes) {
+  static bool done[kMaxDevices] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_shape_mu);
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+      return SPEC_ERR_CUDA;
+    done[dev] = true;
+  }
+  return SPEC_OK;
+}
+
+template <typename E, bool kVec>
+spec_status_t run_finish(const sv::SampleParams& prm, void* stream) {
+  if (prm.nchunks <= sv::kClusterMaxChunks) {
+    const spec_status_t st = ensure_smem<sv::sample_finish_kernel<E, kVec>>(sv::kFinishSmem);
+    if (st != SPEC_OK) return st;
+    return launch(sv::sample_finish_kernel<E, kVec>, prm.B * sv::kClusterCTAs, sv::kFinishSmem,
+                  prm, stream, true, sv::kClusterCTAs);
+  }
+  const spec_status_t st =
+      launch(sv::draw_kernel<E, kVec>, prm.B * prm.nchunks, 0, prm, stream, true);
+  if (st != SPEC_OK) return st;
+  return launch(sv::draw_resolve_kernel<E, kVec>, prm.B, 0, prm, stream, true);
+}
+
 template <typename E>
 spec_status_t run_sample(sv::SampleParams prm, int rows, bool vec, void* stream) {
   prm.items = rows * prm.nchunks;
@@ -157,15 +196,7 @@ spec_status_t run_sample(sv::SampleParams prm, int rows, bool vec, void* stream)
     st = launch(sv::chunk_stats_kernel<E, false>, prm.items, 0, prm, stream, false);
   }
   if (st != SPEC_OK) return st;
-  const int resolve_grid = (prm.B + sv::kWarps - 1) / sv::kWarps;
-  if (vec) {
-    st = launch(sv::draw_kernel<E, true>, prm.B * prm.nchunks, 0, prm, stream, true);
-    if (st != SPEC_OK) return st;
-    return launch(sv::draw_resolve_kernel<E, true>, resolve_grid, 0, prm, stream, true);
-  }
-  st = launch(sv::draw_kernel<E, false>, prm.B * prm.nchunks, 0, prm, stream, true);
-  if (st != SPEC_OK) return st;
-  return launch(sv::draw_resolve_kernel<E, false>, resolve_grid, 0, prm, stream, true);
+  return vec ? run_finish<E, true>(prm, stream) : run_finish<E, false>(prm, stream);
 }
 
 template <typename E>
@@ -390,6 +421,16 @@ spec_status_t spec_verify_greedy_noalloc(const void* target_logits, int dtype,
     return SPEC_ERR_CUDA;
   return spec_verify_greedy(target_logits, dtype, draft_tokens, B, k, V, accepted_len, out_tokens,
                             scratch, (size_t)SPEC_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+spec_status_t spec_verify_selftest_exp2(const float* x, float* y_fma, float* y_sfu, int n,
+                                        void* stream) {
+  if (n < 0 || (n > 0 && (!x || !y_fma || !y_sfu))) return SPEC_ERR_INVALID_ARG;
+  if (n == 0) return SPEC_OK;
+  sv::selftest_exp2_kernel<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(x, y_fma, y_sfu, n);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return SPEC_OK;
 }
 
 uint64_t spec_verify_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

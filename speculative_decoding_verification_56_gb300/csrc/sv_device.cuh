@@ -227,6 +227,27 @@ __device__ __forceinline__ bool arrive_last(unsigned* counter, unsigned n, unsig
 
 __device__ __forceinline__ void set_flag(unsigned* flags, unsigned bit) { atomicOr(flags, bit); }
 
+// 2^x on the FMA pipe, for x <= 0.5: Cody-Waite reduction x = n + f with
+// n = round(x) (the 1.5 * 2^23 shifter), f in [-1/2, 1/2], then a degree-5
+// minimax polynomial for 2^f (relative error below 2e-7; coefficients from
+// fit_exp2_poly.py) and n added to the exponent field.  Inputs below -126
+// are clamped, giving at most 2^-125.5 where 2^x would underflow.
+__device__ __forceinline__ float exp2_fma(float x) {
+  x = fmaxf(x, -126.0f);
+  const float shifter = 12582912.0f;  // 1.5 * 2^23
+  const float t = __fadd_rn(x, shifter);
+  const float n = __fsub_rn(t, shifter);
+  const float f = __fsub_rn(x, n);
+  float q = 1.3276472454890609e-3f;
+  q = __fmaf_rn(q, f, 9.675540961325169e-3f);
+  q = __fmaf_rn(q, f, 5.550713092088699e-2f);
+  q = __fmaf_rn(q, f, 2.4022120237350464e-1f);
+  q = __fmaf_rn(q, f, 6.931469440460205e-1f);
+  q = __fmaf_rn(q, f, 1.0000001192092896f);
+  const int ni = __float_as_int(t) - 0x4B400000;  // round(x) as an integer
+  return __int_as_float(__float_as_int(q) + (ni << 23));
+}
+
 // Packed pairs of floats (f32x2) for the FMA pipe's two-wide instructions.
 __device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
   unsigned long long r;

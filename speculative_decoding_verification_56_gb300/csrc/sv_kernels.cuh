@@ -27,6 +27,8 @@
 // between threads, segments and rows an exact power of two.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "sv_device.cuh"
 
 namespace sv {
@@ -35,10 +37,11 @@ namespace sv {
 // Workspace records
 // ---------------------------------------------------------------------------
 // Segment records: a segment is a run of consecutive chunks of one row handled
-// by one CTA.  Each WARP of that CTA writes its own record for the segment in
-// slot (row, first chunk, warp) with nch = the segment's chunk count, and
-// nch = 0 in the slots (row, other chunks of the segment, warp); so every slot
-// is written on every call and no CTA barrier is needed to publish a result.
+// by one CTA.  The CTA writes one record in slot (row, first chunk) with nch =
+// the segment's chunk count, and nch = 0 in the slots of its other chunks, so
+// every slot is written on every call.  Within the CTA, each warp parks its
+// partial in shared memory and the last warp to arrive combines them (no CTA
+// barrier; see SegSlots).
 struct SoftmaxPartial {
   int ref;
   int nch;
@@ -80,7 +83,7 @@ struct SampleParams {
   float* resid_mass;
   // workspace
   unsigned* flags;
-  SoftmaxPartial* part;  // [B*(2k+1) * nchunks * kWarps]
+  SoftmaxPartial* part;  // [B*(2k+1) * nchunks]
   DrawDesc* desc;        // [B]
   // draw prefix structure per (sequence, chunk): group sums and chunk
   // totals; the _p arrays hold p-only weights of a rejected row (used when
@@ -102,7 +105,7 @@ struct ArgmaxParams {
   int32_t* out_tokens;  // chain: [B, k+1]; tree: [B, max_depth+1]
   int32_t* path_nodes;  // tree: [B, max_depth+1]
   unsigned* flags;
-  ArgPartial* part;   // [B*rows_per_seq * nchunks * kWarps]
+  ArgPartial* part;   // [B*rows_per_seq * nchunks]
   int32_t* rowarg;    // [B*rows_per_seq]
 };
 
@@ -231,40 +234,94 @@ __device__ __forceinline__ void argmax_chunk(const uint4 (&raw)[kVecPerThread], 
 }
 
 // ---------------------------------------------------------------------------
-// Segment records (per warp, no barrier)
+// Segment records: per-warp partials combined by the last warp to arrive
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void emit_stats_warp(const SampleParams& p, const StatsState& st,
-                                                int row, int c_first, int c_last) {
+// Four slots per CTA: in the streaming loop no warp runs more than kStages
+// (= 3) items ahead of the slowest, so at most four segments are open at once.
+constexpr int kSegSlots = 4;
+struct StatsSlot {
+  int ref;
+  float hi, lo;
+  int pad;
+};
+struct ArgSlot {
+  float val;
+  int idx;
+};
+struct SegSlots {
+  int cnt[kSegSlots];
+  StatsSlot st[kSegSlots][kWarps];
+  ArgSlot am[kSegSlots][kWarps];
+};
+
+__device__ __forceinline__ void seg_slots_init(SegSlots& ss) {
+  if (threadIdx.x < kSegSlots) ss.cnt[threadIdx.x] = 0;
+}
+
+// Park this warp's partial in `slot`; returns (to the whole warp) whether it
+// arrived last, in which case the other warps' partials are visible to it.
+__device__ __forceinline__ bool seg_arrive(SegSlots& ss, int slot) {
+  const int lane = threadIdx.x & 31;
+  int last = 0;
+  if (lane == 0) {
+    __threadfence_block();
+    last = atomicAdd(&ss.cnt[slot], 1) == kWarps - 1;
+    if (last) {
+      __threadfence_block();
+      ss.cnt[slot] = 0;  // no warp can reach this slot's next use yet
+    }
+  }
+  return __shfl_sync(0xffffffffu, last, 0) != 0;
+}
+
+__device__ __forceinline__ void emit_stats_seg(const SampleParams& p, const StatsState& st,
+                                               int row, int c_first, int c_last, SegSlots& ss,
+                                               int& seg) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int slot = seg++ & (kSegSlots - 1);
   const int wref = warp_max_i(st.ref);
   FSum mine = st.acc;
   mine.scale(pow2i_f(st.ref - wref));
   const FSum wsum = warp_sum_df(mine);
+  if (lane == 0) ss.st[slot][warp] = StatsSlot{wref, wsum.hi, wsum.lo, 0};
+  if (!seg_arrive(ss, slot)) return;
+  StatsSlot v = lane < kWarps ? ss.st[slot][lane] : StatsSlot{kRefEmpty, 0.0f, 0.0f, 0};
+  const int R = warp_max_i(v.ref);
+  FSum f;
+  f.hi = v.hi;
+  f.lo = v.lo;
+  f.scale(pow2i_f(v.ref - R));
+  const FSum tot = warp_sum_df(f);
   const int n = c_last - c_first + 1;
   for (int i = lane; i < n; i += 32) {
     SoftmaxPartial sp;
-    sp.ref = wref;
+    sp.ref = R;
     sp.nch = i == 0 ? n : 0;
-    sp.hi = i == 0 ? wsum.hi : 0.0f;
-    sp.lo = i == 0 ? wsum.lo : 0.0f;
-    p.part[((size_t)row * p.nchunks + c_first + i) * kWarps + warp] = sp;
+    sp.hi = i == 0 ? tot.hi : 0.0f;
+    sp.lo = i == 0 ? tot.lo : 0.0f;
+    p.part[(size_t)row * p.nchunks + c_first + i] = sp;
   }
 }
 
-__device__ __forceinline__ void emit_arg_warp(const ArgmaxParams& p, const ArgState& st, int row,
-                                              int c_first, int c_last) {
+__device__ __forceinline__ void emit_arg_seg(const ArgmaxParams& p, const ArgState& st, int row,
+                                             int c_first, int c_last, SegSlots& ss, int& seg) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int slot = seg++ & (kSegSlots - 1);
   float v = st.v;
   int i = st.i;
   warp_argmax(v, i);
+  if (lane == 0) ss.am[slot][warp] = ArgSlot{v, i};
+  if (!seg_arrive(ss, slot)) return;
+  ArgSlot a = lane < kWarps ? ss.am[slot][lane] : ArgSlot{-INFINITY, 0x7FFFFFFF};
+  warp_argmax(a.val, a.idx);
   const int n = c_last - c_first + 1;
   for (int t = lane; t < n; t += 32) {
     ArgPartial ap;
-    ap.val = v;
-    ap.idx = i;
+    ap.val = a.val;
+    ap.idx = a.idx;
     ap.nch = t == 0 ? n : 0;
     ap.pad = 0;
-    p.part[((size_t)row * p.nchunks + c_first + t) * kWarps + warp] = ap;
+    p.part[(size_t)row * p.nchunks + c_first + t] = ap;
   }
 }
 
@@ -287,8 +344,8 @@ __device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out
   const int lane = threadIdx.x & 31;
   const int rows_per_seq = 2 * p.k + 1;
   const int b = row / rows_per_seq, r = row - b * rows_per_seq;
-  const SoftmaxPartial* pr = p.part + (size_t)row * p.nchunks * kWarps;
-  const int nrec = p.nchunks * kWarps;
+  const SoftmaxPartial* pr = p.part + (size_t)row * p.nchunks;
+  const int nrec = p.nchunks;
   // the token's logit is fetched alongside the records
   float zx = 0.0f;
   int x = -1;
@@ -346,8 +403,8 @@ __device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out
 // from the sequence's merged rows `rs` (index r of rows_per_seq).  Returns the
 // draw descriptor; with `write`, also stores the call's outputs for b (all
 // but the drawn token) and the descriptor.
-__device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, const RowStats* rs,
-                                       bool write) {
+template <typename RowFn>
+__device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, RowFn rs, bool write) {
   const int lane = threadIdx.x & 31;
   const int k = p.k;
   int n = k;
@@ -355,8 +412,8 @@ __device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, const RowSt
     const int i = i0 + lane;
     bool rej = false;
     if (i < k) {
-      const double pi = rs[i].prob;
-      const double qi = rs[k + 1 + i].prob;
+      const double pi = rs(i).prob;
+      const double qi = rs(k + 1 + i).prob;
       if (write) {
         p.p_out[(size_t)b * k + i] = (float)pi;
         p.q_out[(size_t)b * k + i] = (float)qi;
@@ -368,11 +425,17 @@ __device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, const RowSt
     if (n == k && m) n = i0 + __ffs(m) - 1;
   }
   DrawDesc d;
+  const RowStats rt = rs(n);
   d.n = n;
-  d.nref_t = -(float)rs[n].ref;
-  d.inv_t = rs[n].inv_sum;
-  d.nref_d = n < k ? -(float)rs[k + 1 + n].ref : 0.0f;
-  d.inv_d = n < k ? rs[k + 1 + n].inv_sum : 0.0f;
+  d.nref_t = -(float)rt.ref;
+  d.inv_t = rt.inv_sum;
+  d.nref_d = 0.0f;
+  d.inv_d = 0.0f;
+  if (n < k) {
+    const RowStats rd = rs(k + 1 + n);
+    d.nref_d = -(float)rd.ref;
+    d.inv_d = rd.inv_sum;
+  }
   d.pad[0] = d.pad[1] = d.pad[2] = 0;
   if (write) {
     for (int i = lane; i <= k; i += 32)
@@ -391,7 +454,7 @@ __device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, const RowSt
 __device__ void finalize_arg_rows4(const ArgmaxParams& p, int b, int r0, int stride, int nrows,
                                    int (&g)[4]) {
   const int lane = threadIdx.x & 31;
-  const int nrec = p.nchunks * kWarps;
+  const int nrec = p.nchunks;
   float v[4];
   int i[4];
 #pragma unroll
@@ -649,6 +712,7 @@ template <typename E>
 __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleParams p) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ Ring ring;
+  __shared__ SegSlots ss;
   using S = typename E::storage;
 
   int i0, i1;
@@ -669,9 +733,11 @@ __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleP
              &ring.full[slot]);
   };
 
+  seg_slots_init(ss);
   int issued = ring_init(ring, i0, i1, issue);
 
   StatsState st;
+  int seg = 0;
   int row = i0 / C, c = i0 - row * C, c_first = c;
   int slot = 0;
   unsigned par = 0;
@@ -684,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleP
     if (ok) stats_chunk<E>(raw, p.scale, st);
     const bool row_end = (c + 1 == C);
     if (row_end || it + 1 == i1) {
-      emit_stats_warp(p, st, row, c_first, c);
+      emit_stats_seg(p, st, row, c_first, c, ss, seg);
       st = StatsState();
       c_first = 0;
     }
@@ -706,6 +772,7 @@ template <typename E>
 __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const ArgmaxParams p) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ Ring ring;
+  __shared__ SegSlots ss;
   using S = typename E::storage;
 
   int i0, i1;
@@ -724,9 +791,11 @@ __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const Argmax
              &ring.full[slot]);
   };
 
+  seg_slots_init(ss);
   int issued = ring_init(ring, i0, i1, issue);
 
   ArgState st;
+  int seg = 0;
   int row = i0 / C, c = i0 - row * C, c_first = c;
   int slot = 0;
   unsigned par = 0;
@@ -739,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const Argmax
     if (ok) argmax_chunk<E>(raw, j0, st);
     const bool row_end = (c + 1 == C);
     if (row_end || it + 1 == i1) {
-      emit_arg_warp(p, st, row, c_first, c);
+      emit_arg_seg(p, st, row, c_first, c, ss, seg);
       st = ArgState();
       c_first = 0;
     }
@@ -774,6 +843,10 @@ __device__ __forceinline__ void load_chunk_regs(const typename E::storage* row, 
 
 template <typename E, bool kVec>
 __global__ void __launch_bounds__(kThreads) chunk_stats_kernel(const SampleParams p) {
+  __shared__ SegSlots ss;
+  seg_slots_init(ss);
+  __syncthreads();
+  int seg = 0;
   const int rows_per_seq = 2 * p.k + 1;
   const int item = blockIdx.x;
   const int row = item / p.nchunks, c = item - row * p.nchunks;
@@ -784,11 +857,15 @@ __global__ void __launch_bounds__(kThreads) chunk_stats_kernel(const SampleParam
   asm volatile("griddepcontrol.launch_dependents;");
   StatsState st;
   stats_chunk<E>(raw, p.scale, st);
-  emit_stats_warp(p, st, row, c, c);
+  emit_stats_seg(p, st, row, c, c, ss, seg);
 }
 
 template <typename E, bool kVec>
 __global__ void __launch_bounds__(kThreads) chunk_argmax_kernel(const ArgmaxParams p) {
+  __shared__ SegSlots ss;
+  seg_slots_init(ss);
+  __syncthreads();
+  int seg = 0;
   asm volatile("griddepcontrol.launch_dependents;");
   const int item = blockIdx.x;
   const int row = item / p.nchunks, c = item - row * p.nchunks;
@@ -798,7 +875,7 @@ __global__ void __launch_bounds__(kThreads) chunk_argmax_kernel(const ArgmaxPara
       reinterpret_cast<const typename E::storage*>(p.target) + (size_t)row * p.V, j0, j1, raw);
   ArgState st;
   argmax_chunk<E>(raw, j0, st);
-  emit_arg_warp(p, st, row, c, c);
+  emit_arg_seg(p, st, row, c, c, ss, seg);
 }
 
 // ---------------------------------------------------------------------------
@@ -806,11 +883,12 @@ __global__ void __launch_bounds__(kThreads) chunk_argmax_kernel(const ArgmaxPara
 // ---------------------------------------------------------------------------
 // Prefix structure of one chunk of draw weights, in vector (element) order:
 //   group  g[vi]  sequential float sum of vector vi's weights (2048 groups)
-//   quad   Q      double-float sum of groups 4Q..4Q+3, added to zero in order
-//   lane   l      double-float sum of quads 16l..16l+15, added in order
-//   chunk         inclusive double-float warp scan of the 32 lane values
-// draw_kernel builds it per chunk (group sums kept in the workspace, chunk
-// totals too); draw_resolve_kernel recomputes the lane and quad levels of the
+//   quad   Q      double-float sum of groups 4Q..4Q+3 added to zero in order;
+//                 quad Q belongs to thread Q of a 512-thread CTA
+//   warp   w      inclusive double-float warp scan of quads 32w..32w+31
+//   chunk         the 16 warp totals added in order
+// draw_kernel builds it per chunk (group sums and chunk totals kept in the
+// workspace); draw_resolve_kernel rebuilds the quad and warp levels of the
 // chosen chunk with the same arithmetic and walks down to the token.
 struct DrawRows {
   const void* t;  // target row
@@ -834,20 +912,26 @@ __device__ __forceinline__ DrawRows draw_rows(const SampleParams& p, int b, cons
 }
 
 // p of one target element, and the residual max(0, p - q) with the draft
-// element; explicit round-to-nearest intrinsics keep every evaluation
-// bit-identical wherever it is computed.
-__device__ __forceinline__ float draw_p(float zt, float s, const DrawRows& w) {
-  return __fmul_rn(ex2(__fmaf_rn(zt, s, w.nref_t)), w.inv_t);
+// element.  Element e of a vector takes 2^x on the FMA pipe when e <
+// kDrawPoly, else on the special-function unit (this pass is bound by the
+// latter); explicit round-to-nearest intrinsics keep every evaluation of an
+// element bit-identical wherever it is computed.
+constexpr int kDrawPoly = 2;
+__device__ __forceinline__ float draw_exp2(float x, int e) {
+  return e < kDrawPoly ? exp2_fma(x) : ex2(x);
 }
-__device__ __forceinline__ float draw_r(float pt, float zd, float s, const DrawRows& w) {
-  const float pd = __fmul_rn(ex2(__fmaf_rn(zd, s, w.nref_d)), w.inv_d);
+__device__ __forceinline__ float draw_p(float zt, float s, const DrawRows& w, int e) {
+  return __fmul_rn(draw_exp2(__fmaf_rn(zt, s, w.nref_t), e), w.inv_t);
+}
+__device__ __forceinline__ float draw_r(float pt, float zd, float s, const DrawRows& w, int e) {
+  const float pd = __fmul_rn(draw_exp2(__fmaf_rn(zd, s, w.nref_d), e), w.inv_d);
   return fmaxf(__fsub_rn(pt, pd), 0.0f);
 }
-// Weight of one element: the residual after a rejection, else p.
+// Weight of element e: the residual after a rejection, else p.
 __device__ __forceinline__ float draw_weight(float zt, float zd, float s, const DrawRows& w,
-                                             bool resid) {
-  const float pt = draw_p(zt, s, w);
-  return resid ? draw_r(pt, zd, s, w) : pt;
+                                             bool resid, int e) {
+  const float pt = draw_p(zt, s, w, e);
+  return resid ? draw_r(pt, zd, s, w, e) : pt;
 }
 
 __device__ __forceinline__ FSum quad_sum(const float4& v) {
@@ -859,17 +943,21 @@ __device__ __forceinline__ FSum quad_sum(const float4& v) {
   return a;
 }
 
-// Chunk total from a group array (warp-collective, every lane gets it).
-__device__ __forceinline__ FSum chunk_total_warp(const float* g) {
-  const int lane = threadIdx.x & 31;
-  FSum acc = FSum::zero();
-  for (int qd = 0; qd < 16; ++qd)
-    acc = df_add(acc, quad_sum(*reinterpret_cast<const float4*>(g + (lane * 16 + qd) * 4)));
-  const FSum inc = warp_scan_df(acc);
-  FSum tot;
-  tot.hi = __shfl_sync(0xffffffffu, inc.hi, 31);
-  tot.lo = __shfl_sync(0xffffffffu, inc.lo, 31);
-  return tot;
+// Quad scan of one chunk's group array held in shared memory (512 threads):
+// every thread gets its quad's inclusive scan within its warp; warp totals go
+// to s_w; thread 0 returns the chunk total (the warp totals added in order).
+__device__ __forceinline__ FSum chunk_scan_cta(const float* s_g, FSum* s_w, FSum* my_inc,
+                                               FSum* my_quad) {
+  const FSum q = quad_sum(*reinterpret_cast<const float4*>(s_g + 4 * threadIdx.x));
+  const FSum inc = warp_scan_df(q);
+  if ((threadIdx.x & 31) == 31) s_w[threadIdx.x >> 5] = inc;
+  *my_inc = inc;
+  *my_quad = q;
+  __syncthreads();
+  FSum t = s_w[0];
+  if (threadIdx.x == 0)
+    for (int i = 1; i < kWarps; ++i) t = df_add(t, s_w[i]);
+  return t;
 }
 
 // The sequences's rows are merged by every draw CTA of the sequence (one warp
@@ -884,6 +972,7 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleParams p) {
   __shared__ __align__(16) float s_gp[kVecPerChunk];
   __shared__ RowStats s_rows[kMaxSeqRows];
   __shared__ DrawDesc s_desc;
+  __shared__ FSum s_w[kWarps];
 
   // wait for the statistics kernel's records (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -897,7 +986,8 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleParams p) {
     finalize_stats_row<E>(p, b * rows_per_seq + r, &s_rows[r]);
   __syncthreads();
   if (threadIdx.x < 32) {
-    const DrawDesc dd = resolve_sample_seq(p, b, s_rows, c == 0);
+    const DrawDesc dd =
+        resolve_sample_seq(p, b, [&](int r) { return s_rows[r]; }, c == 0);
     if (threadIdx.x == 0) s_desc = dd;
   }
   __syncthreads();
@@ -925,9 +1015,9 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleParams p) {
     if (vi < nvec) {
 #pragma unroll
       for (int e = 0; e < E::kEPV; ++e) {
-        const float pt = draw_p(E::elem(vt[q], e), p.scale, w);
+        const float pt = draw_p(E::elem(vt[q], e), p.scale, w, e);
         gp = __fadd_rn(gp, pt);
-        g = __fadd_rn(g, resid ? draw_r(pt, E::elem(vd[q], e), p.scale, w) : pt);
+        g = __fadd_rn(g, resid ? draw_r(pt, E::elem(vd[q], e), p.scale, w, e) : pt);
       }
     }
     s_g[vi] = g;
@@ -938,12 +1028,16 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleParams p) {
     }
   }
   __syncthreads();
-  if (threadIdx.x < 32) {
-    const FSum t = chunk_total_warp(s_g);
+  {
+    FSum inc, q;
+    const FSum t = chunk_scan_cta(s_g, s_w, &inc, &q);
     if (threadIdx.x == 0) p.csum[item] = t;
-  } else if (resid && threadIdx.x < 64) {
-    const FSum t = chunk_total_warp(s_gp);
-    if (threadIdx.x == 32) p.csum_p[item] = t;
+  }
+  if (resid) {
+    __syncthreads();
+    FSum inc, q;
+    const FSum t = chunk_scan_cta(s_gp, s_w, &inc, &q);
+    if (threadIdx.x == 0) p.csum_p[item] = t;
   }
 }
 
@@ -1000,119 +1094,343 @@ __device__ __forceinline__ FSum chunk_prefix(const FSum* cs, int C, const FSum* 
   return carry;
 }
 
-// One warp per sequence walks the prefix structure down to the token: chunk,
-// lane (16 quads), quad, vector, element.  Where rounding leaves the target
-// just past a level's end, the last position with positive weight is taken
-// (such a target lies within ~1e-15 of a boundary).
+// Walk one chunk's prefix structure down to the token (whole CTA; the chunk's
+// group sums are in shared memory `s_g`, the target and the chunk's exclusive
+// prefix `base` are known): warp block (16 warp totals), quad (lane of that
+// warp), vector, element.  Where rounding leaves the target just past a
+// level's end, the last position with positive weight is taken (such a target
+// lies within ~1e-15 of a boundary).  Returns the token to every thread.
+struct WalkScratch {
+  FSum w[kWarps];
+  int wb, exact, tok;
+};
+
+template <typename E, bool kVec>
+__device__ int walk_chunk(const SampleParams& p, const DrawRows& w, bool resid, const float* s_g,
+                          int cstar, const FSum& target, const FSum& base, WalkScratch& ws) {
+  using St = typename E::storage;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  FSum inc, quad;
+  chunk_scan_cta(s_g, ws.w, &inc, &quad);
+  if (warp == 0) {
+    const FSum wv = lane < kWarps ? ws.w[lane] : FSum::zero();
+    const FSum winc = df_norm(df_add(base, warp_scan_df(wv)));
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < kWarps && df_less(target, winc));
+    const unsigned pos = __ballot_sync(0xffffffffu, lane < kWarps && wv.hi > 0.0f);
+    if (lane == 0) {
+      ws.wb = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+      ws.exact = hit != 0;
+      ws.tok = -1;
+    }
+  }
+  __syncthreads();
+  const int wb = ws.wb;
+  const bool exact = ws.exact != 0;
+  const int j0 = cstar * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+  if (warp == wb) {
+    // exclusive prefix of this warp block: base + warp totals before it
+    FSum wbase = base;
+    for (int i = 0; i < wb; ++i) wbase = df_add(wbase, ws.w[i]);
+    FSum exc;
+    exc.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
+    exc.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
+    if (lane == 0) exc = FSum::zero();
+    const unsigned hit =
+        __ballot_sync(0xffffffffu, exact && df_less(target, df_norm(df_add(wbase, inc))));
+    const unsigned pos = __ballot_sync(0xffffffffu, quad.hi > 0.0f);
+    const int L = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+    if (lane == L) {
+      const float4 g4 = *reinterpret_cast<const float4*>(s_g + 4 * threadIdx.x);
+      const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+      FSum run = df_add(wbase, exc);
+      int tok = -1, lastv = -1;
+      for (int i = 0; i < 4 && tok < 0; ++i) {
+        if (!(gv[i] > 0.0f)) continue;
+        const int vi = 4 * threadIdx.x + i;  // vector index within the chunk
+        lastv = vi;
+        const FSum nxt = df_add(run, df_from(gv[i]));
+        if (hit && df_less(target, df_norm(nxt))) {
+          const int j = j0 + vi * E::kEPV;
+          const uint4 vt = fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1);
+          const uint4 vd = resid ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
+                                 : make_uint4(0, 0, 0, 0);
+          float part = 0.0f;
+          int lastpos = -1;
+#pragma unroll
+          for (int e = 0; e < E::kEPV; ++e) {
+            const float we = draw_weight(E::elem(vt, e), resid ? E::elem(vd, e) : 0.0f, p.scale,
+                                         w, resid, e);
+            part = __fadd_rn(part, we);
+            if (we > 0.0f && j + e < j1) lastpos = j + e;
+            if (tok < 0 && we > 0.0f && df_less(target, df_norm(df_add(run, df_from(part)))))
+              tok = j + e;
+          }
+          if (tok < 0) tok = lastpos;  // rounding inside the vector
+        }
+        run = nxt;
+      }
+      if (tok < 0 && lastv >= 0) {  // rounding: last positive element of the quad
+        const int j = j0 + lastv * E::kEPV;
+        const uint4 vt = fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1);
+        const uint4 vd = resid ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
+                               : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < E::kEPV; ++e)
+          if (j + e < j1 && draw_weight(E::elem(vt, e), resid ? E::elem(vd, e) : 0.0f, p.scale,
+                                        w, resid, e) > 0.0f)
+            tok = j + e;
+      }
+      ws.tok = tok;
+    }
+  }
+  __syncthreads();
+  int tok = ws.tok;
+  if (tok < 0 || tok >= p.V) tok = min(j0, p.V - 1);  // unreachable with finite inputs
+  return tok;
+}
+
+// Two-kernel path (rows of more than kClusterMaxChunks chunks): one CTA per
+// sequence picks the chunk from the stored chunk totals and walks it.
 template <typename E, bool kVec>
 __global__ void __launch_bounds__(kThreads) draw_resolve_kernel(const SampleParams p) {
-  using St = typename E::storage;
+  __shared__ __align__(16) float s_g[kVecPerChunk];
+  __shared__ WalkScratch ws;
+  __shared__ FSum s_target, s_base;
+  __shared__ int s_c, s_fallback;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (b >= p.B) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x;
   const int C = p.nchunks;
   const DrawDesc d = p.desc[b];
   const DrawRows w = draw_rows<E>(p, b, d);
-  bool resid = d.n < p.k;
-  const FSum* cs = p.csum + (size_t)b * C;
-  const float* gs = p.gsum + (size_t)b * C * kVecPerChunk;
-  int cstar = 0;
-  FSum base = FSum::zero();
-  FSum total = chunk_prefix(cs, C, nullptr, &cstar, &base);
-  bool fallback = false;
-  if (resid && !(total.hi > 0.0f)) {
-    // the residual mass vanished in rounding: sample p of the rejected row
-    fallback = true;
-    resid = false;
-    cs = p.csum_p + (size_t)b * C;
-    gs = p.gsum_p + (size_t)b * C * kVecPerChunk;
+  FSum total = FSum::zero();
+  if (warp == 0) {
+    int cstar = 0;
+    FSum base = FSum::zero();
+    const FSum* cs = p.csum + (size_t)b * C;
     total = chunk_prefix(cs, C, nullptr, &cstar, &base);
-    if (lane == 0) set_flag(p.flags, kFlagResidualFallback);
-  }
-  const FSum target = df_mul_f(p.u_sample[b], total);
-  chunk_prefix(cs, C, &target, &cstar, &base);
-  const int j0 = cstar * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
-
-  // lane level: this lane's 16 quads (64 groups) of the chosen chunk
-  const float* gch = gs + (size_t)cstar * kVecPerChunk;
-  float4 g4[16];
-#pragma unroll
-  for (int qd = 0; qd < 16; ++qd)
-    g4[qd] = __ldcg(reinterpret_cast<const float4*>(gch + (lane * 16 + qd) * 4));
-  FSum acc = FSum::zero();
-#pragma unroll
-  for (int qd = 0; qd < 16; ++qd) acc = df_add(acc, quad_sum(g4[qd]));
-  const FSum inc = warp_scan_df(acc);
-  FSum exc;
-  exc.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
-  exc.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
-  if (lane == 0) exc = FSum::zero();
-  const unsigned hit = __ballot_sync(0xffffffffu, df_less(target, df_norm(df_add(base, inc))));
-  const unsigned pos = __ballot_sync(0xffffffffu, acc.hi > 0.0f);
-  const bool exact = hit != 0;
-  const int L = exact ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
-
-  int tok = -1;
-  if (lane == L) {
-    FSum run = df_add(base, exc);
-    int lastv = -1;
-    for (int qd = 0; qd < 16 && tok < 0; ++qd) {
-      const FSum qs = quad_sum(g4[qd]);
-      const FSum nxt = df_add(run, qs);
-      const float gv[4] = {g4[qd].x, g4[qd].y, g4[qd].z, g4[qd].w};
-      if (exact && df_less(target, df_norm(nxt))) {
-        // the target lies in this quad: walk its groups, then the elements
-        FSum r2 = run;
-        for (int i = 0; i < 4 && tok < 0; ++i) {
-          if (!(gv[i] > 0.0f)) continue;
-          const int vi = (lane * 16 + qd) * 4 + i;
-          lastv = vi;
-          const FSum n2 = df_add(r2, df_from(gv[i]));
-          if (df_less(target, df_norm(n2))) {
-            const int j = j0 + vi * E::kEPV;
-            const uint4 vt = fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1);
-            const uint4 vd = resid
-                                 ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
-                                 : make_uint4(0, 0, 0, 0);
-            float part = 0.0f;
-            int lastpos = -1;
-#pragma unroll
-            for (int e = 0; e < E::kEPV; ++e) {
-              const float we =
-                  draw_weight(E::elem(vt, e), resid ? E::elem(vd, e) : 0.0f, p.scale, w, resid);
-              part = __fadd_rn(part, we);
-              if (we > 0.0f && j + e < j1) lastpos = j + e;
-              if (tok < 0 && we > 0.0f && df_less(target, df_norm(df_add(r2, df_from(part)))))
-                tok = j + e;
-            }
-            if (tok < 0) tok = lastpos;  // rounding inside the vector
-          }
-          r2 = n2;
-        }
-        break;
-      }
-      for (int i = 0; i < 4; ++i)
-        if (gv[i] > 0.0f) lastv = (lane * 16 + qd) * 4 + i;
-      run = nxt;
+    int fb = 0;
+    if (d.n < p.k && !(total.hi > 0.0f)) {
+      // the residual mass vanished in rounding: sample p of the rejected row
+      fb = 1;
+      cs = p.csum_p + (size_t)b * C;
+      total = chunk_prefix(cs, C, nullptr, &cstar, &base);
+      if (lane == 0) set_flag(p.flags, kFlagResidualFallback);
     }
-    if (tok < 0 && lastv >= 0) {  // rounding: last positive element seen
-      const int j = j0 + lastv * E::kEPV;
-      const uint4 vt = fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1);
-      const uint4 vd = resid ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
-                             : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int e = 0; e < E::kEPV; ++e)
-        if (j + e < j1 &&
-            draw_weight(E::elem(vt, e), resid ? E::elem(vd, e) : 0.0f, p.scale, w, resid) > 0.0f)
-          tok = j + e;
+    const FSum target = df_mul_f(p.u_sample[b], total);
+    chunk_prefix(cs, C, &target, &cstar, &base);
+    if (lane == 0) {
+      s_c = cstar;
+      s_base = base;
+      s_target = target;
+      s_fallback = fb;
     }
   }
-  tok = __shfl_sync(0xffffffffu, tok, L);
-  if (lane == 0) {
-    if (tok < 0 || tok >= p.V) tok = min(j0, p.V - 1);  // unreachable with finite inputs
+  __syncthreads();
+  const bool fallback = s_fallback != 0;
+  const bool resid = d.n < p.k && !fallback;
+  const int cstar = s_c;
+  const float* gs = (fallback ? p.gsum_p : p.gsum) + ((size_t)b * C + cstar) * kVecPerChunk;
+#pragma unroll
+  for (int q = 0; q < kVecPerThread; ++q)
+    s_g[q * kThreads + threadIdx.x] = __ldcg(gs + q * kThreads + threadIdx.x);
+  __syncthreads();
+  const int tok = walk_chunk<E, kVec>(p, w, resid, s_g, cstar, s_target, s_base, ws);
+  if (threadIdx.x == 0) {
     p.out_tokens[(size_t)b * (p.k + 1) + d.n] = tok;
     p.resid_mass[b] = (d.n < p.k && !fallback) ? __fadd_rn(total.hi, total.lo) : 0.0f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Cluster path: merge, accept test, draw prefix sums and walk in one kernel
+// ---------------------------------------------------------------------------
+// One cluster of kClusterCTAs CTAs per sequence (rows of up to
+// kClusterMaxChunks chunks).  CTA `rank` merges rows r = rank (mod
+// kClusterCTAs) into its shared memory; after a cluster barrier every CTA
+// reads all merged rows from its peers (distributed shared memory) and runs
+// the accept test itself (rank 0 writes the outputs).  CTA `rank` then builds
+// the prefix structure of chunks c = rank (mod kClusterCTAs) in its shared
+// memory; after a second barrier every CTA reads the chunk totals, picks the
+// chunk, and after a third barrier (no peer reads afterwards) the chunk's
+// owner walks it.  Three hardware cluster barriers replace two kernel
+// boundaries and their global round trips.
+constexpr int kClusterCTAs = 4;
+constexpr int kLocalChunks = 4;
+constexpr int kClusterMaxChunks = kClusterCTAs * kLocalChunks;
+constexpr size_t kFinishSmem = 2ull * kLocalChunks * kVecPerChunk * sizeof(float);
+
+// Exclusive/inclusive double-float scan of lane values (n <= 32 lanes) with
+// the first lane whose inclusive prefix exceeds `target` (else the last lane
+// with positive value).  Returns the total; *sel, *excl for the chosen lane.
+__device__ __forceinline__ FSum lane_prefix_select(const FSum& v, int n, const FSum* target,
+                                                   int* sel, FSum* excl_sel) {
+  const int lane = threadIdx.x & 31;
+  const FSum inc = df_norm(warp_scan_df(v));
+  FSum excl;
+  excl.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
+  excl.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
+  if (lane == 0) excl = FSum::zero();
+  FSum tot;
+  tot.hi = __shfl_sync(0xffffffffu, inc.hi, 31);
+  tot.lo = __shfl_sync(0xffffffffu, inc.lo, 31);
+  if (target) {
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < n && df_less(*target, inc));
+    const unsigned pos = __ballot_sync(0xffffffffu, lane < n && v.hi > 0.0f);
+    const int L = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+    *sel = L;
+    excl_sel->hi = __shfl_sync(0xffffffffu, excl.hi, L);
+    excl_sel->lo = __shfl_sync(0xffffffffu, excl.lo, L);
+  }
+  return tot;
+}
+
+template <typename E, bool kVec>
+__global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const SampleParams p) {
+  using St = typename E::storage;
+  namespace cg = cooperative_groups;
+  extern __shared__ __align__(16) float fin_mem[];
+  float* s_g = fin_mem;                                 // [kLocalChunks][kVecPerChunk]
+  float* s_gp = fin_mem + kLocalChunks * kVecPerChunk;  // p-only sums of a rejected row
+  __shared__ RowStats s_rows[kMaxSeqRows];
+  __shared__ FSum s_ctot[kLocalChunks], s_ctot_p[kLocalChunks];
+  __shared__ WalkScratch ws;
+  __shared__ DrawDesc s_desc;
+  __shared__ FSum s_target, s_base, s_total;
+  __shared__ int s_c, s_fallback;
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / kClusterCTAs;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int C = p.nchunks;
+  const int rows_per_seq = 2 * p.k + 1;
+
+  // wait for the statistics kernel's records (programmatic dependent launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // 1. this CTA's share of the row merges
+  for (int i = warp;; i += kWarps) {
+    const int r = rank + kClusterCTAs * i;
+    if (r >= rows_per_seq) break;
+    finalize_stats_row<E>(p, b * rows_per_seq + r, &s_rows[r]);
+  }
+  cluster.sync();
+
+  // 2. accept test over the whole sequence, rows read from their owners
+  if (warp == 0) {
+    const DrawDesc dd = resolve_sample_seq(
+        p, b, [&](int r) { return *cluster.map_shared_rank(&s_rows[r], r % kClusterCTAs); },
+        rank == 0);
+    if (lane == 0) s_desc = dd;
+  }
+  __syncthreads();
+  const DrawDesc d = s_desc;
+  const bool resid = d.n < p.k;
+  const DrawRows w = draw_rows<E>(p, b, d);
+
+  // 3. prefix structure of this CTA's chunks
+  for (int lc = 0; lc < kLocalChunks; ++lc) {
+    const int c = rank + kClusterCTAs * lc;
+    if (c >= C) break;
+    float* g = s_g + lc * kVecPerChunk;
+    float* gp = s_gp + lc * kVecPerChunk;
+    const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+    const int nvec = (j1 - j0 + E::kEPV - 1) / E::kEPV;
+    uint4 vt[kVecPerThread], vd[kVecPerThread];
+#pragma unroll
+    for (int q = 0; q < kVecPerThread; ++q) {
+      const int vi = q * kThreads + (int)threadIdx.x;
+      const int j = j0 + vi * E::kEPV;
+      vt[q] = vi < nvec ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1)
+                        : make_uint4(0, 0, 0, 0);
+      vd[q] = (resid && vi < nvec) ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
+                                   : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int q = 0; q < kVecPerThread; ++q) {
+      const int vi = q * kThreads + (int)threadIdx.x;
+      float a = 0.0f, ap = 0.0f;
+      if (vi < nvec) {
+#pragma unroll
+        for (int e = 0; e < E::kEPV; ++e) {
+          const float pt = draw_p(E::elem(vt[q], e), p.scale, w, e);
+          ap = __fadd_rn(ap, pt);
+          a = __fadd_rn(a, resid ? draw_r(pt, E::elem(vd[q], e), p.scale, w, e) : pt);
+        }
+      }
+      g[vi] = a;
+      gp[vi] = ap;
+    }
+    __syncthreads();
+    FSum inc, qd;
+    const FSum t = chunk_scan_cta(g, ws.w, &inc, &qd);
+    if (threadIdx.x == 0) s_ctot[lc] = t;
+    __syncthreads();
+  }
+  cluster.sync();
+
+  // 4. chunk totals from their owners; every CTA computes the same total, so
+  // the rare fallback below is taken by the whole cluster or by none of it
+  FSum total = FSum::zero();
+  if (warp == 0) {
+    FSum v = FSum::zero();
+    if (lane < C) v = *cluster.map_shared_rank(&s_ctot[lane / kClusterCTAs], lane % kClusterCTAs);
+    int sel = 0;
+    FSum excl;
+    total = lane_prefix_select(v, C, nullptr, &sel, &excl);
+    if (lane == 0) s_fallback = resid && !(total.hi > 0.0f);
+  }
+  __syncthreads();
+  const bool fallback = s_fallback != 0;
+  if (fallback) {
+    // the residual mass vanished in rounding: sample p of the rejected row,
+    // whose group sums were kept alongside; its chunk totals are built now
+    for (int lc = 0; lc < kLocalChunks; ++lc) {
+      if (rank + kClusterCTAs * lc >= C) break;
+      FSum inc, qd;
+      const FSum t = chunk_scan_cta(s_gp + lc * kVecPerChunk, ws.w, &inc, &qd);
+      if (threadIdx.x == 0) s_ctot_p[lc] = t;
+      __syncthreads();
+    }
+    cluster.sync();
+    if (rank == 0 && threadIdx.x == 0) set_flag(p.flags, kFlagResidualFallback);
+  }
+  if (warp == 0) {
+    const FSum* ct = fallback ? s_ctot_p : s_ctot;
+    FSum v = FSum::zero();
+    if (lane < C) v = *cluster.map_shared_rank(&ct[lane / kClusterCTAs], lane % kClusterCTAs);
+    int sel = 0;
+    FSum excl;
+    total = lane_prefix_select(v, C, nullptr, &sel, &excl);
+    const FSum target = df_mul_f(p.u_sample[b], total);
+    lane_prefix_select(v, C, &target, &sel, &excl);
+    if (lane == 0) {
+      s_c = sel;
+      s_base = excl;
+      s_target = target;
+      s_total = total;
+    }
+  }
+  cluster.sync();  // no CTA reads a peer's shared memory after this point
+
+  // 5. the owner of the chosen chunk walks it
+  const int cstar = s_c;
+  if (cstar % kClusterCTAs != rank) return;
+  const float* gsel = (fallback ? s_gp : s_g) + (cstar / kClusterCTAs) * kVecPerChunk;
+  const int tok =
+      walk_chunk<E, kVec>(p, w, resid && !fallback, gsel, cstar, s_target, s_base, ws);
+  if (threadIdx.x == 0) {
+    p.out_tokens[(size_t)b * (p.k + 1) + d.n] = tok;
+    p.resid_mass[b] = (d.n < p.k && !fallback) ? __fadd_rn(s_total.hi, s_total.lo) : 0.0f;
+  }
+}
+
+__global__ void selftest_exp2_kernel(const float* x, float* y_fma, float* y_sfu, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    y_fma[i] = exp2_fma(x[i]);
+    y_sfu[i] = ex2(x[i]);
   }
 }
 
