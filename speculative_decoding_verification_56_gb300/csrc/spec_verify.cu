@@ -18,6 +18,8 @@
 #include "spec_verify.h"
 #include "sv_kernels.cuh"
 
+static_assert(sv::kMaxDraft == SPEC_MAX_K, "finish kernel buffers are sized for SPEC_MAX_K");
+
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
@@ -36,7 +38,7 @@ int chunk_elems(int dtype) {
 struct Layout {
   size_t bytes = 0;
   int rows = 0, nchunks = 0;
-  size_t off_part = 0, off_desc = 0, off_csum = 0, off_csum_p = 0;  // sample
+  size_t off_part = 0, off_desc = 0, off_csum = 0, off_csum_p = 0, off_zx = 0;  // sample
   size_t off_gsum = 0, off_gsum_p = 0;
   size_t off_arg = 0;                                            // greedy / tree
 };
@@ -77,6 +79,8 @@ bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
     off = align_up(off + bc * sv::kVecPerChunk * sizeof(float));
     L->off_gsum_p = off;
     off = align_up(off + bc * sv::kVecPerChunk * sizeof(float));
+    L->off_zx = off;
+    off = align_up(off + (size_t)rows * sizeof(float));
   } else {
     L->off_part = off;
     off = align_up(off + (size_t)rows * C * sizeof(sv::ArgPartial));
@@ -183,9 +187,17 @@ spec_status_t run_finish(const sv::SampleParams& prm, void* stream) {
   return launch(sv::draw_resolve_kernel<E, kVec>, prm.B, 0, prm, stream, true);
 }
 
+// L2 budget for the rows streamed with a keep hint (well under the 129 MB L2
+// of a GB300, so that the rest of the stream does not evict them).
+constexpr double kKeepBytes = 80.0 * (1 << 20);
+
 template <typename E>
 spec_status_t run_sample(sv::SampleParams prm, int rows, bool vec, void* stream) {
   prm.items = rows * prm.nchunks;
+  {
+    const double pair = 2.0 * prm.B * (double)prm.V * sizeof(typename E::storage);
+    prm.keep_pos = pair > 0 ? std::min(prm.k + 1, (int)(kKeepBytes / pair)) : 0;
+  }
   spec_status_t st;
   if (vec) {
     int grid = 0;
@@ -299,6 +311,7 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   prm.csum_p = reinterpret_cast<sv::FSum*>(ws + L.off_csum_p);
   prm.gsum = reinterpret_cast<float*>(ws + L.off_gsum);
   prm.gsum_p = reinterpret_cast<float*>(ws + L.off_gsum_p);
+  prm.zx = reinterpret_cast<float*>(ws + L.off_zx);
 
   const bool vec = vec_ok(target_logits, V, dtype) && (k == 0 || vec_ok(draft_logits, V, dtype));
   if (dtype == SPEC_DTYPE_BF16) return run_sample<sv::BF16>(prm, L.rows, vec, stream);

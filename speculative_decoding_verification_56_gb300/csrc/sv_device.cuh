@@ -201,30 +201,6 @@ __device__ __forceinline__ FSum warp_scan_df(FSum v) {
   return v;
 }
 
-// Add `n` arrivals to `counter` after this CTA's global writes, and tell
-// whether they completed it (old + n == expected).  The bar.sync orders every
-// thread's writes before thread 0's release fence and atomic (fences are
-// cumulative); the completing CTA's thread 0 fences again (acquire) before
-// the bar.sync that releases its other threads to read what the others wrote
-// (through L2, with ld.cg).  The completing CTA resets the counter, so every
-// call leaves its counters at zero.  Called by every thread of the CTA.
-__device__ __forceinline__ bool arrive_last(unsigned* counter, unsigned n, unsigned expected,
-                                            int* s_flag) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned old = atomicAdd(counter, n);
-    const bool last = (old + n == expected);
-    if (last) {
-      __threadfence();
-      *counter = 0u;
-    }
-    *s_flag = last ? 1 : 0;
-  }
-  __syncthreads();
-  return *s_flag != 0;
-}
-
 __device__ __forceinline__ void set_flag(unsigned* flags, unsigned bit) { atomicOr(flags, bit); }
 
 // 2^x on the FMA pipe, for x <= 0.5: Cody-Waite reduction x = n + f with
@@ -329,6 +305,29 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
           "r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// L2 cache policies for bulk copies: lines that will be read again soon
+// (evict_last) and lines read once (evict_first).
+__device__ __forceinline__ uint64_t l2_policy_keep() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_stream() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, unsigned bytes,
+                                              uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
 

@@ -56,7 +56,6 @@ struct ArgPartial {
 struct RowStats {  // one row after the merge
   int ref;         // integer reference R of the row
   float inv_sum;   // 1 / S rounded to float
-  double sum;      // unused
   double prob;     // p (or q) of the row's draft token, float64
 };
 
@@ -76,6 +75,10 @@ struct SampleParams {
   const float* u_sample;
   float scale;  // log2(e) / T
   int B, k, V, nchunks, items;
+  // rows of draft positions below keep_pos (target and draft) are streamed
+  // with an L2 keep hint: the draw re-reads the rejected position's pair,
+  // and early positions are the likely ones
+  int keep_pos;
   int32_t* accepted_len;
   int32_t* out_tokens;
   float* p_out;
@@ -92,6 +95,7 @@ struct SampleParams {
   float* gsum_p;   // [B*nchunks*kVecPerChunk]
   FSum* csum;      // [B*nchunks]
   FSum* csum_p;    // [B*nchunks]
+  float* zx;  // [rows] logit of each row's draft token, captured while it streams
 };
 
 struct ArgmaxParams {
@@ -146,6 +150,31 @@ __device__ __forceinline__ uint4 fetch_vec(const typename E::storage* row, int j
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
+}
+
+// Draft token of row `row` of the sampling rows (target rows 0..k-1 and the
+// draft rows carry one; the bonus row and rows past the end give -1).
+__device__ __forceinline__ int row_token(const SampleParams& p, int row) {
+  const int rows_per_seq = 2 * p.k + 1;
+  if (row >= p.B * rows_per_seq) return -1;
+  const int b = row / rows_per_seq, r = row - b * rows_per_seq;
+  if (r == p.k) return -1;
+  const int i = r < p.k ? r : r - p.k - 1;
+  return __ldg(p.tokens + (size_t)b * p.k + i);
+}
+
+// The thread holding element x of the chunk [j0, j1) stores that logit, so
+// that the merge needs no dependent load of it.
+template <typename E>
+__device__ __forceinline__ void capture_token(const SampleParams& p,
+                                              const uint4 (&raw)[kVecPerThread], int x, int j0,
+                                              int j1, int row) {
+  if (x < j0 || x >= j1) return;
+  const int off = x - j0, vi = off / E::kEPV;
+  if ((vi & (kThreads - 1)) != (int)threadIdx.x) return;
+  const int q = vi / kThreads;
+  const uint4 v = q == 0 ? raw[0] : q == 1 ? raw[1] : q == 2 ? raw[2] : raw[3];
+  p.zx[row] = E::elem(v, off % E::kEPV);
 }
 
 // ---------------------------------------------------------------------------
@@ -338,21 +367,23 @@ __device__ __forceinline__ double exp2_over(float x, float S) {
 }
 
 // Merge one row's segment records (one warp).  Loads are issued four per
-// lane before use, so a row of up to 128 records costs one round trip.
+// lane before use, so a row of up to 128 records costs one round trip.  The
+// token's logit was captured by the statistics kernel (p.zx); `tok`, when
+// given, holds the sequence's draft tokens (prefetched).
 template <typename E>
-__device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out) {
+__device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out,
+                                   const int* tok = nullptr) {
   const int lane = threadIdx.x & 31;
   const int rows_per_seq = 2 * p.k + 1;
   const int b = row / rows_per_seq, r = row - b * rows_per_seq;
   const SoftmaxPartial* pr = p.part + (size_t)row * p.nchunks;
   const int nrec = p.nchunks;
-  // the token's logit is fetched alongside the records
   float zx = 0.0f;
   int x = -1;
   if (r != p.k && lane == 0) {  // rows with a draft token: target r < k, draft r > k
     const int i = (r < p.k) ? r : r - p.k - 1;
-    x = p.tokens[(size_t)b * p.k + i];
-    if (x >= 0 && x < p.V) zx = E::load1(seq_row_ptr<E>(p, b, r) + x);
+    x = tok ? tok[i] : p.tokens[(size_t)b * p.k + i];
+    zx = __ldcg(p.zx + row);
   }
   // one pass: running (reference, double-float sum), rescaled exactly when
   // a record's reference is larger
@@ -393,7 +424,6 @@ __device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out
     RowStats rs;
     rs.ref = R;
     rs.inv_sum = __frcp_rn(S.hi);
-    rs.sum = 0.0;
     rs.prob = prob;
     *out = rs;
   }
@@ -404,7 +434,9 @@ __device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out
 // draw descriptor; with `write`, also stores the call's outputs for b (all
 // but the drawn token) and the descriptor.
 template <typename RowFn>
-__device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, RowFn rs, bool write) {
+__device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, RowFn rs, bool write,
+                                       const float* ua = nullptr) {
+  if (!ua) ua = p.u_accept + (size_t)b * p.k;
   const int lane = threadIdx.x & 31;
   const int k = p.k;
   int n = k;
@@ -418,7 +450,7 @@ __device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, RowFn rs, b
         p.p_out[(size_t)b * k + i] = (float)pi;
         p.q_out[(size_t)b * k + i] = (float)qi;
       }
-      const double u = (double)p.u_accept[(size_t)b * k + i];
+      const double u = (double)ua[i];
       rej = !(u * qi < pi);
     }
     const unsigned m = __ballot_sync(0xffffffffu, rej);
@@ -450,7 +482,9 @@ __device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, RowFn rs, b
 
 // Merge the argmax records of rows r0, r0+stride, r0+2*stride, r0+3*stride
 // of sequence b (one warp; rows past `nrows` are skipped).  All loads of a
-// pass are issued before any is used.  Returns the lane-uniform argmaxes.
+// pass (T records per lane and row) are issued before any is used.  Returns
+// the lane-uniform argmaxes.
+template <int T>
 __device__ void finalize_arg_rows4(const ArgmaxParams& p, int b, int r0, int stride, int nrows,
                                    int (&g)[4]) {
   const int lane = threadIdx.x & 31;
@@ -462,14 +496,14 @@ __device__ void finalize_arg_rows4(const ArgmaxParams& p, int b, int r0, int str
     v[u] = -INFINITY;
     i[u] = 0x7FFFFFFF;
   }
-  for (int base = lane; base < nrec; base += 128) {
-    int4 rec[4][4];
+  for (int base = lane; base < nrec; base += 32 * T) {
+    int4 rec[4][T];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int r = r0 + u * stride;
       const ArgPartial* pr = p.part + ((size_t)b * p.rows_per_seq + r) * nrec;
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
+      for (int t = 0; t < T; ++t)
         rec[u][t] = (r < nrows && base + 32 * t < nrec)
                         ? __ldcg(reinterpret_cast<const int4*>(pr + base + 32 * t))
                         : make_int4(0, 0, 0, 0);
@@ -477,7 +511,7 @@ __device__ void finalize_arg_rows4(const ArgmaxParams& p, int b, int r0, int str
 #pragma unroll
     for (int u = 0; u < 4; ++u)
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
+      for (int t = 0; t < T; ++t)
         if (rec[u][t].z > 0 && better(__int_as_float(rec[u][t].x), rec[u][t].y, v[u], i[u])) {
           v[u] = __int_as_float(rec[u][t].x);
           i[u] = rec[u][t].y;
@@ -589,10 +623,12 @@ __device__ void resolve_tree(const ArgmaxParams& p, int b, const int32_t* par,
 // parents, tokens and row argmaxes; larger ones read global memory.
 constexpr int kTreeSmemNodes = 2048;
 
-__global__ void __launch_bounds__(kThreads) argmax_resolve_kernel(const ArgmaxParams p) {
-  __shared__ int32_t s_par[kTreeSmemNodes], s_tok[kTreeSmemNodes], s_g[kTreeSmemNodes];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = blockIdx.x;
+// Merge the rows of sequence (tree) b and resolve it (whole CTA; the three
+// scratch arrays hold kTreeSmemNodes entries each, in shared memory).  T:
+// records per lane and row loaded at once.
+template <int T>
+__device__ void resolve_sequence(const ArgmaxParams& p, int b, int32_t* s_par, int32_t* s_tok,
+                                 int32_t* s_g) {
   const int N = p.rows_per_seq;
   const bool in_smem = p.tree && N <= kTreeSmemNodes;
   if (in_smem) {  // independent loads, issued before the merges
@@ -603,7 +639,7 @@ __global__ void __launch_bounds__(kThreads) argmax_resolve_kernel(const ArgmaxPa
   }
   for (int r0 = threadIdx.x >> 5; r0 < N; r0 += 4 * kWarps) {
     int g[4];
-    finalize_arg_rows4(p, b, r0, kWarps, N, g);
+    finalize_arg_rows4<T>(p, b, r0, kWarps, N, g);
     if (in_smem && (threadIdx.x & 31) == 0)
 #pragma unroll
       for (int u = 0; u < 4; ++u)
@@ -620,6 +656,12 @@ __global__ void __launch_bounds__(kThreads) argmax_resolve_kernel(const ArgmaxPa
       resolve_tree(p, b, p.parents + (size_t)b * N, p.tokens + (size_t)b * N,
                    p.rowarg + (size_t)b * N);
   }
+}
+
+__global__ void __launch_bounds__(kThreads) argmax_resolve_kernel(const ArgmaxParams p) {
+  __shared__ int32_t s_par[kTreeSmemNodes], s_tok[kTreeSmemNodes], s_g[kTreeSmemNodes];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  resolve_sequence<4>(p, blockIdx.x, s_par, s_tok, s_g);
 }
 
 // ---------------------------------------------------------------------------
@@ -723,14 +765,16 @@ __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleP
   const int C = p.nchunks;
   const int rows_per_seq = 2 * p.k + 1;
 
+  const uint64_t pol_keep = l2_policy_keep(), pol_stream = l2_policy_stream();
   auto issue = [&](int item, int slot) {
     const int row = item / C, c = item - (item / C) * C;
     const int b = row / rows_per_seq, r = row - b * rows_per_seq;
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     const unsigned bytes = (unsigned)(j1 - j0) * (unsigned)sizeof(S);
+    const int pos = r <= p.k ? r : r - p.k - 1;  // draft position of the row
     mbar_expect_tx(&ring.full[slot], bytes);
-    bulk_g2s(stage_mem + (size_t)slot * kChunkBytes, seq_row_ptr<E>(p, b, r) + j0, bytes,
-             &ring.full[slot]);
+    bulk_g2s_hint(stage_mem + (size_t)slot * kChunkBytes, seq_row_ptr<E>(p, b, r) + j0, bytes,
+                  &ring.full[slot], pos < p.keep_pos ? pol_keep : pol_stream);
   };
 
   seg_slots_init(ss);
@@ -741,13 +785,18 @@ __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleP
   int row = i0 / C, c = i0 - row * C, c_first = c;
   int slot = 0;
   unsigned par = 0;
+  // draft tokens of the current row and the next (loaded one row ahead)
+  int tok = row_token(p, row), tok_next = row_token(p, row + 1);
   for (int it = i0; it < i1; ++it) {
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     uint4 raw[kVecPerThread];
     const bool ok = ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw);
     if (threadIdx.x == 0)
       issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
-    if (ok) stats_chunk<E>(raw, p.scale, st);
+    if (ok) {
+      stats_chunk<E>(raw, p.scale, st);
+      capture_token<E>(p, raw, tok, j0, j1, row);
+    }
     const bool row_end = (c + 1 == C);
     if (row_end || it + 1 == i1) {
       emit_stats_seg(p, st, row, c_first, c, ss, seg);
@@ -757,6 +806,8 @@ __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleP
     if (row_end) {
       c = 0;
       ++row;
+      tok = tok_next;
+      tok_next = row_token(p, row + 1);
     } else {
       ++c;
     }
@@ -854,9 +905,11 @@ __global__ void __launch_bounds__(kThreads) chunk_stats_kernel(const SampleParam
   const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
   uint4 raw[kVecPerThread];
   load_chunk_regs<E, kVec>(seq_row_ptr<E>(p, b, r), j0, j1, raw);
+  const int tok = row_token(p, row);
   asm volatile("griddepcontrol.launch_dependents;");
   StatsState st;
   stats_chunk<E>(raw, p.scale, st);
+  capture_token<E>(p, raw, tok, j0, j1, row);
   emit_stats_seg(p, st, row, c, c, ss, seg);
 }
 
@@ -963,7 +1016,8 @@ __device__ __forceinline__ FSum chunk_scan_cta(const float* s_g, FSum* s_w, FSum
 // The sequences's rows are merged by every draw CTA of the sequence (one warp
 // per row), into shared memory, followed by the accept test: the CTA of chunk
 // 0 writes the outputs.  Limits: 2k+1 <= kMaxSeqRows.
-constexpr int kMaxSeqRows = 2 * 256 + 1;
+constexpr int kMaxDraft = 256;  // draft positions per sequence (the C interface's limit)
+constexpr int kMaxSeqRows = 2 * kMaxDraft + 1;
 
 template <typename E, bool kVec>
 __global__ void __launch_bounds__(kThreads) draw_kernel(const SampleParams p) {
@@ -1246,19 +1300,22 @@ __global__ void __launch_bounds__(kThreads) draw_resolve_kernel(const SamplePara
 // Cluster path: merge, accept test, draw prefix sums and walk in one kernel
 // ---------------------------------------------------------------------------
 // One cluster of kClusterCTAs CTAs per sequence (rows of up to
-// kClusterMaxChunks chunks).  CTA `rank` merges rows r = rank (mod
-// kClusterCTAs) into its shared memory; after a cluster barrier every CTA
-// reads all merged rows from its peers (distributed shared memory) and runs
-// the accept test itself (rank 0 writes the outputs).  CTA `rank` then builds
-// the prefix structure of chunks c = rank (mod kClusterCTAs) in its shared
-// memory; after a second barrier every CTA reads the chunk totals, picks the
-// chunk, and after a third barrier (no peer reads afterwards) the chunk's
-// owner walks it.  Three hardware cluster barriers replace two kernel
-// boundaries and their global round trips.
+// kClusterMaxChunks chunks).  Before waiting for the statistics kernel, each
+// CTA loads the sequence's draft tokens and uniforms (inputs the statistics
+// kernel does not write).  Every CTA merges all of the sequence's rows (one
+// warp per row; the records are few and in L2) and runs the accept test
+// itself (rank 0 writes the outputs).  CTA `rank` then builds the prefix
+// structure of chunks c = rank (mod kClusterCTAs) in its shared memory: its
+// first chunk through registers while a bulk async copy brings the second
+// (target and draft) into a staging buffer, and so on alternately.  After a
+// cluster barrier every CTA reads the chunk totals (distributed shared
+// memory), picks the chunk, and after a second barrier (no peer reads
+// afterwards) the chunk's owner walks it.
 constexpr int kClusterCTAs = 4;
 constexpr int kLocalChunks = 4;
 constexpr int kClusterMaxChunks = kClusterCTAs * kLocalChunks;
-constexpr size_t kFinishSmem = 2ull * kLocalChunks * kVecPerChunk * sizeof(float);
+constexpr size_t kFinishGroupBytes = (size_t)kLocalChunks * kVecPerChunk * sizeof(float);
+constexpr size_t kFinishSmem = kFinishGroupBytes + 2 * (size_t)kChunkBytes;
 
 // Exclusive/inclusive double-float scan of lane values (n <= 32 lanes) with
 // the first lane whose inclusive prefix exceeds `target` (else the last lane
@@ -1285,18 +1342,43 @@ __device__ __forceinline__ FSum lane_prefix_select(const FSum& v, int n, const F
   return tot;
 }
 
+// Group sums of one chunk's draw weights from 16-byte vectors already in
+// registers (vt: target, vd: draft) into g[vi]; with `gp`, the p-only sums
+// too.
+template <typename E>
+__device__ __forceinline__ void draw_groups_from(const SampleParams& p, const DrawRows& w,
+                                                 bool resid, int nvec, const uint4 (&vt)[kVecPerThread],
+                                                 const uint4 (&vd)[kVecPerThread], float* g) {
+#pragma unroll
+  for (int q = 0; q < kVecPerThread; ++q) {
+    const int vi = q * kThreads + (int)threadIdx.x;
+    float a = 0.0f;
+    if (vi < nvec) {
+#pragma unroll
+      for (int e = 0; e < E::kEPV; ++e) {
+        const float pt = draw_p(E::elem(vt[q], e), p.scale, w, e);
+        a = __fadd_rn(a, resid ? draw_r(pt, E::elem(vd[q], e), p.scale, w, e) : pt);
+      }
+    }
+    g[vi] = a;
+  }
+}
+
 template <typename E, bool kVec>
 __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const SampleParams p) {
   using St = typename E::storage;
   namespace cg = cooperative_groups;
-  extern __shared__ __align__(16) float fin_mem[];
-  float* s_g = fin_mem;                                 // [kLocalChunks][kVecPerChunk]
-  float* s_gp = fin_mem + kLocalChunks * kVecPerChunk;  // p-only sums of a rejected row
+  extern __shared__ __align__(128) uint8_t fin_mem[];
+  float* s_g = reinterpret_cast<float*>(fin_mem);  // [kLocalChunks][kVecPerChunk]
+  uint8_t* s_stage = fin_mem + kFinishGroupBytes;  // target chunk | draft chunk
   __shared__ RowStats s_rows[kMaxSeqRows];
-  __shared__ FSum s_ctot[kLocalChunks], s_ctot_p[kLocalChunks];
+  __shared__ int s_tok[kMaxDraft];
+  __shared__ float s_ua[kMaxDraft];
+  __shared__ FSum s_ctot[kLocalChunks];
   __shared__ WalkScratch ws;
   __shared__ DrawDesc s_desc;
   __shared__ FSum s_target, s_base, s_total;
+  __shared__ uint64_t s_bar;
   __shared__ int s_c, s_fallback;
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -1306,22 +1388,28 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   const int C = p.nchunks;
   const int rows_per_seq = 2 * p.k + 1;
 
-  // wait for the statistics kernel's records (programmatic dependent launch)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // 1. this CTA's share of the row merges
-  for (int i = warp;; i += kWarps) {
-    const int r = rank + kClusterCTAs * i;
-    if (r >= rows_per_seq) break;
-    finalize_stats_row<E>(p, b * rows_per_seq + r, &s_rows[r]);
+  // 0. inputs the statistics kernel does not write, before waiting for it
+  for (int i = threadIdx.x; i < p.k; i += kThreads) {
+    s_tok[i] = p.tokens[(size_t)b * p.k + i];
+    s_ua[i] = p.u_accept[(size_t)b * p.k + i];
   }
-  cluster.sync();
+  const float u_sample = p.u_sample[b];
+  if (kVec && threadIdx.x == 0) {
+    mbar_init(&s_bar, 1);
+    mbar_init_fence();
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
 
-  // 2. accept test over the whole sequence, rows read from their owners
+  // 1. merge every row of the sequence
+  for (int r = warp; r < rows_per_seq; r += kWarps)
+    finalize_stats_row<E>(p, b * rows_per_seq + r, &s_rows[r], s_tok);
+  __syncthreads();
+
+  // 2. accept test over the whole sequence
   if (warp == 0) {
-    const DrawDesc dd = resolve_sample_seq(
-        p, b, [&](int r) { return *cluster.map_shared_rank(&s_rows[r], r % kClusterCTAs); },
-        rank == 0);
+    const DrawDesc dd =
+        resolve_sample_seq(p, b, [&](int r) { return s_rows[r]; }, rank == 0, s_ua);
     if (lane == 0) s_desc = dd;
   }
   __syncthreads();
@@ -1329,39 +1417,52 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   const bool resid = d.n < p.k;
   const DrawRows w = draw_rows<E>(p, b, d);
 
-  // 3. prefix structure of this CTA's chunks
+  // 3. prefix structure of this CTA's chunks: even local chunks through
+  // registers, odd ones through the staging buffer (bulk async copies)
+  auto stage_issue = [&](int lc) {  // thread 0
+    const int c = rank + kClusterCTAs * lc;
+    const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+    const unsigned bytes = (unsigned)(j1 - j0) * (unsigned)sizeof(St);
+    mbar_expect_tx(&s_bar, resid ? 2 * bytes : bytes);
+    bulk_g2s(s_stage, reinterpret_cast<const St*>(w.t) + j0, bytes, &s_bar);
+    if (resid) bulk_g2s(s_stage + kChunkBytes, reinterpret_cast<const St*>(w.d) + j0, bytes, &s_bar);
+  };
+  if (kVec && threadIdx.x == 0 && rank + kClusterCTAs < C) stage_issue(1);
+  bool stage_ok = true;
   for (int lc = 0; lc < kLocalChunks; ++lc) {
     const int c = rank + kClusterCTAs * lc;
     if (c >= C) break;
     float* g = s_g + lc * kVecPerChunk;
-    float* gp = s_gp + lc * kVecPerChunk;
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     const int nvec = (j1 - j0 + E::kEPV - 1) / E::kEPV;
     uint4 vt[kVecPerThread], vd[kVecPerThread];
-#pragma unroll
-    for (int q = 0; q < kVecPerThread; ++q) {
-      const int vi = q * kThreads + (int)threadIdx.x;
-      const int j = j0 + vi * E::kEPV;
-      vt[q] = vi < nvec ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1)
-                        : make_uint4(0, 0, 0, 0);
-      vd[q] = (resid && vi < nvec) ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
-                                   : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int q = 0; q < kVecPerThread; ++q) {
-      const int vi = q * kThreads + (int)threadIdx.x;
-      float a = 0.0f, ap = 0.0f;
-      if (vi < nvec) {
-#pragma unroll
-        for (int e = 0; e < E::kEPV; ++e) {
-          const float pt = draw_p(E::elem(vt[q], e), p.scale, w, e);
-          ap = __fadd_rn(ap, pt);
-          a = __fadd_rn(a, resid ? draw_r(pt, E::elem(vd[q], e), p.scale, w, e) : pt);
-        }
+    if (kVec && (lc & 1)) {
+      if (!mbar_wait_bounded(&s_bar, (unsigned)(lc >> 1) & 1u)) {
+        stage_ok = false;
+        if (threadIdx.x == 0) set_flag(p.flags, kFlagTimeout);
       }
-      g[vi] = a;
-      gp[vi] = ap;
+#pragma unroll
+      for (int q = 0; q < kVecPerThread; ++q) {
+        const int vi = q * kThreads + (int)threadIdx.x;
+        const bool in = stage_ok && vi < nvec;
+        vt[q] = in ? lds128(s_stage + (size_t)vi * 16) : make_uint4(0, 0, 0, 0);
+        vd[q] = in && resid ? lds128(s_stage + kChunkBytes + (size_t)vi * 16)
+                            : make_uint4(0, 0, 0, 0);
+      }
+      __syncthreads();  // staging buffer free
+      if (threadIdx.x == 0 && stage_ok && c + 2 * kClusterCTAs < C) stage_issue(lc + 2);
+    } else {
+#pragma unroll
+      for (int q = 0; q < kVecPerThread; ++q) {
+        const int vi = q * kThreads + (int)threadIdx.x;
+        const int j = j0 + vi * E::kEPV;
+        vt[q] = vi < nvec ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1)
+                          : make_uint4(0, 0, 0, 0);
+        vd[q] = (resid && vi < nvec) ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
+                                     : make_uint4(0, 0, 0, 0);
+      }
     }
+    draw_groups_from<E>(p, w, resid, nvec, vt, vd, g);
     __syncthreads();
     FSum inc, qd;
     const FSum t = chunk_scan_cta(g, ws.w, &inc, &qd);
@@ -1372,38 +1473,52 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
 
   // 4. chunk totals from their owners; every CTA computes the same total, so
   // the rare fallback below is taken by the whole cluster or by none of it
-  FSum total = FSum::zero();
   if (warp == 0) {
     FSum v = FSum::zero();
     if (lane < C) v = *cluster.map_shared_rank(&s_ctot[lane / kClusterCTAs], lane % kClusterCTAs);
     int sel = 0;
     FSum excl;
-    total = lane_prefix_select(v, C, nullptr, &sel, &excl);
+    const FSum total = lane_prefix_select(v, C, nullptr, &sel, &excl);
     if (lane == 0) s_fallback = resid && !(total.hi > 0.0f);
   }
   __syncthreads();
   const bool fallback = s_fallback != 0;
   if (fallback) {
-    // the residual mass vanished in rounding: sample p of the rejected row,
-    // whose group sums were kept alongside; its chunk totals are built now
+    // the residual mass vanished in rounding: sample p of the rejected row;
+    // its group sums and chunk totals replace the residual ones
+    cluster.sync();  // every CTA has read the residual totals
     for (int lc = 0; lc < kLocalChunks; ++lc) {
-      if (rank + kClusterCTAs * lc >= C) break;
+      const int c = rank + kClusterCTAs * lc;
+      if (c >= C) break;
+      float* g = s_g + lc * kVecPerChunk;
+      const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+      const int nvec = (j1 - j0 + E::kEPV - 1) / E::kEPV;
+      uint4 vt[kVecPerThread], vd[kVecPerThread];
+#pragma unroll
+      for (int q = 0; q < kVecPerThread; ++q) {
+        const int vi = q * kThreads + (int)threadIdx.x;
+        vt[q] = vi < nvec ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t),
+                                                j0 + vi * E::kEPV, j1)
+                          : make_uint4(0, 0, 0, 0);
+        vd[q] = make_uint4(0, 0, 0, 0);
+      }
+      draw_groups_from<E>(p, w, false, nvec, vt, vd, g);
+      __syncthreads();
       FSum inc, qd;
-      const FSum t = chunk_scan_cta(s_gp + lc * kVecPerChunk, ws.w, &inc, &qd);
-      if (threadIdx.x == 0) s_ctot_p[lc] = t;
+      const FSum t = chunk_scan_cta(g, ws.w, &inc, &qd);
+      if (threadIdx.x == 0) s_ctot[lc] = t;
       __syncthreads();
     }
     cluster.sync();
     if (rank == 0 && threadIdx.x == 0) set_flag(p.flags, kFlagResidualFallback);
   }
   if (warp == 0) {
-    const FSum* ct = fallback ? s_ctot_p : s_ctot;
     FSum v = FSum::zero();
-    if (lane < C) v = *cluster.map_shared_rank(&ct[lane / kClusterCTAs], lane % kClusterCTAs);
+    if (lane < C) v = *cluster.map_shared_rank(&s_ctot[lane / kClusterCTAs], lane % kClusterCTAs);
     int sel = 0;
     FSum excl;
-    total = lane_prefix_select(v, C, nullptr, &sel, &excl);
-    const FSum target = df_mul_f(p.u_sample[b], total);
+    const FSum total = lane_prefix_select(v, C, nullptr, &sel, &excl);
+    const FSum target = df_mul_f(u_sample, total);
     lane_prefix_select(v, C, &target, &sel, &excl);
     if (lane == 0) {
       s_c = sel;
@@ -1414,10 +1529,15 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   }
   cluster.sync();  // no CTA reads a peer's shared memory after this point
 
+  // a staging copy whose wait ran out may still be in flight: wait again
+  // (bounded) before leaving
+  if (kVec && !stage_ok && threadIdx.x == 0)
+    for (int ph = 0; ph < 2; ++ph) mbar_wait_bounded(&s_bar, (unsigned)ph);
+
   // 5. the owner of the chosen chunk walks it
   const int cstar = s_c;
   if (cstar % kClusterCTAs != rank) return;
-  const float* gsel = (fallback ? s_gp : s_g) + (cstar / kClusterCTAs) * kVecPerChunk;
+  const float* gsel = s_g + (cstar / kClusterCTAs) * kVecPerChunk;
   const int tok =
       walk_chunk<E, kVec>(p, w, resid && !fallback, gsel, cstar, s_target, s_base, ws);
   if (threadIdx.x == 0) {

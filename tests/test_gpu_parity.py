@@ -322,9 +322,12 @@ def test_exp2_fma_accuracy():
 
 
 def test_launch_count():
-    c = synth.make_chain_case(B=2, k=2, V=100, dtype="f32", seed=0)
-    n0 = sv.spec_verify_launch_count()
-    gpu_sample(c)
-    assert sv.spec_verify_launch_count() - n0 == 2   # statistics + cluster finish
-    gpu_greedy(c)
-    assert sv.spec_verify_launch_count() - n0 == 4
+    # statistics + clustered finish for sampling; argmax + resolve for greedy,
+    # on the bulk-copy path (rows of whole 16-byte vectors) and the other
+    for V in (100, 101):
+        c = synth.make_chain_case(B=2, k=2, V=V, dtype="f32", seed=0)
+        n0 = sv.spec_verify_launch_count()
+        gpu_sample(c)
+        assert sv.spec_verify_launch_count() - n0 == 2
+        gpu_greedy(c)
+        assert sv.spec_verify_launch_count() - n0 == 4
