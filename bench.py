@@ -351,13 +351,13 @@ def run_ours(args, rank, world, local_rank):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": E}
 
     # ---- roofline of the dominant kernel ----
-    names = ["stream_stats + sample_resolve + draw + draw_resolve kernels",
+    names = ["stream_stats + sample_finish (4-CTA clusters) kernels",
              "stream_argmax + argmax_resolve kernels (greedy)",
              "stream_argmax + argmax_resolve kernels (tree)"]
     byts = [bytes_sample, bytes_greedy, bytes_tree]
     peak, peak_kind = measured_peak()
     dom = int(np.argmax(mean_ms))
-    dom_name = ["spec_verify_sample (stream_stats, sample_resolve, draw, draw_resolve)",
+    dom_name = ["spec_verify_sample (stream_stats, sample_finish)",
                 "spec_verify_greedy (stream_argmax, argmax_resolve)",
                 "spec_verify_tree_greedy (stream_argmax, argmax_resolve)"][dom]
     achieved = byts[dom] / (mean_ms[dom] / 1e3) / 1e9
