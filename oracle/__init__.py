@@ -66,6 +66,8 @@ def _bind(lib):
     lib.oracle_verify_greedy.restype = I
     lib.oracle_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P]
     lib.oracle_verify_tree_greedy.restype = I
+    lib.oracle_tree_mask.argtypes = [P, I, I, P, P]
+    lib.oracle_tree_mask.restype = I
     lib.oracle_expected_tokens.argtypes = [D, I]
     lib.oracle_expected_tokens.restype = D
     lib.oracle_speedup_model.argtypes = [D, I, D]
@@ -176,6 +178,23 @@ def verify_tree_greedy(target, tokens, parents, max_depth, dtype="bf16", lib=Non
                                        _ptr(out["out_tokens"]))
     _check(rc)
     return out
+
+
+def tree_mask(parents, lib=None):
+    """Tree attention mask (reading R9 of spec_oracle.c): returns
+    ``(mask, depth, malformed)`` with mask uint32 [B, N, ceil(N/32)] (node u
+    of row v is bit u % 32 of word u // 32), depth int32 [B, N] and whether
+    some chain met an invalid parent."""
+    lib = lib or _load()
+    par = np.ascontiguousarray(parents, dtype=np.int32)
+    B, N = par.shape
+    W = (N + 31) // 32
+    mask = np.zeros((B, N, W), dtype=np.uint32)
+    depth = np.zeros((B, N), dtype=np.int32)
+    rc = lib.oracle_tree_mask(_ptr(par), B, N, _ptr(mask), _ptr(depth))
+    if rc not in (0, 4):
+        _check(rc)
+    return mask, depth, rc == 4
 
 
 def expected_tokens(alpha: float, gamma: int, lib=None) -> float:

@@ -32,6 +32,12 @@
  *      accepted nodes are those whose every edge root->v matches the parent
  *      row's argmax; the deepest accepted node wins, ties to the lowest node
  *      index; the bonus token is the argmax of the winner's own row.
+ *   R9 tree attention mask: row v of a tree holds node u iff u = v or u is an
+ *      ancestor of v (the shared prefix is visible to every node and is not
+ *      part of the tree block); depth(v) counts the edges to the root.  A
+ *      chain that meets an invalid parent (p < 0 or p >= child) stops there:
+ *      the row keeps the nodes walked so far, the depth is -1, and the call
+ *      reports a malformed tree.
  *   Non-finite logits are outside the method's domain (rejected here).
  */
 #include <math.h>
@@ -337,6 +343,42 @@ int oracle_verify_tree_greedy(const void* target, int dtype, const int32_t* node
   free(depth);
   free(ok);
   return rc;
+}
+
+/*
+ * Tree attention mask.  [REVIEW] "EAGLE-2: Does Every Context Need the Same
+ * Draft Tree?" (the mask lets each node see only the shared prefix and its
+ * own ancestors), "Must the Feature Be Predicted Exactly?" (draft nodes see
+ * the shared prefix and only their parent and ancestors, never another
+ * branch), "The Complete EAGLE-3 Inference Process" step 3; [MATH] "EAGLE-2:
+ * dynamic draft trees".  Reading R9.
+ *
+ * parents [B, N]; mask [B, N, W] 32-bit words with W = ceil(N / 32): node u
+ * of row v is bit (u % 32) of word u / 32; depth [B, N].  Returns OR_OK, or
+ * OR_ERR_TREE when some chain met an invalid parent (outputs still written).
+ */
+int oracle_tree_mask(const int32_t* parents, int B, int N, uint32_t* mask, int32_t* depth) {
+  if (B < 0 || N < 1) return OR_ERR_ARG;
+  const int W = (N + 31) / 32;
+  int bad = 0;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parents + (size_t)b * N;
+    for (int v = 0; v < N; ++v) {
+      uint32_t* row = mask + ((size_t)b * N + v) * (size_t)W;
+      for (int w = 0; w < W; ++w) row[w] = 0u;
+      int cur = v, d = 0;
+      row[cur / 32] |= 1u << (cur % 32);
+      while (cur != 0) { /* walk to the root, one parent at a time */
+        int p = par[cur];
+        if (p < 0 || p >= cur) { d = -1; bad = 1; break; }
+        cur = p;
+        row[cur / 32] |= 1u << (cur % 32);
+        ++d;
+      }
+      depth[(size_t)b * N + v] = d;
+    }
+  }
+  return bad ? OR_ERR_TREE : OR_OK;
 }
 
 /* Expected tokens per verification pass with per-token acceptance alpha and

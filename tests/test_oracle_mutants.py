@@ -39,6 +39,11 @@ MUTANTS = {
     "greedy_emits_draft": ("else if (i == n) v = g[n];",
                            "else if (i == n) v = (n < k) ? tokens[(size_t)b * k + n] : g[n];"),
     "expected_tokens_short": ("for (int i = 0; i <= gamma; ++i) {", "for (int i = 0; i < gamma; ++i) {"),
+    "mask_no_self": ("      int cur = v, d = 0;\n      row[cur / 32] |= 1u << (cur % 32);\n",
+                     "      int cur = v, d = 0;\n"),
+    "mask_parent_only": ("        ++d;\n      }", "        ++d;\n        break;\n      }"),
+    "mask_wrong_word": ("        row[cur / 32] |= 1u << (cur % 32);\n        ++d;",
+                        "        row[cur % W] |= 1u << (cur % 32);\n        ++d;"),
 }
 
 
@@ -59,6 +64,9 @@ class _Variant:
     def verify_tree_greedy(self, *a, **kw):
         return oracle.verify_tree_greedy(*a, lib=self.lib, **kw)
 
+    def tree_mask(self, *a, **kw):
+        return oracle.tree_mask(*a, lib=self.lib, **kw)
+
     def expected_tokens(self, *a, **kw):
         return oracle.expected_tokens(*a, lib=self.lib, **kw)
 
@@ -75,6 +83,8 @@ def _pin_checks(o):
     yield lambda: pins.test_greedy_equals_argmax_decoding(o, "f32", 5)
     yield lambda: pins.test_tree_bruteforce(o, 1)
     yield lambda: pins.test_star_tree(o)
+    yield lambda: pins.test_tree_mask_chain_is_causal(o)
+    yield lambda: pins.test_tree_mask_equals_closure(o, 1)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

@@ -429,3 +429,84 @@ def test_malformed_trees_raise(oracle_mod):
             oracle_mod.verify_tree_greedy(zt, tok, np.array([par], np.int32), 5, dtype="f32")
     with pytest.raises(oracle_mod.OracleError):   # depth 3 > max_depth 2
         oracle_mod.verify_tree_greedy(zt, tok, np.array([[-1, 0, 1, 2]], np.int32), 2, dtype="f32")
+
+
+# ---------------------------------------------------------------------------
+# Tree attention mask (review page, "EAGLE-2: Does Every Context Need the Same
+# Draft Tree?" and "Must the Feature Be Predicted Exactly?": each node sees
+# the shared prefix, its parent and its ancestors, and no other branch)
+# ---------------------------------------------------------------------------
+
+def _mask_bool(mask, N):
+    """uint32 words [..., W] -> bool [..., N]."""
+    bits = np.unpackbits(mask.view(np.uint8), axis=-1, bitorder="little")
+    return bits[..., :N].astype(bool)
+
+
+def _closure(par):
+    """Reflexive-transitive closure of the child->parent relation by
+    Warshall's algorithm on the adjacency matrix: reach[v, u] iff u is v or
+    an ancestor of v."""
+    N = len(par)
+    reach = np.eye(N, dtype=bool)
+    for v in range(1, N):
+        reach[v, par[v]] = True
+    for m in range(N):
+        reach |= reach[:, m:m + 1] & reach[m:m + 1, :]
+    return reach
+
+
+def test_tree_mask_chain_is_causal(oracle_mod):
+    # a chain is ordinary decoding: the tree block is the lower-triangular mask
+    for N in (1, 2, 31, 32, 33, 70):
+        par = np.array([[-1] + list(range(N - 1))], dtype=np.int32)
+        mask, depth, bad = oracle_mod.tree_mask(par)
+        assert not bad
+        assert np.array_equal(_mask_bool(mask[0], N), np.tri(N, dtype=bool))
+        assert np.array_equal(depth[0], np.arange(N))
+
+
+def test_tree_mask_star_sees_root_and_self(oracle_mod):
+    N = 40
+    par = np.array([[-1] + [0] * (N - 1)], dtype=np.int32)
+    mask, depth, bad = oracle_mod.tree_mask(par)
+    want = np.eye(N, dtype=bool)
+    want[:, 0] = True
+    assert not bad
+    assert np.array_equal(_mask_bool(mask[0], N), want)
+    assert np.array_equal(depth[0], [0] + [1] * (N - 1))
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_tree_mask_equals_closure(oracle_mod, seed):
+    rng = np.random.default_rng(seed)
+    B, N = 3, [5, 33, 97][seed % 3]
+    par = np.stack([synth.make_tree_parents(rng, N, max_depth=8, max_children=4)
+                    for _ in range(B)]).astype(np.int32)
+    mask, depth, bad = oracle_mod.tree_mask(par)
+    assert not bad
+    for b in range(B):
+        reach = _closure(par[b])
+        got = _mask_bool(mask[b], N)
+        assert np.array_equal(got, reach)
+        assert np.array_equal(depth[b], reach.sum(1) - 1)  # ancestors + self
+        # siblings never see each other
+        for u in range(1, N):
+            for v in range(u + 1, N):
+                if par[b, u] == par[b, v]:
+                    assert not got[u, v] and not got[v, u]
+        # no bit past N in the last word
+        W = mask.shape[-1]
+        if N % 32:
+            assert not (mask[b, :, W - 1] >> np.uint32(N % 32)).any()
+
+
+def test_tree_mask_malformed(oracle_mod):
+    # node 2 points forward: its chain stops at itself; node 3 below it too
+    par = np.array([[-1, 0, 3, 2, 1]], dtype=np.int32)
+    mask, depth, bad = oracle_mod.tree_mask(par)
+    got = _mask_bool(mask[0], 5)
+    assert bad
+    assert got[2].nonzero()[0].tolist() == [2] and depth[0, 2] == -1
+    assert got[3].nonzero()[0].tolist() == [2, 3] and depth[0, 3] == -1
+    assert got[4].nonzero()[0].tolist() == [0, 1, 4] and depth[0, 4] == 2
