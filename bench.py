@@ -41,9 +41,10 @@ METRIC = ("verified draft positions/sec and achieved HBM GB/s (% of GB300 peak) 
 UNIT = "positions/s"
 NSETS = 4
 FALLBACK_HBM_GBS = 6800.0
+# the files holding the verification kernels (the recorded traffic is valid
+# while they are unchanged)
 KERNEL_SOURCES = ["speculative_decoding_verification_56_gb300/csrc/sv_device.cuh",
-                  "speculative_decoding_verification_56_gb300/csrc/sv_kernels.cuh",
-                  "speculative_decoding_verification_56_gb300/csrc/spec_verify.cu"]
+                  "speculative_decoding_verification_56_gb300/csrc/sv_kernels.cuh"]
 
 
 def parse_args():
@@ -304,6 +305,7 @@ def run_ours(args, rank, world, local_rank):
         mean_ms.append(e0.elapsed_time(e1) / K)
     mean_ms = np.array(mean_ms)
     clk = clocks.stop(t_wall0, t_wall1) if clocks else None
+    next_rows = measure_next_rows(dev, stream, tree, K) if rank == 0 else None
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([total_ms], device=dev)
@@ -393,6 +395,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clk,
+        "next_rows": next_rows,
     }
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         result["cpu_baseline"] = cpu_baseline(samp, greedy, tree, args.cpu_seconds)
@@ -401,6 +404,41 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def _time_loop(fn, stream, K):
+    """Mean ms of fn() over K back-to-back calls on `stream` (3 untimed first)."""
+    import torch
+    for _ in range(3):
+        fn()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        fn()
+    e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / K
+
+
+def measure_next_rows(dev, stream, tree, K):
+    """The kernels around the draft tree (each timed alone, outside the step):
+    tree attention mask of the tree workload's trees."""
+    import torch
+    import speculative_decoding_verification_56_gb300 as sv
+    out = {}
+    Bt, N = tree.parents.shape
+    W = (N + 31) // 32
+    par = torch.from_numpy(tree.parents).to(dev)
+    mask = torch.empty(Bt, N, W, dtype=torch.int32, device=dev)
+    depth = torch.empty(Bt, N, dtype=torch.int32, device=dev)
+    wsm = sv.alloc_workspace(sv.SPEC_MODE_TREE_MASK, Bt, N, 1, sv.SPEC_DTYPE_F32, dev)
+    ms = _time_loop(lambda: sv.spec_tree_attention_mask(par, mask, depth, wsm, stream), stream, K)
+    out["tree_mask"] = {"workload": f"B={Bt} N={N} trees (the tree-verification workload)",
+                        "us_per_call": round(ms * 1e3, 3),
+                        "bytes": int(Bt * N * 4 + Bt * N * W * 4 + Bt * N * 4),
+                        "bound": "launch latency (one kernel, a few KB)"}
+    return out
 
 
 def cpu_baseline(samp, greedy, tree, budget_s):

@@ -70,7 +70,8 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
 typedef enum {
   SPEC_MODE_SAMPLE = 0,
   SPEC_MODE_GREEDY = 1,
-  SPEC_MODE_TREE_GREEDY = 2
+  SPEC_MODE_TREE_GREEDY = 2,
+  SPEC_MODE_TREE_MASK = 3 /* spec_tree_attention_mask: the flag header only */
 } spec_mode_t;
 
 /* Bits of the workspace flag word (sticky until read with clear != 0). */
@@ -175,6 +176,30 @@ SPEC_API spec_status_t spec_verify_tree_greedy(const void* target_logits, int dt
                                       int32_t* accepted_len, int32_t* path_nodes,
                                       int32_t* out_tokens, void* workspace,
                                       size_t workspace_bytes, void* stream);
+
+/*
+ * Tree attention mask of B draft trees ("EAGLE-3 speculative decoding
+ * review", "EAGLE-2: Does Every Context Need the Same Draft Tree?" and "Must
+ * the Feature Be Predicted Exactly?": each node sees the shared prefix and
+ * only its own ancestors; "The Complete EAGLE-3 Inference Process" step 3).
+ * The prefix columns are visible to every node and are not written; this
+ * call writes the tree block.
+ *   parents  int32 [B, N]  parents[b,0] ignored (node 0 is the root, the
+ *                          last committed token); 0 <= parents[b,v] < v
+ * Outputs:
+ *   mask     uint32 [B, N, W], W = (N + 31) / 32: bit (u % 32) of word u / 32
+ *            of row (b, v) is set iff u == v or u is an ancestor of v; the
+ *            bits past N in the last word are 0
+ *   depth    int32 [B, N] or NULL: edges from v to the root
+ * A node whose ancestor chain meets a parent outside [0, child) keeps the
+ * nodes walked so far, gets depth -1 and raises SPEC_FLAG_BAD_PARENT.
+ * Pointers: device memory, 4-byte aligned; workspace of at least
+ * spec_verify_workspace_bytes(SPEC_MODE_TREE_MASK, ...) bytes (the flag
+ * header), 256-byte aligned.  One kernel launch; N <= SPEC_MAX_TREE_NODES.
+ */
+SPEC_API spec_status_t spec_tree_attention_mask(const int32_t* parents, int B, int N,
+                                                uint32_t* mask, int32_t* depth, void* workspace,
+                                                size_t workspace_bytes, void* stream);
 
 /*
  * Copy the workspace's flag word to *host_flags (synchronises `stream`); with

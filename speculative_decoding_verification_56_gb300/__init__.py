@@ -10,11 +10,13 @@ Entry points (same names as the C ABI):
 * :func:`spec_verify_sample`      -- rejection-sampling verification of chains
 * :func:`spec_verify_greedy`      -- greedy verification of chains
 * :func:`spec_verify_tree_greedy` -- greedy verification of draft trees
+* :func:`spec_tree_attention_mask` -- ancestor bitmask + depth of draft trees
 * :func:`spec_verify_workspace_bytes`, :func:`spec_verify_read_flags`,
   :func:`spec_verify_launch_count`, :func:`spec_status_string`
 
 Convenience wrappers that also allocate outputs and a workspace with torch:
-:func:`verify_sample`, :func:`verify_greedy`, :func:`verify_tree_greedy`.
+:func:`verify_sample`, :func:`verify_greedy`, :func:`verify_tree_greedy`,
+:func:`tree_attention_mask`.
 """
 from __future__ import annotations
 
@@ -37,6 +39,7 @@ SPEC_DTYPE_BF16 = 1
 SPEC_MODE_SAMPLE = 0
 SPEC_MODE_GREEDY = 1
 SPEC_MODE_TREE_GREEDY = 2
+SPEC_MODE_TREE_MASK = 3
 SPEC_FLAG_TOKEN_RANGE = 1
 SPEC_FLAG_BAD_PARENT = 2
 SPEC_FLAG_DEPTH = 4
@@ -77,6 +80,8 @@ def load_library(path: str = LIB_PATH):
         lib.spec_verify_greedy_noalloc.restype = I
         lib.spec_verify_selftest_exp2.argtypes = [P, P, P, I, P]
         lib.spec_verify_selftest_exp2.restype = I
+        lib.spec_tree_attention_mask.argtypes = [P, I, I, P, P, P, Z, P]
+        lib.spec_tree_attention_mask.restype = I
         lib.spec_verify_read_flags.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I, P]
         lib.spec_verify_read_flags.restype = I
         lib.spec_verify_launch_count.argtypes = []
@@ -241,6 +246,20 @@ def spec_verify_tree_greedy(target_logits, node_tokens, parents, max_depth, acce
     _check(st, "spec_verify_tree_greedy")
 
 
+def spec_tree_attention_mask(parents, mask, depth, workspace, stream=None):
+    """Tree attention mask (C ABI ``spec_tree_attention_mask``): ``mask``
+    int32/uint32-sized [B, N, ceil(N/32)] words, ``depth`` int32 [B, N] or
+    None."""
+    torch = _torch()
+    B, N = parents.shape
+    st = load_library().spec_tree_attention_mask(
+        _dev(parents, "parents", torch.int32), B, N, _dev(mask, "mask"),
+        _dev(depth, "depth", torch.int32, optional=True),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream))
+    _check(st, "spec_tree_attention_mask")
+
+
 def spec_verify_read_flags(workspace, clear: bool = True, stream=None) -> int:
     """Device flag bits recorded in ``workspace`` (synchronises the stream)."""
     out = ctypes.c_uint32(0)
@@ -311,6 +330,21 @@ def verify_tree_greedy(target_logits, node_tokens, parents, max_depth, workspace
                             out["accepted_len"], out["path_nodes"], out["out_tokens"],
                             workspace, stream)
     return out
+
+
+def tree_attention_mask(parents, workspace=None, stream=None):
+    """Ancestor bitmask and depth of B draft trees: returns ``(mask, depth)``
+    with mask int32 [B, N, ceil(N/32)] (the bit patterns of the C ABI's
+    uint32 words) and depth int32 [B, N]."""
+    torch = _torch()
+    B, N = parents.shape
+    dev = parents.device
+    if workspace is None:
+        workspace = alloc_workspace(SPEC_MODE_TREE_MASK, B, N, 1, SPEC_DTYPE_F32, dev)
+    mask = torch.empty(B, N, (N + 31) // 32, dtype=torch.int32, device=dev)
+    depth = torch.empty(B, N, dtype=torch.int32, device=dev)
+    spec_tree_attention_mask(parents, mask, depth, workspace, stream)
+    return mask, depth
 
 
 def to_device_logits(arr, dtype: str, device="cuda"):

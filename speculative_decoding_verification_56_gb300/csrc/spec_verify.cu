@@ -17,6 +17,7 @@
 
 #include "spec_verify.h"
 #include "sv_kernels.cuh"
+#include "sv_tree.cuh"
 
 static_assert(sv::kMaxDraft == SPEC_MAX_K, "finish kernel buffers are sized for SPEC_MAX_K");
 
@@ -45,6 +46,11 @@ struct Layout {
 
 // Returns false for arguments outside the documented limits.
 bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
+  if (mode == SPEC_MODE_TREE_MASK) {  // the flag header only
+    if (B < 0 || kN < 1 || kN > SPEC_MAX_TREE_NODES) return false;
+    L->bytes = kHeaderBytes;
+    return true;
+  }
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return false;
   if (B < 0 || V < 1 || V > SPEC_MAX_V) return false;
   const int C = (V + chunk_elems(dtype) - 1) / chunk_elems(dtype);
@@ -396,6 +402,27 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, int dtype,
   prm.out_tokens = out_tokens;
   prm.path_nodes = path_nodes;
   return argmax_common(prm, L, workspace, dtype, stream);
+}
+
+spec_status_t spec_tree_attention_mask(const int32_t* parents, int B, int N, uint32_t* mask,
+                                       int32_t* depth, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!parents || !mask) return SPEC_ERR_INVALID_ARG;
+  if (!aligned(parents, 4) || !aligned(mask, 4) || (depth && !aligned(depth, 4)))
+    return SPEC_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < kHeaderBytes) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
+  const int W = (N + 31) / 32;
+  const long long threads = (long long)B * N * W;
+  const long long blocks = (threads + sv::kMaskThreads - 1) / sv::kMaskThreads;
+  if (blocks > 0x7FFFFFFFLL) return SPEC_ERR_INVALID_ARG;
+  sv::tree_mask_kernel<<<(unsigned)blocks, sv::kMaskThreads, 0, (cudaStream_t)stream>>>(
+      parents, B, N, W, mask, depth, reinterpret_cast<unsigned*>(workspace));
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return SPEC_OK;
 }
 
 spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_flags, int clear,

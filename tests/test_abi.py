@@ -124,6 +124,24 @@ def test_noalloc_host_validation(lib):
     assert f(FAKE, 1, FAKE, 4096, 8, 1 << 20, FAKE, FAKE, None) == 5   # beyond the scratch
 
 
+def test_tree_mask_host_validation(lib):
+    f = lib.spec_tree_attention_mask
+    assert lib.spec_verify_workspace_bytes(3, 16, 60, 0, 7) == 256   # flag header only
+    assert lib.spec_verify_workspace_bytes(3, 16, 0, 0, 0) == 0
+    assert lib.spec_verify_workspace_bytes(3, 16, 65537, 0, 0) == 0
+    assert f(FAKE, -1, 60, FAKE, FAKE, FAKE, 256, None) == 1
+    assert f(FAKE, 4, 0, FAKE, FAKE, FAKE, 256, None) == 1
+    assert f(FAKE, 4, 65537, FAKE, FAKE, FAKE, 256, None) == 1
+    assert f(None, 4, 60, FAKE, FAKE, FAKE, 256, None) == 1
+    assert f(FAKE, 4, 60, None, FAKE, FAKE, 256, None) == 1
+    assert f(FAKE + 2, 4, 60, FAKE, FAKE, FAKE, 256, None) == 2
+    assert f(FAKE, 4, 60, FAKE, FAKE + 1, FAKE, 256, None) == 2
+    assert f(FAKE, 4, 60, FAKE, FAKE, FAKE, 255, None) == 3
+    assert f(FAKE, 4, 60, FAKE, FAKE, None, 256, None) == 3
+    assert f(FAKE, 4, 60, FAKE, FAKE, FAKE + 16, 256, None) == 2
+    assert f(FAKE, 0, 60, FAKE, FAKE, FAKE, 256, None) == 0            # B = 0: no work
+
+
 def test_read_flags_validation(lib):
     v = ctypes.c_uint32(0)
     assert lib.spec_verify_read_flags(None, ctypes.byref(v), 0, None) == 1
