@@ -68,6 +68,9 @@ def _bind(lib):
     lib.oracle_verify_tree_greedy.restype = I
     lib.oracle_tree_mask.argtypes = [P, I, I, P, P]
     lib.oracle_tree_mask.restype = I
+    LL = ctypes.c_longlong
+    lib.oracle_kv_commit.argtypes = [P, P, ctypes.c_size_t, I, I, LL, LL, I, I, I, P, P, P, I, P]
+    lib.oracle_kv_commit.restype = I
     lib.oracle_expected_tokens.argtypes = [D, I]
     lib.oracle_expected_tokens.restype = D
     lib.oracle_speedup_model.argtypes = [D, I, D]
@@ -195,6 +198,27 @@ def tree_mask(parents, lib=None):
     if rc not in (0, 4):
         _check(rc)
     return mask, depth, rc == 4
+
+
+def kv_commit(cache, base_len, accepted_len, path_nodes, N, lib=None):
+    """KV commit of the accepted path (reading R10 of spec_oracle.c), out of
+    place.  ``cache``: array [planes, B, L, E] of any dtype (E elements per
+    entry).  Returns ``(new_cache, new_len, malformed)``."""
+    lib = lib or _load()
+    c = np.ascontiguousarray(cache)
+    planes, B, L = c.shape[:3]
+    eb = c[0, 0, 0].nbytes
+    out = np.empty_like(c)
+    path = np.ascontiguousarray(path_nodes, dtype=np.int32)
+    base = np.ascontiguousarray(base_len, dtype=np.int32)
+    acc = np.ascontiguousarray(accepted_len, dtype=np.int32)
+    new_len = np.zeros(B, dtype=np.int32)
+    rc = lib.oracle_kv_commit(_ptr(c), _ptr(out), c.nbytes, B, planes, B * L * eb, L * eb, eb,
+                              L, int(N), _ptr(base), _ptr(acc), _ptr(path), path.shape[1] - 1,
+                              _ptr(new_len))
+    if rc not in (0, 4):
+        _check(rc)
+    return out, new_len, rc == 4
 
 
 def expected_tokens(alpha: float, gamma: int, lib=None) -> float:

@@ -38,6 +38,14 @@
  *      chain that meets an invalid parent (p < 0 or p >= child) stops there:
  *      the row keeps the nodes walked so far, the depth is -1, and the call
  *      reports a malformed tree.
+ *   R10 KV commit of the accepted path: tree node v >= 1 holds its keys and
+ *      values at cache position base + v - 1 (the tree is appended after the
+ *      committed prefix of length base, whose last token is the root); the
+ *      accepted path 0, v_1, ..., v_d moves node v_i's entries to position
+ *      base + i - 1 in every plane (layer, K or V), leaves every other
+ *      position as it was, and commits base + d positions (the bonus token
+ *      has no cache entry yet).  A sequence whose path is malformed is left
+ *      untouched and reported.
  *   Non-finite logits are outside the method's domain (rejected here).
  */
 #include <math.h>
@@ -377,6 +385,46 @@ int oracle_tree_mask(const int32_t* parents, int B, int N, uint32_t* mask, int32
       }
       depth[(size_t)b * N + v] = d;
     }
+  }
+  return bad ? OR_ERR_TREE : OR_OK;
+}
+
+/*
+ * KV commit of the accepted path.  [REVIEW] "The Complete EAGLE-3 Inference
+ * Process" step 5 (keep only the KV cache of the accepted path, discard the
+ * rejected branches, resume from the committed prefix).  Reading R10.
+ *
+ * cache_in / cache_out: the same byte layout; entry (plane p, sequence b,
+ * position t) starts at p * plane_stride + b * seq_stride + t * entry_bytes.
+ * base_len [B], accepted_len [B], path_nodes [B, max_depth + 1] (as written
+ * by tree verification); new_len [B] out.  Out of place: cache_out starts as
+ * a copy of cache_in.  Returns OR_ERR_TREE if some sequence was malformed.
+ */
+int oracle_kv_commit(const uint8_t* cache_in, uint8_t* cache_out, size_t cache_bytes, int B,
+                     int planes, long long plane_stride, long long seq_stride, int entry_bytes,
+                     int L, int N, const int32_t* base_len, const int32_t* accepted_len,
+                     const int32_t* path_nodes, int max_depth, int32_t* new_len) {
+  if (B < 0 || planes < 1 || entry_bytes < 1 || L < 1 || N < 1 || max_depth < 0)
+    return OR_ERR_ARG;
+  memcpy(cache_out, cache_in, cache_bytes);
+  int bad = 0;
+  const int W = max_depth + 1;
+  for (int b = 0; b < B; ++b) {
+    const int base = base_len[b], d = accepted_len[b];
+    const int32_t* path = path_nodes + (size_t)b * W;
+    int ok = base >= 1 && base + N - 1 <= L && d >= 0 && d <= max_depth && path[0] == 0;
+    for (int i = 1; ok && i <= d; ++i)
+      if (path[i] < 1 || path[i] >= N) ok = 0;
+    if (!ok) { bad = 1; new_len[b] = base; continue; }
+    for (int i = 1; i <= d; ++i) {
+      const long long src = (long long)(base + path[i] - 1) * entry_bytes;
+      const long long dst = (long long)(base + i - 1) * entry_bytes;
+      for (int p = 0; p < planes; ++p) {
+        const long long row = (long long)p * plane_stride + (long long)b * seq_stride;
+        memcpy(cache_out + row + dst, cache_in + row + src, (size_t)entry_bytes);
+      }
+    }
+    new_len[b] = base + d;
   }
   return bad ? OR_ERR_TREE : OR_OK;
 }

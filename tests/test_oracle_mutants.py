@@ -42,6 +42,13 @@ MUTANTS = {
     "mask_no_self": ("      int cur = v, d = 0;\n      row[cur / 32] |= 1u << (cur % 32);\n",
                      "      int cur = v, d = 0;\n"),
     "mask_parent_only": ("        ++d;\n      }", "        ++d;\n        break;\n      }"),
+    "kv_no_offset": ("const long long src = (long long)(base + path[i] - 1) * entry_bytes;",
+                     "const long long src = (long long)(base + path[i]) * entry_bytes;"),
+    "kv_scatter": ("memcpy(cache_out + row + dst, cache_in + row + src, (size_t)entry_bytes);",
+                   "memcpy(cache_out + row + src, cache_in + row + dst, (size_t)entry_bytes);"),
+    "kv_len_counts_bonus": ("new_len[b] = base + d;\n", "new_len[b] = base + d + 1;\n"),
+    "kv_previous_node": ("const long long src = (long long)(base + path[i] - 1) * entry_bytes;",
+                         "const long long src = (long long)(base + path[i - 1]) * entry_bytes;"),
     "mask_wrong_word": ("        row[cur / 32] |= 1u << (cur % 32);\n        ++d;",
                         "        row[cur % W] |= 1u << (cur % 32);\n        ++d;"),
 }
@@ -67,6 +74,9 @@ class _Variant:
     def tree_mask(self, *a, **kw):
         return oracle.tree_mask(*a, lib=self.lib, **kw)
 
+    def kv_commit(self, *a, **kw):
+        return oracle.kv_commit(*a, lib=self.lib, **kw)
+
     def expected_tokens(self, *a, **kw):
         return oracle.expected_tokens(*a, lib=self.lib, **kw)
 
@@ -85,6 +95,8 @@ def _pin_checks(o):
     yield lambda: pins.test_star_tree(o)
     yield lambda: pins.test_tree_mask_chain_is_causal(o)
     yield lambda: pins.test_tree_mask_equals_closure(o, 1)
+    yield lambda: pins.test_kv_commit_equals_appending_the_path(o, 0)
+    yield lambda: pins.test_kv_commit_chain_and_empty_paths_change_nothing(o)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

@@ -510,3 +510,98 @@ def test_tree_mask_malformed(oracle_mod):
     assert got[2].nonzero()[0].tolist() == [2] and depth[0, 2] == -1
     assert got[3].nonzero()[0].tolist() == [2, 3] and depth[0, 3] == -1
     assert got[4].nonzero()[0].tolist() == [0, 1, 4] and depth[0, 4] == 2
+
+
+# ---------------------------------------------------------------------------
+# KV commit of the accepted path (review page, "The Complete EAGLE-3
+# Inference Process" step 5: keep only the accepted path's cache entries)
+# ---------------------------------------------------------------------------
+
+def _tagged_cache(planes, B, L, E, base, N):
+    """Entries tagged by what they hold: prefix position t -> (p, b, t, 0);
+    tree node v (at base + v - 1) -> (p, b, v, 1); unused tail -> (p, b, t, 2)."""
+    c = np.zeros((planes, B, L, E), dtype=np.int32)
+    for p in range(planes):
+        for b in range(B):
+            for t in range(L):
+                v = t - base[b] + 1
+                kind = 0 if t < base[b] else (1 if v < N else 2)
+                tag = v if kind == 1 else t
+                c[p, b, t, :] = [p, b, tag, kind] + [1000 * p + 10 * b + kind] * (E - 4)
+    return c
+
+
+def _appended(c, b, base, path, d):
+    """The cache a plain decoder would hold after appending the accepted
+    tokens one by one: prefix, then the entries of nodes v_1..v_d in order."""
+    planes = c.shape[0]
+    rows = []
+    for p in range(planes):
+        prefix = [c[p, b, t].copy() for t in range(base)]
+        acc = [c[p, b, base + path[i] - 1].copy() for i in range(1, d + 1)]
+        rows.append(np.array(prefix + acc))
+    return rows
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_kv_commit_equals_appending_the_path(oracle_mod, seed):
+    rng = np.random.default_rng(seed)
+    planes, B, N, E, W = 3, 4, 12, 6, 7
+    base = rng.integers(1, 8, size=B).astype(np.int32)
+    L = int(base.max()) + N + 3
+    c = _tagged_cache(planes, B, L, E, base, N)
+    par = np.stack([synth.make_tree_parents(rng, N, max_depth=W - 1) for _ in range(B)])
+    path = np.full((B, W), -1, dtype=np.int32)
+    acc = np.zeros(B, dtype=np.int32)
+    for b in range(B):                      # a random root-to-node path
+        v = int(rng.integers(N))
+        chain = [v]
+        while chain[-1] != 0:
+            chain.append(int(par[b, chain[-1]]))
+        chain = chain[::-1]
+        acc[b] = len(chain) - 1
+        path[b, :len(chain)] = chain
+    out, new_len, bad = oracle_mod.kv_commit(c, base, acc, path, N)
+    assert not bad
+    assert np.array_equal(new_len, base + acc)
+    for b in range(B):
+        want = _appended(c, b, base[b], path[b], acc[b])
+        for p in range(planes):
+            n = base[b] + acc[b]
+            assert np.array_equal(out[p, b, :n], want[p])
+            assert np.array_equal(out[p, b, n:], c[p, b, n:])   # untouched past the new end
+            # the accepted entries are the path's nodes, in order
+            assert out[p, b, base[b]:n, 2].tolist() == path[b, 1:acc[b] + 1].tolist()
+
+
+def test_kv_commit_chain_and_empty_paths_change_nothing(oracle_mod):
+    planes, B, N, E = 2, 3, 8, 4
+    base = np.array([2, 5, 1], dtype=np.int32)
+    L = 16
+    c = _tagged_cache(planes, B, L, E, base, N)
+    path = np.full((B, 6), -1, dtype=np.int32)
+    path[:, 0] = 0
+    path[0, 1:4] = [1, 2, 3]                 # a chain: nodes already in place
+    acc = np.array([3, 0, 0], dtype=np.int32)
+    out, new_len, bad = oracle_mod.kv_commit(c, base, acc, path, N)
+    assert not bad and np.array_equal(out, c)
+    assert new_len.tolist() == [5, 5, 1]
+
+
+def test_kv_commit_overlapping_moves(oracle_mod):
+    # path 0 -> 2 -> 3 -> 5: node 2 moves onto node 1's slot while node 3
+    # moves onto node 2's old slot (a source of an earlier move)
+    c = _tagged_cache(1, 1, 12, 4, np.array([2]), 8)
+    path = np.array([[0, 2, 3, 5, -1]], dtype=np.int32)
+    out, new_len, _ = oracle_mod.kv_commit(c, [2], [3], path, 8)
+    assert out[0, 0, 2:5, 2].tolist() == [2, 3, 5]
+    assert new_len.tolist() == [5]
+
+
+def test_kv_commit_malformed_left_untouched(oracle_mod):
+    c = _tagged_cache(2, 3, 10, 4, np.array([2, 2, 2]), 6)
+    path = np.array([[1, 2, -1], [0, 6, -1], [0, 1, -1]], dtype=np.int32)
+    out, new_len, bad = oracle_mod.kv_commit(c, [2, 2, 6], [1, 1, 1], path, 6)
+    assert bad
+    assert np.array_equal(out, c)            # bad root, node >= N, tree past L
+    assert new_len.tolist() == [2, 2, 6]
