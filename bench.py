@@ -406,24 +406,37 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(result), flush=True)
 
 
-def _time_loop(fn, stream, K):
-    """Mean ms of fn() over K back-to-back calls on `stream` (3 untimed first)."""
+def _time_loop(fn, stream, K, per_graph=20):
+    """Mean ms of one fn() call on `stream`: `per_graph` calls are captured in
+    a CUDA graph and the graph is replayed until K calls have run (3 untimed
+    replays first), so host-side call overhead does not pace small kernels."""
     import torch
-    for _ in range(3):
-        fn()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        fn()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
     stream.synchronize()
-    return e0.elapsed_time(e1) / K
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(per_graph):
+            fn()
+    reps = max(1, K // per_graph)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / (reps * per_graph)
 
 
 def measure_next_rows(dev, stream, tree, K):
     """The kernels around the draft tree (each timed alone, outside the step):
-    tree attention mask of the tree workload's trees."""
+    tree attention mask of the tree workload's trees, and the KV commit of
+    the paths tree verification accepts on it."""
     import torch
     import speculative_decoding_verification_56_gb300 as sv
     out = {}
@@ -437,7 +450,39 @@ def measure_next_rows(dev, stream, tree, K):
     out["tree_mask"] = {"workload": f"B={Bt} N={N} trees (the tree-verification workload)",
                         "us_per_call": round(ms * 1e3, 3),
                         "bytes": int(Bt * N * 4 + Bt * N * W * 4 + Bt * N * 4),
-                        "bound": "launch latency (one kernel, a few KB)"}
+                        "bound": "launch latency (one kernel, a few KB)",
+                        "timed": "CUDA-graph replay of 20 calls"}
+
+    # KV commit of the paths that tree verification accepts on that workload:
+    # 32 layers x (K, V) planes, 8 KV heads x 128 bf16 per entry, 400+ prefix
+    res = sv.verify_tree_greedy(sv.to_device_logits(tree.target, tree.dtype, dev),
+                                torch.from_numpy(tree.tokens).to(dev), par, tree.max_depth)
+    path, acc = res["path_nodes"], res["accepted_len"]
+    planes, E, L = 64, 1024, 512
+    # successive calls use 12 prefix lengths 100, 130, ..., 430, so the entries
+    # they move (12 x ~12.6 MB) do not stay in the 129 MB L2 between calls
+    bases = [(100 + 30 * j + torch.arange(Bt, dtype=torch.int32, device=dev) % 2).contiguous()
+             for j in range(12)]
+    cache = torch.empty(planes, Bt, L, E, dtype=torch.bfloat16, device=dev).normal_()
+    new_len = torch.empty(Bt, dtype=torch.int32, device=dev)
+    wsk = sv.alloc_workspace(sv.SPEC_MODE_KV_COMMIT, Bt, N, 1, sv.SPEC_DTYPE_F32, dev)
+    p_np, a_np = path.cpu().numpy(), acc.cpu().numpy()
+    moves = sum(int((p_np[b, 1:a_np[b] + 1] != np.arange(1, a_np[b] + 1)).sum()) for b in range(Bt))
+    turn = [0]
+
+    def kv_call():
+        sv.spec_kv_commit_path(cache, bases[turn[0] % 12], acc, path, N, new_len, wsk, stream)
+        turn[0] += 1
+    ms = _time_loop(kv_call, stream, K, per_graph=24)
+    byts = 2 * moves * planes * E * 2
+    out["kv_commit"] = {"workload": f"B={Bt} accepted tree paths ({int(a_np.sum())} nodes, "
+                                    f"{moves} moved), {planes} planes x {E} bf16 per entry; "
+                                    "12 rotating prefix lengths (151 MB touched > L2)",
+                        "us_per_call": round(ms * 1e3, 3), "bytes": int(byts),
+                        "gb_s": round(byts / (ms / 1e3) / 1e9, 1),
+                        "bound": "HBM gather, latency at this size",
+                        "timed": "CUDA-graph replay of 24 calls"}
+    del cache
     return out
 
 

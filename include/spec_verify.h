@@ -71,7 +71,8 @@ typedef enum {
   SPEC_MODE_SAMPLE = 0,
   SPEC_MODE_GREEDY = 1,
   SPEC_MODE_TREE_GREEDY = 2,
-  SPEC_MODE_TREE_MASK = 3 /* spec_tree_attention_mask: the flag header only */
+  SPEC_MODE_TREE_MASK = 3, /* spec_tree_attention_mask: the flag header only */
+  SPEC_MODE_KV_COMMIT = 4  /* spec_kv_commit_path: the flag header only */
 } spec_mode_t;
 
 /* Bits of the workspace flag word (sticky until read with clear != 0). */
@@ -83,6 +84,11 @@ typedef enum {
 #define SPEC_FLAG_TIMEOUT 16u          /* a kernel gave up waiting for its own
                                           bulk copies (outputs of that call are
                                           unspecified); never expected */
+#define SPEC_FLAG_BAD_PATH 32u         /* spec_kv_commit_path: a path that does
+                                          not start at node 0, names a node
+                                          outside [1, N), is longer than
+                                          max_depth, or a tree that does not fit
+                                          the cache; that sequence is untouched */
 
 /* Limits checked on the host. */
 #define SPEC_MAX_V (1 << 26)
@@ -200,6 +206,38 @@ SPEC_API spec_status_t spec_verify_tree_greedy(const void* target_logits, int dt
 SPEC_API spec_status_t spec_tree_attention_mask(const int32_t* parents, int B, int N,
                                                 uint32_t* mask, int32_t* depth, void* workspace,
                                                 size_t workspace_bytes, void* stream);
+
+/*
+ * KV commit of the accepted path ("EAGLE-3 speculative decoding review",
+ * "The Complete EAGLE-3 Inference Process" step 5: keep only the accepted
+ * path's cache entries, discard the rejected branches, resume drafting from
+ * the committed prefix).  Tree node v >= 1 of sequence b holds its entries at
+ * cache position base_len[b] + v - 1 (the tree follows the committed prefix,
+ * whose last token is the root).  For the path 0, v_1, ..., v_d written by
+ * spec_verify_tree_greedy (d = accepted_len[b]), node v_i's entry moves to
+ * position base_len[b] + i - 1 in every plane, in place; every other
+ * position keeps its contents; new_len[b] = base_len[b] + d (the bonus token
+ * has no cache entry yet).
+ *   cache        device bytes; entry (plane p, sequence b, position t) starts
+ *                at p * plane_stride + b * seq_stride + t * entry_bytes (a
+ *                plane is one layer's K or V); 16-byte aligned, entry_bytes
+ *                and both strides multiples of 16; entries must not overlap
+ *   L            positions per sequence; N tree nodes; base_len[b] >= 1 and
+ *                base_len[b] + N - 1 <= L
+ *   base_len, accepted_len  int32 [B]; path_nodes int32 [B, max_depth + 1]
+ *   new_len      int32 [B] out
+ * A malformed sequence (see SPEC_FLAG_BAD_PATH) is left untouched with
+ * new_len = base_len.  Workspace: spec_verify_workspace_bytes(
+ * SPEC_MODE_KV_COMMIT, ...) bytes (the flag header).  One kernel launch (one
+ * CTA per sequence and plane; the moved entries are staged in shared memory
+ * before any is stored); planes <= 65535.
+ */
+SPEC_API spec_status_t spec_kv_commit_path(void* cache, int B, int planes, long long plane_stride,
+                                           long long seq_stride, int entry_bytes, int L, int N,
+                                           const int32_t* base_len, const int32_t* accepted_len,
+                                           const int32_t* path_nodes, int max_depth,
+                                           int32_t* new_len, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 
 /*
  * Copy the workspace's flag word to *host_flags (synchronises `stream`); with

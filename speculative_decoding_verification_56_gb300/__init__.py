@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
 * :func:`spec_verify_greedy`      -- greedy verification of chains
 * :func:`spec_verify_tree_greedy` -- greedy verification of draft trees
 * :func:`spec_tree_attention_mask` -- ancestor bitmask + depth of draft trees
+* :func:`spec_kv_commit_path`     -- move the accepted path's KV entries into place
 * :func:`spec_verify_workspace_bytes`, :func:`spec_verify_read_flags`,
   :func:`spec_verify_launch_count`, :func:`spec_status_string`
 
@@ -40,11 +41,13 @@ SPEC_MODE_SAMPLE = 0
 SPEC_MODE_GREEDY = 1
 SPEC_MODE_TREE_GREEDY = 2
 SPEC_MODE_TREE_MASK = 3
+SPEC_MODE_KV_COMMIT = 4
 SPEC_FLAG_TOKEN_RANGE = 1
 SPEC_FLAG_BAD_PARENT = 2
 SPEC_FLAG_DEPTH = 4
 SPEC_FLAG_RESIDUAL_FALLBACK = 8
 SPEC_FLAG_TIMEOUT = 16
+SPEC_FLAG_BAD_PATH = 32
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +85,9 @@ def load_library(path: str = LIB_PATH):
         lib.spec_verify_selftest_exp2.restype = I
         lib.spec_tree_attention_mask.argtypes = [P, I, I, P, P, P, Z, P]
         lib.spec_tree_attention_mask.restype = I
+        LL = ctypes.c_longlong
+        lib.spec_kv_commit_path.argtypes = [P, I, I, LL, LL, I, I, I, P, P, P, I, P, P, Z, P]
+        lib.spec_kv_commit_path.restype = I
         lib.spec_verify_read_flags.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I, P]
         lib.spec_verify_read_flags.restype = I
         lib.spec_verify_launch_count.argtypes = []
@@ -258,6 +264,24 @@ def spec_tree_attention_mask(parents, mask, depth, workspace, stream=None):
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream_ptr(stream))
     _check(st, "spec_tree_attention_mask")
+
+
+def spec_kv_commit_path(cache, base_len, accepted_len, path_nodes, N, new_len, workspace,
+                        stream=None):
+    """KV commit of the accepted path (C ABI ``spec_kv_commit_path``), in
+    place.  ``cache``: contiguous CUDA tensor [planes, B, L, ...] (one entry =
+    the trailing dimensions of one position)."""
+    torch = _torch()
+    planes, B, L = cache.shape[:3]
+    entry = cache[0, 0, 0].numel() * cache.element_size()
+    st = load_library().spec_kv_commit_path(
+        _dev(cache, "cache"), B, planes, B * L * entry, L * entry, entry, L, int(N),
+        _dev(base_len, "base_len", torch.int32), _dev(accepted_len, "accepted_len", torch.int32),
+        _dev(path_nodes, "path_nodes", torch.int32), path_nodes.shape[1] - 1,
+        _dev(new_len, "new_len", torch.int32),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream))
+    _check(st, "spec_kv_commit_path")
 
 
 def spec_verify_read_flags(workspace, clear: bool = True, stream=None) -> int:

@@ -46,7 +46,7 @@ struct Layout {
 
 // Returns false for arguments outside the documented limits.
 bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
-  if (mode == SPEC_MODE_TREE_MASK) {  // the flag header only
+  if (mode == SPEC_MODE_TREE_MASK || mode == SPEC_MODE_KV_COMMIT) {  // the flag header only
     if (B < 0 || kN < 1 || kN > SPEC_MAX_TREE_NODES) return false;
     L->bytes = kHeaderBytes;
     return true;
@@ -420,6 +420,51 @@ spec_status_t spec_tree_attention_mask(const int32_t* parents, int B, int N, uin
   if (blocks > 0x7FFFFFFFLL) return SPEC_ERR_INVALID_ARG;
   sv::tree_mask_kernel<<<(unsigned)blocks, sv::kMaskThreads, 0, (cudaStream_t)stream>>>(
       parents, B, N, W, mask, depth, reinterpret_cast<unsigned*>(workspace));
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return SPEC_OK;
+}
+
+spec_status_t spec_kv_commit_path(void* cache, int B, int planes, long long plane_stride,
+                                  long long seq_stride, int entry_bytes, int L, int N,
+                                  const int32_t* base_len, const int32_t* accepted_len,
+                                  const int32_t* path_nodes, int max_depth, int32_t* new_len,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || planes < 1 || planes > 65535 || entry_bytes < 16 || L < 1 || N < 1 ||
+      N > SPEC_MAX_TREE_NODES || max_depth < 0 || max_depth > SPEC_MAX_TREE_DEPTH ||
+      plane_stride < 0 || seq_stride < 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!cache || !base_len || !accepted_len || !path_nodes || !new_len)
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned(cache, 16) || entry_bytes % 16 || plane_stride % 16 || seq_stride % 16 ||
+      !aligned(base_len, 4) || !aligned(accepted_len, 4) || !aligned(path_nodes, 4) ||
+      !aligned(new_len, 4))
+    return SPEC_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < kHeaderBytes) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
+  sv::KvCommitParams prm;
+  prm.cache = static_cast<uint8_t*>(cache);
+  prm.plane_stride = plane_stride;
+  prm.seq_stride = seq_stride;
+  prm.entry_bytes = entry_bytes;
+  prm.L = L;
+  prm.N = N;
+  prm.max_depth = max_depth;
+  prm.planes = planes;
+  prm.base_len = base_len;
+  prm.accepted_len = accepted_len;
+  prm.path_nodes = path_nodes;
+  prm.new_len = new_len;
+  prm.flags = reinterpret_cast<unsigned*>(workspace);
+  // stage every moved entry of a pass in at most 40 KB of dynamic shared
+  // memory (under the 48 KB default with the kernel's static arrays)
+  constexpr int kStageBytes = 40 * 1024;
+  const int moves = std::max(1, std::min(max_depth, sv::kKvMaxMoves));
+  prm.slice_bytes = std::min(entry_bytes, kStageBytes / moves / 16 * 16);
+  const size_t smem = (size_t)prm.slice_bytes * moves;
+  sv::kv_commit_kernel<<<dim3((unsigned)B, (unsigned)planes), sv::kKvThreads, smem,
+                         (cudaStream_t)stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return SPEC_OK;

@@ -28,6 +28,7 @@ constexpr unsigned kFlagBadParent = 2u;
 constexpr unsigned kFlagDepth = 4u;
 constexpr unsigned kFlagResidualFallback = 8u;
 constexpr unsigned kFlagTimeout = 16u;
+constexpr unsigned kFlagBadPath = 32u;
 
 // Element storage traits: 16-byte vectors hold kEPV elements; kNegInf is a
 // vector of -inf used to pad past the end of a row.

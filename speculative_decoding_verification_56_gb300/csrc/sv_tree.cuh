@@ -8,6 +8,12 @@
 // is not materialised; the kernel writes the tree block: for node v of tree b,
 // a row of W = ceil(N/32) 32-bit words whose bit u % 32 of word u / 32 is set
 // iff u = v or u is an ancestor of v, plus depth(v).
+//
+// KV commit of the accepted path (same page, "The Complete EAGLE-3 Inference
+// Process" step 5: keep only the accepted path's cache entries and resume
+// from the committed prefix).  Tree node v >= 1 holds its entries at cache
+// position base + v - 1; the path 0, v_1, ..., v_d moves node v_i's entry to
+// position base + i - 1 in every plane (layer, K or V), in place.
 #pragma once
 
 #include "sv_device.cuh"
@@ -54,6 +60,85 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_kernel(const int32_t* 
   if (w == 0) {
     if (depth) depth[(size_t)b * N + v] = bad ? -1 : d;
     if (bad) set_flag(flags, kFlagBadParent);
+  }
+}
+
+struct KvCommitParams {
+  uint8_t* cache;
+  long long plane_stride, seq_stride;  // bytes
+  int entry_bytes, L, N, max_depth, planes;
+  const int32_t* base_len;
+  const int32_t* accepted_len;
+  const int32_t* path_nodes;  // [B, max_depth + 1]
+  int32_t* new_len;
+  unsigned* flags;
+  int slice_bytes;  // bytes of each moved entry staged per pass (multiple of 16)
+};
+
+
+constexpr int kKvMaxMoves = 64;  // path nodes staged per pass
+constexpr int kKvThreads = 128;
+
+// One CTA per (sequence, plane).  Thread 0 validates the path and lists the
+// moves (entries already in place, v_i == i, are skipped).  For every column
+// slice of the entries, all threads stage every moved entry in shared memory
+// with 16-byte asynchronous copies, wait for all of them, and only then store
+// them to their new positions, so an entry that is both moved and overwritten
+// is read first.
+__global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(const KvCommitParams p) {
+  extern __shared__ __align__(128) uint8_t kv_stage[];
+  __shared__ int s_src[kKvMaxMoves], s_dst[kKvMaxMoves];
+  __shared__ int s_ok, s_m;
+  const int b = blockIdx.x, plane = blockIdx.y;
+  const int base = p.base_len[b], d = p.accepted_len[b];
+  const int32_t* path = p.path_nodes + (size_t)b * (p.max_depth + 1);
+  if (threadIdx.x == 0) {
+    bool ok = base >= 1 && (long long)base + p.N - 1 <= p.L && d >= 0 && d <= p.max_depth &&
+              path[0] == 0;
+    for (int i = 1; ok && i <= d; ++i)
+      if (path[i] < 1 || path[i] >= p.N) ok = false;
+    if (plane == 0) {
+      p.new_len[b] = ok ? base + d : base;
+      if (!ok) set_flag(p.flags, kFlagBadPath);
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  uint8_t* row = p.cache + (long long)plane * p.plane_stride + (long long)b * p.seq_stride;
+  for (int i0 = 1; i0 <= d; i0 += kKvMaxMoves) {
+    const int i1 = min(d, i0 + kKvMaxMoves - 1);
+    if (threadIdx.x == 0) {
+      int m = 0;
+      for (int i = i0; i <= i1; ++i)
+        if (path[i] != i) {
+          s_src[m] = base + path[i] - 1;
+          s_dst[m] = base + i - 1;
+          ++m;
+        }
+      s_m = m;
+    }
+    __syncthreads();
+    const int m = s_m;
+    for (int c0 = 0; m > 0 && c0 < p.entry_bytes; c0 += p.slice_bytes) {
+      const int vps = min(p.slice_bytes, p.entry_bytes - c0) / 16;  // vectors per entry slice
+      for (int idx = threadIdx.x; idx < m * vps; idx += kKvThreads) {
+        const int j = idx / vps, e = idx - (idx / vps) * vps;
+        const uint8_t* src = row + (long long)s_src[j] * p.entry_bytes + c0 + e * 16;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                         smem_addr(kv_stage + (size_t)j * p.slice_bytes + e * 16)),
+                     "l"(src)
+                     : "memory");
+      }
+      asm volatile("cp.async.commit_group;\ncp.async.wait_all;" ::: "memory");
+      __syncthreads();  // every moved entry of this slice is staged
+      for (int idx = threadIdx.x; idx < m * vps; idx += kKvThreads) {
+        const int j = idx / vps, e = idx - (idx / vps) * vps;
+        const uint4 v = lds128(kv_stage + (size_t)j * p.slice_bytes + e * 16);
+        *reinterpret_cast<uint4*>(row + (long long)s_dst[j] * p.entry_bytes + c0 + e * 16) = v;
+      }
+      __syncthreads();  // the staging buffer is free again
+    }
   }
 }
 

@@ -142,6 +142,27 @@ def test_tree_mask_host_validation(lib):
     assert f(FAKE, 0, 60, FAKE, FAKE, FAKE, 256, None) == 0            # B = 0: no work
 
 
+def test_kv_commit_host_validation(lib):
+    f = lib.spec_kv_commit_path
+    ok = [FAKE, 4, 64, 1 << 24, 1 << 20, 2048, 512, 60, FAKE, FAKE, FAKE, 6, FAKE, FAKE, 256, None]
+
+    def call(**kw):
+        a = list(ok)
+        names = ["cache", "B", "planes", "ps", "ss", "eb", "L", "N", "base", "acc", "path",
+                 "md", "nl", "ws", "wsb", "stream"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+    assert lib.spec_verify_workspace_bytes(4, 16, 60, 0, 0) == 256
+    assert call(B=-1) == 1 and call(planes=0) == 1 and call(planes=65536) == 1
+    assert call(eb=8) == 1 and call(N=0) == 1 and call(md=-1) == 1 and call(md=1025) == 1
+    assert call(cache=None) == 1 and call(path=None) == 1 and call(nl=None) == 1
+    assert call(cache=FAKE + 8) == 2 and call(eb=2056) == 2 and call(ps=(1 << 24) + 4) == 2
+    assert call(base=FAKE + 2) == 2
+    assert call(ws=None) == 3 and call(wsb=100) == 3 and call(ws=FAKE + 16) == 2
+    assert call(B=0) == 0
+
+
 def test_read_flags_validation(lib):
     v = ctypes.c_uint32(0)
     assert lib.spec_verify_read_flags(None, ctypes.byref(v), 0, None) == 1

@@ -98,3 +98,105 @@ def test_tree_mask_malformed_is_flagged_and_matches():
     assert bad and flags & sv.SPEC_FLAG_BAD_PARENT
     assert np.array_equal(m_g, m_o) and np.array_equal(d_g, d_o)
     assert (d_g[0] >= 0).all()
+
+
+# ---------------------------------------------------------------------------
+# KV commit of the accepted path
+# ---------------------------------------------------------------------------
+
+def _random_paths(rng, par, W):
+    """A random root-to-node path per tree (as tree verification writes it)."""
+    B, N = par.shape
+    path = np.full((B, W), -1, dtype=np.int32)
+    acc = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        v = int(rng.integers(N))
+        chain = [v]
+        while chain[-1] != 0:
+            chain.append(int(par[b, chain[-1]]))
+        chain = chain[::-1][:W]
+        acc[b] = len(chain) - 1
+        path[b, :len(chain)] = chain
+    return path, acc
+
+
+def _gpu_kv(cache, base, acc, path, N):
+    c = torch.from_numpy(np.ascontiguousarray(cache)).cuda()
+    B = cache.shape[1]
+    ws = sv.alloc_workspace(sv.SPEC_MODE_KV_COMMIT, B, N, 1, sv.SPEC_DTYPE_F32)
+    new_len = torch.empty(B, dtype=torch.int32, device="cuda")
+    sv.spec_kv_commit_path(c, torch.from_numpy(np.asarray(base, np.int32)).cuda(),
+                           torch.from_numpy(np.asarray(acc, np.int32)).cuda(),
+                           torch.from_numpy(np.ascontiguousarray(path, np.int32)).cuda(), N,
+                           new_len, ws)
+    torch.cuda.synchronize()
+    return c.cpu().numpy(), new_len.cpu().numpy(), sv.spec_verify_read_flags(ws)
+
+
+@pytest.mark.parametrize("planes,B,N,E,W,seed", [
+    (1, 1, 8, 8, 6, 0),          # 16-byte entries (bf16 x 8)
+    (4, 5, 30, 64, 7, 1),
+    (64, 16, 60, 1024, 7, 2),    # 32 layers x K/V, 8 heads x 128 bf16
+    (3, 4, 200, 40, 40, 3),      # deep paths
+    (2, 3, 300, 8, 120, 4),      # more moves than one staging pass holds
+    (2, 2, 20, 40000, 10, 5),    # entries sliced across passes
+])
+def test_kv_commit_matches_oracle(planes, B, N, E, W, seed):
+    rng = np.random.default_rng(seed)
+    depth = W - 1
+    if W >= 100:  # deep, mostly two-way trees: paths longer than one staging pass
+        par = np.stack([np.concatenate([[-1, 0], np.arange(2, N) - rng.integers(1, 3, N - 2)])
+                        for _ in range(B)]).astype(np.int32)
+    else:
+        par = np.stack([synth.make_tree_parents(rng, N, max_depth=depth, max_children=3)
+                        for _ in range(B)]).astype(np.int32)
+    base = rng.integers(1, 50, size=B).astype(np.int32)
+    L = int(base.max()) + N + int(rng.integers(0, 5))
+    cache = rng.integers(-30000, 30000, size=(planes, B, L, E), dtype=np.int16)
+    path, acc = _random_paths(rng, par, W)
+    want, want_len, bad = oracle.kv_commit(cache, base, acc, path, N)
+    got, got_len, flags = _gpu_kv(cache, base, acc, path, N)
+    assert not bad and flags == 0
+    assert np.array_equal(got_len, want_len)
+    assert np.array_equal(got, want)
+
+
+def test_kv_commit_overlaps_chain_empty_and_malformed():
+    rng = np.random.default_rng(9)
+    planes, B, N, E, W = 3, 6, 10, 16, 6
+    base = np.array([2, 3, 1, 4, 2, 9], dtype=np.int32)
+    L = 20
+    cache = rng.integers(-30000, 30000, size=(planes, B, L, E), dtype=np.int16)
+    path = np.full((B, W), -1, dtype=np.int32)
+    path[:, 0] = 0
+    path[0, 1:4] = [2, 3, 5]        # overlapping moves
+    path[1, 1:4] = [1, 2, 3]        # a chain: nothing moves
+    acc = np.array([3, 3, 0, 2, 1, 1], dtype=np.int32)   # seq 2: empty path
+    path[3, 1:3] = [4, 10]          # node outside [1, N): malformed
+    path[4, 0] = 1                  # does not start at the root: malformed
+    path[5, 1] = 1                  # tree past the cache end: malformed
+    want, want_len, bad = oracle.kv_commit(cache, base, acc, path, N)
+    got, got_len, flags = _gpu_kv(cache, base, acc, path, N)
+    assert bad and flags & sv.SPEC_FLAG_BAD_PATH
+    assert np.array_equal(got_len, want_len) and np.array_equal(got, want)
+    assert np.array_equal(got[:, 1:3], cache[:, 1:3])      # chain and empty: untouched
+
+
+def test_kv_commit_after_tree_verification():
+    # the path written by spec_verify_tree_greedy drives the commit
+    t = synth.tree(seed=1)
+    out = sv.verify_tree_greedy(sv.to_device_logits(t.target, t.dtype),
+                                torch.from_numpy(t.tokens).cuda(),
+                                torch.from_numpy(t.parents).cuda(), t.max_depth)
+    torch.cuda.synchronize()
+    path = out["path_nodes"].cpu().numpy()
+    acc = out["accepted_len"].cpu().numpy()
+    rng = np.random.default_rng(3)
+    planes, E = 8, 256
+    base = (100 + np.arange(t.B)).astype(np.int32)
+    L = int(base.max()) + t.N
+    cache = rng.integers(-30000, 30000, size=(planes, t.B, L, E), dtype=np.int16)
+    want, want_len, bad = oracle.kv_commit(cache, base, acc, path, t.N)
+    got, got_len, flags = _gpu_kv(cache, base, acc, path, t.N)
+    assert not bad and flags == 0
+    assert np.array_equal(got_len, want_len) and np.array_equal(got, want)
