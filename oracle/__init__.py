@@ -71,6 +71,8 @@ def _bind(lib):
     LL = ctypes.c_longlong
     lib.oracle_kv_commit.argtypes = [P, P, ctypes.c_size_t, I, I, LL, LL, I, I, I, P, P, P, I, P]
     lib.oracle_kv_commit.restype = I
+    lib.oracle_lm_head_greedy.argtypes = [P, P, P, I, I, I, I, P, I, P, P, P, P, P]
+    lib.oracle_lm_head_greedy.restype = I
     lib.oracle_expected_tokens.argtypes = [D, I]
     lib.oracle_expected_tokens.restype = D
     lib.oracle_speedup_model.argtypes = [D, I, D]
@@ -219,6 +221,33 @@ def kv_commit(cache, base_len, accepted_len, path_nodes, N, lib=None):
     if rc not in (0, 4):
         _check(rc)
     return out, new_len, rc == 4
+
+
+def lm_head_greedy(hidden, w_lm, tokens, seqs=None, lib=None):
+    """LM head fused with greedy verification (reading R11 of spec_oracle.c).
+    ``hidden`` uint16 bf16 bits [B*(k+1), d], ``w_lm`` uint16 bf16 bits
+    [V, d], ``tokens`` int32 [B, k]; ``seqs``: the sequences to evaluate
+    (default all).  Returns dict(accepted_len [B], out_tokens [B, k+1],
+    argmax, gap, mag [B*(k+1)]); entries of sequences not evaluated are -2 /
+    NaN."""
+    lib = lib or _load()
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    B, k = tok.shape
+    H = np.ascontiguousarray(hidden, dtype=np.uint16)
+    Wm = np.ascontiguousarray(w_lm, dtype=np.uint16)
+    V, d = Wm.shape
+    assert H.shape == (B * (k + 1), d)
+    res = dict(accepted_len=np.full(B, -2, np.int32),
+               out_tokens=np.full((B, k + 1), -2, np.int32),
+               argmax=np.full(B * (k + 1), -2, np.int32),
+               gap=np.full(B * (k + 1), np.nan), mag=np.full(B * (k + 1), np.nan))
+    sq = None if seqs is None else np.ascontiguousarray(seqs, dtype=np.int32)
+    rc = lib.oracle_lm_head_greedy(_ptr(H), _ptr(Wm), _ptr(tok), B, k, d, V,
+                                   None if sq is None else _ptr(sq), 0 if sq is None else len(sq),
+                                   _ptr(res["accepted_len"]), _ptr(res["out_tokens"]),
+                                   _ptr(res["argmax"]), _ptr(res["gap"]), _ptr(res["mag"]))
+    _check(rc)
+    return res
 
 
 def expected_tokens(alpha: float, gamma: int, lib=None) -> float:

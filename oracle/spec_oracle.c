@@ -46,6 +46,12 @@
  *      position as it was, and commits base + d positions (the bonus token
  *      has no cache entry yet).  A sequence whose path is malformed is left
  *      untouched and reported.
+ *   R11 LM head fused with greedy verification: z = W_LM h for every target
+ *      position (h the position's hidden state, W_LM [V, d]), exact in
+ *      float64 from the bf16 inputs; then R7 on z.  The argmax gap (top-1
+ *      minus top-2) and the magnitude sum |W_j*| . |h| of the winner are
+ *      reported so that a comparison can excuse rows whose argmax a float32
+ *      accumulation could legitimately move.
  *   Non-finite logits are outside the method's domain (rejected here).
  */
 #include <math.h>
@@ -427,6 +433,67 @@ int oracle_kv_commit(const uint8_t* cache_in, uint8_t* cache_out, size_t cache_b
     new_len[b] = base + d;
   }
   return bad ? OR_ERR_TREE : OR_OK;
+}
+
+/*
+ * LM head fused with greedy verification.  [MATH] "Why feature drafting
+ * lands a higher acceptance rate" (drafted features go through the target's
+ * own LM head: logits z = W_LM h); [REVIEW] "Does Using a Small Model's
+ * Answer Reduce Quality?" greedy bullets (accept while the draft equals the
+ * target argmax, then emit the target's token).  Reading R11.
+ *
+ * hidden [B*(k+1), d] bf16 (row b*(k+1)+i is target position i of sequence
+ * b), w_lm [V, d] bf16, tokens [B, k].  Sequences listed in `seqs` (nseq of
+ * them; NULL = all) are evaluated; outputs are indexed by sequence and row:
+ * accepted_len [B], out_tokens [B, k+1], argmax [B*(k+1)], gap and mag
+ * [B*(k+1)] (float64).
+ */
+int oracle_lm_head_greedy(const uint16_t* hidden, const uint16_t* w_lm, const int32_t* tokens,
+                          int B, int k, int d, int V, const int32_t* seqs, int nseq,
+                          int32_t* accepted_len, int32_t* out_tokens, int32_t* argmax,
+                          double* gap, double* mag) {
+  if (B < 0 || k < 0 || d < 1 || V < 1) return OR_ERR_ARG;
+  double* h = (double*)malloc(sizeof(double) * (size_t)d);
+  if (!h) return OR_ERR_NOMEM;
+  const int rows = k + 1;
+  const int n = seqs ? nseq : B;
+  for (int s = 0; s < n; ++s) {
+    const int b = seqs ? seqs[s] : s;
+    if (b < 0 || b >= B) { free(h); return OR_ERR_ARG; }
+    for (int i = 0; i < rows; ++i) {
+      const size_t row = (size_t)b * rows + i;
+      for (int c = 0; c < d; ++c) h[c] = logit_at(hidden, OR_BF16, row * (size_t)d + c);
+      double best = -INFINITY, second = -INFINITY;
+      int bj = 0;
+      for (int j = 0; j < V; ++j) {
+        double z = 0.0;
+        for (int c = 0; c < d; ++c) z += logit_at(w_lm, OR_BF16, (size_t)j * d + c) * h[c];
+        if (z > best) { second = best; best = z; bj = j; }
+        else if (z > second) second = z;
+      }
+      double m = 0.0;
+      for (int c = 0; c < d; ++c) m += fabs(logit_at(w_lm, OR_BF16, (size_t)bj * d + c) * h[c]);
+      argmax[row] = bj;
+      gap[row] = best - second;
+      mag[row] = m;
+    }
+    /* R7 on the row argmaxes */
+    int na = k;
+    for (int i = 0; i < k; ++i) {
+      const int x = tokens[(size_t)b * k + i];
+      if (x < 0 || x >= V) { free(h); return OR_ERR_TOKEN; }
+      if (x != argmax[(size_t)b * rows + i]) { na = i; break; }
+    }
+    accepted_len[b] = na;
+    for (int i = 0; i <= k; ++i) {
+      int v = -1;
+      if (i < na) v = tokens[(size_t)b * k + i];
+      else if (i == na) v = argmax[(size_t)b * rows + na];
+      out_tokens[(size_t)b * rows + i] = v;
+    }
+  }
+  free(h);
+  return OR_OK;
 }
 
 /* Expected tokens per verification pass with per-token acceptance alpha and

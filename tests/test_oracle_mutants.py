@@ -49,6 +49,12 @@ MUTANTS = {
     "kv_len_counts_bonus": ("new_len[b] = base + d;\n", "new_len[b] = base + d + 1;\n"),
     "kv_previous_node": ("const long long src = (long long)(base + path[i] - 1) * entry_bytes;",
                          "const long long src = (long long)(base + path[i - 1]) * entry_bytes;"),
+    "lm_head_transposed": ("z += logit_at(w_lm, OR_BF16, (size_t)j * d + c) * h[c];",
+                           "z += logit_at(w_lm, OR_BF16, (size_t)c * V + j) * h[c];"),
+    "lm_head_last_tie": ("if (z > best) { second = best; best = z; bj = j; }",
+                         "if (z >= best) { second = best; best = z; bj = j; }"),
+    "lm_head_emits_draft": ("else if (i == na) v = argmax[(size_t)b * rows + na];",
+                            "else if (i == na) v = na < k ? tokens[(size_t)b * k + na] : argmax[(size_t)b * rows + na];"),
     "mask_wrong_word": ("        row[cur / 32] |= 1u << (cur % 32);\n        ++d;",
                         "        row[cur % W] |= 1u << (cur % 32);\n        ++d;"),
 }
@@ -77,6 +83,9 @@ class _Variant:
     def kv_commit(self, *a, **kw):
         return oracle.kv_commit(*a, lib=self.lib, **kw)
 
+    def lm_head_greedy(self, *a, **kw):
+        return oracle.lm_head_greedy(*a, lib=self.lib, **kw)
+
     def expected_tokens(self, *a, **kw):
         return oracle.expected_tokens(*a, lib=self.lib, **kw)
 
@@ -97,6 +106,9 @@ def _pin_checks(o):
     yield lambda: pins.test_tree_mask_equals_closure(o, 1)
     yield lambda: pins.test_kv_commit_equals_appending_the_path(o, 0)
     yield lambda: pins.test_kv_commit_chain_and_empty_paths_change_nothing(o)
+    yield lambda: pins.test_lm_head_matches_float64_matmul(o)
+    yield lambda: pins.test_lm_head_equals_unfused_greedy_on_exact_logits(o, 0)
+    yield lambda: pins.test_lm_head_ties_and_subset(o)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

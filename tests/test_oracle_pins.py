@@ -605,3 +605,61 @@ def test_kv_commit_malformed_left_untouched(oracle_mod):
     assert bad
     assert np.array_equal(out, c)            # bad root, node >= N, tree past L
     assert new_len.tolist() == [2, 2, 6]
+
+
+# ---------------------------------------------------------------------------
+# LM head fused with greedy verification ("EAGLE math", "Why feature drafting
+# lands a higher acceptance rate": logits come from the target's LM head,
+# z = W_LM h; review page greedy bullets)
+# ---------------------------------------------------------------------------
+
+def _bf16_normal(rng, shape, scale=1.0):
+    return synth.f32_to_bf16_bits((scale * rng.standard_normal(shape)).astype(np.float32))
+
+
+def test_lm_head_matches_float64_matmul(oracle_mod):
+    rng = np.random.default_rng(0)
+    B, k, d, V = 3, 2, 48, 257
+    H = _bf16_normal(rng, (B * (k + 1), d))
+    W = _bf16_normal(rng, (V, d), 0.5)
+    res = oracle_mod.lm_head_greedy(H, W, np.zeros((B, k), np.int32))
+    z = synth.bf16_bits_to_f32(H).astype(np.float64) @ synth.bf16_bits_to_f32(W).astype(np.float64).T
+    assert np.array_equal(res["argmax"], z.argmax(1))
+    top2 = np.sort(z, axis=1)[:, -2:]
+    assert np.allclose(res["gap"], top2[:, 1] - top2[:, 0], rtol=1e-12, atol=1e-12)
+    wa = synth.bf16_bits_to_f32(W).astype(np.float64)[res["argmax"]]
+    assert np.allclose(res["mag"], np.abs(wa * synth.bf16_bits_to_f32(H)).sum(1), rtol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_lm_head_equals_unfused_greedy_on_exact_logits(oracle_mod, seed):
+    # small integers: every logit is exact in float32, so verifying the
+    # materialised logits must give the same acceptance as the fused form
+    rng = np.random.default_rng(seed)
+    B, k, d, V = 6, 4, 40, 300
+    H = synth.f32_to_bf16_bits(rng.integers(-3, 4, (B * (k + 1), d)).astype(np.float32))
+    W = synth.f32_to_bf16_bits(rng.integers(-3, 4, (V, d)).astype(np.float32))
+    z = (synth.bf16_bits_to_f32(H).astype(np.float64) @
+         synth.bf16_bits_to_f32(W).astype(np.float64).T).astype(np.float32)
+    g = z.reshape(B, k + 1, V).argmax(-1)
+    tokens = np.where(rng.random((B, k)) < 0.7, g[:, :k], rng.integers(0, V, (B, k))).astype(np.int32)
+    fused = oracle_mod.lm_head_greedy(H, W, tokens)
+    plain = oracle_mod.verify_greedy(z.reshape(B, k + 1, V), tokens, dtype="f32")
+    assert np.array_equal(fused["accepted_len"], plain["accepted_len"])
+    assert np.array_equal(fused["out_tokens"], plain["out_tokens"])
+
+
+def test_lm_head_ties_and_subset(oracle_mod):
+    rng = np.random.default_rng(5)
+    B, k, d, V = 4, 1, 16, 20
+    H = _bf16_normal(rng, (B * (k + 1), d))
+    W = _bf16_normal(rng, (V, d))
+    W[7] = W[3]                                # identical vocabulary rows
+    h = synth.bf16_bits_to_f32(H).astype(np.float64)
+    W[3] = synth.f32_to_bf16_bits(np.float32(4.0) * np.sign(h[0]).astype(np.float32))
+    W[7] = W[3]
+    res = oracle_mod.lm_head_greedy(H, W, np.zeros((B, k), np.int32))
+    assert res["argmax"][0] == 3 and res["gap"][0] == 0.0   # lowest index wins a tie
+    sub = oracle_mod.lm_head_greedy(H, W, np.zeros((B, k), np.int32), seqs=[2])
+    assert np.array_equal(sub["argmax"][4:6], res["argmax"][4:6])
+    assert (sub["argmax"][:4] == -2).all()
