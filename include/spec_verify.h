@@ -72,7 +72,8 @@ typedef enum {
   SPEC_MODE_GREEDY = 1,
   SPEC_MODE_TREE_GREEDY = 2,
   SPEC_MODE_TREE_MASK = 3, /* spec_tree_attention_mask: the flag header only */
-  SPEC_MODE_KV_COMMIT = 4  /* spec_kv_commit_path: the flag header only */
+  SPEC_MODE_KV_COMMIT = 4, /* spec_kv_commit_path: the flag header only */
+  SPEC_MODE_LM_HEAD_GREEDY = 5 /* spec_lm_head_verify_greedy (k_or_N = k) */
 } spec_mode_t;
 
 /* Bits of the workspace flag word (sticky until read with clear != 0). */
@@ -238,6 +239,32 @@ SPEC_API spec_status_t spec_kv_commit_path(void* cache, int B, int planes, long 
                                            const int32_t* path_nodes, int max_depth,
                                            int32_t* new_len, void* workspace,
                                            size_t workspace_bytes, void* stream);
+
+/*
+ * The target's LM head fused with greedy verification ("EAGLE math", "Why
+ * feature drafting lands a higher acceptance rate": the target's logits are
+ * its LM head applied to the hidden state, z = W_LM h; "EAGLE-3 speculative
+ * decoding review", "Does Using a Small Model's Answer Reduce Quality?"
+ * greedy bullets).  Computes every target row's argmax of z = W_LM h on the
+ * tensor cores without writing the logits, then the same acceptance as
+ * spec_verify_greedy.
+ *   hidden       bf16 [B*(k+1), d]  row b*(k+1)+i: the target's hidden state
+ *                                   at draft position i of sequence b
+ *   w_lm         bf16 [V, d]        the LM head, row j = vocabulary entry j
+ *   draft_tokens int32 [B, k]
+ *   d            multiple of 8; hidden and w_lm 16-byte aligned
+ * Outputs as spec_verify_greedy.  The argmax is of the float32-accumulated
+ * products (lowest index among equal values); rows whose top two logits lie
+ * closer than the accumulation error may pick either.  Two kernel launches
+ * (tcgen05 GEMM with an argmax epilogue; record merge + chain resolve).
+ * Workspace: spec_verify_workspace_bytes(SPEC_MODE_LM_HEAD_GREEDY, B, k, V,
+ * SPEC_DTYPE_BF16).
+ */
+SPEC_API spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
+                                                  const int32_t* draft_tokens, int B, int k,
+                                                  int d, int V, int32_t* accepted_len,
+                                                  int32_t* out_tokens, void* workspace,
+                                                  size_t workspace_bytes, void* stream);
 
 /*
  * Copy the workspace's flag word to *host_flags (synchronises `stream`); with

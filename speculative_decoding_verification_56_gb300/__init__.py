@@ -12,6 +12,7 @@ Entry points (same names as the C ABI):
 * :func:`spec_verify_tree_greedy` -- greedy verification of draft trees
 * :func:`spec_tree_attention_mask` -- ancestor bitmask + depth of draft trees
 * :func:`spec_kv_commit_path`     -- move the accepted path's KV entries into place
+* :func:`spec_lm_head_verify_greedy` -- LM head (tcgen05 GEMM) fused with greedy verification
 * :func:`spec_verify_workspace_bytes`, :func:`spec_verify_read_flags`,
   :func:`spec_verify_launch_count`, :func:`spec_status_string`
 
@@ -42,6 +43,7 @@ SPEC_MODE_GREEDY = 1
 SPEC_MODE_TREE_GREEDY = 2
 SPEC_MODE_TREE_MASK = 3
 SPEC_MODE_KV_COMMIT = 4
+SPEC_MODE_LM_HEAD_GREEDY = 5
 SPEC_FLAG_TOKEN_RANGE = 1
 SPEC_FLAG_BAD_PARENT = 2
 SPEC_FLAG_DEPTH = 4
@@ -88,6 +90,8 @@ def load_library(path: str = LIB_PATH):
         LL = ctypes.c_longlong
         lib.spec_kv_commit_path.argtypes = [P, I, I, LL, LL, I, I, I, P, P, P, I, P, P, Z, P]
         lib.spec_kv_commit_path.restype = I
+        lib.spec_lm_head_verify_greedy.argtypes = [P, P, P, I, I, I, I, P, P, P, Z, P]
+        lib.spec_lm_head_verify_greedy.restype = I
         lib.spec_verify_read_flags.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I, P]
         lib.spec_verify_read_flags.restype = I
         lib.spec_verify_launch_count.argtypes = []
@@ -284,6 +288,27 @@ def spec_kv_commit_path(cache, base_len, accepted_len, path_nodes, N, new_len, w
     _check(st, "spec_kv_commit_path")
 
 
+def spec_lm_head_verify_greedy(hidden, w_lm, draft_tokens, accepted_len, out_tokens, workspace,
+                               stream=None):
+    """LM head fused with greedy verification (C ABI
+    ``spec_lm_head_verify_greedy``): ``hidden`` bf16 [B*(k+1), d], ``w_lm``
+    bf16 [V, d], ``draft_tokens`` int32 [B, k]."""
+    torch = _torch()
+    B, k = draft_tokens.shape
+    rows, d = hidden.shape
+    V = w_lm.shape[0]
+    if rows != B * (k + 1) or w_lm.shape[1] != d:
+        raise ValueError("hidden must be [B*(k+1), d] and w_lm [V, d]")
+    st = load_library().spec_lm_head_verify_greedy(
+        _dev(hidden, "hidden", torch.bfloat16), _dev(w_lm, "w_lm", torch.bfloat16),
+        _dev(draft_tokens, "draft_tokens", torch.int32), B, k, d, V,
+        _dev(accepted_len, "accepted_len", torch.int32),
+        _dev(out_tokens, "out_tokens", torch.int32),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream))
+    _check(st, "spec_lm_head_verify_greedy")
+
+
 def spec_verify_read_flags(workspace, clear: bool = True, stream=None) -> int:
     """Device flag bits recorded in ``workspace`` (synchronises the stream)."""
     out = ctypes.c_uint32(0)
@@ -369,6 +394,21 @@ def tree_attention_mask(parents, workspace=None, stream=None):
     depth = torch.empty(B, N, dtype=torch.int32, device=dev)
     spec_tree_attention_mask(parents, mask, depth, workspace, stream)
     return mask, depth
+
+
+def lm_head_verify_greedy(hidden, w_lm, draft_tokens, workspace=None, stream=None):
+    """Greedy verification straight from hidden states and the LM head."""
+    torch = _torch()
+    B, k = draft_tokens.shape
+    dev = hidden.device
+    if workspace is None:
+        workspace = alloc_workspace(SPEC_MODE_LM_HEAD_GREEDY, B, k, w_lm.shape[0],
+                                    SPEC_DTYPE_BF16, dev)
+    out = dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+               out_tokens=torch.empty(B, k + 1, dtype=torch.int32, device=dev))
+    spec_lm_head_verify_greedy(hidden, w_lm, draft_tokens, out["accepted_len"],
+                               out["out_tokens"], workspace, stream)
+    return out
 
 
 def to_device_logits(arr, dtype: str, device="cuda"):

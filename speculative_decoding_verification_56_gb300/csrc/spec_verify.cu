@@ -13,11 +13,14 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "spec_verify.h"
 #include "sv_kernels.cuh"
 #include "sv_tree.cuh"
+#include "sv_lmhead.cuh"
 
 static_assert(sv::kMaxDraft == SPEC_MAX_K, "finish kernel buffers are sized for SPEC_MAX_K");
 
@@ -28,6 +31,7 @@ std::atomic<uint64_t> g_launches{0};
 constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kDataOffset = kHeaderBytes;
+constexpr int kLmMaxGrid = 1024;  // CTAs (records per row) of the fused LM-head kernel
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -49,6 +53,20 @@ bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
   if (mode == SPEC_MODE_TREE_MASK || mode == SPEC_MODE_KV_COMMIT) {  // the flag header only
     if (B < 0 || kN < 1 || kN > SPEC_MAX_TREE_NODES) return false;
     L->bytes = kHeaderBytes;
+    return true;
+  }
+  if (mode == SPEC_MODE_LM_HEAD_GREEDY) {  // argmax records of up to kLmMaxGrid CTAs per row
+    if (B < 0 || kN < 0 || kN > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return false;
+    const long long rows = (long long)B * (kN + 1);
+    if (rows * kLmMaxGrid > 0x7FFFFFFFLL) return false;
+    L->rows = (int)rows;
+    L->nchunks = kLmMaxGrid;
+    size_t off = kDataOffset;
+    L->off_part = off;
+    off = align_up(off + (size_t)rows * kLmMaxGrid * sizeof(sv::ArgPartial));
+    L->off_arg = off;
+    off = align_up(off + (size_t)rows * sizeof(int32_t));
+    L->bytes = off;
     return true;
   }
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return false;
@@ -177,6 +195,37 @@ spec_status_t ensure_smem(size_t bytes) {
     done[dev] = true;
   }
   return SPEC_OK;
+}
+
+// TMA descriptor of a row-major bf16 matrix [outer, inner] read as K-major
+// boxes of 64 x box_outer with 128-byte swizzle (out-of-range rows and
+// columns read as zero).  The driver's encoder is looked up once.
+std::mutex g_encode_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+spec_status_t encode_bf16_kmajor(CUtensorMap* map, const void* base, int inner, int outer,
+                                 int box_outer) {
+  {
+    std::lock_guard<std::mutex> lock(g_encode_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return SPEC_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)sv::kLmBK, (cuuint32_t)box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SPEC_OK : SPEC_ERR_INVALID_ARG;
 }
 
 template <typename E, bool kVec>
@@ -468,6 +517,100 @@ spec_status_t spec_kv_commit_path(void* cache, int B, int planes, long long plan
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return SPEC_OK;
+}
+
+spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
+                                         const int32_t* draft_tokens, int B, int k, int d, int V,
+                                         int32_t* accepted_len, int32_t* out_tokens,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || k < 0 || k > SPEC_MAX_K || d < 8 || d > (1 << 20) || d % 8 || V < 1 ||
+      V > SPEC_MAX_V)
+    return SPEC_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(SPEC_MODE_LM_HEAD_GREEDY, B, k, V, SPEC_DTYPE_BF16, &L))
+    return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!hidden || !w_lm || !accepted_len || !out_tokens || (k > 0 && !draft_tokens))
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(w_lm, 16) || !aligned(accepted_len, 4) ||
+      !aligned(out_tokens, 4) || (k > 0 && !aligned(draft_tokens, 4)))
+    return SPEC_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
+  const int rows = L.rows;
+  const int ntiles = (V + sv::kLmBV - 1) / sv::kLmBV;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  // one CTA per SM in clusters of kLmCluster: as many clusters as can be
+  // resident at once (measured for this launch shape)
+  int max_clusters = 0;
+  // row groups of at most kLmMaxRows rows, split evenly, each a multiple of
+  // the 64-row H box (so two MMAs of equal N stay multiples of 16)
+  const int gy = (rows + sv::kLmMaxRows - 1) / sv::kLmMaxRows;
+  if (gy > 65535) return SPEC_ERR_INVALID_ARG;
+  const int grp = ((rows + gy - 1) / gy + sv::kLmHBox - 1) / sv::kLmHBox * sv::kLmHBox;
+  const int stage_bytes = sv::kLmABytes + grp * 128;
+  const int smem = sv::kLmStages * stage_bytes + 1024;
+  spec_status_t st = ensure_smem<sv::lmhead_argmax_kernel>(
+      (size_t)sv::kLmStages * (sv::kLmABytes + sv::kLmBBytes) + 1024);
+  if (st != SPEC_OK) return st;
+  CUtensorMap map_h, map_w;
+  st = encode_bf16_kmajor(&map_h, hidden, d, rows, sv::kLmHBox);
+  if (st != SPEC_OK) return st;
+  st = encode_bf16_kmajor(&map_w, w_lm, d, V, sv::kLmBV);
+  if (st != SPEC_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  sv::LmHeadParams lp;
+  lp.rows = rows;
+  lp.d = d;
+  lp.V = V;
+  lp.ntiles = ntiles;
+  lp.grp_rows = grp;
+  lp.stage_bytes = stage_bytes;
+  lp.part = reinterpret_cast<sv::ArgPartial*>(ws + L.off_part);
+  lp.flags = reinterpret_cast<unsigned*>(ws);
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = sv::kLmCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(sv::kLmThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = (cudaStream_t)stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)(sms / sv::kLmCluster * sv::kLmCluster), (unsigned)gy, 1);
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, sv::lmhead_argmax_kernel, &cfg) !=
+          cudaSuccess ||
+      max_clusters < 1)
+    return SPEC_ERR_CUDA;
+  const int nclusters = std::max(1, std::min(std::min(max_clusters, (ntiles + 1) / 2),
+                                             kLmMaxGrid / sv::kLmCluster));
+  const int gx = nclusters * sv::kLmCluster;
+  lp.nclusters = nclusters;
+  cfg.gridDim = dim3((unsigned)gx, (unsigned)gy, 1);
+  if (cudaLaunchKernelEx(&cfg, sv::lmhead_argmax_kernel, map_h, map_w, lp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  // merge the per-CTA records and resolve the chains (the greedy resolve)
+  sv::ArgmaxParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  prm.tokens = draft_tokens;
+  prm.B = B;
+  prm.rows_per_seq = k + 1;
+  prm.V = V;
+  prm.nchunks = gx;
+  prm.tree = 0;
+  prm.accepted_len = accepted_len;
+  prm.out_tokens = out_tokens;
+  prm.flags = lp.flags;
+  prm.part = lp.part;
+  prm.rowarg = reinterpret_cast<int32_t*>(ws + L.off_arg);
+  return launch(sv::argmax_resolve_kernel, B, 0, prm, stream, true);
 }
 
 spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_flags, int clear,

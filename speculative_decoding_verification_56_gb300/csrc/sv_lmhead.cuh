@@ -1,0 +1,392 @@
+// sv_lmhead.cuh -- the target's LM head fused with greedy verification, on
+// the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// "EAGLE math", "Why feature drafting lands a higher acceptance rate": the
+// target's logits are its LM head applied to the hidden state, z = W_LM h.
+// Greedy verification ("EAGLE-3 speculative decoding review", "Does Using a
+// Small Model's Answer Reduce Quality?" greedy bullets) needs only each
+// target row's argmax, so the GEMM's epilogue keeps a running (max, lowest
+// index) per row and the [rows, V] logits are never written.
+//
+//   Z tile^T = W_LM[v0 : v0+128, :] x H[rows, :]^T   (both K-major, bf16)
+//
+// The vocabulary is the MMA's M (128 tensor-memory lanes per tile) and the
+// rows are its N (up to 384 columns, one or two MMAs of N <= 256), so rows
+// are padded only to a multiple of 64.  One CTA per SM walks a contiguous
+// range of vocabulary tiles for a group of rows.  Warp roles (192 threads):
+//   warp 0     TMA producer: per 64-wide K step, the tile's W slice and the
+//              rows' H slice (128-byte swizzled) into a 3-stage ring
+//   warp 1     allocates tensor memory; lane 0 issues tcgen05.mma
+//              (M=128, N=rows/2 or rows, K=16) into a 128 x rows fp32
+//              accumulator and commits stage releases and tile completion
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quadrant, a butterfly
+//              reduction across lanes per column (row), a merge of the four
+//              quadrants in shared memory and a running argmax per row
+//              (lowest index wins ties); the accumulator is released as
+//              soon as it has been read
+// Each CTA writes one argmax record per row for its vocabulary segment, in
+// the layout the greedy resolve kernel merges.  Every wait is bounded.
+#pragma once
+
+#include <cuda.h>
+
+#include "sv_kernels.cuh"
+
+namespace sv {
+
+constexpr int kLmBV = 128;         // vocabulary per tile (UMMA M, tensor-memory lanes)
+constexpr int kLmMaxRows = 384;    // rows per row group (UMMA N total, tensor-memory columns;
+                                   // three stages of 16 KB + 48 KB fit in shared memory)
+constexpr int kLmMaxN = 256;       // N of one MMA instruction
+constexpr int kLmBK = 64;          // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kLmStages = 3;
+constexpr int kLmThreads = 192;
+constexpr int kLmABytes = kLmBV * kLmBK * 2;          // 16 KB: W slice
+constexpr int kLmBBytes = kLmMaxRows * kLmBK * 2;     // up to 48 KB: H slice
+constexpr int kLmHBox = 64;                           // rows per H box (TMA)
+constexpr int kLmTmemCols = 512;
+constexpr int kLmCluster = 2;      // CTAs sharing each H slice (TMA multicast)
+
+struct LmHeadParams {
+  int rows, d, V;       // rows = B * (k+1)
+  int ntiles;           // ceil(V / kLmBV)
+  int nclusters;        // gridDim.x / kLmCluster
+  int grp_rows;         // rows per row group (multiple of kLmHBox, <= kLmMaxRows)
+  int stage_bytes;      // kLmABytes + grp_rows * 128
+  ArgPartial* part;     // [rows, gridDim.x] one record per CTA segment
+  unsigned* flags;
+};
+
+// --- tcgen05 / TMA helpers (inline PTX) ------------------------------------
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand:
+// start address >> 4 (bits 0-13), leading-byte offset 0 (unused for swizzled
+// K-major), stride-byte offset 1024 >> 4 between 8-row groups (bits 32-45),
+// descriptor version 1 (bits 46-47), layout "128-byte swizzle" = 2 (bits
+// 61-63).  The operand tile starts on a 1024-byte boundary; a K step of 16
+// elements inside the 128-byte row advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_byte_addr) {
+  return (uint64_t)((smem_byte_addr & 0x3FFFFu) >> 4) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and
+// B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
+// (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// The same, landing at this offset in every CTA of `mask` (a cluster), each
+// copy completing on that CTA's barrier at the same offset.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
+                                               uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued completes.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+// Arrive on the barrier at this offset in every CTA of `mask` once every
+// tcgen05 operation this thread issued completes.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of the warp's 32 lanes: thread t gets lane
+// (quadrant base + t), columns [col, col + 32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+
+// (value, index) comparison: larger value, then lower index.
+__device__ __forceinline__ bool lm_better(float v1, int i1, float v2, int i2) {
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lmhead_argmax_kernel(const __grid_constant__ CUtensorMap map_h,
+                         const __grid_constant__ CUtensorMap map_w, const LmHeadParams p) {
+  extern __shared__ uint8_t lm_raw[];
+  __shared__ uint64_t full[kLmStages], empty[kLmStages];
+  __shared__ uint64_t acc_full, acc_empty, drain;
+  __shared__ uint32_t tmem_base_holder;
+  __shared__ int s_abort;
+  __shared__ float red_v[4][kLmMaxRows];  // per-quadrant column maxima of one tile
+  __shared__ int red_i[4][kLmMaxRows];
+
+  // 1024-byte aligned operand ring (128-byte swizzle atoms)
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(lm_raw) + 1023) & ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = blockIdx.y * p.grp_rows;  // first row of this CTA's row group
+  const int R = p.grp_rows;                  // columns used (rows past p.rows read as 0)
+  // The cluster owns tiles [T0, T1); member `crank` takes T0 + crank, T0 +
+  // crank + kLmCluster, ...  Every member runs the same number of steps (the
+  // H slices are shared); a step past T1 loads and multiplies the range's
+  // last tile again and its result is ignored.
+  const int crank = (int)cluster_rank();
+  const uint16_t cmask = (uint16_t)((1u << kLmCluster) - 1);
+  int T0, T1;
+  {
+    const long long G = p.nclusters, g = blockIdx.x / kLmCluster;
+    T0 = (int)((long long)p.ntiles * g / G);
+    T1 = (int)((long long)p.ntiles * (g + 1) / G);
+  }
+  const int nsteps = (T1 - T0 + kLmCluster - 1) / kLmCluster;
+  auto tile_of = [&](int j) { return min(T0 + j * kLmCluster + crank, T1 - 1); };
+  auto tile_real = [&](int j) { return T0 + j * kLmCluster + crank < T1; };
+  const int nk = (p.d + kLmBK - 1) / kLmBK;
+  const int nmma = (R + kLmMaxN - 1) / kLmMaxN;  // MMAs per K step of 16
+  const int nper = R / nmma;                     // N of each (a multiple of 16)
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLmStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kLmCluster);  // released by every member's MMAs
+    }
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, 4);
+    mbar_init(&drain, 1);
+    s_abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) {  // tensor memory for the accumulators (whole warp)
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+            smem_addr(&tmem_base_holder)),
+        "r"(kLmTmemCols)
+        : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tmem_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // peers' barriers are initialised before any multicast
+  tmem_fence_after();
+  const uint32_t tmem_base = tmem_base_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0, issued = 0;
+    unsigned phase = 0;
+    const unsigned bytes = (unsigned)p.stage_bytes;
+    for (int j = 0; j < nsteps && !*(volatile int*)&s_abort; ++j) {
+      const int t = tile_of(j);
+      for (int kb = 0; kb < nk; ++kb) {
+        // every member has released this stage (its H part lands in all of them)
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) {
+          s_abort = 1;
+          set_flag(p.flags, kFlagTimeout);
+          break;
+        }
+        ++issued;
+        uint8_t* st = ring + (size_t)stage * p.stage_bytes;
+        mbar_expect_tx(&full[stage], bytes);
+        tma_load_2d(st, &map_w, kb * kLmBK, t * kLmBV, &full[stage]);
+        for (int r = crank * kLmHBox; r < R; r += kLmCluster * kLmHBox)
+          tma_load_2d_mc(st + kLmABytes + r * 128, &map_h, kb * kLmBK, row0 + r, &full[stage],
+                         cmask);
+        if (++stage == kLmStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // every copy this thread issued has landed before the CTA can leave
+    for (int j = max(0, issued - kLmStages); j < issued; ++j)
+      mbar_wait_bounded(&full[j % kLmStages], (unsigned)((j / kLmStages) & 1));
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc = umma_idesc_bf16_f32(kLmBV, nper);
+    int stage = 0;
+    unsigned phase = 0, acc_phase = 0;
+    for (int j = 0; j < nsteps && !*(volatile int*)&s_abort; ++j) {
+      if (!mbar_wait_bounded(&acc_empty, acc_phase ^ 1u)) {
+        s_abort = 1;
+        set_flag(p.flags, kFlagTimeout);
+        break;
+      }
+      tmem_fence_after();
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait_bounded(&full[stage], phase)) {
+          s_abort = 1;
+          set_flag(p.flags, kFlagTimeout);
+          break;
+        }
+        tmem_fence_after();
+        const uint32_t ast = smem_addr(ring + (size_t)stage * p.stage_bytes);
+        const uint32_t bst = ast + kLmABytes;
+#pragma unroll
+        for (int kk = 0; kk < kLmBK / 16; ++kk)
+          for (int m = 0; m < nmma; ++m)
+            umma_bf16(tmem_base + m * nper, umma_desc_sw128(ast + kk * 32),
+                      umma_desc_sw128(bst + m * nper * 128 + kk * 32), idesc,
+                      (kb > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_mc(&empty[stage], cmask);  // free in every member once these finish
+        if (++stage == kLmStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      umma_commit(&acc_full);  // the tile's accumulators are complete
+      acc_phase ^= 1u;
+    }
+    // every MMA this thread issued has completed before tensor memory is freed
+    umma_commit(&drain);
+    mbar_wait_bounded(&drain, 0);
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    // Accumulator lane = vocabulary entry of the tile, column = row.  Each
+    // warp reduces its 32 lanes per column with a butterfly that leaves
+    // column c's (max, lowest index) in lane c; the four quadrants' results
+    // meet in shared memory and each epilogue thread keeps the running best
+    // of rows e, e + 128, ... over the CTA's tiles.
+    const int q = warp & 3;   // tensor-memory lane quadrant of this warp
+    const int e = threadIdx.x - 64;  // 0..127 among the epilogue threads
+    float best[kLmMaxRows / 128];
+    int bidx[kLmMaxRows / 128];
+#pragma unroll
+    for (int j = 0; j < kLmMaxRows / 128; ++j) {
+      best[j] = -INFINITY;
+      bidx[j] = 0x7FFFFFFF;
+    }
+    unsigned acc_phase = 0;
+    for (int j = 0; j < nsteps; ++j) {
+      if (!mbar_wait_bounded(&acc_full, acc_phase)) {
+        s_abort = 1;
+        set_flag(p.flags, kFlagTimeout);
+        break;
+      }
+      tmem_fence_after();
+      const int vocab = tile_of(j) * kLmBV + 32 * q + lane;
+      const bool valid = tile_real(j) && vocab < p.V;
+      for (int cb = 0; cb < R / 32; ++cb) {
+        uint32_t r[32];
+        tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + cb * 32, r);
+        float v[32];
+        int ix[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          v[c] = valid ? __uint_as_float(r[c]) : -INFINITY;
+          ix[c] = valid ? vocab : 0x7FFFFFFF;
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const bool upper = (lane & off) != 0;
+#pragma unroll
+          for (int j = 0; j < off; ++j) {
+            const float send_v = upper ? v[j] : v[j + off];
+            const int send_i = upper ? ix[j] : ix[j + off];
+            const float keep_v = upper ? v[j + off] : v[j];
+            const int keep_i = upper ? ix[j + off] : ix[j];
+            const float got_v = __shfl_xor_sync(0xffffffffu, send_v, off);
+            const int got_i = __shfl_xor_sync(0xffffffffu, send_i, off);
+            const bool take = lm_better(got_v, got_i, keep_v, keep_i);
+            v[j] = take ? got_v : keep_v;
+            ix[j] = take ? got_i : keep_i;
+          }
+        }
+        red_v[q][cb * 32 + lane] = v[0];
+        red_i[q][cb * 32 + lane] = ix[0];
+      }
+      tmem_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty);  // tensor memory read: next tile may start
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four quadrants' maxima are in
+#pragma unroll
+      for (int j = 0; j < kLmMaxRows / 128; ++j) {
+        const int c = e + 128 * j;
+        if (c < R) {
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            if (lm_better(red_v[qq][c], red_i[qq][c], best[j], bidx[j])) {
+              best[j] = red_v[qq][c];
+              bidx[j] = red_i[qq][c];
+            }
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the scratch may be reused
+      acc_phase ^= 1u;
+    }
+    const int C = gridDim.x;
+#pragma unroll
+    for (int j = 0; j < kLmMaxRows / 128; ++j) {
+      const int row = row0 + e + 128 * j;
+      if (e + 128 * j < R && row < p.rows)
+        p.part[(size_t)row * C + blockIdx.x] =
+            ArgPartial{best[j], bidx[j], tile_real(0) ? 1 : 0, 0};
+    }
+  }
+  tmem_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no peer still writes into this CTA or arrives on its barriers
+  if (warp == 1) {
+    tmem_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kLmTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace sv

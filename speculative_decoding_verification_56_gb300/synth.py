@@ -334,3 +334,35 @@ WORKLOADS = {
     "zipf152k": zipf152k,
     "tree": tree,
 }
+
+
+# ---------------------------------------------------------------------------
+# LM-head inputs: hidden states and LM-head weights (bf16 bits)
+# ---------------------------------------------------------------------------
+
+def make_lm_head_case(*, B, k, d, V, seed=0, peak=6.0, p_match=0.7, flat_frac=0.1):
+    """Synthetic LM head W [V, d] ~ N(0, 1/d) and hidden states H [B*(k+1), d].
+    Most rows point at a random 'intended' token j (h = peak * sqrt(d) *
+    W[j] / |W[j]|^2 ... scaled so z_j ~ peak above the N(0, 1) background,
+    plus N(0, 1) noise), like a confident LM; a fraction `flat_frac` of rows
+    are pure noise (no clear winner).  Draft tokens equal the intended token
+    with probability p_match, else a uniform token.  Returns (H bits, W bits,
+    tokens, intended)."""
+    rng = np.random.default_rng(seed)
+    W_bits = np.empty((V, d), dtype=np.uint16)
+    for v0 in range(0, V, 8192):  # in slices: the full-size head is 128256 x 4096
+        v1 = min(V, v0 + 8192)
+        W_bits[v0:v1] = f32_to_bf16_bits(
+            (rng.standard_normal((v1 - v0, d), dtype=np.float32) / np.float32(np.sqrt(d))))
+    rows = B * (k + 1)
+    intended = rng.integers(0, V, rows)
+    Hm = rng.standard_normal((rows, d))
+    wj = bf16_bits_to_f32(W_bits[intended]).astype(np.float64)
+    coef = peak / np.maximum((wj * wj).sum(1), 1e-12)
+    flat = rng.random(rows) < flat_frac
+    Hm = Hm + np.where(flat[:, None], 0.0, coef[:, None] * wj)
+    H_bits = f32_to_bf16_bits(Hm.astype(np.float32))
+    draft_int = intended.reshape(B, k + 1)[:, :k]
+    tokens = np.where(rng.random((B, k)) < p_match, draft_int,
+                      rng.integers(0, V, (B, k))).astype(np.int32)
+    return H_bits, W_bits, tokens, intended.astype(np.int32)

@@ -1,0 +1,95 @@
+"""GPU parity of the LM head fused with greedy verification (tcgen05 GEMM with
+an argmax epilogue) against the float64 oracle.
+
+The kernel's logits are float32 accumulations of exact bf16 products; the
+oracle's are exact.  A row's argmax is compared exactly unless its top two
+exact logits lie within a bound of the float32 accumulation error, in which
+case either index is correct (the row is counted as flagged)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_56_gb300 as sv
+from speculative_decoding_verification_56_gb300 import build, synth
+
+pytestmark = pytest.mark.gpu
+
+U32 = 2.0 ** -24
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build_library()
+    sv.load_library()
+    oracle.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _flag_bound(d, mag):
+    # recursive float32 summation of d exact products: |error| <= d u sum|x_i y_i|
+    # (for each of the two competing logits), with a safety factor of 4
+    return 8.0 * d * U32 * mag
+
+
+def _gpu(H, W, tok):
+    out = sv.lm_head_verify_greedy(_bf16(H), _bf16(W), torch.from_numpy(tok).cuda())
+    torch.cuda.synchronize()
+    return {key: v.cpu().numpy() for key, v in out.items()}
+
+
+def _rows_argmax(H, W):
+    """Per-row argmax from the GPU: every row as its own sequence with k = 0."""
+    rows = H.shape[0]
+    return _gpu(H, W, np.zeros((rows, 0), np.int32))["out_tokens"][:, 0]
+
+
+@pytest.mark.parametrize("B,k,d,V,seed", [
+    (1, 0, 64, 1, 0), (2, 3, 64, 300, 1), (3, 4, 128, 1000, 2), (4, 1, 72, 129, 3),
+    (2, 2, 200, 5000, 4), (100, 4, 64, 700, 5),        # 500 rows: two row groups
+    (1, 0, 8, 257, 6),
+])
+def test_lm_head_rows_and_chains(B, k, d, V, seed):
+    H, W, tok, _ = synth.make_lm_head_case(B=B, k=k, d=d, V=V, seed=seed)
+    res = oracle.lm_head_greedy(H, W, tok)
+    flagged = res["gap"] <= _flag_bound(d, res["mag"])
+    g_arg = _rows_argmax(H, W)
+    assert np.array_equal(g_arg[~flagged], res["argmax"][~flagged])
+    assert flagged.mean() <= 0.05
+    out = _gpu(H, W, tok)
+    seq_ok = ~flagged.reshape(B, k + 1).any(1)   # sequences with no flagged row
+    assert np.array_equal(out["accepted_len"][seq_ok], res["accepted_len"][seq_ok])
+    assert np.array_equal(out["out_tokens"][seq_ok], res["out_tokens"][seq_ok])
+
+
+def test_lm_head_tie_picks_lowest_index():
+    rng = np.random.default_rng(11)
+    d, V = 64, 400
+    H, W, _, intended = synth.make_lm_head_case(B=8, k=0, d=d, V=V, seed=11, flat_frac=0.0)
+    for r, j in enumerate(intended):         # duplicate each intended row at a lower index
+        lo = int(rng.integers(0, j + 1))
+        W[lo] = W[j]
+        intended[r] = lo
+    res = oracle.lm_head_greedy(H, W, np.zeros((8, 0), np.int32))
+    g = _rows_argmax(H, W)
+    assert np.array_equal(res["argmax"], g)
+
+
+@pytest.mark.slow
+def test_lm_head_full_size_sampled_rows():
+    # the greedy workload's shape: B=64, k=4, d=4096 (hidden), V=128256
+    B, k, d, V = 64, 4, 4096, 128256
+    H, W, tok, _ = synth.make_lm_head_case(B=B, k=k, d=d, V=V, seed=0)
+    out = _gpu(H, W, tok)
+    seqs = [0, 37]
+    res = oracle.lm_head_greedy(H, W, tok, seqs=seqs)
+    for b in seqs:
+        rws = slice(b * (k + 1), (b + 1) * (k + 1))
+        if (res["gap"][rws] <= _flag_bound(d, res["mag"][rws])).any():
+            continue
+        assert out["accepted_len"][b] == res["accepted_len"][b]
+        assert np.array_equal(out["out_tokens"][b], res["out_tokens"][b])
