@@ -73,6 +73,8 @@ def _bind(lib):
     lib.oracle_kv_commit.restype = I
     lib.oracle_lm_head_greedy.argtypes = [P, P, P, I, I, I, I, P, I, P, P, P, P, P]
     lib.oracle_lm_head_greedy.restype = I
+    lib.oracle_tree_grow.argtypes = [P, I, I, I, I, I, D, I, P, P, P, P, P]
+    lib.oracle_tree_grow.restype = I
     lib.oracle_expected_tokens.argtypes = [D, I]
     lib.oracle_expected_tokens.restype = D
     lib.oracle_speedup_model.argtypes = [D, I, D]
@@ -248,6 +250,24 @@ def lm_head_greedy(hidden, w_lm, tokens, seqs=None, lib=None):
                                    _ptr(res["argmax"]), _ptr(res["gap"]), _ptr(res["mag"]))
     _check(rc)
     return res
+
+
+def tree_grow(logits, temperature, M, dtype="bf16", lib=None):
+    """EAGLE-2 tree growth (reading R12 of spec_oracle.c).  ``logits``
+    [B, D, K, V] draft rows by layer and frontier slot.  Returns dict with
+    tokens, parents, depth [B, M+1] int32, values [B, M+1] float64 and
+    min_gap [B] (smallest value gap at a selection boundary)."""
+    lib = lib or _load()
+    z = _logits(logits, dtype)
+    B, D, K, V = z.shape
+    out = dict(tokens=np.zeros((B, M + 1), np.int32), parents=np.zeros((B, M + 1), np.int32),
+               depth=np.zeros((B, M + 1), np.int32), values=np.zeros((B, M + 1)),
+               min_gap=np.zeros(B))
+    rc = lib.oracle_tree_grow(_ptr(z), _dtype_code(dtype), B, D, K, V, float(temperature), int(M),
+                              _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["depth"]),
+                              _ptr(out["values"]), _ptr(out["min_gap"]))
+    _check(rc)
+    return out
 
 
 def expected_tokens(alpha: float, gamma: int, lib=None) -> float:

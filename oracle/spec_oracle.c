@@ -52,6 +52,18 @@
  *      minus top-2) and the magnitude sum |W_j*| . |h| of the winner are
  *      reported so that a comparison can excuse rows whose argmax a float32
  *      accumulation could legitimately move.
+ *   R12 EAGLE-2 tree growth: node 0 is the root (value 0).  At layer l the
+ *      frontier (slot j holds a node; layer 0: the root in slot 0) is
+ *      expanded with draft row logits[b, l, j]: q = softmax(z / T); the
+ *      node's children are its K most probable tokens (ties: lower token),
+ *      each with value = parent value + ln q(token).  The next frontier is
+ *      the K children of the layer with the highest values (ties: creation
+ *      order, i.e. parent slot then rank).  After D layers the tree is the
+ *      root plus the M non-root nodes with the highest values (ties:
+ *      creation order), listed in creation order (parents before children)
+ *      with parents renumbered.  A child never outranks its parent (ln q
+ *      <= 0 and the parent was created first), so the tree is closed under
+ *      ancestors.
  *   Non-finite logits are outside the method's domain (rejected here).
  */
 #include <math.h>
@@ -494,6 +506,112 @@ int oracle_lm_head_greedy(const uint16_t* hidden, const uint16_t* w_lm, const in
   }
   free(h);
   return OR_OK;
+}
+
+/*
+ * EAGLE-2 dynamic draft tree growth.  [MATH] "EAGLE-2: dynamic draft trees"
+ * (grow the tree greedily from the draft probabilities: expand the nodes with
+ * the highest cumulative draft probability, prune low-probability paths,
+ * re-rank which candidates to keep under an unchanged node budget); [REVIEW]
+ * "EAGLE-2: Does Every Context Need the Same Draft Tree?".  Reading R12.
+ *
+ * logits [B, D, K, V] (draft rows by layer and frontier slot), T, node
+ * budget M.  Outputs [B, M+1]: tokens (root -1), parents (root -1), depth,
+ * values (float64).  Also reports, per tree, the smallest value gap at any
+ * selection boundary (frontier cut or final cut; +inf if none) in min_gap.
+ */
+static int cand_before(double va, int ca, double vb, int cb) {
+  return va > vb || (va == vb && ca < cb); /* higher value, then earlier creation */
+}
+
+int oracle_tree_grow(const void* logits, int dtype, int B, int D, int K, int V, double T, int M,
+                     int32_t* tokens, int32_t* parents, int32_t* depth, double* values,
+                     double* min_gap) {
+  if (B < 0 || D < 1 || K < 1 || V < K || !(T > 0.0) || M < 0) return OR_ERR_ARG;
+  const int maxn = 1 + K + (D - 1) * K * K;
+  if (M > maxn - 1) return OR_ERR_ARG;
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  double* val = (double*)malloc(sizeof(double) * (size_t)maxn);
+  int32_t* par = (int32_t*)malloc(sizeof(int32_t) * (size_t)maxn);
+  int32_t* tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)maxn);
+  int32_t* dep = (int32_t*)malloc(sizeof(int32_t) * (size_t)maxn);
+  int32_t* front = (int32_t*)malloc(sizeof(int32_t) * (size_t)K);
+  int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)maxn);
+  int32_t* newid = (int32_t*)malloc(sizeof(int32_t) * (size_t)maxn);
+  char* used = (char*)malloc((size_t)V);
+  if (!q || !val || !par || !tok || !dep || !front || !order || !newid || !used) {
+    free(q); free(val); free(par); free(tok); free(dep); free(front); free(order);
+    free(newid); free(used);
+    return OR_ERR_NOMEM;
+  }
+  int rc = OR_OK;
+  for (int b = 0; b < B && rc == OR_OK; ++b) {
+    int n = 1, nfront = 1;
+    val[0] = 0.0; par[0] = -1; tok[0] = -1; dep[0] = 0; front[0] = 0;
+    double gap = INFINITY;
+    for (int l = 0; l < D; ++l) {
+      const int first = n; /* this layer's children are n .. */
+      for (int j = 0; j < nfront; ++j) {
+        const size_t off = (((size_t)b * D + l) * K + j) * (size_t)V;
+        if (softmax_row(logits, dtype, off, V, T, q)) { rc = OR_ERR_NONFINITE; break; }
+        memset(used, 0, (size_t)V);
+        for (int r = 0; r < K; ++r) { /* r-th most probable token, lowest index on ties */
+          int best = -1;
+          for (int x = 0; x < V; ++x)
+            if (!used[x] && (best < 0 || q[x] > q[best])) best = x;
+          used[best] = 1;
+          val[n] = val[front[j]] + log(q[best]);
+          par[n] = front[j]; tok[n] = best; dep[n] = l + 1;
+          ++n;
+        }
+      }
+      if (rc != OR_OK) break;
+      if (l + 1 < D) { /* next frontier: the K best children of this layer */
+        const int nc = n - first;
+        for (int c = 0; c < nc; ++c) order[c] = first + c;
+        for (int a = 0; a < nc; ++a)       /* selection sort: plain and small */
+          for (int c = a + 1; c < nc; ++c)
+            if (cand_before(val[order[c]], order[c], val[order[a]], order[a])) {
+              int t = order[a]; order[a] = order[c]; order[c] = t;
+            }
+        nfront = nc < K ? nc : K;
+        for (int j = 0; j < nfront; ++j) front[j] = order[j];
+        if (nc > K) { double g = val[order[K - 1]] - val[order[K]]; if (g < gap) gap = g; }
+      }
+    }
+    if (rc != OR_OK) break;
+    /* re-rank: the M best non-root nodes */
+    const int nn = n - 1;
+    for (int c = 0; c < nn; ++c) order[c] = 1 + c;
+    for (int a = 0; a < nn; ++a)
+      for (int c = a + 1; c < nn; ++c)
+        if (cand_before(val[order[c]], order[c], val[order[a]], order[a])) {
+          int t = order[a]; order[a] = order[c]; order[c] = t;
+        }
+    if (nn > M && M > 0) { double g = val[order[M - 1]] - val[order[M]]; if (g < gap) gap = g; }
+    for (int c = 0; c < n; ++c) newid[c] = -1;
+    newid[0] = 0;
+    for (int c = 0; c < M; ++c) newid[order[c]] = 1; /* mark */
+    int id = 1;
+    for (int c = 1; c < n; ++c) /* creation order is topological */
+      if (newid[c] == 1) newid[c] = id++;
+      else newid[c] = c == 0 ? 0 : -1;
+    const size_t ob = (size_t)b * (M + 1);
+    tokens[ob] = -1; parents[ob] = -1; depth[ob] = 0; values[ob] = 0.0;
+    for (int c = 1; c < n; ++c) {
+      if (newid[c] < 1) continue;
+      const int o = newid[c];
+      if (newid[par[c]] < 0) { rc = OR_ERR_TREE; break; } /* cannot happen (closure) */
+      tokens[ob + o] = tok[c];
+      parents[ob + o] = newid[par[c]];
+      depth[ob + o] = dep[c];
+      values[ob + o] = val[c];
+    }
+    min_gap[b] = gap;
+  }
+  free(q); free(val); free(par); free(tok); free(dep); free(front); free(order);
+  free(newid); free(used);
+  return rc;
 }
 
 /* Expected tokens per verification pass with per-token acceptance alpha and

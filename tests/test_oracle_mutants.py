@@ -55,6 +55,13 @@ MUTANTS = {
                          "if (z >= best) { second = best; best = z; bj = j; }"),
     "lm_head_emits_draft": ("else if (i == na) v = argmax[(size_t)b * rows + na];",
                             "else if (i == na) v = na < k ? tokens[(size_t)b * k + na] : argmax[(size_t)b * rows + na];"),
+    "grow_value_not_cumulative": ("val[n] = val[front[j]] + log(q[best]);", "val[n] = log(q[best]);"),
+    "grow_frontier_by_creation": ("if (cand_before(val[order[c]], order[c], val[order[a]], order[a])) {\n              int t = order[a]; order[a] = order[c]; order[c] = t;\n            }\n        nfront",
+                                  "if (0) {\n              int t = order[a]; order[a] = order[c]; order[c] = t;\n            }\n        nfront"),
+    "grow_token_highest_tie": ("if (!used[x] && (best < 0 || q[x] > q[best])) best = x;",
+                               "if (!used[x] && (best < 0 || q[x] >= q[best])) best = x;"),
+    "grow_wrong_depth": ("par[n] = front[j]; tok[n] = best; dep[n] = l + 1;",
+                         "par[n] = front[j]; tok[n] = best; dep[n] = l;"),
     "mask_wrong_word": ("        row[cur / 32] |= 1u << (cur % 32);\n        ++d;",
                         "        row[cur % W] |= 1u << (cur % 32);\n        ++d;"),
 }
@@ -86,6 +93,9 @@ class _Variant:
     def lm_head_greedy(self, *a, **kw):
         return oracle.lm_head_greedy(*a, lib=self.lib, **kw)
 
+    def tree_grow(self, *a, **kw):
+        return oracle.tree_grow(*a, lib=self.lib, **kw)
+
     def expected_tokens(self, *a, **kw):
         return oracle.expected_tokens(*a, lib=self.lib, **kw)
 
@@ -109,6 +119,12 @@ def _pin_checks(o):
     yield lambda: pins.test_lm_head_matches_float64_matmul(o)
     yield lambda: pins.test_lm_head_equals_unfused_greedy_on_exact_logits(o, 0)
     yield lambda: pins.test_lm_head_ties_and_subset(o)
+    yield lambda: pins.test_tree_grow_one_layer_is_top_m_of_the_root_row(o)
+    yield lambda: pins.test_tree_grow_worked_example_frontier_by_value(o)
+    yield lambda: pins.test_tree_grow_ties_take_the_lower_token(o)
+    yield lambda: pins.test_tree_grow_two_layers_full_expansion(o)
+    yield lambda: pins.test_tree_grow_k1_is_the_greedy_chain(o)
+    yield lambda: pins.test_tree_grow_structure(o, 0)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

@@ -663,3 +663,129 @@ def test_lm_head_ties_and_subset(oracle_mod):
     sub = oracle_mod.lm_head_greedy(H, W, np.zeros((B, k), np.int32), seqs=[2])
     assert np.array_equal(sub["argmax"][4:6], res["argmax"][4:6])
     assert (sub["argmax"][:4] == -2).all()
+
+
+# ---------------------------------------------------------------------------
+# EAGLE-2 tree growth ("EAGLE math", "EAGLE-2: dynamic draft trees": expand
+# the nodes with the highest cumulative draft probability, re-rank under a
+# fixed node budget)
+# ---------------------------------------------------------------------------
+
+def _softmax64(z, T):
+    z = np.asarray(z, np.float64) / T
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+def test_tree_grow_one_layer_is_top_m_of_the_root_row(oracle_mod):
+    rng = np.random.default_rng(0)
+    B, K, V, T, M = 3, 12, 40, 0.9, 7
+    z = (2 * rng.standard_normal((B, 1, K, V))).astype(np.float32)
+    r = oracle_mod.tree_grow(z, T, M, dtype="f32")
+    for b in range(B):
+        q = _softmax64(z[b, 0, 0], T)
+        top = np.argsort(-q, kind="stable")[:M]      # library sort, lowest index on ties
+        assert r["tokens"][b, 1:].tolist() == sorted(top.tolist(), key=lambda x: -q[x])
+        assert (r["parents"][b, 1:] == 0).all() and (r["depth"][b, 1:] == 1).all()
+        assert np.allclose(r["values"][b, 1:], np.log(q[r["tokens"][b, 1:]]), atol=1e-12)
+
+
+def test_tree_grow_two_layers_full_expansion(oracle_mod):
+    # K = V: every token is expanded; the frontier is every child ranked by
+    # value; the result is the M most probable paths of length <= 2
+    rng = np.random.default_rng(1)
+    V = K = 4
+    T, M = 1.0, 9
+    z = (1.5 * rng.standard_normal((1, 2, K, V))).astype(np.float32)
+    r = oracle_mod.tree_grow(z, T, M, dtype="f32")
+    q0 = _softmax64(z[0, 0, 0], T)
+    rank = sorted(range(V), key=lambda x: (-q0[x], x))   # frontier slot of child x
+    paths = [((x,), np.log(q0[x])) for x in range(V)]
+    for slot, x in enumerate(rank):
+        q1 = _softmax64(z[0, 1, slot], T)
+        paths += [((x, y), np.log(q0[x]) + np.log(q1[y])) for y in range(V)]
+    best = sorted(paths, key=lambda p: -p[1])[:M]
+    got = set()
+    for v in range(1, M + 1):
+        chain = [r["tokens"][0, v]]
+        p = r["parents"][0, v]
+        while p != 0:
+            chain.append(r["tokens"][0, p])
+            p = r["parents"][0, p]
+        got.add(tuple(chain[::-1]))
+    assert got == {p[0] for p in best}
+
+
+def test_tree_grow_k1_is_the_greedy_chain(oracle_mod):
+    rng = np.random.default_rng(2)
+    B, D, V = 2, 5, 30
+    z = (2 * rng.standard_normal((B, D, 1, V))).astype(np.float32)
+    r = oracle_mod.tree_grow(z, 1.0, D, dtype="f32")
+    for b in range(B):
+        assert r["tokens"][b, 1:].tolist() == [int(np.argmax(z[b, d, 0])) for d in range(D)]
+        assert r["parents"][b, 1:].tolist() == list(range(D))
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_tree_grow_structure(oracle_mod, seed):
+    rng = np.random.default_rng(seed)
+    B, D, K, V, M = 4, 4, 3, 50, 15
+    z = (2 * rng.standard_normal((B, D, K, V))).astype(np.float32)
+    r = oracle_mod.tree_grow(z, 0.8, M, dtype="f32")
+    for b in range(B):
+        par, dep, val = r["parents"][b], r["depth"][b], r["values"][b]
+        assert par[0] == -1 and dep[0] == 0
+        for v in range(1, M + 1):
+            assert 0 <= par[v] < v                       # topological, closed
+            assert dep[v] == dep[par[v]] + 1
+            assert val[v] <= val[par[v]]                  # probabilities multiply
+        # siblings carry distinct tokens
+        for p in set(par[1:].tolist()):
+            kids = r["tokens"][b, 1:][par[1:] == p]
+            assert len(set(kids.tolist())) == len(kids)
+
+
+def _logp_rows(*rows, V=6):
+    """Draft rows given as probabilities (the rest spread evenly): logits are
+    their logs, so softmax at T = 1 returns them."""
+    out = []
+    for spec in rows:
+        p = np.full(V, 0.0)
+        for tok, pr in spec.items():
+            p[tok] = pr
+        rest = [x for x in range(V) if x not in spec]
+        p[rest] = (1.0 - sum(spec.values())) / len(rest)
+        out.append(np.log(p).astype(np.float32))
+    return np.array(out)
+
+
+def test_tree_grow_worked_example_frontier_by_value(oracle_mod):
+    # root: a=0 (0.6), b=1 (0.3).  a's row: x=2 (0.5), y=3 (0.4); b's row:
+    # u=4 (0.9), v=5 (0.05).  Candidates: a.x 0.30, a.y 0.24, b.u 0.27,
+    # b.v 0.015 -> the depth-2 frontier is (a.x, b.u), not the first two
+    # created (a.x, a.y).  Their rows (slots 0, 1) put token 5 and token 0 on top.
+    K, D, V = 2, 3, 6
+    z = np.zeros((1, D, K, V), np.float32)
+    z[0, 0, 0] = _logp_rows({0: 0.6, 1: 0.3})[0]
+    z[0, 0, 1] = z[0, 0, 0]                        # unused slot at layer 0
+    z[0, 1] = _logp_rows({2: 0.5, 3: 0.4}, {4: 0.9, 5: 0.05})
+    z[0, 2] = _logp_rows({5: 0.7, 1: 0.2}, {0: 0.8, 2: 0.1})
+    M = 1 + K + K * K + K * K - 1                   # every node but the worst
+    r = oracle_mod.tree_grow(z, 1.0, M, dtype="f32")
+    tok, par = r["tokens"][0], r["parents"][0]
+    path = lambda v: (tuple(path(par[v])) if par[v] > 0 else ()) + (int(tok[v]),)
+    depth3_parents = {path(par[v]) for v in range(1, M + 1) if r["depth"][0, v] == 3}
+    assert depth3_parents == {(0, 2), (1, 4)}
+    vals = {path(v): r["values"][0, v] for v in range(1, M + 1)}
+    assert (1, 4, 0) in vals and (0, 2, 5) in vals
+    assert np.isclose(vals[(1, 4, 0)], np.log(0.3 * 0.9 * 0.8))
+    assert np.isclose(vals[(0, 2, 5)], np.log(0.6 * 0.5 * 0.7))
+
+
+def test_tree_grow_ties_take_the_lower_token(oracle_mod):
+    z = np.zeros((1, 1, 2, 8), np.float32)
+    z[0, 0, 0] = [0, 1, 3, 0, 0, 3, 2, 0]       # tokens 2 and 5 tie for the top
+    r = oracle_mod.tree_grow(z, 1.0, 1, dtype="f32")
+    assert r["tokens"][0, 1] == 2
+    r = oracle_mod.tree_grow(z, 1.0, 2, dtype="f32")
+    assert r["tokens"][0, 1:].tolist() == [2, 5]
