@@ -533,6 +533,29 @@ def measure_next_rows(dev, stream, tree, K):
         "bound": "W_LM stream (1.05 GB) and tensor cores, about balanced at 320 rows",
         "timed": "CUDA-graph replay of 4 calls"}
     del H, Wm, logits
+
+    # EAGLE-2 tree growth producing the tree workload's shape (16 trees of 60
+    # nodes): 6 layers of 8 frontier rows over V=128256 bf16 draft rows
+    Bg, Dg, Kg, Mg = 16, 6, 8, 59
+    zg = synth.make_grow_logits(B=Bg, D=Dg, K=Kg, V=Vl, seed=2)
+    zt = sv.to_device_logits(zg, "bf16", dev)
+    del zg
+    gi = dict(dtype=torch.int32, device=dev)
+    g_tok, g_par, g_dep = (torch.empty(Bg, Mg + 1, **gi) for _ in range(3))
+    g_val = torch.empty(Bg, Mg + 1, dtype=torch.float32, device=dev)
+    wsgr = sv.alloc_workspace(sv.SPEC_MODE_TREE_GROW, Bg, Kg, Vl, sv.SPEC_DTYPE_BF16, dev)
+    ms_g = _time_loop(lambda: sv.spec_tree_grow(zt, 1.0, Mg, g_tok, g_par, g_dep, g_val, wsgr,
+                                                stream), stream, max(40, K // 10), per_graph=8)
+    rows_read = Bg * (1 + (Dg - 1) * Kg)
+    gbytes = rows_read * Vl * 2
+    out["tree_grow"] = {"workload": f"B={Bg} trees, {Dg} layers x {Kg} frontier rows, V={Vl} "
+                                    f"bf16, budget {Mg} nodes",
+                        "us_per_call": round(ms_g * 1e3, 2), "bytes": int(gbytes),
+                        "gb_s": round(gbytes / (ms_g / 1e3) / 1e9, 1),
+                        "launches": 2,
+                        "bound": "HBM (top-k + normaliser per draft row) and launch latency",
+                        "timed": "CUDA-graph replay of 8 calls"}
+    del zt
     return out
 
 

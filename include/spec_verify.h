@@ -73,7 +73,8 @@ typedef enum {
   SPEC_MODE_TREE_GREEDY = 2,
   SPEC_MODE_TREE_MASK = 3, /* spec_tree_attention_mask: the flag header only */
   SPEC_MODE_KV_COMMIT = 4, /* spec_kv_commit_path: the flag header only */
-  SPEC_MODE_LM_HEAD_GREEDY = 5 /* spec_lm_head_verify_greedy (k_or_N = k) */
+  SPEC_MODE_LM_HEAD_GREEDY = 5, /* spec_lm_head_verify_greedy (k_or_N = k) */
+  SPEC_MODE_TREE_GROW = 6       /* spec_tree_grow (k_or_N = K children per node) */
 } spec_mode_t;
 
 /* Bits of the workspace flag word (sticky until read with clear != 0). */
@@ -265,6 +266,38 @@ SPEC_API spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void
                                                   int d, int V, int32_t* accepted_len,
                                                   int32_t* out_tokens, void* workspace,
                                                   size_t workspace_bytes, void* stream);
+
+/*
+ * EAGLE-2 dynamic draft-tree growth ("EAGLE math", "EAGLE-2: dynamic draft
+ * trees": expand the nodes with the highest cumulative draft probability,
+ * prune low-probability paths, re-rank under an unchanged node budget;
+ * "EAGLE-3 speculative decoding review", "EAGLE-2: Does Every Context Need
+ * the Same Draft Tree?").  Layer l expands the frontier (slot j holds a node;
+ * layer 0: the root in slot 0) with the draft row draft_logits[b, l, j]:
+ * q = softmax(z / T); the node's children are its K most probable tokens
+ * (ties: lower token), valued parent + ln q(token) (root 0); the next
+ * frontier is the layer's K best children (ties: creation order).  After D
+ * layers the tree is the root plus the M best nodes (ties: creation order),
+ * listed in creation order (parents before children) with parents
+ * renumbered, ready for spec_verify_tree_greedy and spec_tree_attention_mask.
+ *   draft_logits  [B, D, K, V] dtype (slot j of layer 0 is read for j = 0 only)
+ *   K             1..16 children per node and frontier size; D 1..16 layers
+ *   M             node budget, 0 <= M <= K + (D-1) K^2
+ * Outputs [B, M+1]: tokens (root -1), parents (root -1), depth, values
+ * (float32 cumulative ln probability; computed in float64).  Token choices
+ * compare raw logits (exact); node values near a selection boundary may
+ * order differently from a float64 reference when within ~1e-12.
+ * Workspace: spec_verify_workspace_bytes(SPEC_MODE_TREE_GROW, B, K, V, dtype)
+ * (sized for up to 16 layers); requires ceil(V / chunk) * K <= 2048 (chunk =
+ * 16384 bf16 / 8192 fp32 elements).  Two kernel launches: the K best tokens
+ * and softmax normaliser of every draft row read (B (1 + (D-1) K) rows, one
+ * streaming pass), then one CTA per tree for the layer-by-layer expansion
+ * and the final re-ranking.
+ */
+SPEC_API spec_status_t spec_tree_grow(const void* draft_logits, int dtype, float temperature,
+                                      int B, int D, int K, int V, int M, int32_t* tokens,
+                                      int32_t* parents, int32_t* depth, float* values,
+                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Copy the workspace's flag word to *host_flags (synchronises `stream`); with

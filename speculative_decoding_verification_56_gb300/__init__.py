@@ -13,6 +13,7 @@ Entry points (same names as the C ABI):
 * :func:`spec_tree_attention_mask` -- ancestor bitmask + depth of draft trees
 * :func:`spec_kv_commit_path`     -- move the accepted path's KV entries into place
 * :func:`spec_lm_head_verify_greedy` -- LM head (tcgen05 GEMM) fused with greedy verification
+* :func:`spec_tree_grow`          -- EAGLE-2 dynamic draft-tree growth
 * :func:`spec_verify_workspace_bytes`, :func:`spec_verify_read_flags`,
   :func:`spec_verify_launch_count`, :func:`spec_status_string`
 
@@ -44,6 +45,7 @@ SPEC_MODE_TREE_GREEDY = 2
 SPEC_MODE_TREE_MASK = 3
 SPEC_MODE_KV_COMMIT = 4
 SPEC_MODE_LM_HEAD_GREEDY = 5
+SPEC_MODE_TREE_GROW = 6
 SPEC_FLAG_TOKEN_RANGE = 1
 SPEC_FLAG_BAD_PARENT = 2
 SPEC_FLAG_DEPTH = 4
@@ -92,6 +94,8 @@ def load_library(path: str = LIB_PATH):
         lib.spec_kv_commit_path.restype = I
         lib.spec_lm_head_verify_greedy.argtypes = [P, P, P, I, I, I, I, P, P, P, Z, P]
         lib.spec_lm_head_verify_greedy.restype = I
+        lib.spec_tree_grow.argtypes = [P, I, F, I, I, I, I, I, P, P, P, P, P, Z, P]
+        lib.spec_tree_grow.restype = I
         lib.spec_verify_read_flags.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I, P]
         lib.spec_verify_read_flags.restype = I
         lib.spec_verify_launch_count.argtypes = []
@@ -309,6 +313,22 @@ def spec_lm_head_verify_greedy(hidden, w_lm, draft_tokens, accepted_len, out_tok
     _check(st, "spec_lm_head_verify_greedy")
 
 
+def spec_tree_grow(draft_logits, temperature, M, tokens, parents, depth, values, workspace,
+                   stream=None):
+    """EAGLE-2 tree growth (C ABI ``spec_tree_grow``): ``draft_logits``
+    [B, D, K, V] bf16 or fp32; outputs [B, M+1]."""
+    torch = _torch()
+    B, D, K, V = draft_logits.shape
+    st = load_library().spec_tree_grow(
+        _dev(draft_logits, "draft_logits"), _dtype_code(draft_logits), float(temperature),
+        B, D, K, V, int(M), _dev(tokens, "tokens", torch.int32),
+        _dev(parents, "parents", torch.int32), _dev(depth, "depth", torch.int32),
+        _dev(values, "values", torch.float32),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream))
+    _check(st, "spec_tree_grow")
+
+
 def spec_verify_read_flags(workspace, clear: bool = True, stream=None) -> int:
     """Device flag bits recorded in ``workspace`` (synchronises the stream)."""
     out = ctypes.c_uint32(0)
@@ -408,6 +428,22 @@ def lm_head_verify_greedy(hidden, w_lm, draft_tokens, workspace=None, stream=Non
                out_tokens=torch.empty(B, k + 1, dtype=torch.int32, device=dev))
     spec_lm_head_verify_greedy(hidden, w_lm, draft_tokens, out["accepted_len"],
                                out["out_tokens"], workspace, stream)
+    return out
+
+
+def tree_grow(draft_logits, temperature, M, workspace=None, stream=None):
+    """Grow B draft trees; returns dict(tokens, parents, depth, values) [B, M+1]."""
+    torch = _torch()
+    B, D, K, V = draft_logits.shape
+    dev = draft_logits.device
+    if workspace is None:
+        workspace = alloc_workspace(SPEC_MODE_TREE_GROW, B, K, V, _dtype_code(draft_logits), dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(tokens=torch.empty(B, M + 1, **i32), parents=torch.empty(B, M + 1, **i32),
+               depth=torch.empty(B, M + 1, **i32),
+               values=torch.empty(B, M + 1, dtype=torch.float32, device=dev))
+    spec_tree_grow(draft_logits, temperature, M, out["tokens"], out["parents"], out["depth"],
+                   out["values"], workspace, stream)
     return out
 
 

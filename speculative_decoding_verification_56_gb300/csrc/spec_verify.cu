@@ -21,6 +21,7 @@
 #include "sv_kernels.cuh"
 #include "sv_tree.cuh"
 #include "sv_lmhead.cuh"
+#include "sv_grow.cuh"
 
 static_assert(sv::kMaxDraft == SPEC_MAX_K, "finish kernel buffers are sized for SPEC_MAX_K");
 
@@ -53,6 +54,23 @@ bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
   if (mode == SPEC_MODE_TREE_MASK || mode == SPEC_MODE_KV_COMMIT) {  // the flag header only
     if (B < 0 || kN < 1 || kN > SPEC_MAX_TREE_NODES) return false;
     L->bytes = kHeaderBytes;
+    return true;
+  }
+  if (mode == SPEC_MODE_TREE_GROW) {  // kN = K (children per node); records and node arrays
+    const int K = kN;
+    if (B < 0 || K < 1 || K > sv::kGrowMaxK || V < K || V > SPEC_MAX_V) return false;
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return false;
+    const int C = (V + chunk_elems(dtype) - 1) / chunk_elems(dtype);
+    if ((long long)C * K > sv::kGrowMaxCand) return false;
+    L->nchunks = C;
+    size_t off = kDataOffset;
+    L->off_part = off;  // GrowRec [B, 1 + (kGrowMaxD - 1) K, C]: every row of up to 16 layers
+    off = align_up(off + (size_t)B * (1 + (sv::kGrowMaxD - 1) * K) * C * sizeof(sv::GrowRec));
+    L->off_desc = off;  // node values, float64 [B, kGrowMaxNodes]
+    off = align_up(off + (size_t)B * sv::kGrowMaxNodes * sizeof(double));
+    L->off_gsum = off;  // parent, token, depth [3][B, kGrowMaxNodes]
+    off = align_up(off + 3 * (size_t)B * sv::kGrowMaxNodes * sizeof(int32_t));
+    L->bytes = off;
     return true;
   }
   if (mode == SPEC_MODE_LM_HEAD_GREEDY) {  // argmax records of up to kLmMaxGrid CTAs per row
@@ -611,6 +629,77 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   prm.part = lp.part;
   prm.rowarg = reinterpret_cast<int32_t*>(ws + L.off_arg);
   return launch(sv::argmax_resolve_kernel, B, 0, prm, stream, true);
+}
+
+spec_status_t spec_tree_grow(const void* draft_logits, int dtype, float temperature, int B,
+                             int D, int K, int V, int M, int32_t* tokens, int32_t* parents,
+                             int32_t* depth, float* values, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || D < 1 || D > sv::kGrowMaxD || K < 1 || K > sv::kGrowMaxK || V < K ||
+      V > SPEC_MAX_V || !(temperature > 0.0f) || !std::isfinite(temperature))
+    return SPEC_ERR_INVALID_ARG;
+  const int nnodes = 1 + K + (D - 1) * K * K;
+  if (M < 0 || M > nnodes - 1) return SPEC_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(SPEC_MODE_TREE_GROW, B, K, V, dtype, &L)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!draft_logits || !tokens || !parents || !depth || !values) return SPEC_ERR_INVALID_ARG;
+  if (!aligned(draft_logits, elem_bytes(dtype)) || !aligned(tokens, 4) || !aligned(parents, 4) ||
+      !aligned(depth, 4) || !aligned(values, 4))
+    return SPEC_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
+  char* ws = static_cast<char*>(workspace);
+  sv::GrowParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  prm.logits = draft_logits;
+  prm.scale = (float)(1.4426950408889634 / (double)temperature);
+  prm.B = B;
+  prm.D = D;
+  prm.K = K;
+  prm.V = V;
+  prm.M = M;
+  prm.nchunks = L.nchunks;
+  prm.rec = reinterpret_cast<sv::GrowRec*>(ws + L.off_part);
+  prm.nval = reinterpret_cast<double*>(ws + L.off_desc);
+  prm.npar = reinterpret_cast<int32_t*>(ws + L.off_gsum);
+  prm.ntok = prm.npar + (size_t)B * sv::kGrowMaxNodes;
+  prm.ndep = prm.ntok + (size_t)B * sv::kGrowMaxNodes;
+  prm.tokens = tokens;
+  prm.parents = parents;
+  prm.depth = depth;
+  prm.values = values;
+  prm.flags = reinterpret_cast<unsigned*>(ws);
+  // every draft row the growth reads, reduced in one streaming launch
+  prm.rows_per_tree = 1 + (D - 1) * K;
+  if ((long long)B * prm.rows_per_tree * prm.nchunks > INT32_MAX) return SPEC_ERR_INVALID_ARG;
+  prm.items = B * prm.rows_per_tree * prm.nchunks;
+  const bool vec = vec_ok(draft_logits, V, dtype);  // whole 16-byte vectors per row
+  spec_status_t st;
+  if (vec) {
+    int grid = 0;
+    if (dtype == SPEC_DTYPE_BF16) {
+      st = persistent_grid<sv::grow_topk_stream_kernel<sv::BF16>>(prm.items, &grid);
+      if (st == SPEC_OK)
+        st = launch(sv::grow_topk_stream_kernel<sv::BF16>, grid, kStreamSmem, prm, stream, false);
+    } else {
+      st = persistent_grid<sv::grow_topk_stream_kernel<sv::F32>>(prm.items, &grid);
+      if (st == SPEC_OK)
+        st = launch(sv::grow_topk_stream_kernel<sv::F32>, grid, kStreamSmem, prm, stream, false);
+    }
+  } else if (dtype == SPEC_DTYPE_BF16) {
+    st = launch(sv::grow_topk_kernel<sv::BF16, false>, prm.items, 0, prm, stream, false);
+  } else {
+    st = launch(sv::grow_topk_kernel<sv::F32, false>, prm.items, 0, prm, stream, false);
+  }
+  if (st != SPEC_OK) return st;
+  // the node bookkeeping of every layer and the final ranking, one CTA per tree
+  st = ensure_smem<sv::grow_tree_kernel>(sv::kGrowTreeSmem);
+  if (st != SPEC_OK) return st;
+  return launch(sv::grow_tree_kernel, B,
+                sv::grow_tree_smem(L.nchunks, K, prm.rows_per_tree, nnodes), prm, stream,
+                true);
 }
 
 spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_flags, int clear,

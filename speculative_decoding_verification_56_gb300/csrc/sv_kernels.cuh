@@ -207,9 +207,10 @@ __device__ __forceinline__ void vec_pairs<F32>(const uint4& v, unsigned long lon
 // exponentials on the special-function unit; one two-sum per chunk.
 template <typename E>
 __device__ __forceinline__ void stats_chunk(const uint4 (&raw)[kVecPerThread], float s,
-                                            StatsState& st) {
-  // past-the-end vectors hold -inf: they raise no maximum and add 2^-inf = 0
-  const int r = exp_ref(vec4_max<E>(raw), s);
+                                            StatsState& st, float m) {
+  // past-the-end vectors hold -inf: they raise no maximum and add 2^-inf = 0;
+  // m is the maximum of the thread's elements
+  const int r = exp_ref(m, s);
   if (r > st.ref) {  // exact rescale of the running sum by 2^(old - new)
     st.acc.scale(pow2i_f(st.ref - r));
     st.ref = r;
@@ -237,6 +238,12 @@ __device__ __forceinline__ void stats_chunk(const uint4 (&raw)[kVecPerThread], f
   float a0, a1;
   f2unpack(add2(add2(vs[0], vs[1]), add2(vs[2], vs[3])), a0, a1);
   st.acc.add(__fadd_rn(a0, a1));
+}
+
+template <typename E>
+__device__ __forceinline__ void stats_chunk(const uint4 (&raw)[kVecPerThread], float s,
+                                            StatsState& st) {
+  stats_chunk<E>(raw, s, st, vec4_max<E>(raw));
 }
 
 struct ArgState {

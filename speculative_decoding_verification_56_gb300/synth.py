@@ -366,3 +366,21 @@ def make_lm_head_case(*, B, k, d, V, seed=0, peak=6.0, p_match=0.7, flat_frac=0.
     tokens = np.where(rng.random((B, k)) < p_match, draft_int,
                       rng.integers(0, V, (B, k))).astype(np.int32)
     return H_bits, W_bits, tokens, intended.astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# Draft rows for tree growth
+# ---------------------------------------------------------------------------
+
+def make_grow_logits(*, B, D, K, V, dtype=DTYPE_BF16, sigma=3.0, zipf=True, seed=0):
+    """Draft logits [B, D, K, V] (stored bits) for tree growth: Gaussian
+    N(0, sigma^2) plus, with ``zipf``, the per-sequence Zipf(1.1) log-bias of
+    the verification workloads (a peaked, LM-like distribution)."""
+    rng = np.random.default_rng(seed)
+    z = _gauss(rng, (B, D, K, V), sigma)
+    if zipf:
+        bias = _zipf_bias_rows(rng, B, V)
+        z += bias[:, None, None, :]
+    out = _store(z, dtype)
+    del z
+    return out

@@ -200,3 +200,79 @@ def test_kv_commit_after_tree_verification():
     got, got_len, flags = _gpu_kv(cache, base, acc, path, t.N)
     assert not bad and flags == 0
     assert np.array_equal(got_len, want_len) and np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# EAGLE-2 tree growth
+# ---------------------------------------------------------------------------
+
+def _gpu_grow(z, dtype, T, M):
+    t = sv.to_device_logits(z, dtype)
+    out = sv.tree_grow(t, T, M)
+    torch.cuda.synchronize()
+    return {key: v.cpu().numpy() for key, v in out.items()}
+
+
+@pytest.mark.parametrize("B,D,K,V,M,T,dtype,seed", [
+    (1, 1, 1, 8, 1, 1.0, "f32", 0),
+    (3, 2, 4, 100, 10, 1.0, "f32", 1),
+    (4, 4, 3, 1000, 20, 0.7, "bf16", 2),
+    (2, 6, 8, 20000, 59, 1.0, "bf16", 3),       # crosses 32 KB chunks
+    (2, 3, 16, 33000, 100, 1.3, "f32", 4),
+    (2, 5, 5, 5001, 40, 1.0, "bf16", 5),        # odd vocabulary: plain loads
+])
+def test_tree_grow_matches_oracle(B, D, K, V, M, T, dtype, seed):
+    z = synth.make_grow_logits(B=B, D=D, K=K, V=V, dtype=dtype, seed=seed)
+    ref = oracle.tree_grow(z, T, M, dtype=dtype)
+    got = _gpu_grow(z, dtype, T, M)
+    ok = ref["min_gap"] > 1e-9          # trees with a near-tie at a cut may differ
+    assert ok.mean() >= 0.5
+    for key in ("tokens", "parents", "depth"):
+        assert np.array_equal(got[key][ok], ref[key][ok]), key
+    assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("B,D,K,V,M,dtype", [
+    (2, 4, 4, 20000, 12, "bf16"),
+    (2, 3, 16, 40000, 32, "f32"),
+])
+def test_tree_grow_tied_block(B, D, K, V, M, dtype):
+    # 3000 equal logits on top of every row: more tied candidates than the
+    # top-k buffer holds, so the exact per-warp fallback ranks the chunk;
+    # the K lowest indices of the block win
+    z = synth.logits_as_f32(synth.make_grow_logits(B=B, D=D, K=K, V=V, dtype=dtype, seed=11), dtype)
+    z[..., :3000] = z.max(axis=-1, keepdims=True) + 0.5
+    if dtype == "bf16":
+        z = synth.f32_to_bf16_bits(z)
+    ref = oracle.tree_grow(z, 1.0, M, dtype=dtype)
+    got = _gpu_grow(z, dtype, 1.0, M)
+    assert set(np.unique(ref["tokens"][:, 1:])) <= set(range(K))
+    ok = ref["min_gap"] > 1e-9
+    assert ok.mean() >= 0.5
+    for key in ("tokens", "parents", "depth"):
+        assert np.array_equal(got[key][ok], ref[key][ok]), key
+    assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("V", [1000, 1001])
+def test_tree_grow_launch_count(V):
+    # one top-k pass over every draft row, one tree kernel; on the bulk-copy
+    # path (rows of whole 16-byte vectors) and the plain-load path
+    z = synth.make_grow_logits(B=2, D=5, K=4, V=V, dtype="f32", seed=1)
+    t = sv.to_device_logits(z, "f32")
+    n0 = sv.spec_verify_launch_count()
+    sv.tree_grow(t, 1.0, 20)
+    torch.cuda.synchronize()
+    assert sv.spec_verify_launch_count() - n0 == 2
+
+
+def test_tree_grow_feeds_verification_and_mask():
+    # the grown tree is a valid input of tree verification and of the mask
+    B, D, K, V, M = 4, 6, 8, 128256, 59
+    z = synth.make_grow_logits(B=B, D=D, K=K, V=V, seed=7)
+    got = _gpu_grow(z, "bf16", 1.0, M)
+    par = got["parents"]
+    assert (par[:, 0] == -1).all()
+    assert ((par[:, 1:] >= 0) & (par[:, 1:] < np.arange(1, M + 1))).all()
+    m_o, d_o, bad = oracle.tree_mask(par)
+    assert not bad and np.array_equal(d_o, got["depth"])
