@@ -74,7 +74,8 @@ __device__ __forceinline__ bool grow_better(float v1, int i1, float v2, int i2) 
 // key(a) < key(b), with -0.0 folded onto +0.0.  Orders of node values are
 // taken on these keys, in integer arithmetic, rather than by double compares.
 __device__ __forceinline__ unsigned long long grow_key(double x) {
-  const unsigned long long u = (unsigned long long)__double_as_longlong(x + 0.0);
+  unsigned long long u = (unsigned long long)__double_as_longlong(x);
+  if (u == 0x8000000000000000ull) u = 0;  // -0.0
   return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
 }
 
@@ -371,9 +372,14 @@ __host__ __device__ inline size_t grow_row_bytes(int rows, int K) {
   return (b + 15) & ~(size_t)15;
 }
 __host__ __device__ inline size_t grow_stage_bytes(int nchunks, int K) {
-  // candidates (value, token), then per chunk: head pointer, reference, sum (hi, lo)
+  // candidates (value, token), then per chunk: head pointer, reference, sum
+  // (hi, lo); then 32 gathered candidates (value, token)
   return (size_t)nchunks * K * (sizeof(float) + sizeof(int)) +
-         (size_t)nchunks * (2 * sizeof(int) + 2 * sizeof(float));
+         (size_t)nchunks * (2 * sizeof(int) + 2 * sizeof(float)) + 32 * (sizeof(float) + sizeof(int));
+}
+
+__device__ __forceinline__ void grow_cp4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 __host__ __device__ inline int grow_nstage(int nchunks, int K) {
   const size_t fit = kGrowStageBudget / grow_stage_bytes(nchunks, K);
@@ -399,13 +405,12 @@ constexpr size_t kGrowTreeSmem =
 // depend on which node the frontier put in the row's slot, so every row of
 // the tree is reduced first, nstage rows at a time: the CTA stages the rows'
 // chunk records in shared memory, then warp w takes row q0 + w, merges the
-// chunk normalisers and picks the K best tokens by K rounds of a head merge
-// over the chunk lists (each sorted best first; each lane owns some lists; a
-// round takes the best head); then
+// chunk normalisers and picks the K best tokens from the chunk lists (each
+// sorted best first) by a threshold and a shuffle ranking; then
 // a thread per row takes log2 of the row sum and a thread per (row, rank)
 // its ln q = (z s - R - log2 S) ln 2, in float64.  The layers are then one
 // warp's work: a child's value is its parent's plus the row's ln q, and the
-// next frontier merges the slots' child lists (each sorted by value).
+// next frontier is the K children ranked best among the layer's children.
 // Finally every non-root node is sorted by (value desc, creation asc), the
 // first M are kept and renumbered in creation order.  Launched
 // programmatically after the top-k grid and waits for it before reading the
@@ -448,23 +453,25 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
     for (int q0 = 0; q0 < rows; q0 += nstage) {
       const int nb = min(nstage, rows - q0);
       const GrowRec* rec0 = p.rec + ((size_t)b * rows + q0) * p.nchunks;
+      // asynchronous 4-byte copies: every load of the batch is in flight at once
       for (int i = threadIdx.x; i < nb * ncand; i += kThreads) {
         const int w = i / ncand, k = i - w * ncand;
         const int c = k / K, r = k - c * K;
         const GrowRec& g = rec0[(size_t)w * p.nchunks + c];
         float* cv = reinterpret_cast<float*>(stage0 + (size_t)w * sb);
-        cv[k] = g.val[r];
-        reinterpret_cast<int*>(cv + ncand)[k] = g.idx[r];
+        grow_cp4(cv + k, &g.val[r]);
+        grow_cp4(reinterpret_cast<int*>(cv + ncand) + k, &g.idx[r]);
       }
       for (int i = threadIdx.x; i < nb * p.nchunks; i += kThreads) {
         const int w = i / p.nchunks, c = i - w * p.nchunks;
         const GrowRec& g = rec0[i];
         int* hp = reinterpret_cast<int*>(stage0 + (size_t)w * sb) + 2 * (size_t)ncand;
         hp[c] = 0;
-        hp[p.nchunks + c] = g.ref;
-        reinterpret_cast<float*>(hp + 2 * p.nchunks)[c] = g.hi;
-        reinterpret_cast<float*>(hp + 3 * p.nchunks)[c] = g.lo;
+        grow_cp4(hp + p.nchunks + c, &g.ref);
+        grow_cp4(hp + 2 * p.nchunks + c, &g.hi);
+        grow_cp4(hp + 3 * p.nchunks + c, &g.lo);
       }
+      asm volatile("cp.async.commit_group;\ncp.async.wait_all;" ::: "memory");
       __syncthreads();
       if (warp < nb) {
         const int q = q0 + warp;
@@ -497,30 +504,88 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
           r_hi[q] = S.hi;
           r_lo[q] = S.lo;
         }
-        // K rounds: the best head over the lists; placeholders of short
-        // chunks (index >= V) end a list
-        for (int r = 0; r < K; ++r) {
-          float bv = -INFINITY;
-          int bi = 0x7FFFFFFF, bc = -1;
-          for (int c = lane; c < p.nchunks; c += 32) {
-            const int h = hp[c];
-            if (h < K) {
-              const float v = cv[c * K + h];
-              const int ix = ci[c * K + h];
-              if (ix < p.V && grow_better(v, ix, bv, bi)) {
-                bv = v;
-                bi = ix;
-                bc = c;
-              }
+        // K best over the chunk lists (each sorted best first; placeholders
+        // of short chunks, index >= V, end a list).  A lane samples entry h
+        // of list c (the first m = 32 / nchunks entries of every list);
+        // theta = the K-th best sample: at least K entries reach it, so the
+        // K best are among the entries >= theta, a prefix of each list; when
+        // they fit in the 32 lanes, a lane each, they are ranked against one
+        // another (broadcast shared-memory reads)
+        int total = 0;  // 0: not done here
+        float* gv = const_cast<float*>(clo) + p.nchunks;
+        int* gx = reinterpret_cast<int*>(gv + 32);
+        if (p.nchunks <= 32) {
+          const int m = min(K, 32 / p.nchunks);
+          const int sc = lane / m, sh = lane - sc * m;
+          float hv = -INFINITY;
+          int hx = 0x7FFFFFFF;
+          if (sc < p.nchunks && ci[sc * K + sh] < p.V) {
+            hv = cv[sc * K + sh];
+            hx = ci[sc * K + sh];
+          }
+          gv[lane] = hv;
+          gx[lane] = hx;
+          __syncwarp();
+          int hr = 0;
+#pragma unroll 8
+          for (int u = 0; u < 32; ++u) hr += grow_better(gv[u], gx[u], hv, hx) ? 1 : 0;
+          const unsigned sel = __ballot_sync(0xffffffffu, hx != 0x7FFFFFFF && hr == K - 1);
+          const float theta = sel ? __shfl_sync(0xffffffffu, hv, __ffs(sel) - 1) : -INFINITY;
+          int cnt = 0;
+          if (lane < p.nchunks)
+            for (int h = 0; h < K; ++h)
+              cnt += (ci[lane * K + h] < p.V && cv[lane * K + h] >= theta) ? 1 : 0;
+          int incl = cnt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const int all = __shfl_sync(0xffffffffu, incl, 31);
+          __syncwarp();  // the samples are read before the candidates replace them
+          if (all <= 32) {
+            total = all;
+            for (int h = 0; h < cnt; ++h) {
+              gv[incl - cnt + h] = cv[lane * K + h];
+              gx[incl - cnt + h] = ci[lane * K + h];
+            }
+            __syncwarp();
+            const float v = lane < total ? gv[lane] : -INFINITY;
+            const int x = lane < total ? gx[lane] : 0x7FFFFFFF;
+            int rank = 0;
+            for (int u = 0; u < total; ++u) rank += grow_better(gv[u], gx[u], v, x) ? 1 : 0;
+            if (lane < total && rank < K) {
+              r_z[q * K + rank] = v;
+              r_tok[q * K + rank] = x;
             }
           }
-          float wv = bv;
-          int wi = bi;
-          grow_warp_best(wv, wi);
-          if (bc >= 0 && wi == bi) {  // token indices are unique: one winner
-            ++hp[bc];
-            r_z[q * K + r] = wv;
-            r_tok[q * K + r] = wi;
+        }
+        if (total == 0) {  // too many candidates: K rounds of a head merge
+          // K rounds: the best head over the lists; placeholders of short
+          // chunks (index >= V) end a list
+          for (int r = 0; r < K; ++r) {
+            float bv = -INFINITY;
+            int bi = 0x7FFFFFFF, bc = -1;
+            for (int c = lane; c < p.nchunks; c += 32) {
+              const int h = hp[c];
+              if (h < K) {
+                const float v = cv[c * K + h];
+                const int ix = ci[c * K + h];
+                if (ix < p.V && grow_better(v, ix, bv, bi)) {
+                  bv = v;
+                  bi = ix;
+                  bc = c;
+                }
+              }
+            }
+            float wv = bv;
+            int wi = bi;
+            grow_warp_best(wv, wi);
+            if (bc >= 0 && wi == bi) {  // token indices are unique: one winner
+              ++hp[bc];
+              r_z[q * K + r] = wv;
+              r_tok[q * K + r] = wi;
+            }
           }
         }
       }
@@ -567,35 +632,19 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
       }
       __syncwarp();
       if (layer + 1 < p.D) {
-        int h = 0;  // this lane's slot list (lane < nfront) consumed so far
-        int nf = 0;
-        double nv = 0.0;
-        for (int r = 0; r < K; ++r) {
-          unsigned long long kv = 0;  // below every key
-          int kt = 0x7FFFFFFF;
-          if (lane < nfront && h < K) {
-            kt = lane * K + h;
-            kv = s_val[kt];
+        // a child's rank = the children before it (independent loads)
+        for (int t = lane; t < nc; t += 32) {
+          const unsigned long long v = s_val[t];
+          int rank = 0;
+#pragma unroll 8
+          for (int u = 0; u < nc; ++u) {
+            const unsigned long long o = s_val[u];
+            rank += (o > v || (o == v && u < t)) ? 1 : 0;
           }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long ov = __shfl_xor_sync(0xffffffffu, kv, o);
-            const int ot = __shfl_xor_sync(0xffffffffu, kt, o);
-            if (ov > kv || (ov == kv && ot < kt)) {
-              kv = ov;
-              kt = ot;
-            }
+          if (rank < K) {
+            s_front[rank] = base + t;
+            s_fval[rank] = s_dval[t];
           }
-          if (lane < nfront && h < K && kt == lane * K + h) ++h;
-          if (lane == r) {
-            nf = base + kt;
-            nv = s_dval[kt];
-          }
-        }
-        __syncwarp();
-        if (lane < K) {
-          s_front[lane] = nf;
-          s_fval[lane] = nv;
         }
         __syncwarp();
       }
