@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU baseline (0 disables it)")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--profile-case", choices=["lm_head_greedy", "tree_grow"], default=None,
+                    help="only run that kernel --calls times, untimed (for ncu)")
+    ap.add_argument("--calls", type=int, default=3)
     return ap.parse_args()
 
 
@@ -443,6 +446,58 @@ def _time_loop(fn, stream, K, per_graph=20):
     return e0.elapsed_time(e1) / (reps * per_graph)
 
 
+def lm_head_case(dev):
+    """LM head fused with greedy verification on the greedy workload's shape:
+    B=64, k=4 (320 target rows), hidden 4096, V=128256, bf16."""
+    import torch
+    import speculative_decoding_verification_56_gb300 as sv
+    from speculative_decoding_verification_56_gb300 import synth
+    Bl, kl, d, Vl = 64, 4, 4096, 128256
+    Hb, Wb, tokl, _ = synth.make_lm_head_case(B=Bl, k=kl, d=d, V=Vl, seed=1)
+    c = {"B": Bl, "k": kl, "d": d, "V": Vl, "rows": Bl * (kl + 1)}
+    c["H"] = torch.from_numpy(Hb.view(np.int16)).view(torch.bfloat16).to(dev)
+    c["W"] = torch.from_numpy(Wb.view(np.int16)).view(torch.bfloat16).to(dev)
+    del Hb, Wb
+    c["tokens"] = torch.from_numpy(tokl).to(dev)
+    c["acc"] = torch.empty(Bl, dtype=torch.int32, device=dev)
+    c["out"] = torch.empty(Bl, kl + 1, dtype=torch.int32, device=dev)
+    c["ws"] = sv.alloc_workspace(sv.SPEC_MODE_LM_HEAD_GREEDY, Bl, kl, Vl, sv.SPEC_DTYPE_BF16, dev)
+    c["call"] = lambda stream: sv.spec_lm_head_verify_greedy(c["H"], c["W"], c["tokens"], c["acc"],
+                                                             c["out"], c["ws"], stream)
+    return c
+
+
+def grow_case(dev):
+    """EAGLE-2 tree growth producing the tree workload's shape (16 trees of 60
+    nodes): 6 layers of 8 frontier rows over V=128256 bf16 draft rows."""
+    import torch
+    import speculative_decoding_verification_56_gb300 as sv
+    from speculative_decoding_verification_56_gb300 import synth
+    Bg, Dg, Kg, Mg, Vg = 16, 6, 8, 59, 128256
+    zg = synth.make_grow_logits(B=Bg, D=Dg, K=Kg, V=Vg, seed=2)
+    c = {"B": Bg, "D": Dg, "K": Kg, "M": Mg, "V": Vg}
+    c["z"] = sv.to_device_logits(zg, "bf16", dev)
+    del zg
+    gi = dict(dtype=torch.int32, device=dev)
+    c["out"] = [torch.empty(Bg, Mg + 1, **gi) for _ in range(3)] + \
+        [torch.empty(Bg, Mg + 1, dtype=torch.float32, device=dev)]
+    c["ws"] = sv.alloc_workspace(sv.SPEC_MODE_TREE_GROW, Bg, Kg, Vg, sv.SPEC_DTYPE_BF16, dev)
+    c["call"] = lambda stream: sv.spec_tree_grow(c["z"], 1.0, Mg, *c["out"], c["ws"], stream)
+    return c
+
+
+def profile_case(name, calls):
+    """Run one of the kernels around the draft tree `calls` times, untimed:
+    the program ncu profiles (`--profile-case`)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    c = {"lm_head_greedy": lm_head_case, "tree_grow": grow_case}[name](dev)
+    for _ in range(calls):
+        c["call"](None)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": name, "calls": calls}), flush=True)
+
+
 def measure_next_rows(dev, stream, tree, K):
     """The kernels around the draft tree (each timed alone, outside the step):
     tree attention mask of the tree workload's trees, and the KV commit of
@@ -498,17 +553,9 @@ def measure_next_rows(dev, stream, tree, K):
     # (B=64, k=4 -> 320 target rows) with hidden size 4096 and V=128256,
     # against the unfused path (cuBLAS GEMM writing the logits, then greedy
     # verification of the logits)
-    from speculative_decoding_verification_56_gb300 import synth
-    Bl, kl, d, Vl = 64, 4, 4096, 128256
-    Hb, Wb, tokl, _ = synth.make_lm_head_case(B=Bl, k=kl, d=d, V=Vl, seed=1)
-    H = torch.from_numpy(Hb.view(np.int16)).view(torch.bfloat16).to(dev)
-    Wm = torch.from_numpy(Wb.view(np.int16)).view(torch.bfloat16).to(dev)
-    del Hb, Wb
-    tk = torch.from_numpy(tokl).to(dev)
-    rows = Bl * (kl + 1)
-    acc_l = torch.empty(Bl, dtype=torch.int32, device=dev)
-    out_l = torch.empty(Bl, kl + 1, dtype=torch.int32, device=dev)
-    wsl = sv.alloc_workspace(sv.SPEC_MODE_LM_HEAD_GREEDY, Bl, kl, Vl, sv.SPEC_DTYPE_BF16, dev)
+    lm = lm_head_case(dev)
+    Bl, kl, d, Vl, rows = lm["B"], lm["k"], lm["d"], lm["V"], lm["rows"]
+    H, Wm, tk, acc_l, out_l, wsl = lm["H"], lm["W"], lm["tokens"], lm["acc"], lm["out"], lm["ws"]
     wsg = sv.alloc_workspace(sv.SPEC_MODE_GREEDY, Bl, kl, Vl, sv.SPEC_DTYPE_BF16, dev)
     logits = torch.empty(rows, Vl, dtype=torch.bfloat16, device=dev)
     ms_f = _time_loop(lambda: sv.spec_lm_head_verify_greedy(H, Wm, tk, acc_l, out_l, wsl, stream),
@@ -532,30 +579,24 @@ def measure_next_rows(dev, stream, tree, K):
         "unfused": "torch.matmul (cuBLAS) writing bf16 logits, then spec_verify_greedy",
         "bound": "W_LM stream (1.05 GB) and tensor cores, about balanced at 320 rows",
         "timed": "CUDA-graph replay of 4 calls"}
-    del H, Wm, logits
+    del H, Wm, logits, lm
 
     # EAGLE-2 tree growth producing the tree workload's shape (16 trees of 60
     # nodes): 6 layers of 8 frontier rows over V=128256 bf16 draft rows
-    Bg, Dg, Kg, Mg = 16, 6, 8, 59
-    zg = synth.make_grow_logits(B=Bg, D=Dg, K=Kg, V=Vl, seed=2)
-    zt = sv.to_device_logits(zg, "bf16", dev)
-    del zg
-    gi = dict(dtype=torch.int32, device=dev)
-    g_tok, g_par, g_dep = (torch.empty(Bg, Mg + 1, **gi) for _ in range(3))
-    g_val = torch.empty(Bg, Mg + 1, dtype=torch.float32, device=dev)
-    wsgr = sv.alloc_workspace(sv.SPEC_MODE_TREE_GROW, Bg, Kg, Vl, sv.SPEC_DTYPE_BF16, dev)
-    ms_g = _time_loop(lambda: sv.spec_tree_grow(zt, 1.0, Mg, g_tok, g_par, g_dep, g_val, wsgr,
-                                                stream), stream, max(40, K // 10), per_graph=8)
+    gr = grow_case(dev)
+    Bg, Dg, Kg, Mg, Vg = gr["B"], gr["D"], gr["K"], gr["M"], gr["V"]
+    ms_g = _time_loop(lambda: gr["call"](stream), stream, max(40, K // 10), per_graph=8)
     rows_read = Bg * (1 + (Dg - 1) * Kg)
-    gbytes = rows_read * Vl * 2
-    out["tree_grow"] = {"workload": f"B={Bg} trees, {Dg} layers x {Kg} frontier rows, V={Vl} "
+    gbytes = rows_read * Vg * 2
+    out["tree_grow"] = {"workload": f"B={Bg} trees, {Dg} layers x {Kg} frontier rows, V={Vg} "
                                     f"bf16, budget {Mg} nodes",
                         "us_per_call": round(ms_g * 1e3, 2), "bytes": int(gbytes),
                         "gb_s": round(gbytes / (ms_g / 1e3) / 1e9, 1),
                         "launches": 2,
-                        "bound": "HBM (top-k + normaliser per draft row) and launch latency",
+                        "bound": "streaming top-k: issue and CTA-barrier latency (HBM at 1/3); "
+                                 "per-tree bookkeeping: latency chain on 16 CTAs",
                         "timed": "CUDA-graph replay of 8 calls"}
-    del zt
+    del gr
     return out
 
 
@@ -641,7 +682,9 @@ def run_reference(args, rank, world):
 def main():
     args = parse_args()
     rank, world, local_rank = dist_env()
-    if args.impl == "reference":
+    if args.profile_case:
+        profile_case(args.profile_case, args.calls)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)
