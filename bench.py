@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--profile-case", choices=["lm_head_greedy", "tree_grow"], default=None,
                     help="only run that kernel --calls times, untimed (for ncu)")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--skip-next-rows", action="store_true",
+                    help="leave out the kernels around the draft tree (next_rows)")
     return ap.parse_args()
 
 
@@ -318,7 +320,8 @@ def run_ours(args, rank, world, local_rank):
         mean_ms.append(e0.elapsed_time(e1) / K)
     mean_ms = np.array(mean_ms)
     clk = clocks.stop(t_wall0, t_wall1) if clocks else None
-    next_rows = measure_next_rows(dev, stream, tree, K) if rank == 0 else None
+    next_rows = measure_next_rows(dev, stream, tree, K) \
+        if rank == 0 and not args.skip_next_rows else None
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([total_ms], device=dev)
