@@ -31,6 +31,8 @@
 // choices are exact; node values are float64.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "sv_kernels.cuh"
 
 namespace sv {
@@ -92,30 +94,6 @@ __device__ __forceinline__ void grow_warp_best(float& v, int& i) {
   }
 }
 
-constexpr int kGrowCand = 512;  // candidates above the threshold kept per chunk
-
-// outv/outi[r] = the r-th best of n (value, index) candidates, for r < K;
-// ranks past n get (-inf, INT_MAX).  Every thread of the CTA takes part: a
-// candidate's rank is the number of candidates better than it, which the
-// strict order of grow_better makes unique.
-__device__ __forceinline__ void grow_rank_select(const float* cv, const int* ci, int n, int K,
-                                                 float* outv, int* outi) {
-  for (int t = threadIdx.x; t < n; t += kThreads) {
-    const float v = cv[t];
-    const int i = ci[t];
-    int rank = 0;
-    for (int u = 0; u < n && rank < K; ++u) rank += grow_better(cv[u], ci[u], v, i);
-    if (rank < K) {
-      outv[rank] = v;
-      outi[rank] = i;
-    }
-  }
-  for (int r = n + (int)threadIdx.x; r < K; r += kThreads) {
-    outv[r] = -INFINITY;
-    outi[r] = 0x7FFFFFFF;
-  }
-}
-
 // Draft row q of a tree: q = 0 is layer 0's slot 0; q = 1 + (l - 1) K + j is
 // layer l's slot j.  Returns the row's element offset in logits [B, D, K, V].
 __device__ __forceinline__ size_t grow_row_offset(const GrowParams& p, int rowi) {
@@ -125,14 +103,52 @@ __device__ __forceinline__ size_t grow_row_offset(const GrowParams& p, int rowi)
   return (((size_t)b * p.D + layer) * p.K + slot) * (size_t)p.V;
 }
 
-struct GrowTopkSmem {
-  float cv[kGrowCand];  // candidates >= theta
-  int ci[kGrowCand];
-  float wm[kWarps];     // warp maxima
-  StatsSlot st[kWarps]; // warp softmax partials of the segment ending here
-  int n;                // candidates found
-  int seg_end;          // this item ends a row segment: st holds its partials
+// Streaming top-k over row segments.  A CTA walks contiguous items (row,
+// 32 KB chunk); a row segment is its run of items of one row.  Each warp
+// keeps the candidates of its own 1024 elements per item in a small buffer
+// for the whole segment, with a running threshold thr: at least K of the
+// warp's elements so far are >= thr, so no element below it can be among the
+// segment's K best -- in this warp or any other, so the warps publish their
+// thresholds (an atomic max in shared memory) and each uses the largest.  The
+// first item of a segment takes thr = the K-th largest of the 16 warp maxima
+// (one CTA barrier); a full buffer is compacted to its K best, whose K-th
+// value raises thr.  Elements are tested against thr eight at a time
+// (packed compares) and only vectors whose maximum reaches thr are looked at.
+// Only at a segment end do the warps meet (CTA barriers):
+// the 16 warp lists are merged into the record of the segment's last item,
+// with the segment's softmax partial; the segment's other records carry an
+// empty list and an empty partial.
+constexpr int kGrowBuf = 32;  // candidates per warp buffer
+struct GrowSegSmem {
+  uint2 buf[kWarps][kGrowBuf];        // (value bits, index) of the warp's candidates
+  int n[kWarps];                      // entries appended (more than kGrowBuf: overflow)
+  uint2 lists[kWarps * kGrowMaxK];    // warp w's [w kGrowMaxK, +kGrowMaxK): compaction
+                                      // scratch, and its K best at a segment end
+  StatsSlot st[kWarps];
+  float wm[kWarps];                   // warp maxima of a segment's first item
+  unsigned thr_key;                   // largest published warp threshold (grow_fkey)
 };
+
+// Order-preserving unsigned key of a non-NaN float and back, for atomicMax.
+__device__ __forceinline__ unsigned grow_fkey(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u >> 31) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float grow_funkey(unsigned k) {
+  return __uint_as_float((k >> 31) ? (k & 0x7FFFFFFFu) : ~k);
+}
+__device__ __forceinline__ void grow_seg_smem_init(GrowSegSmem& sh) {
+  if (threadIdx.x < kWarps) sh.n[threadIdx.x] = 0;
+  if (threadIdx.x == 0) sh.thr_key = grow_fkey(-INFINITY);
+}
+
+__device__ __forceinline__ uint2 grow_pack(float v, int i) {
+  return make_uint2(__float_as_uint(v), (unsigned)i);
+}
+// a before (v, i): larger value, then lower index
+__device__ __forceinline__ bool grow_before(uint2 a, float v, int i) {
+  return grow_better(__uint_as_float(a.x), (int)a.y, v, i);
+}
 
 // Largest element of one 16-byte vector.
 template <typename E>
@@ -148,119 +164,90 @@ __device__ __forceinline__ float grow_vec_max<BF16>(const uint4& v) {
   return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// The second step of an item's top-k (every thread, after the item's
-// grow_topk_collect and before barrier A of the next one): ranks the
-// buffer's candidates into the item's record and, if the item ends a row
-// segment, merges the warps' softmax partials of the segment into it (other
-// records carry an empty partial).  No CTA barrier.
-__device__ __forceinline__ void grow_topk_finish(const GrowParams& p, int item,
-                                                 const GrowTopkSmem& b) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  GrowRec* out = p.rec + item;  // item = row * nchunks + chunk
-  grow_rank_select(b.cv, b.ci, b.n, p.K, out->val, out->idx);
-  if (warp == kWarps - 1) {
-    int R = kRefEmpty;
-    FSum tot = FSum::zero();
-    if (b.seg_end) {
-      StatsSlot v = lane < kWarps ? b.st[lane] : StatsSlot{kRefEmpty, 0.0f, 0.0f, 0};
-      R = warp_max_i(v.ref);
-      FSum f;
-      f.hi = v.hi;
-      f.lo = v.lo;
-      f.scale(pow2i_f(v.ref - R));
-      tot = warp_sum_df(f);
-    }
-    if (lane == 0) {
-      out->ref = R;
-      out->hi = tot.hi;
-      out->lo = tot.lo;
-      out->nk = p.K;
-    }
+// Bit e set iff element e of the 16-byte vector is >= thr (bf16: thr is a
+// bf16 value, so the packed compare is exact).
+template <typename E>
+__device__ __forceinline__ unsigned grow_ge_mask(const uint4& v, float thr);
+template <>
+__device__ __forceinline__ unsigned grow_ge_mask<F32>(const uint4& v, float thr) {
+  return (__uint_as_float(v.x) >= thr ? 1u : 0u) | (__uint_as_float(v.y) >= thr ? 2u : 0u) |
+         (__uint_as_float(v.z) >= thr ? 4u : 0u) | (__uint_as_float(v.w) >= thr ? 8u : 0u);
+}
+template <>
+__device__ __forceinline__ unsigned grow_ge_mask<BF16>(const uint4& v, float thr) {
+  const __nv_bfloat16 tb = __float2bfloat16_rn(thr);
+  const __nv_bfloat162 t2 = __halves2bfloat162(tb, tb);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  unsigned m = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const unsigned c = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[k]), t2);
+    m |= ((c & 1u) | ((c >> 15) & 2u)) << (2 * k);
   }
+  return m;
 }
 
-// Top-k of one (draft row, 32 KB chunk) item in two steps, so that a CTA
-// streaming several items overlaps the ranking of one with the
-// exponentials of the next.  theta, the K-th largest of the 16 warp maxima,
-// is reached by at least K elements, so the chunk's K largest are all
-// >= theta: only vectors whose maximum reaches theta are searched for
-// candidates (a few dozen elements per chunk).  The softmax partial runs on
-// in each thread over a row's consecutive chunks (st) and is reduced over
-// the CTA once per row segment.  Consecutive items alternate between two
-// buffers.
-//
-// grow_topk_collect (every thread, the item's vectors in registers, past-
-// the-end elements -inf): the partial, the warp maxima, theta and the
-// candidates into sh[cur]; if ties at theta overflow the buffer, the 16
-// warps' exact K best (K rounds each) replace the candidates.  Between the
-// exponentials and the first CTA barrier it finishes the previous item
-// (prev >= 0, held in sh[cur ^ 1]), then clears sh[cur ^ 1].n.  Two CTA
-// barriers; sh[cur].n is 0 on entry.  seg_end is uniform over the CTA.
-template <typename E>
-__device__ __forceinline__ void grow_topk_collect(const GrowParams& p,
-                                                  const uint4 (&raw)[kVecPerThread], int item,
-                                                  bool seg_end, StatsState& st, int prev,
-                                                  GrowTopkSmem* sh, int cur) {
-  GrowTopkSmem& b = sh[cur];
+// Whole warp: keep the K best of the first m (<= kGrowBuf) entries of the
+// warp's buffer, best first at buf[0 ..), and return how many remain
+// (min(m, K)).  Entries are distinct (distinct indices), so ranks are too.
+__device__ __forceinline__ int grow_warp_compact(GrowSegSmem& sh, int m, int K) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c = item % p.nchunks;
-  const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
-  const int K = p.K;
-  float vm[kVecPerThread];
-#pragma unroll
-  for (int q = 0; q < kVecPerThread; ++q) vm[q] = grow_vec_max<E>(raw[q]);
-  const float tmax = fmaxf(fmaxf(vm[0], vm[1]), fmaxf(vm[2], vm[3]));
-  stats_chunk<E>(raw, p.scale, st, tmax);
-  const float wmax = warp_max_f(tmax);
-  if (seg_end) {
-    const int wref = warp_max_i(st.ref);
-    FSum mine = st.acc;
-    mine.scale(pow2i_f(st.ref - wref));
-    const FSum wsum = warp_sum_df(mine);
-    if (lane == 0) b.st[warp] = StatsSlot{wref, wsum.hi, wsum.lo, 0};
-    st = StatsState();
+  uint2* buf = sh.buf[warp];
+  uint2* tmp = sh.lists + warp * kGrowMaxK;
+  __syncwarp();
+  if (lane < m) {
+    const uint2 me = buf[lane];
+    const float v = __uint_as_float(me.x);
+    const int x = (int)me.y;
+    int rank = 0;
+    for (int u = 0; u < m; ++u) rank += grow_before(buf[u], v, x) ? 1 : 0;
+    if (rank < K) tmp[rank] = me;
   }
-  if (lane == 0) b.wm[warp] = wmax;
-  if (threadIdx.x == 0) b.seg_end = seg_end;
-  if (prev >= 0) grow_topk_finish(p, prev, sh[cur ^ 1]);
-  __syncthreads();  // A
-  if (threadIdx.x == 0) sh[cur ^ 1].n = 0;
-  // theta: the K-th largest warp maximum, by a bitonic sort of the 16
-  // maxima over lanes 0..15 (largest first); every warp finds it on its own
-  float theta;
-  {
-    float v = lane < kWarps ? b.wm[lane] : -INFINITY;
+  __syncwarp();
+  const int kept = min(m, K);
+  if (lane < kept) buf[lane] = tmp[lane];
+  __syncwarp();
+  return kept;
+}
+
+// Whole warp: append this item's elements >= thr to the warp's buffer (each
+// thread walks only its vectors whose maximum reaches thr; past-the-end
+// elements are -inf, so the index test matters only for thr = -inf).  If
+// the buffer overflows, the item's own K best are found exactly (K rounds)
+// instead and merged with the earlier entries.  Compacts a buffer that is
+// more than half full.  Returns the new entry count; thr may rise.
+template <typename E>
+__device__ __forceinline__ int grow_warp_append(GrowSegSmem& sh, const uint4 (&raw)[kVecPerThread],
+                                                const float (&vm)[kVecPerThread], int j0, int j1,
+                                                int K, int nb, float& thr) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint2* buf = sh.buf[warp];
+  thr = fmaxf(thr, grow_funkey(*(volatile unsigned*)&sh.thr_key));
+  const float seen = thr;  // published already, or this warp's own segment threshold
+  unsigned mx = 0;  // 1 + the highest slot this lane took
 #pragma unroll
-    for (int k = 2; k <= kWarps; k <<= 1)
-#pragma unroll
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, v, j);
-        v = (((lane & j) == 0) == ((lane & k) == 0)) ? fmaxf(v, o) : fminf(v, o);
-      }
-    theta = __shfl_sync(0xffffffffu, v, K - 1);
-  }
-  if (tmax >= theta) {
-#pragma unroll
-    for (int q = 0; q < kVecPerThread; ++q) {
-      if (vm[q] < theta) continue;
-#pragma unroll
-      for (int e = 0; e < E::kEPV; ++e) {
-        const float z = E::elem(raw[q], e);
-        const int j = j0 + (q * kThreads + (int)threadIdx.x) * E::kEPV + e;
-        if (z >= theta && j < j1) {
-          const int at = atomicAdd(&b.n, 1);
-          if (at < kGrowCand) {
-            b.cv[at] = z;
-            b.ci[at] = j;
-          }
-        }
-      }
+  for (int q = 0; q < kVecPerThread; ++q) {
+    if (!(vm[q] >= thr)) continue;
+    const int jb = j0 + (q * kThreads + (int)threadIdx.x) * E::kEPV;
+    unsigned em = grow_ge_mask<E>(raw[q], thr);
+    if (!(thr > -INFINITY)) em &= (1u << max(0, min(E::kEPV, j1 - jb))) - 1u;  // real elements
+    while (em) {
+      const int e = __ffs(em) - 1;
+      em &= em - 1;
+      const int at = atomicAdd(&sh.n[warp], 1);
+      mx = (unsigned)(at + 1);
+      if (at < kGrowBuf) buf[at] = grow_pack(E::elem(raw[q], e), jb + e);
     }
   }
-  __syncthreads();  // C
-  if (b.n > kGrowCand) {  // uniform: every thread reads the same count
-    __syncthreads();
+  int n = max(nb, (int)__reduce_max_sync(0xffffffffu, mx));  // the count after this item
+  if (n <= kGrowBuf / 2) return n;  // the usual case: the count is already in place
+  __syncwarp();  // every lane's entries are visible
+  if (n > kGrowBuf) {
+    // ties at thr: drop this item's entries, keep the earlier ones' K best,
+    // and add the item's exact K best (K rounds over the warp's elements)
+    n = nb > K ? grow_warp_compact(sh, nb, K) : nb;
     uint32_t used = 0;
+    int added = 0;
     for (int r = 0; r < K; ++r) {
       float bv = -INFINITY;
       int bi = 0x7FFFFFFF, bslot = -1;
@@ -280,22 +267,198 @@ __device__ __forceinline__ void grow_topk_collect(const GrowParams& p,
       float wv = bv;
       int wi = bi;
       grow_warp_best(wv, wi);
+      if (wi == 0x7FFFFFFF) break;  // no element left (uniform)
       if (bslot >= 0 && wi == bi) used |= 1u << bslot;
+      if (lane == 0) buf[n + added] = grow_pack(wv, wi);
+      ++added;
+    }
+    n = grow_warp_compact(sh, n + added, K);  // n + added <= 2 K <= kGrowBuf
+    if (n == K) thr = fmaxf(thr, __uint_as_float(buf[K - 1].x));
+  } else {
+    n = grow_warp_compact(sh, n, K);  // n > 16 >= K: the K best, sorted
+    thr = fmaxf(thr, __uint_as_float(buf[K - 1].x));
+  }
+  __syncwarp();
+  if (lane == 0) {
+    sh.n[warp] = n;
+    if (thr > seen) atomicMax(&sh.thr_key, grow_fkey(thr));  // only a raised threshold
+  }
+  __syncwarp();
+  return n;
+}
+
+// One item for the whole CTA (every thread calls it with the same flags):
+// the softmax partial runs on in st; the warp appends its candidates; at a
+// segment end (last) the 16 warp lists and partials are merged into the
+// item's record (two CTA barriers), otherwise one warp writes the item's
+// empty record.  first: the item opens a segment (thr is set here).
+template <typename E>
+__device__ __forceinline__ void grow_seg_item(const GrowParams& p,
+                                              const uint4 (&raw)[kVecPerThread], int item,
+                                              bool first, bool last, StatsState& st, float& thr,
+                                              GrowSegSmem& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = item % p.nchunks;
+  const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+  const int K = p.K;
+  float vm[kVecPerThread];
+#pragma unroll
+  for (int q = 0; q < kVecPerThread; ++q) vm[q] = grow_vec_max<E>(raw[q]);
+  const float tmax = fmaxf(fmaxf(vm[0], vm[1]), fmaxf(vm[2], vm[3]));
+  stats_chunk<E>(raw, p.scale, st, tmax);
+  if (first) {
+    // thr = the K-th largest of the 16 warp maxima (at least K of the
+    // chunk's elements reach it); every warp sorts them (bitonic over lanes
+    // 0..15, largest first) after one CTA barrier
+    const float wmax = warp_max_f(tmax);
+    if (lane == 0) sh.wm[warp] = wmax;
+    __syncthreads();
+    float v = lane < kWarps ? sh.wm[lane] : -INFINITY;
+#pragma unroll
+    for (int k = 2; k <= kWarps; k <<= 1)
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, j);
+        v = (((lane & j) == 0) == ((lane & k) == 0)) ? fmaxf(v, o) : fminf(v, o);
+      }
+    thr = __shfl_sync(0xffffffffu, v, K - 1);
+  }
+  const int nb = sh.n[warp];  // 0 when the segment opens
+  int n = grow_warp_append<E>(sh, raw, vm, j0, j1, K, nb, thr);
+  GrowRec* out = p.rec + item;  // item = row * nchunks + chunk
+  if (!last) {
+    if (warp == item % kWarps) {
+      if (lane < K) {
+        out->val[lane] = -INFINITY;
+        out->idx[lane] = 0x7FFFFFFF;
+      }
       if (lane == 0) {
-        b.cv[warp * K + r] = wv;
-        b.ci[warp * K + r] = wi;
+        out->ref = kRefEmpty;
+        out->hi = 0.0f;
+        out->lo = 0.0f;
+        out->nk = K;
       }
     }
-    if (threadIdx.x == 0) b.n = kWarps * K;
-    __syncthreads();
+    return;
   }
+  // segment end: the warp's K best, best first, at lists[warp kGrowMaxK ..]
+  // (the compaction leaves them there); placeholders fill a short list
+  n = grow_warp_compact(sh, n, K);
+  uint2* lw = sh.lists + warp * kGrowMaxK;
+  for (int r = n + lane; r < K; r += 32) lw[r] = grow_pack(-INFINITY, 0x7FFFFFFF);
+  {
+    const int wref = warp_max_i(st.ref);
+    FSum mine = st.acc;
+    mine.scale(pow2i_f(st.ref - wref));
+    const FSum wsum = warp_sum_df(mine);
+    if (lane == 0) sh.st[warp] = StatsSlot{wref, wsum.hi, wsum.lo, 0};
+    st = StatsState();
+  }
+  __syncthreads();
+  // the K best of the 16 sorted lists, by warp 0: lane l samples entry l % 2
+  // of list l / 2; theta, the K-th best sample, is reached by at least K
+  // entries, so the K best are among the entries >= theta (a prefix of every
+  // list), ranked against one another in the warp's scratch when they fit;
+  // otherwise every entry is ranked by the whole CTA
+  int gather = 0;  // warp 0: candidates gathered (0: use the fallback)
+  if (warp == 0) {
+    uint2* g = sh.buf[0];  // warp 0's buffer is free at a segment end
+    const int sw = lane >> 1, sp = lane & 1;
+    const uint2 smp = sp < K ? sh.lists[sw * kGrowMaxK + sp] : grow_pack(-INFINITY, 0x7FFFFFFF);
+    const float sv = __uint_as_float(smp.x);
+    const int sx = (int)smp.y;
+    g[lane] = smp;
+    __syncwarp();
+    int srank = 0;
+    if (sx != 0x7FFFFFFF)
+      for (int u = 0; u < 32; ++u) srank += grow_before(g[u], sv, sx) ? 1 : 0;
+    const unsigned sel = __ballot_sync(0xffffffffu, sx != 0x7FFFFFFF && srank == K - 1);
+    const float theta = sel ? __shfl_sync(0xffffffffu, sv, __ffs(sel) - 1) : -INFINITY;
+    int cnt = 0;
+    if (lane < kWarps)
+      for (int h = 0; h < K; ++h) {
+        const uint2 e = sh.lists[lane * kGrowMaxK + h];
+        cnt += (e.y != 0x7FFFFFFFu && __uint_as_float(e.x) >= theta) ? 1 : 0;
+      }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    __syncwarp();  // the samples are read before the candidates replace them
+    if (total <= 32) {
+      for (int h = 0; h < cnt; ++h) g[incl - cnt + h] = sh.lists[lane * kGrowMaxK + h];
+      __syncwarp();
+      if (lane < total) {
+        const uint2 me = g[lane];
+        const float v = __uint_as_float(me.x);
+        const int x = (int)me.y;
+        int rank = 0;
+        for (int u = 0; u < total; ++u) rank += grow_before(g[u], v, x) ? 1 : 0;
+        if (rank < K) {
+          out->val[rank] = v;
+          out->idx[rank] = x;
+        }
+      }
+      for (int r = total + lane; r < K; r += 32) {  // fewer than K elements in the segment
+        out->val[r] = -INFINITY;
+        out->idx[r] = 0x7FFFFFFF;
+      }
+      gather = total;
+    }
+    if (lane == 0) sh.n[0] = gather;  // tells the other warps whether to fall back
+  }
+  __syncthreads();
+  if (sh.n[0] == 0) {
+    // each real entry's rank among all of them, by the CTA
+    const int T = kWarps * K;
+    const int t = threadIdx.x;
+    const int tw = t / K;
+    const uint2 me = t < T ? sh.lists[tw * kGrowMaxK + (t - tw * K)] : grow_pack(-INFINITY, 0x7FFFFFFF);
+    const bool real = t < T && me.y != 0x7FFFFFFFu;
+    int rank = 0;
+    if (real)
+      for (int w = 0; w < kWarps; ++w)
+        for (int r = 0; r < K; ++r)
+          rank += grow_before(sh.lists[w * kGrowMaxK + r], __uint_as_float(me.x), (int)me.y) ? 1 : 0;
+    const int nreal = __syncthreads_count(real);
+    if (real && rank < K) {
+      out->val[rank] = __uint_as_float(me.x);
+      out->idx[rank] = (int)me.y;
+    }
+    if (t >= nreal && t < K) {
+      out->val[t] = -INFINITY;
+      out->idx[t] = 0x7FFFFFFF;
+    }
+  }
+  if (threadIdx.x == 0) sh.thr_key = grow_fkey(-INFINITY);  // every warp is done with the segment
+  if (warp == kWarps - 1) {
+    StatsSlot v = lane < kWarps ? sh.st[lane] : StatsSlot{kRefEmpty, 0.0f, 0.0f, 0};
+    const int R = warp_max_i(v.ref);
+    FSum f;
+    f.hi = v.hi;
+    f.lo = v.lo;
+    f.scale(pow2i_f(v.ref - R));
+    const FSum tot = warp_sum_df(f);
+    if (lane == 0) {
+      out->ref = R;
+      out->hi = tot.hi;
+      out->lo = tot.lo;
+      out->nk = K;
+    }
+  }
+  __syncthreads();  // the lists and partials are read before the next segment
+  if (lane == 0) sh.n[warp] = 0;
+  __syncwarp();
 }
 
 // One CTA per item, plain loads (any row size and alignment).
 template <typename E, bool kVec>
 __global__ void __launch_bounds__(kThreads, 2) grow_topk_kernel(const GrowParams p) {
   using St = typename E::storage;
-  __shared__ GrowTopkSmem sh[2];
+  __shared__ GrowSegSmem sh;
   asm volatile("griddepcontrol.launch_dependents;");
   const int item = blockIdx.x;
   const int rowi = item / p.nchunks, c = item - rowi * p.nchunks;
@@ -303,20 +466,21 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_kernel(const GrowParams
   const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
   uint4 raw[kVecPerThread];
   load_chunk_regs<E, kVec>(row, j0, j1, raw);  // past-the-end elements are -inf
-  if (threadIdx.x == 0) sh[0].n = 0;
+  grow_seg_smem_init(sh);
+  __syncthreads();
   StatsState st;
-  grow_topk_collect<E>(p, raw, item, true, st, -1, sh, 0);
-  grow_topk_finish(p, item, sh[0]);
+  float thr = -INFINITY;
+  grow_seg_item<E>(p, raw, item, true, true, st, thr, sh);
 }
 
 // Persistent CTAs over contiguous item ranges, the chunks streamed through
 // the bulk-copy ring of the verification kernels (rows of whole 16-byte
-// vectors), so the copies of the next items overlap this item's ranking.
+// vectors).  Within a row segment the loop has no CTA barrier.
 template <typename E>
 __global__ void __launch_bounds__(kThreads, 2) grow_topk_stream_kernel(const GrowParams p) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ Ring ring;
-  __shared__ GrowTopkSmem sh[2];
+  __shared__ GrowSegSmem sh;
   using St = typename E::storage;
   int i0, i1;
   item_range(p.items, i0, i1);
@@ -333,11 +497,12 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_stream_kernel(const Gro
              reinterpret_cast<const St*>(p.logits) + grow_row_offset(p, rowi) + j0, bytes,
              &ring.full[slot]);
   };
-  if (threadIdx.x == 0) sh[0].n = 0;  // ring_init ends with a CTA barrier
+  grow_seg_smem_init(sh);  // ring_init ends with a CTA barrier
   int issued = ring_init(ring, i0, i1, issue);
   int slot = 0;
   unsigned par = 0;
   StatsState st;  // this thread's partial over the current row segment
+  float thr = -INFINITY;
   for (int it = i0; it < i1; ++it) {
     const int c = it % C;
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
@@ -346,14 +511,12 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_stream_kernel(const Gro
     if (threadIdx.x == 0)
       issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
     // an aborted CTA ranks -inf: its flag is set
-    grow_topk_collect<E>(p, raw, it, c + 1 == C || it + 1 == i1, st, it > i0 ? it - 1 : -1, sh,
-                         (it - i0) & 1);
+    grow_seg_item<E>(p, raw, it, it == i0 || c == 0, c + 1 == C || it + 1 == i1, st, thr, sh);
     if (++slot == kStages) {
       slot = 0;
       par ^= 1u;
     }
   }
-  grow_topk_finish(p, i1 - 1, sh[(i1 - 1 - i0) & 1]);
   if (threadIdx.x == 0) ring_drain(ring, i0, issued);
 }
 
@@ -699,7 +862,7 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
         }
       }
     __syncthreads();
-    if (i < p.M) s_new[id] = 1;
+    if (i < p.M && id >= 1 && id < nnodes) s_new[id] = 1;
   } else {
     // several elements per thread: the same network through shared memory
     for (int k = 2; k <= P; k <<= 1)
@@ -721,7 +884,8 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
         }
         __syncthreads();
       }
-    for (int i = threadIdx.x; i < p.M; i += kThreads) s_new[s_id[i]] = 1;
+    for (int i = threadIdx.x; i < p.M; i += kThreads)
+      if (s_id[i] >= 1 && s_id[i] < nnodes) s_new[s_id[i]] = 1;
   }
   __syncthreads();
   {
