@@ -254,6 +254,30 @@ def test_tree_grow_tied_block(B, D, K, V, M, dtype):
     assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)
 
 
+def test_tree_grow_largest_tree_and_budgets():
+    # 16 layers x 16 frontier rows (3857 nodes, 241 draft rows per tree):
+    # the node sort takes its shared-memory path; budgets 0, 1, all nodes
+    B, D, K, V = 2, 16, 16, 3000
+    z = synth.make_grow_logits(B=B, D=D, K=K, V=V, dtype="f32", seed=21)
+    t = sv.to_device_logits(z, "f32")
+    for M in (0, 1, 700, 3856):
+        ref = oracle.tree_grow(z, 1.0, M, dtype="f32")
+        out = sv.tree_grow(t, 1.0, M)
+        torch.cuda.synchronize()
+        got = {key: v.cpu().numpy() for key, v in out.items()}
+        ok = ref["min_gap"] > 1e-9
+        assert ok.any()
+        for key in ("tokens", "parents", "depth"):
+            assert np.array_equal(got[key][ok], ref[key][ok]), (M, key)
+        assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)
+
+
+def test_tree_grow_empty_batch():
+    z = synth.make_grow_logits(B=1, D=2, K=2, V=64, dtype="f32", seed=0)[:0]
+    out = sv.tree_grow(sv.to_device_logits(z, "f32"), 1.0, 3)
+    assert out["tokens"].shape == (0, 4)
+
+
 @pytest.mark.parametrize("V", [1000, 1001])
 def test_tree_grow_launch_count(V):
     # one top-k pass over every draft row, one tree kernel; on the bulk-copy
