@@ -184,3 +184,65 @@ def test_product_path_never_touches_the_oracle():
                 assert not re.search(r"^\s*(import|from)\s+oracle", text, re.M), f
                 assert "spec_oracle" not in text, f
                 assert "libspecoracle" not in text, f
+
+
+# ---------------------------------------------------------------------------
+# EAGLE-2 tree growth and the fused LM head: host validation only
+# ---------------------------------------------------------------------------
+
+def _grow(lib, **over):
+    a = dict(z=FAKE, dtype=1, T=1.0, B=2, D=3, K=4, V=1000, M=10, tok=FAKE, par=FAKE, dep=FAKE,
+             val=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(over)
+    return lib.spec_tree_grow(a["z"], a["dtype"], a["T"], a["B"], a["D"], a["K"], a["V"], a["M"],
+                              a["tok"], a["par"], a["dep"], a["val"], a["ws"], a["wsb"],
+                              a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(dtype=7), 1), (dict(T=0.0), 1), (dict(T=float("nan")), 1), (dict(T=float("inf")), 1),
+    (dict(B=-1), 1), (dict(D=0), 1), (dict(D=17), 1), (dict(K=0), 1), (dict(K=17), 1),
+    (dict(V=3, K=4), 1),                                  # fewer tokens than children
+    (dict(M=-1), 1), (dict(M=4 + 2 * 16 + 1), 1),         # budget past the tree's nodes
+    (dict(K=16, V=3_000_000, dtype=0), 1),                # more than 2048 chunk lists
+    (dict(z=0), 1), (dict(tok=0), 1), (dict(par=0), 1), (dict(dep=0), 1), (dict(val=0), 1),
+    (dict(z=MISALIGNED, dtype=0), 2), (dict(val=MISALIGNED), 2),
+    (dict(ws=0), 3), (dict(wsb=16), 3), (dict(ws=FAKE + 16), 2),
+])
+def test_tree_grow_rejects_bad_arguments(lib, over, status):
+    assert _grow(lib, **over) == status
+
+
+def test_tree_grow_empty_batch_is_a_no_op(lib):
+    assert _grow(lib, B=0, z=0, tok=0, par=0, dep=0, val=0, ws=0, wsb=0) == 0
+
+
+def test_tree_grow_workspace_grows_with_the_batch(lib):
+    ws = sv.spec_verify_workspace_bytes
+    a = ws(sv.SPEC_MODE_TREE_GROW, 16, 8, 128256, sv.SPEC_DTYPE_BF16)
+    b = ws(sv.SPEC_MODE_TREE_GROW, 32, 8, 128256, sv.SPEC_DTYPE_BF16)
+    assert 0 < a < b
+    assert ws(sv.SPEC_MODE_TREE_GROW, 16, 17, 128256, sv.SPEC_DTYPE_BF16) == 0
+
+
+def _lm(lib, **over):
+    a = dict(h=FAKE, w=FAKE, tok=FAKE, B=2, k=3, d=64, V=1000, acc=FAKE, out=FAKE, ws=FAKE,
+             wsb=1 << 30, stream=None)
+    a.update(over)
+    return lib.spec_lm_head_verify_greedy(a["h"], a["w"], a["tok"], a["B"], a["k"], a["d"],
+                                          a["V"], a["acc"], a["out"], a["ws"], a["wsb"],
+                                          a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(B=-1), 1), (dict(k=-1), 1), (dict(d=4), 1), (dict(d=68), 1), (dict(V=0), 1),
+    (dict(h=0), 1), (dict(w=0), 1), (dict(acc=0), 1), (dict(out=0), 1), (dict(tok=0), 1),
+    (dict(h=FAKE + 8), 2), (dict(w=FAKE + 8), 2), (dict(out=MISALIGNED), 2),
+    (dict(ws=0), 3), (dict(wsb=16), 3),
+])
+def test_lm_head_rejects_bad_arguments(lib, over, status):
+    assert _lm(lib, **over) == status
+
+
+def test_lm_head_empty_batch_is_a_no_op(lib):
+    assert _lm(lib, B=0, h=0, w=0, tok=0, acc=0, out=0, ws=0, wsb=0) == 0
