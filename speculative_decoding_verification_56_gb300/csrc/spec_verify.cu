@@ -142,11 +142,11 @@ bool vec_ok(const void* p, int V, int dtype) {
 
 template <typename KernelT, typename ParamT>
 spec_status_t launch(KernelT kernel, int grid, size_t smem, const ParamT& prm, void* stream,
-                     bool pdl, int cluster = 1) {
+                     bool pdl, int cluster = 1, int threads = sv::kThreads) {
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(sv::kThreads, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[2];
@@ -699,7 +699,7 @@ spec_status_t spec_tree_grow(const void* draft_logits, int dtype, float temperat
   if (st != SPEC_OK) return st;
   return launch(sv::grow_tree_kernel, B,
                 sv::grow_tree_smem(L.nchunks, K, prm.rows_per_tree, nnodes), prm, stream,
-                true);
+                true, 1, sv::kGrowTreeThreads);
 }
 
 spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_flags, int clear,

@@ -544,9 +544,15 @@ __host__ __device__ inline size_t grow_stage_bytes(int nchunks, int K) {
 __device__ __forceinline__ void grow_cp4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
+// The tree kernel's block: 32 warps, so a tree's 41 draft rows (6 layers of
+// 8) are staged and merged in two batches and a 512-node sort keeps one
+// element per thread.
+constexpr int kGrowTreeThreads = 1024;
+constexpr int kGrowTreeWarps = kGrowTreeThreads / 32;
+
 __host__ __device__ inline int grow_nstage(int nchunks, int K) {
   const size_t fit = kGrowStageBudget / grow_stage_bytes(nchunks, K);
-  return (int)(fit < (size_t)kWarps ? fit : (size_t)kWarps);
+  return (int)(fit < (size_t)kGrowTreeWarps ? fit : (size_t)kGrowTreeWarps);
 }
 __host__ __device__ inline int grow_sort_n(int nnodes) {
   int P = 1;
@@ -578,14 +584,14 @@ constexpr size_t kGrowTreeSmem =
 // first M are kept and renumbered in creation order.  Launched
 // programmatically after the top-k grid and waits for it before reading the
 // records.
-__global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p) {
+__global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const GrowParams p) {
   extern __shared__ __align__(16) uint8_t grow_mem[];
   constexpr int kMaxKids = kGrowMaxK * kGrowMaxK;
   __shared__ double s_dval[kMaxKids];             // the layer's children: value
   __shared__ unsigned long long s_val[kMaxKids];  // ... its order key
   __shared__ int s_front[kGrowMaxK];              // frontier: node id
   __shared__ double s_fval[kGrowMaxK];            // ... and value
-  __shared__ int s_wtot[kWarps];
+  __shared__ int s_wtot[kGrowTreeWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.x;
   const int K = p.K;
@@ -617,7 +623,7 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
       const int nb = min(nstage, rows - q0);
       const GrowRec* rec0 = p.rec + ((size_t)b * rows + q0) * p.nchunks;
       // asynchronous 4-byte copies: every load of the batch is in flight at once
-      for (int i = threadIdx.x; i < nb * ncand; i += kThreads) {
+      for (int i = threadIdx.x; i < nb * ncand; i += kGrowTreeThreads) {
         const int w = i / ncand, k = i - w * ncand;
         const int c = k / K, r = k - c * K;
         const GrowRec& g = rec0[(size_t)w * p.nchunks + c];
@@ -625,7 +631,7 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
         grow_cp4(cv + k, &g.val[r]);
         grow_cp4(reinterpret_cast<int*>(cv + ncand) + k, &g.idx[r]);
       }
-      for (int i = threadIdx.x; i < nb * p.nchunks; i += kThreads) {
+      for (int i = threadIdx.x; i < nb * p.nchunks; i += kGrowTreeThreads) {
         const int w = i / p.nchunks, c = i - w * p.nchunks;
         const GrowRec& g = rec0[i];
         int* hp = reinterpret_cast<int*>(stage0 + (size_t)w * sb) + 2 * (size_t)ncand;
@@ -756,10 +762,10 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
     }
   }
   // 2. float64, a thread per row, then a thread per (row, rank)
-  for (int q = threadIdx.x; q < rows; q += kThreads)
+  for (int q = threadIdx.x; q < rows; q += kGrowTreeThreads)
     r_l2[q] = log2((double)r_hi[q] + (double)r_lo[q]);
   __syncthreads();
-  for (int t = threadIdx.x; t < rows * K; t += kThreads) {
+  for (int t = threadIdx.x; t < rows * K; t += kGrowTreeThreads) {
     const int q = t / K;
     r_lnq[t] = ((double)r_z[t] * (double)p.scale - (double)r_R[q] - r_l2[q]) * 0.6931471805599453;
   }
@@ -821,53 +827,54 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(grow_mem);  // [P]
   int* s_id = reinterpret_cast<int*>(s_key + P);                                // [P]
   int* s_new = s_id + P;                                                        // [nnodes]
-  for (int i = threadIdx.x; i < P; i += kThreads) {
+  for (int i = threadIdx.x; i < P; i += kGrowTreeThreads) {
     s_key[i] = grow_key(i < n ? nval[i + 1] : -INFINITY);
     s_id[i] = i < n ? i + 1 : 0x7FFFFFFF;
   }
-  for (int i = threadIdx.x; i < nnodes; i += kThreads) s_new[i] = 0;
+  for (int i = threadIdx.x; i < nnodes; i += kGrowTreeThreads) s_new[i] = 0;
   __syncthreads();
-  if (P <= kThreads) {
+  if (P <= kGrowTreeThreads) {
     // one element per thread, in registers: partners closer than 32 are in
     // the same warp (shuffles), farther ones are exchanged through shared
-    // memory.  "Before" = larger key, then smaller id; after the sort the
-    // thread i < M holds the i-th best.
+    // memory among the sorting warps only (named barrier 1 over the first
+    // `act` threads, a multiple of 32).  "Before" = larger key, then smaller
+    // id; after the sort the thread i < M holds the i-th best.
     const int i = threadIdx.x;
-    unsigned long long key = i < P ? s_key[i] : 0ull;
-    int id = i < P ? s_id[i] : 0x7FFFFFFF;
-    for (int k = 2; k <= P; k <<= 1)
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        unsigned long long okey;
-        int oid;
-        if (j < 32) {
-          okey = __shfl_xor_sync(0xffffffffu, key, j);
-          oid = __shfl_xor_sync(0xffffffffu, id, j);
-        } else {
-          __syncthreads();  // every read of the previous exchange is done
-          if (i < P) {
+    const int act = P < 32 ? 32 : P;
+    if (i < act) {
+      unsigned long long key = i < P ? s_key[i] : 0ull;
+      int id = i < P ? s_id[i] : 0x7FFFFFFF;
+      for (int k = 2; k <= P; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          unsigned long long okey;
+          int oid;
+          if (j < 32) {
+            okey = __shfl_xor_sync(0xffffffffu, key, j);
+            oid = __shfl_xor_sync(0xffffffffu, id, j);
+          } else {  // P >= 64 here, so act = P and every thread holds an element
+            asm volatile("bar.sync 1, %0;" ::"r"(act) : "memory");  // the last exchange is read
             s_key[i] = key;
             s_id[i] = id;
+            asm volatile("bar.sync 1, %0;" ::"r"(act) : "memory");
+            okey = s_key[i ^ j];
+            oid = s_id[i ^ j];
           }
-          __syncthreads();
-          okey = i < P ? s_key[i ^ j] : 0ull;
-          oid = i < P ? s_id[i ^ j] : 0x7FFFFFFF;
-        }
-        if (i < P) {
-          const bool other_before = okey > key || (okey == key && oid < id);
-          const bool keep_before = (i < (i ^ j)) == ((i & k) == 0);
-          if (other_before == keep_before) {
-            key = okey;
-            id = oid;
+          if (i < P) {
+            const bool other_before = okey > key || (okey == key && oid < id);
+            const bool keep_before = (i < (i ^ j)) == ((i & k) == 0);
+            if (other_before == keep_before) {
+              key = okey;
+              id = oid;
+            }
           }
         }
-      }
-    __syncthreads();
-    if (i < p.M && id >= 1 && id < nnodes) s_new[id] = 1;
+      if (i < p.M && id >= 1 && id < nnodes) s_new[id] = 1;
+    }
   } else {
     // several elements per thread: the same network through shared memory
     for (int k = 2; k <= P; k <<= 1)
       for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = threadIdx.x; i < P; i += kThreads) {
+        for (int i = threadIdx.x; i < P; i += kGrowTreeThreads) {
           const int l = i ^ j;
           if (l > i) {
             const bool up = (i & k) == 0;
@@ -884,7 +891,7 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
         }
         __syncthreads();
       }
-    for (int i = threadIdx.x; i < p.M; i += kThreads)
+    for (int i = threadIdx.x; i < p.M; i += kGrowTreeThreads)
       if (s_id[i] >= 1 && s_id[i] < nnodes) s_new[s_id[i]] = 1;
   }
   __syncthreads();
@@ -892,7 +899,7 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
     // renumber in creation order (parents come first): thread t owns the
     // contiguous ids [t per, (t + 1) per) of 1..nnodes-1; an exclusive scan
     // of the kept counts gives each range's first new id
-    const int per = (n + kThreads - 1) / kThreads;
+    const int per = (n + kGrowTreeThreads - 1) / kGrowTreeThreads;
     const int v0 = 1 + (int)threadIdx.x * per, v1 = min(nnodes, v0 + per);
     int cnt = 0;
     for (int v = v0; v < v1; ++v) cnt += s_new[v];
@@ -916,7 +923,7 @@ __global__ void __launch_bounds__(kThreads) grow_tree_kernel(const GrowParams p)
     p.depth[ob] = 0;
     p.values[ob] = 0.0f;
   }
-  for (int v = 1 + threadIdx.x; v < nnodes; v += kThreads) {
+  for (int v = 1 + threadIdx.x; v < nnodes; v += kGrowTreeThreads) {
     const int o = s_new[v];
     if (o < 1) continue;
     const int par = npar[v];
