@@ -70,6 +70,31 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def replica_seed(seed, rank):
+    """Each rank verifies its own batches (sequences are independent): the
+    workload of rank r is drawn from seed + 1000 r."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(x, device):
+    """The largest of every rank's x (the step time of the slowest rank); x
+    itself on one rank.  `device` holds the reduction tensor: a CUDA device
+    under NCCL, the CPU under gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, steps, units_per_step, total_ms):
+    """Whole-job units/s: every rank ran `steps` steps of `units_per_step`
+    units; the job takes the slowest rank's `total_ms`."""
+    return world * steps * units_per_step / (total_ms / 1e3)
+
+
 def workload(seed):
     from speculative_decoding_verification_56_gb300 import synth
     samp = synth.zipf128k(seed=seed)
@@ -204,7 +229,7 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    samp, greedy, tree = workload(args.seed + 1000 * rank)
+    samp, greedy, tree = workload(replica_seed(args.seed, rank))
     pos_step = positions(samp, greedy, tree)
     eb = samp.elem_bytes
     B, k, V = samp.B, samp.k, samp.V
@@ -322,13 +347,9 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop(t_wall0, t_wall1) if clocks else None
     next_rows = measure_next_rows(dev, stream, tree, K) \
         if rank == 0 and not args.skip_next_rows else None
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_step = total_ms / K
-    value = world * K * pos_step / (total_ms / 1e3)
+    value = job_rate(world, K, pos_step, total_ms)
 
     # ---- e2e through the public API: pinned host in, results back each step ----
     E = args.e2e_steps
@@ -364,8 +385,8 @@ def run_ours(args, rank, world, local_rank):
                 e2e_step(sets[0])
             e1.record(stream)
             stream.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        e2e = {"value": round(world * E * pos_step / (e2e_ms / 1e3), 1), "unit": UNIT,
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e = {"value": round(job_rate(world, E, pos_step, e2e_ms), 1), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": E}
 
     # ---- roofline of the dominant kernel ----
