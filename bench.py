@@ -231,6 +231,7 @@ def run_ours(args, rank, world, local_rank):
 
     samp, greedy, tree = workload(replica_seed(args.seed, rank))
     pos_step = positions(samp, greedy, tree)
+    seqs_step = samp.B + greedy.B + tree.B  # sequences and trees verified per step
     eb = samp.elem_bytes
     B, k, V = samp.B, samp.k, samp.V
     Bt, N, Vt = tree.B, tree.N, tree.V
@@ -327,6 +328,17 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     total_ms = ev0.elapsed_time(ev1)
 
+    # ---- spread of single steps: each of up to 200 steps between its own
+    # pair of events (a step's calls stay chained inside it) ----
+    NS = min(200, K)
+    sev = [torch.cuda.Event(enable_timing=True) for _ in range(NS + 1)]
+    sev[0].record(stream)
+    for i in range(NS):
+        step(i)
+        sev[i + 1].record(stream)
+    stream.synchronize()
+    step_samples = np.array([sev[i].elapsed_time(sev[i + 1]) for i in range(NS)])
+
     # ---- per-call durations: each call alone, K times, same rotation ----
     # (events between calls chained by programmatic dependent launch distort
     # the chain, so each call type gets its own timed loop)
@@ -422,6 +434,11 @@ def run_ours(args, rank, world, local_rank):
                          "246 MB tree read (> 129 MB L2)",
                    "parallelism": f"replicas x{world} (sequences shard, no collective)"},
         "hbm_gbs": round(step_gbs, 1), "hbm_frac_of_peak": round(step_gbs / peak, 4),
+        "sequences_per_s": round(job_rate(world, K, seqs_step, total_ms), 1),
+        "step_ms_percentiles": {"p10": round(float(np.percentile(step_samples, 10)), 5),
+                                "p50": round(float(np.percentile(step_samples, 50)), 5),
+                                "p90": round(float(np.percentile(step_samples, 90)), 5),
+                                "steps": int(NS), "timed": "one event pair per step"},
         "roofline": {"bound": "hbm", "kernel": dom_name, "timed": "whole call, its own loop of K calls",
                      "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
