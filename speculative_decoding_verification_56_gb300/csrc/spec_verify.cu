@@ -606,8 +606,9 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
           cudaSuccess ||
       max_clusters < 1)
     return SPEC_ERR_CUDA;
-  const int nclusters = std::max(1, std::min(std::min(max_clusters, (ntiles + 1) / 2),
-                                             kLmMaxGrid / sv::kLmCluster));
+  const int nclusters =
+      std::max(1, std::min(std::min(max_clusters, (ntiles + sv::kLmCluster - 1) / sv::kLmCluster),
+                           kLmMaxGrid / sv::kLmCluster));
   const int gx = nclusters * sv::kLmCluster;
   lp.nclusters = nclusters;
   cfg.gridDim = dim3((unsigned)gx, (unsigned)gy, 1);
