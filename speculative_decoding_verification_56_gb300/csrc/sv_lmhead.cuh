@@ -313,7 +313,17 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     }
     unsigned acc_phase = 0;
     for (int j = 0; j < nsteps; ++j) {
-      if (!mbar_wait_bounded(&acc_full, acc_phase)) {
+      // every epilogue thread takes the same decision, so none is left at a
+      // named barrier the others no longer reach
+      const unsigned ok = mbar_wait_bounded(&acc_full, acc_phase) ? 1u : 0u;
+      unsigned all_ok;
+      asm volatile(
+          "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n bar.red.and.pred b, 1, 128, a;\n"
+          " selp.u32 %0, 1, 0, b;\n}"
+          : "=r"(all_ok)
+          : "r"(ok)
+          : "memory");
+      if (!all_ok) {
         s_abort = 1;
         set_flag(p.flags, kFlagTimeout);
         break;

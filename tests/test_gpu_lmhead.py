@@ -50,8 +50,9 @@ def _rows_argmax(H, W):
 
 @pytest.mark.parametrize("B,k,d,V,seed", [
     (1, 0, 64, 1, 0), (2, 3, 64, 300, 1), (3, 4, 128, 1000, 2), (4, 1, 72, 129, 3),
-    (2, 2, 200, 5000, 4), (100, 4, 64, 700, 5),        # 500 rows: two row groups
-    (1, 0, 8, 257, 6),
+    (2, 2, 200, 5000, 4), (100, 4, 64, 700, 5),        # 500 rows: two halves of 256
+    (1, 0, 8, 257, 6), (130, 4, 64, 700, 7),           # 650 rows: two row groups
+    (41, 0, 96, 20000, 8),                             # 41 rows: halves of 32, one partly empty
 ])
 def test_lm_head_rows_and_chains(B, k, d, V, seed):
     H, W, tok, _ = synth.make_lm_head_case(B=B, k=k, d=d, V=V, seed=seed)
