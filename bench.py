@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--skip-next-rows", action="store_true",
                     help="leave out the kernels around the draft tree (next_rows)")
+    ap.add_argument("--skip-large", action="store_true",
+                    help="leave out the large-batch measurement (at_scale)")
     return ap.parse_args()
 
 
@@ -359,6 +361,8 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop(t_wall0, t_wall1) if clocks else None
     next_rows = measure_next_rows(dev, stream, tree, K) \
         if rank == 0 and not args.skip_next_rows else None
+    at_scale = measure_at_scale(dev, stream, min(K, 400), measured_peak()[0]) \
+        if rank == 0 and not args.skip_large else None
     total_ms = max_over_ranks(total_ms, dev)
     ms_step = total_ms / K
     value = job_rate(world, K, pos_step, total_ms)
@@ -450,6 +454,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "clocks": clk,
         "next_rows": next_rows,
+        "at_scale": at_scale,
     }
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         result["cpu_baseline"] = cpu_baseline(samp, greedy, tree, args.cpu_seconds)
@@ -458,6 +463,67 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def measure_at_scale(dev, stream, K, peak):
+    """The sampling and greedy calls on the large-batch workload (B=256
+    sequences of k=7 drafts over V=151936, bf16, T=0.7; 1.17 GB of target and
+    draft rows per sampling call, far above L2): each call type in its own
+    loop of K calls, inputs resident in HBM."""
+    import torch
+    import speculative_decoding_verification_56_gb300 as sv
+    from speculative_decoding_verification_56_gb300 import synth
+    c = synth.zipf152k(seed=0)
+    g = synth.greedy_variant(c, 0.7)
+    B, k, V = c.B, c.k, c.V
+    t = sv.to_device_logits(c.target, c.dtype, dev)
+    d = sv.to_device_logits(c.draft, c.dtype, dev)
+    tok = torch.from_numpy(c.tokens).to(dev)
+    gtok = torch.from_numpy(g.tokens).to(dev)
+    ua = torch.from_numpy(c.u_accept).to(dev)
+    us = torch.from_numpy(c.u_sample).to(dev)
+    del c, g
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    n, otok = torch.empty(B, **i32), torch.empty(B, k + 1, **i32)
+    p, q, R = torch.empty(B, k, **f32), torch.empty(B, k, **f32), torch.empty(B, **f32)
+    ws = sv.alloc_workspace(sv.SPEC_MODE_SAMPLE, B, k, V, sv.SPEC_DTYPE_BF16, dev)
+    wg = sv.alloc_workspace(sv.SPEC_MODE_GREEDY, B, k, V, sv.SPEC_DTYPE_BF16, dev)
+
+    def call_sample():
+        sv.spec_verify_sample(t, d, tok, ua, us, 0.7, n, otok, p, q, R, ws, stream)
+
+    def call_greedy():
+        sv.spec_verify_greedy(t, gtok, n, otok, wg, stream)
+
+    out = {"workload": f"sample and greedy B={B} k={k} V={V} bf16 T=0.7 (Zipf-biased Gaussian "
+                       "target, draft = target + N(0, 1.5^2))",
+           "timed": f"each call type in its own loop of {K} calls"}
+    with torch.cuda.stream(stream):
+        call_sample()
+    stream.synchronize()
+    pass2 = int(np.where(n.cpu().numpy() < k, 2, 1).sum())
+    for name, fn, byts, pos in (
+            ("sample", call_sample, (B * (2 * k + 1) + pass2) * V * 2, B * k),
+            ("greedy", call_greedy, B * (k + 1) * V * 2, B * k)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(K):
+                fn()
+            e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1) / K
+        gbs = byts / (ms / 1e3) / 1e9
+        out[name] = {"us_per_call": round(ms * 1e3, 2), "algorithmic_bytes": int(byts),
+                     "gb_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                     "positions_per_s": round(pos / (ms / 1e3), 1)}
+    del t, d, ws, wg
+    torch.cuda.empty_cache()
+    return out
 
 
 def _time_loop(fn, stream, K, per_graph=20):
