@@ -36,6 +36,12 @@
  *     every access, treat the item as not matching, and set a bit of the
  *     workspace's flag word (spec_verify_read_flags).
  *   - B = 0 is a no-op that returns SPEC_OK.
+ *   - The verification calls' kernels are programmatic dependent launches:
+ *     the first kernel of a call waits for the kernel before it in the
+ *     stream to finish (and its writes to be visible) before it reads or
+ *     writes memory, and the last kernel of a call lets the next kernel in
+ *     the stream be scheduled early.  Consecutive calls on one stream thus
+ *     overlap their launches, never their memory accesses.
  */
 #ifndef SPEC_VERIFY_H_
 #define SPEC_VERIFY_H_

@@ -276,7 +276,7 @@ spec_status_t run_sample(sv::SampleParams prm, int rows, bool vec, void* stream)
     int grid = 0;
     st = persistent_grid<sv::stream_stats_kernel<E>>(prm.items, &grid);
     if (st != SPEC_OK) return st;
-    st = launch(sv::stream_stats_kernel<E>, grid, kStreamSmem, prm, stream, false);
+    st = launch(sv::stream_stats_kernel<E>, grid, kStreamSmem, prm, stream, true);
   } else {
     st = launch(sv::chunk_stats_kernel<E, false>, prm.items, 0, prm, stream, false);
   }
@@ -291,7 +291,7 @@ spec_status_t run_argmax(sv::ArgmaxParams prm, int rows, bool vec, void* stream)
     int grid = 0;
     spec_status_t st = persistent_grid<sv::stream_argmax_kernel<E>>(prm.items, &grid);
     if (st != SPEC_OK) return st;
-    st = launch(sv::stream_argmax_kernel<E>, grid, kStreamSmem, prm, stream, false);
+    st = launch(sv::stream_argmax_kernel<E>, grid, kStreamSmem, prm, stream, true);
     if (st != SPEC_OK) return st;
   } else {
     const spec_status_t st =

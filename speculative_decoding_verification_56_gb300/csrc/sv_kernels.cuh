@@ -668,6 +668,9 @@ __device__ void resolve_sequence(const ArgmaxParams& p, int b, int32_t* s_par, i
 __global__ void __launch_bounds__(kThreads) argmax_resolve_kernel(const ArgmaxParams p) {
   __shared__ int32_t s_par[kTreeSmemNodes], s_tok[kTreeSmemNodes], s_g[kTreeSmemNodes];
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next call's streaming kernel may become resident now; it waits for
+  // this grid before touching memory
+  asm volatile("griddepcontrol.launch_dependents;");
   resolve_sequence<4>(p, blockIdx.x, s_par, s_tok, s_g);
 }
 
@@ -764,6 +767,9 @@ __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleP
   __shared__ SegSlots ss;
   using S = typename E::storage;
 
+  // launched as a programmatic dependent of whatever kernel precedes it in
+  // the stream: nothing is read or written before that grid has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int i0, i1;
   item_range(p.items, i0, i1);
   // the dependent draw kernel may begin launching; it waits for this grid
@@ -833,6 +839,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const Argmax
   __shared__ SegSlots ss;
   using S = typename E::storage;
 
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in stream_stats_kernel
   int i0, i1;
   item_range(p.items, i0, i1);
   asm volatile("griddepcontrol.launch_dependents;");
@@ -1259,6 +1266,7 @@ __global__ void __launch_bounds__(kThreads) draw_resolve_kernel(const SamplePara
   __shared__ FSum s_target, s_base;
   __shared__ int s_c, s_fallback;
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");  // see argmax_resolve_kernel
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.x;
   const int C = p.nchunks;
@@ -1406,6 +1414,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
     mbar_init_fence();
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");  // see argmax_resolve_kernel
   __syncthreads();
 
   // 1. merge every row of the sequence

@@ -293,6 +293,42 @@ def test_workspace_reuse_across_shapes_and_modes():
     sample_parity(c2, ws=big, allow_flags=0)
 
 
+def test_inputs_written_by_the_kernel_just_before():
+    # The first kernel of every call is a programmatic dependent launch: it
+    # must see everything the preceding kernel in the stream wrote.  Here a
+    # torch kernel writes the logits (and an extra one the draft tokens) right
+    # before each call, with no synchronisation in between.
+    c = synth.zipf128k(seed=4)
+    o = oracle_sample(c)
+    x = dev_chain(c)
+    t_src, d_src, tok_src = x["t"], x["d"], x["tok"]
+    t = torch.zeros_like(t_src)
+    d = torch.zeros_like(d_src)
+    tok = torch.zeros_like(tok_src)
+    ws = sv.alloc_workspace(sv.SPEC_MODE_SAMPLE, c.B, c.k, c.V, sv.SPEC_DTYPE_BF16)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        d.copy_(d_src)
+        tok.copy_(tok_src)
+        t.zero_()
+        torch.add(t_src, 0, out=t)             # the kernel right before the call
+        out = sv.verify_sample(t, d, tok, x["ua"], x["us"], c.temperature, workspace=ws)
+        g = {k: v.cpu().numpy() for k, v in out.items()}
+        ph.compare_sample(g, o, V=c.V)
+        t.zero_()
+        d.zero_()
+        tok.zero_()
+    cg = synth.greedy_variant(c, 0.7)
+    og = oracle.verify_greedy(cg.target, cg.tokens, dtype=cg.dtype)
+    gt = torch.from_numpy(cg.tokens).cuda()
+    for _ in range(2):
+        t.zero_()
+        torch.add(t_src, 0, out=t)
+        out = sv.verify_greedy(t, gt, workspace=ws)
+        ph.compare_exact({k: v.cpu().numpy() for k, v in out.items()}, og,
+                         ["accepted_len", "out_tokens"])
+
+
 def test_deterministic_and_side_stream():
     c = synth.make_chain_case(B=16, k=4, V=50000, dtype="bf16", seed=6)
     a = gpu_sample(c)
