@@ -11,7 +11,8 @@ step) and the achieved HBM bandwidth on the logits the method must read.
 Inputs are generated once on the host (seeded) and copied to 4 device sets used
 in rotation; every tree call reads 246 MB (> the 129 MB L2) between two uses of
 any set, so every read comes from HBM.  `value` is timed with CUDA events on the
-launching stream with inputs resident in HBM; `e2e` repeats the step through the
+launching stream with inputs resident in HBM, the steps replayed from CUDA graphs
+(so that Python does not pace the launches); `e2e` repeats the step through the
 same public API with inputs copied from pinned host memory and results copied
 back inside the timed region.
 
@@ -306,8 +307,25 @@ def run_ours(args, rank, world, local_rank):
         step(i)
     stream.synchronize()
 
-    # ---- headline: K whole steps, events only around the timed region ----
+    # ---- headline: K whole steps replayed from CUDA graphs, events only
+    # around the timed region.  One graph holds one rotation period of the
+    # input sets (NSETS steps), so replays continue the rotation; a second
+    # graph holds the K % NSETS steps left over.  Python and ctypes would
+    # otherwise pace the launches: the host needs about as long to enqueue a
+    # step's three calls as the GPU needs to run them. ----
     K = args.steps
+    with torch.cuda.stream(stream):
+        launches0 = sv.spec_verify_launch_count()
+        step(0)
+        launches_per_step = sv.spec_verify_launch_count() - launches0
+    stream.synchronize()
+    g_main = capture_graph(lambda: [step(i) for i in range(NSETS)], stream)
+    g_tail = capture_graph(lambda: [step(i) for i in range(K % NSETS)], stream) \
+        if K % NSETS else None
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g_main.replay()
+    stream.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank) if rank == 0 else None
@@ -317,46 +335,55 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    launches0 = sv.spec_verify_launch_count()
     t_wall0 = time.time()
-    ev0.record(stream)
-    for i in range(K):
-        step(i)
-    ev1.record(stream)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(K // NSETS):
+            g_main.replay()
+        if g_tail is not None:
+            g_tail.replay()
+        ev1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
-    launches = sv.spec_verify_launch_count() - launches0
+    launches = int(round(launches_per_step * K))
     if world > 1:
         torch.distributed.barrier()
     total_ms = ev0.elapsed_time(ev1)
 
-    # ---- spread of single steps: each of up to 200 steps between its own
-    # pair of events (a step's calls stay chained inside it) ----
+    # ---- spread of single steps: up to 200 steps, each a replay of a
+    # one-step graph between its own pair of events (a step's calls stay
+    # chained inside it) ----
     NS = min(200, K)
+    g_one = [capture_graph(lambda i=i: step(i), stream) for i in range(NSETS)]
     sev = [torch.cuda.Event(enable_timing=True) for _ in range(NS + 1)]
-    sev[0].record(stream)
-    for i in range(NS):
-        step(i)
-        sev[i + 1].record(stream)
+    with torch.cuda.stream(stream):
+        sev[0].record(stream)
+        for i in range(NS):
+            g_one[i % NSETS].replay()
+            sev[i + 1].record(stream)
     stream.synchronize()
     step_samples = np.array([sev[i].elapsed_time(sev[i + 1]) for i in range(NS)])
 
-    # ---- per-call durations: each call alone, K times, same rotation ----
-    # (events between calls chained by programmatic dependent launch distort
-    # the chain, so each call type gets its own timed loop)
+    # ---- per-call durations: each call alone, K times, same rotation, from
+    # CUDA graphs of NSETS calls (events between calls chained by programmatic
+    # dependent launch distort the chain, so each call type gets its own
+    # timed loop) ----
     mean_ms = []
     for name in ("sample", "greedy", "tree"):
         fn = calls[name]
-        for i in range(3):
-            fn(sets[i % NSETS])
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(K):
-            fn(sets[i % NSETS])
-        e1.record(stream)
+        g_call = capture_graph(lambda: [fn(sets[i]) for i in range(NSETS)], stream)
+        reps = max(1, K // NSETS)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_call.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g_call.replay()
+            e1.record(stream)
         stream.synchronize()
-        mean_ms.append(e0.elapsed_time(e1) / K)
+        mean_ms.append(e0.elapsed_time(e1) / (reps * NSETS))
     mean_ms = np.array(mean_ms)
     clk = clocks.stop(t_wall0, t_wall1) if clocks else None
     next_rows = measure_next_rows(dev, stream, tree, K) \
@@ -442,8 +469,8 @@ def run_ours(args, rank, world, local_rank):
         "step_ms_percentiles": {"p10": round(float(np.percentile(step_samples, 10)), 5),
                                 "p50": round(float(np.percentile(step_samples, 50)), 5),
                                 "p90": round(float(np.percentile(step_samples, 90)), 5),
-                                "steps": int(NS), "timed": "one event pair per step"},
-        "roofline": {"bound": "hbm", "kernel": dom_name, "timed": "whole call, its own loop of K calls",
+                                "steps": int(NS), "timed": "one event pair per step (a one-step graph replay)"},
+        "roofline": {"bound": "hbm", "kernel": dom_name, "timed": "whole call, its own loop of K calls (CUDA-graph replay)",
                      "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
@@ -524,6 +551,19 @@ def measure_at_scale(dev, stream, K, peak):
     del t, d, ws, wg
     torch.cuda.empty_cache()
     return out
+
+
+def capture_graph(body, stream):
+    """A CUDA graph of whatever `body` enqueues on `stream` (after one eager
+    run of it, so every lazily initialised resource exists)."""
+    import torch
+    with torch.cuda.stream(stream):
+        body()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        body()
+    return g
 
 
 def _time_loop(fn, stream, K, per_graph=20):

@@ -36,7 +36,7 @@
  *     every access, treat the item as not matching, and set a bit of the
  *     workspace's flag word (spec_verify_read_flags).
  *   - B = 0 is a no-op that returns SPEC_OK.
- *   - The verification calls' kernels are programmatic dependent launches:
+ *   - Every call's kernels are programmatic dependent launches:
  *     the first kernel of a call waits for the kernel before it in the
  *     stream to finish (and its writes to be visible) before it reads or
  *     writes memory, and the last kernel of a call lets the next kernel in

@@ -171,6 +171,21 @@ spec_status_t launch(KernelT kernel, int grid, size_t smem, const ParamT& prm, v
   return SPEC_OK;
 }
 
+// Launch configuration of a programmatic dependent launch (the kernel waits
+// for the preceding kernel in the stream with griddepcontrol.wait).
+void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, dim3 grid, dim3 block,
+                size_t smem, void* stream) {
+  std::memset(cfg, 0, sizeof *cfg);
+  cfg->gridDim = grid;
+  cfg->blockDim = block;
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = (cudaStream_t)stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
 // Per-device launch shape of a persistent streaming kernel: the shared-memory
 // opt-in is set once per device, the grid is SMs x resident CTAs per SM.
 constexpr int kMaxDevices = 64;
@@ -485,9 +500,12 @@ spec_status_t spec_tree_attention_mask(const int32_t* parents, int B, int N, uin
   const long long threads = (long long)B * N * W;
   const long long blocks = (threads + sv::kMaskThreads - 1) / sv::kMaskThreads;
   if (blocks > 0x7FFFFFFFLL) return SPEC_ERR_INVALID_ARG;
-  sv::tree_mask_kernel<<<(unsigned)blocks, sv::kMaskThreads, 0, (cudaStream_t)stream>>>(
-      parents, B, N, W, mask, depth, reinterpret_cast<unsigned*>(workspace));
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(&cfg, attr, dim3((unsigned)blocks), dim3(sv::kMaskThreads), 0, stream);
+  if (cudaLaunchKernelEx(&cfg, sv::tree_mask_kernel, parents, B, N, W, mask, depth,
+                         reinterpret_cast<unsigned*>(workspace)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return SPEC_OK;
 }
@@ -530,9 +548,11 @@ spec_status_t spec_kv_commit_path(void* cache, int B, int planes, long long plan
   const int moves = std::max(1, std::min(max_depth, sv::kKvMaxMoves));
   prm.slice_bytes = std::min(entry_bytes, kStageBytes / moves / 16 * 16);
   const size_t smem = (size_t)prm.slice_bytes * moves;
-  sv::kv_commit_kernel<<<dim3((unsigned)B, (unsigned)planes), sv::kKvThreads, smem,
-                         (cudaStream_t)stream>>>(prm);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(&cfg, attr, dim3((unsigned)B, (unsigned)planes), dim3(sv::kKvThreads), smem,
+             stream);
+  if (cudaLaunchKernelEx(&cfg, sv::kv_commit_kernel, prm) != cudaSuccess) return SPEC_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return SPEC_OK;
 }
@@ -591,11 +611,13 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   lp.flags = reinterpret_cast<unsigned*>(ws);
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = sv::kLmCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(sv::kLmThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = (cudaStream_t)stream;
@@ -612,6 +634,7 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   const int gx = nclusters * sv::kLmCluster;
   lp.nclusters = nclusters;
   cfg.gridDim = dim3((unsigned)gx, (unsigned)gy, 1);
+  cfg.numAttrs = 2;  // the cluster shape (queried above) and the dependent launch
   if (cudaLaunchKernelEx(&cfg, sv::lmhead_argmax_kernel, map_h, map_w, lp) != cudaSuccess)
     return SPEC_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -683,16 +706,16 @@ spec_status_t spec_tree_grow(const void* draft_logits, int dtype, float temperat
     if (dtype == SPEC_DTYPE_BF16) {
       st = persistent_grid<sv::grow_topk_stream_kernel<sv::BF16>>(prm.items, &grid);
       if (st == SPEC_OK)
-        st = launch(sv::grow_topk_stream_kernel<sv::BF16>, grid, kStreamSmem, prm, stream, false);
+        st = launch(sv::grow_topk_stream_kernel<sv::BF16>, grid, kStreamSmem, prm, stream, true);
     } else {
       st = persistent_grid<sv::grow_topk_stream_kernel<sv::F32>>(prm.items, &grid);
       if (st == SPEC_OK)
-        st = launch(sv::grow_topk_stream_kernel<sv::F32>, grid, kStreamSmem, prm, stream, false);
+        st = launch(sv::grow_topk_stream_kernel<sv::F32>, grid, kStreamSmem, prm, stream, true);
     }
   } else if (dtype == SPEC_DTYPE_BF16) {
-    st = launch(sv::grow_topk_kernel<sv::BF16, false>, prm.items, 0, prm, stream, false);
+    st = launch(sv::grow_topk_kernel<sv::BF16, false>, prm.items, 0, prm, stream, true);
   } else {
-    st = launch(sv::grow_topk_kernel<sv::F32, false>, prm.items, 0, prm, stream, false);
+    st = launch(sv::grow_topk_kernel<sv::F32, false>, prm.items, 0, prm, stream, true);
   }
   if (st != SPEC_OK) return st;
   // the node bookkeeping of every layer and the final ranking, one CTA per tree

@@ -459,6 +459,9 @@ template <typename E, bool kVec>
 __global__ void __launch_bounds__(kThreads, 2) grow_topk_kernel(const GrowParams p) {
   using St = typename E::storage;
   __shared__ GrowSegSmem sh;
+  // a programmatic dependent of the kernel before it in the stream: nothing
+  // is read or written before that grid has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int item = blockIdx.x;
   const int rowi = item / p.nchunks, c = item - rowi * p.nchunks;
@@ -482,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_stream_kernel(const Gro
   __shared__ Ring ring;
   __shared__ GrowSegSmem sh;
   using St = typename E::storage;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in grow_topk_kernel
   int i0, i1;
   item_range(p.items, i0, i1);
   // the tree kernel may begin launching; it waits for this grid
@@ -612,6 +616,8 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
   float* r_hi = reinterpret_cast<float*>(r_R + rows);
   float* r_lo = r_hi + rows;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the top-k records
+  // the next call's first kernel may become resident; it waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;");
 
   // 1. every row of the tree: normaliser and K best tokens (float
   //    arithmetic), nstage rows at a time: the CTA stages the rows' chunk

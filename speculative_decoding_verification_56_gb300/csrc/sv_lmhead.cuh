@@ -225,6 +225,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   cluster_sync_all();  // peers' barriers are initialised before any multicast
   tmem_fence_after();
   const uint32_t tmem_base = tmem_base_holder;
+  // a programmatic dependent of the kernel before it in the stream: the set-up
+  // above overlaps that kernel's end; no global memory is touched before it
+  // has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------

@@ -33,6 +33,10 @@ __global__ void __launch_bounds__(kMaskThreads) tree_mask_kernel(const int32_t* 
                                                                  uint32_t* __restrict__ mask,
                                                                  int32_t* __restrict__ depth,
                                                                  unsigned* flags) {
+  // a programmatic dependent of the kernel before it in the stream: nothing
+  // is read or written before that grid has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const long long t = (long long)blockIdx.x * kMaskThreads + threadIdx.x;
   const long long per_tree = (long long)N * W;
   if (t >= per_tree * B) return;
@@ -89,6 +93,8 @@ __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(const KvCommitPar
   extern __shared__ __align__(128) uint8_t kv_stage[];
   __shared__ int s_src[kKvMaxMoves], s_dst[kKvMaxMoves];
   __shared__ int s_ok, s_m;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in tree_mask_kernel
+  asm volatile("griddepcontrol.launch_dependents;");
   const int b = blockIdx.x, plane = blockIdx.y;
   const int base = p.base_len[b], d = p.accepted_len[b];
   const int32_t* path = p.path_nodes + (size_t)b * (p.max_depth + 1);
