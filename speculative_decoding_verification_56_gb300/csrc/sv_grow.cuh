@@ -553,6 +553,7 @@ __device__ __forceinline__ void grow_cp4(void* dst, const void* src) {
 // element per thread.
 constexpr int kGrowTreeThreads = 1024;
 constexpr int kGrowTreeWarps = kGrowTreeThreads / 32;
+constexpr int kGrowLayerThreads = 128;  // warps that run the frontier layers
 
 __host__ __device__ inline int grow_nstage(int nchunks, int K) {
   const size_t fit = kGrowStageBudget / grow_stage_bytes(nchunks, K);
@@ -563,12 +564,13 @@ __host__ __device__ inline int grow_sort_n(int nnodes) {
   while (P < nnodes - 1) P <<= 1;
   return P;
 }
+// The rows' results, then one area used first for staging the rows' chunk
+// records and then, once every row is reduced, for the final sort.
 __host__ __device__ inline size_t grow_tree_smem(int nchunks, int K, int rows, int nnodes) {
-  const size_t work = grow_row_bytes(rows, K) +
-                      (size_t)grow_nstage(nchunks, K) * grow_stage_bytes(nchunks, K);
+  const size_t stage = (size_t)grow_nstage(nchunks, K) * grow_stage_bytes(nchunks, K);
   const size_t sort = (size_t)grow_sort_n(nnodes) * (sizeof(unsigned long long) + sizeof(int)) +
                       (size_t)nnodes * sizeof(int);
-  return work > sort ? work : sort;
+  return grow_row_bytes(rows, K) + (stage > sort ? stage : sort);
 }
 constexpr size_t kGrowTreeSmem =
     ((size_t)kGrowMaxRows * kGrowMaxK * 16 + (size_t)kGrowMaxRows * 20 + 15) / 16 * 16 +
@@ -581,8 +583,8 @@ constexpr size_t kGrowTreeSmem =
 // chunk normalisers and picks the K best tokens from the chunk lists (each
 // sorted best first) by a threshold and a shuffle ranking; then
 // a thread per row takes log2 of the row sum and a thread per (row, rank)
-// its ln q = (z s - R - log2 S) ln 2, in float64.  The layers are then one
-// warp's work: a child's value is its parent's plus the row's ln q, and the
+// its ln q = (z s - R - log2 S) ln 2, in float64.  The layers then run on
+// four warps: a child's value is its parent's plus the row's ln q, and the
 // next frontier is the K children ranked best among the layer's children.
 // Finally every non-root node is sorted by (value desc, creation asc), the
 // first M are kept and renumbered in creation order.  Launched
@@ -777,10 +779,22 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
   }
   __syncthreads();
 
-  // 3. the layers, one warp: children values, then the next frontier by K
-  //    rounds of a head merge over the slots' child lists
-  if (warp == 0) {
-    if (lane == 0) {  // the root
+  // the sort's arrays, in the staging area (free now): the layers write each
+  // child's key and id as they create it, the other warps the padding
+  const int n = nnodes - 1;  // non-root nodes, ids 1..nnodes-1
+  const int P = grow_sort_n(nnodes);
+  unsigned long long* s_key =
+      reinterpret_cast<unsigned long long*>(grow_mem + grow_row_bytes(rows, K));  // [P]
+  int* s_id = reinterpret_cast<int*>(s_key + P);                                  // [P]
+  int* s_new = s_id + P;                                                          // [nnodes]
+
+  // 3. the layers, on warps 0-3 (named barrier 2 over their 128 threads):
+  //    the children's values, then the next frontier, the K children of best
+  //    rank; a child's rank (the children before it) is counted by two
+  //    threads over half of the layer's children each
+  if (threadIdx.x < kGrowLayerThreads) {
+    const int lt = threadIdx.x;
+    if (lt == 0) {  // the root
       nval[0] = 0.0;
       npar[0] = -1;
       ntok[0] = -1;
@@ -788,13 +802,13 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
       s_front[0] = 0;
       s_fval[0] = 0.0;
     }
-    __syncwarp();
+    asm volatile("bar.sync 2, %0;" ::"n"(kGrowLayerThreads) : "memory");
     for (int layer = 0; layer < p.D; ++layer) {
       const int nfront = layer == 0 ? 1 : K;
       const int base = layer == 0 ? 1 : 1 + K + (layer - 1) * K * K;
       const int q0 = layer == 0 ? 0 : 1 + (layer - 1) * K;  // the layer's first row
       const int nc = nfront * K;
-      for (int t = lane; t < nc; t += 32) {
+      for (int t = lt; t < nc; t += kGrowLayerThreads) {
         const int slot = t / K;
         const double val = s_fval[slot] + r_lnq[(size_t)q0 * K + t];
         const int id = base + t;
@@ -803,42 +817,49 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
         ntok[id] = r_tok[(size_t)q0 * K + t];
         ndep[id] = layer + 1;
         s_dval[t] = val;
-        s_val[t] = grow_key(val);
+        const unsigned long long key = grow_key(val);
+        s_val[t] = key;
+        s_key[id - 1] = key;
+        s_id[id - 1] = id;
       }
-      __syncwarp();
+      asm volatile("bar.sync 2, %0;" ::"n"(kGrowLayerThreads) : "memory");
       if (layer + 1 < p.D) {
-        // a child's rank = the children before it (independent loads)
-        for (int t = lane; t < nc; t += 32) {
-          const unsigned long long v = s_val[t];
+        const int half = nc >> 1;
+        const int u0 = (lt & 1) ? half : 0, u1 = (lt & 1) ? nc : half;
+        // every thread runs the same trips: the pair's shuffle is warp-wide
+        for (int c0 = 0; c0 < nc; c0 += kGrowLayerThreads / 2) {
+          const int c = c0 + (lt >> 1);
+          const bool have = c < nc;
           int rank = 0;
+          if (have) {
+            const unsigned long long v = s_val[c];
 #pragma unroll 8
-          for (int u = 0; u < nc; ++u) {
-            const unsigned long long o = s_val[u];
-            rank += (o > v || (o == v && u < t)) ? 1 : 0;
+            for (int u = u0; u < u1; ++u) {
+              const unsigned long long o = s_val[u];
+              rank += (o > v || (o == v && u < c)) ? 1 : 0;
+            }
           }
-          if (rank < K) {
-            s_front[rank] = base + t;
-            s_fval[rank] = s_dval[t];
+          rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+          if (have && (lt & 1) == 0 && rank < K) {
+            s_front[rank] = base + c;
+            s_fval[rank] = s_dval[c];
           }
         }
-        __syncwarp();
+        asm volatile("bar.sync 2, %0;" ::"n"(kGrowLayerThreads) : "memory");
       }
     }
+  } else {
+    const int t = threadIdx.x - kGrowLayerThreads;
+    constexpr int kOthers = kGrowTreeThreads - kGrowLayerThreads;
+    for (int i = n + t; i < P; i += kOthers) {
+      s_key[i] = grow_key(-INFINITY);
+      s_id[i] = 0x7FFFFFFF;
+    }
+    for (int i = t; i < nnodes; i += kOthers) s_new[i] = 0;
   }
   __syncthreads();
 
   // keep the M best non-root nodes: bitonic sort of (value key desc, id asc)
-  const int n = nnodes - 1;  // non-root nodes, ids 1..nnodes-1
-  const int P = grow_sort_n(nnodes);
-  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(grow_mem);  // [P]
-  int* s_id = reinterpret_cast<int*>(s_key + P);                                // [P]
-  int* s_new = s_id + P;                                                        // [nnodes]
-  for (int i = threadIdx.x; i < P; i += kGrowTreeThreads) {
-    s_key[i] = grow_key(i < n ? nval[i + 1] : -INFINITY);
-    s_id[i] = i < n ? i + 1 : 0x7FFFFFFF;
-  }
-  for (int i = threadIdx.x; i < nnodes; i += kGrowTreeThreads) s_new[i] = 0;
-  __syncthreads();
   if (P <= kGrowTreeThreads) {
     // one element per thread, in registers: partners closer than 32 are in
     // the same warp (shuffles), farther ones are exchanged through shared
