@@ -258,39 +258,61 @@ def run_ours(args, rank, world, local_rank):
                 gn=torch.empty(B, **i32), gtok=torch.empty(B, k + 1, **i32),
                 tn=torch.empty(Bt, **i32), tpath=torch.empty(Bt, tree.max_depth + 1, **i32),
                 ttok=torch.empty(Bt, tree.max_depth + 1, **i32))
-    ws_bytes = max(sv.spec_verify_workspace_bytes(sv.SPEC_MODE_SAMPLE, B, k, V, 1),
-                   sv.spec_verify_workspace_bytes(sv.SPEC_MODE_GREEDY, B, k, V, 1),
-                   sv.spec_verify_workspace_bytes(sv.SPEC_MODE_TREE_GREEDY, Bt, N, Vt, 1))
-    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.Stream(device=dev)
+    # one workspace per call type: the three calls of a step run concurrently
+    wsb = {"sample": sv.spec_verify_workspace_bytes(sv.SPEC_MODE_SAMPLE, B, k, V, 1),
+           "greedy": sv.spec_verify_workspace_bytes(sv.SPEC_MODE_GREEDY, B, k, V, 1),
+           "tree": sv.spec_verify_workspace_bytes(sv.SPEC_MODE_TREE_GREEDY, Bt, N, Vt, 1)}
+    wss = {key: torch.zeros(n, dtype=torch.uint8, device=dev) for key, n in wsb.items()}
+    stream = torch.cuda.Stream(device=dev)   # the step's stream (and the sampling call's)
+    side = {"greedy": torch.cuda.Stream(device=dev), "tree": torch.cuda.Stream(device=dev)}
     sp = stream.cuda_stream
     O = {key: v.data_ptr() for key, v in outs.items()}
-    wsp = ws.data_ptr()
+    W = {key: v.data_ptr() for key, v in wss.items()}
     T = float(samp.temperature)
 
-    def call_sample(s):
+    def call_sample(s, st_ptr=None):
         st = lib.spec_verify_sample(s["t"].data_ptr(), s["d"].data_ptr(), 1, s["tok"].data_ptr(),
                                     s["ua"].data_ptr(), s["us"].data_ptr(), T, B, k, V, O["n"],
-                                    O["tok"], O["p"], O["q"], O["R"], wsp, ws_bytes, sp)
+                                    O["tok"], O["p"], O["q"], O["R"], W["sample"],
+                                    wsb["sample"], st_ptr or sp)
         assert st == 0, st
 
-    def call_greedy(s):
+    def call_greedy(s, st_ptr=None):
         st = lib.spec_verify_greedy(s["t"].data_ptr(), 1, s["gtok"].data_ptr(), B, k, V,
-                                    O["gn"], O["gtok"], wsp, ws_bytes, sp)
+                                    O["gn"], O["gtok"], W["greedy"], wsb["greedy"], st_ptr or sp)
         assert st == 0, st
 
-    def call_tree(s):
+    def call_tree(s, st_ptr=None):
         st = lib.spec_verify_tree_greedy(s["tt"].data_ptr(), 1, s["ttok"].data_ptr(),
                                          s["tpar"].data_ptr(), Bt, N, Vt, tree.max_depth,
-                                         O["tn"], O["tpath"], O["ttok"], wsp, ws_bytes, sp)
+                                         O["tn"], O["tpath"], O["ttok"], W["tree"], wsb["tree"],
+                                         st_ptr or sp)
         assert st == 0, st
 
     calls = {"sample": call_sample, "greedy": call_greedy, "tree": call_tree}
 
-    def step(i):
+    def step_serial(i):
+        """The step's three calls one after another on the step's stream."""
         call_sample(sets[(2 * i) % NSETS])
         call_greedy(sets[(2 * i + 1) % NSETS])
         call_tree(sets[i % NSETS])
+
+    ev_fork = torch.cuda.Event()
+    ev_join = {key: torch.cuda.Event() for key in side}
+
+    def step(i):
+        """The step's three calls (independent batches) forked onto three
+        streams and joined before the step ends: each call's serial tail (the
+        finish and resolve kernels) overlaps the other calls' streaming."""
+        ev_fork.record(stream)
+        for key, sd in side.items():
+            sd.wait_event(ev_fork)
+        call_sample(sets[(2 * i) % NSETS])
+        call_greedy(sets[(2 * i + 1) % NSETS], side["greedy"].cuda_stream)
+        call_tree(sets[i % NSETS], side["tree"].cuda_stream)
+        for key, sd in side.items():
+            ev_join[key].record(sd)
+            stream.wait_event(ev_join[key])
 
     # second-pass bytes depend on each set's accept outcomes (same data in all sets)
     with torch.cuda.stream(stream):
@@ -350,6 +372,21 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     total_ms = ev0.elapsed_time(ev1)
 
+    # ---- the same K steps with the three calls serialised on one stream
+    # (reported beside the headline) ----
+    g_serial = capture_graph(lambda: [step_serial(i) for i in range(NSETS)], stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g_serial.replay()
+        es0 = torch.cuda.Event(enable_timing=True)
+        es1 = torch.cuda.Event(enable_timing=True)
+        es0.record(stream)
+        for _ in range(max(1, K // NSETS)):
+            g_serial.replay()
+        es1.record(stream)
+    stream.synchronize()
+    serial_ms_step = es0.elapsed_time(es1) / (max(1, K // NSETS) * NSETS)
+
     # ---- spread of single steps: up to 200 steps, each a replay of a
     # one-step graph between its own pair of events (a step's calls stay
     # chained inside it) ----
@@ -408,12 +445,12 @@ def run_ours(args, rank, world, local_rank):
         sv.spec_verify_sample(s["t"].view(torch.bfloat16).view(B, k + 1, V),
                               s["d"].view(torch.bfloat16).view(B, k, V), s["tok"],
                               s["ua"], s["us"], T, outs["n"], outs["tok"], outs["p"],
-                              outs["q"], outs["R"], ws, stream)
+                              outs["q"], outs["R"], wss["sample"], stream)
         sv.spec_verify_greedy(s["t"].view(torch.bfloat16).view(B, k + 1, V), s["gtok"],
-                              outs["gn"], outs["gtok"], ws, stream)
+                              outs["gn"], outs["gtok"], wss["greedy"], stream)
         sv.spec_verify_tree_greedy(s["tt"].view(torch.bfloat16).view(Bt, N, Vt),
                                    s["ttok"], s["tpar"], tree.max_depth, outs["tn"],
-                                   outs["tpath"], outs["ttok"], ws, stream)
+                                   outs["tpath"], outs["ttok"], wss["tree"], stream)
         for key in outs:
             out_host[key].copy_(outs[key], non_blocking=True)
 
@@ -463,7 +500,11 @@ def run_ours(args, rank, world, local_rank):
                    "positions_per_step": pos_step, "algorithmic_bytes_per_step": bytes_step,
                    "l2": f"{NSETS} rotating input sets; every set is reused only after a "
                          "246 MB tree read (> 129 MB L2)",
-                   "parallelism": f"replicas x{world} (sequences shard, no collective)"},
+                   "parallelism": f"replicas x{world} (sequences shard, no collective)",
+                   "streams": "each step forks its sampling, greedy and tree calls (independent "
+                              "batches, one workspace each) onto three streams and joins them "
+                              "before the next step"},
+        "serial_ms_per_step": round(serial_ms_step, 5),
         "hbm_gbs": round(step_gbs, 1), "hbm_frac_of_peak": round(step_gbs / peak, 4),
         "sequences_per_s": round(job_rate(world, K, seqs_step, total_ms), 1),
         "step_ms_percentiles": {"p10": round(float(np.percentile(step_samples, 10)), 5),

@@ -329,6 +329,42 @@ def test_inputs_written_by_the_kernel_just_before():
                          ["accepted_len", "out_tokens"])
 
 
+def test_three_calls_on_three_streams():
+    # the benchmark step's layout: sampling, greedy and tree calls forked onto
+    # three streams, one workspace each, running at the same time
+    c = synth.zipf128k(seed=5)
+    cg = synth.greedy_variant(c, 0.7)
+    t = synth.tree(seed=5)
+    o = oracle_sample(c)
+    og = oracle.verify_greedy(cg.target, cg.tokens, dtype=cg.dtype)
+    ot = oracle.verify_tree_greedy(t.target, t.tokens, t.parents, t.max_depth, dtype=t.dtype)
+    x = dev_chain(c)
+    gt = torch.from_numpy(cg.tokens).cuda()
+    tt = sv.to_device_logits(t.target, t.dtype)
+    ttok, tpar = torch.from_numpy(t.tokens).cuda(), torch.from_numpy(t.parents).cuda()
+    ws = {m: sv.alloc_workspace(m, Bm, km, c.V, sv.SPEC_DTYPE_BF16)
+          for m, Bm, km in ((sv.SPEC_MODE_SAMPLE, c.B, c.k), (sv.SPEC_MODE_GREEDY, c.B, c.k),
+                            (sv.SPEC_MODE_TREE_GREEDY, t.B, t.N))}
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        fork = torch.cuda.Event()
+        fork.record(torch.cuda.current_stream())
+        for st in streams:
+            st.wait_event(fork)
+        gs = sv.verify_sample(x["t"], x["d"], x["tok"], x["ua"], x["us"], c.temperature,
+                              workspace=ws[sv.SPEC_MODE_SAMPLE], stream=streams[0])
+        gg = sv.verify_greedy(x["t"], gt, workspace=ws[sv.SPEC_MODE_GREEDY], stream=streams[1])
+        gtr = sv.verify_tree_greedy(tt, ttok, tpar, t.max_depth,
+                                    workspace=ws[sv.SPEC_MODE_TREE_GREEDY], stream=streams[2])
+        torch.cuda.synchronize()
+        ph.compare_sample({k: v.cpu().numpy() for k, v in gs.items()}, o, V=c.V)
+        ph.compare_exact({k: v.cpu().numpy() for k, v in gg.items()}, og,
+                         ["accepted_len", "out_tokens"])
+        ph.compare_exact({k: v.cpu().numpy() for k, v in gtr.items()}, ot,
+                         ["accepted_len", "path_nodes", "out_tokens"])
+
+
 def test_deterministic_and_side_stream():
     c = synth.make_chain_case(B=16, k=4, V=50000, dtype="bf16", seed=6)
     a = gpu_sample(c)
