@@ -247,6 +247,54 @@ def test_tree_random(seed, N, V, depth, dtype):
     ph.compare_exact(g, o, ["accepted_len", "path_nodes", "out_tokens"])
 
 
+@pytest.mark.parametrize("dtype,V,noise", [("f32", 300, 0.0), ("bf16", 1000, 0.05)])
+def test_sample_longest_draft(dtype, V, noise):
+    # k at the interface's limit (256 drafts, 513 rows per sequence); with no
+    # draft noise every draft is accepted and the bonus comes from row 256
+    k = 256
+    c = synth.make_chain_case(B=2, k=k, V=V, dtype=dtype, target_sigma=1.0, draft_noise=noise,
+                              seed=31)
+    s, g, _ = sample_parity(c, allow_flags=1)
+    if noise == 0.0:
+        assert (g["accepted_len"] == k).all()
+
+
+def test_greedy_longest_draft():
+    k = 256
+    c = synth.make_chain_case(B=3, k=k, V=500, dtype="bf16", greedy_force=0.995, seed=32)
+    g = gpu_greedy(c)
+    o = oracle.verify_greedy(c.target, c.tokens, dtype="bf16")
+    ph.compare_exact(g, o, ["accepted_len", "out_tokens"])
+    assert g["accepted_len"].max() > 32
+
+
+def test_tree_large_and_deep():
+    # 3000 nodes (more than the resolve kernel keeps in shared memory: its
+    # global-memory path) and paths hundreds of levels deep under the
+    # interface's depth limit; most tokens follow the parent's argmax
+    rng = np.random.default_rng(33)
+    B, N, V, max_depth = 2, 3000, 64, 1024
+    target = synth.make_tree_case(B=B, N=N, V=V, dtype="f32", seed=33).target
+    g_arg = np.argmax(target, axis=-1)
+    par = np.full((B, N), -1, np.int32)
+    tok = np.zeros((B, N), np.int32)
+    for b in range(B):
+        depth = np.zeros(N, np.int64)
+        for v in range(1, N):
+            while True:
+                p = v - 1 if rng.random() < 0.7 else int(rng.integers(max(0, v - 40), v))
+                if depth[p] < max_depth:
+                    break
+            par[b, v] = p
+            depth[v] = depth[p] + 1
+            tok[b, v] = g_arg[b, p] if rng.random() < 0.995 else int(rng.integers(0, V))
+    t = synth.TreeInputs("deep", B, N, V, "f32", max_depth, target, tok, par)
+    g = gpu_tree(t)
+    o = oracle.verify_tree_greedy(target, tok, par, max_depth, dtype="f32")
+    ph.compare_exact(g, o, ["accepted_len", "path_nodes", "out_tokens"])
+    assert g["accepted_len"].max() > 100
+
+
 def test_chain_tree_matches_gpu_greedy():
     c = synth.make_chain_case(B=20, k=6, V=5000, dtype="bf16", greedy_force=0.85, seed=4)
     par = np.tile(np.arange(-1, c.k, dtype=np.int32), (c.B, 1))
