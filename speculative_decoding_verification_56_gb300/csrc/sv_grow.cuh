@@ -559,16 +559,13 @@ __host__ __device__ inline int grow_nstage(int nchunks, int K) {
   const size_t fit = kGrowStageBudget / grow_stage_bytes(nchunks, K);
   return (int)(fit < (size_t)kGrowTreeWarps ? fit : (size_t)kGrowTreeWarps);
 }
-__host__ __device__ inline int grow_sort_n(int nnodes) {
-  int P = 1;
-  while (P < nnodes - 1) P <<= 1;
-  return P;
-}
 // The rows' results, then one area used first for staging the rows' chunk
 // records and then, once every row is reduced, for the final sort.
 __host__ __device__ inline size_t grow_tree_smem(int nchunks, int K, int rows, int nnodes) {
   const size_t stage = (size_t)grow_nstage(nchunks, K) * grow_stage_bytes(nchunks, K);
-  const size_t sort = (size_t)grow_sort_n(nnodes) * (sizeof(unsigned long long) + sizeof(int)) +
+  // the selection: every non-root node's key by id and by layer rank, its
+  // rank within its layer, and the kept flags / new ids
+  const size_t sort = (size_t)(nnodes - 1) * (2 * sizeof(unsigned long long) + sizeof(int)) +
                       (size_t)nnodes * sizeof(int);
   return grow_row_bytes(rows, K) + (stage > sort ? stage : sort);
 }
@@ -586,8 +583,10 @@ constexpr size_t kGrowTreeSmem =
 // its ln q = (z s - R - log2 S) ln 2, in float64.  The layers then run on
 // four warps: a child's value is its parent's plus the row's ln q, and the
 // next frontier is the K children ranked best among the layer's children.
-// Finally every non-root node is sorted by (value desc, creation asc), the
-// first M are kept and renumbered in creation order.  Launched
+// Finally the M best non-root nodes by (value desc, creation asc) are kept:
+// each layer's children are ranked while the layer runs, and a node's rank
+// over all layers adds binary searches in the other layers' ranked keys.
+// The kept nodes are renumbered in creation order.  Launched
 // programmatically after the top-k grid and waits for it before reading the
 // records.
 __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const GrowParams p) {
@@ -779,14 +778,16 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
   }
   __syncthreads();
 
-  // the sort's arrays, in the staging area (free now): the layers write each
-  // child's key and id as they create it, the other warps the padding
+  // the selection's arrays, in the staging area (free now), written by the
+  // layers: each non-root node's key by id (node id - 1), each layer's keys in
+  // rank order (the layer's block of the same index range) and each node's
+  // rank within its layer; the other warps clear the kept flags meanwhile
   const int n = nnodes - 1;  // non-root nodes, ids 1..nnodes-1
-  const int P = grow_sort_n(nnodes);
-  unsigned long long* s_key =
-      reinterpret_cast<unsigned long long*>(grow_mem + grow_row_bytes(rows, K));  // [P]
-  int* s_id = reinterpret_cast<int*>(s_key + P);                                  // [P]
-  int* s_new = s_id + P;                                                          // [nnodes]
+  unsigned long long* s_ikey =
+      reinterpret_cast<unsigned long long*>(grow_mem + grow_row_bytes(rows, K));  // [n]
+  unsigned long long* s_lkey = s_ikey + n;                                        // [n]
+  int* s_lrank = reinterpret_cast<int*>(s_lkey + n);                              // [n]
+  int* s_new = s_lrank + n;                                                       // [nnodes]
 
   // 3. the layers, on warps 0-3 (named barrier 2 over their 128 threads):
   //    the children's values, then the next frontier, the K children of best
@@ -819,11 +820,10 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
         s_dval[t] = val;
         const unsigned long long key = grow_key(val);
         s_val[t] = key;
-        s_key[id - 1] = key;
-        s_id[id - 1] = id;
+        s_ikey[id - 1] = key;
       }
       asm volatile("bar.sync 2, %0;" ::"n"(kGrowLayerThreads) : "memory");
-      if (layer + 1 < p.D) {
+      {  // every layer's ranks (the last layer's for the selection only)
         const int half = nc >> 1;
         const int u0 = (lt & 1) ? half : 0, u1 = (lt & 1) ? nc : half;
         // every thread runs the same trips: the pair's shuffle is warp-wide
@@ -840,9 +840,13 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
             }
           }
           rank += __shfl_xor_sync(0xffffffffu, rank, 1);
-          if (have && (lt & 1) == 0 && rank < K) {
-            s_front[rank] = base + c;
-            s_fval[rank] = s_dval[c];
+          if (have && (lt & 1) == 0) {
+            s_lkey[base - 1 + rank] = s_val[c];
+            s_lrank[base - 1 + c] = rank;
+            if (rank < K && layer + 1 < p.D) {
+              s_front[rank] = base + c;
+              s_fval[rank] = s_dval[c];
+            }
           }
         }
         asm volatile("bar.sync 2, %0;" ::"n"(kGrowLayerThreads) : "memory");
@@ -850,76 +854,34 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
     }
   } else {
     const int t = threadIdx.x - kGrowLayerThreads;
-    constexpr int kOthers = kGrowTreeThreads - kGrowLayerThreads;
-    for (int i = n + t; i < P; i += kOthers) {
-      s_key[i] = grow_key(-INFINITY);
-      s_id[i] = 0x7FFFFFFF;
-    }
-    for (int i = t; i < nnodes; i += kOthers) s_new[i] = 0;
+    for (int i = t; i < nnodes; i += kGrowTreeThreads - kGrowLayerThreads) s_new[i] = 0;
   }
   __syncthreads();
 
-  // keep the M best non-root nodes: bitonic sort of (value key desc, id asc)
-  if (P <= kGrowTreeThreads) {
-    // one element per thread, in registers: partners closer than 32 are in
-    // the same warp (shuffles), farther ones are exchanged through shared
-    // memory among the sorting warps only (named barrier 1 over the first
-    // `act` threads, a multiple of 32).  "Before" = larger key, then smaller
-    // id; after the sort the thread i < M holds the i-th best.
-    const int i = threadIdx.x;
-    const int act = P < 32 ? 32 : P;
-    if (i < act) {
-      unsigned long long key = i < P ? s_key[i] : 0ull;
-      int id = i < P ? s_id[i] : 0x7FFFFFFF;
-      for (int k = 2; k <= P; k <<= 1)
-        for (int j = k >> 1; j > 0; j >>= 1) {
-          unsigned long long okey;
-          int oid;
-          if (j < 32) {
-            okey = __shfl_xor_sync(0xffffffffu, key, j);
-            oid = __shfl_xor_sync(0xffffffffu, id, j);
-          } else {  // P >= 64 here, so act = P and every thread holds an element
-            asm volatile("bar.sync 1, %0;" ::"r"(act) : "memory");  // the last exchange is read
-            s_key[i] = key;
-            s_id[i] = id;
-            asm volatile("bar.sync 1, %0;" ::"r"(act) : "memory");
-            okey = s_key[i ^ j];
-            oid = s_id[i ^ j];
-          }
-          if (i < P) {
-            const bool other_before = okey > key || (okey == key && oid < id);
-            const bool keep_before = (i < (i ^ j)) == ((i & k) == 0);
-            if (other_before == keep_before) {
-              key = okey;
-              id = oid;
-            }
-          }
-        }
-      if (i < p.M && id >= 1 && id < nnodes) s_new[id] = 1;
-    }
-  } else {
-    // several elements per thread: the same network through shared memory
-    for (int k = 2; k <= P; k <<= 1)
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = threadIdx.x; i < P; i += kGrowTreeThreads) {
-          const int l = i ^ j;
-          if (l > i) {
-            const bool up = (i & k) == 0;
-            const bool lbefore = s_key[l] > s_key[i] || (s_key[l] == s_key[i] && s_id[l] < s_id[i]);
-            if (lbefore == up) {
-              const unsigned long long tk = s_key[i];
-              s_key[i] = s_key[l];
-              s_key[l] = tk;
-              const int ti = s_id[i];
-              s_id[i] = s_id[l];
-              s_id[l] = ti;
-            }
-          }
-        }
-        __syncthreads();
+  // keep the M best non-root nodes by (value key desc, id asc): a node's
+  // rank among all of them is its rank within its layer plus, for every other
+  // layer, how many of that layer's children come before it, found by binary
+  // search in the layer's keys in rank order.  On equal keys the node with
+  // the smaller id comes first, and every id of an earlier layer is smaller.
+  for (int i = threadIdx.x; i < n; i += kGrowTreeThreads) {
+    const int L = i < K ? 0 : 1 + (i - K) / (K * K);
+    const unsigned long long v = s_ikey[i];
+    int g = s_lrank[i];
+    for (int L2 = 0; L2 < p.D && g < p.M; ++L2) {
+      if (L2 == L) continue;
+      const int b0 = L2 == 0 ? 0 : K + (L2 - 1) * K * K;
+      int lo = 0, hi = L2 == 0 ? K : K * K;  // the first entry not before v
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const unsigned long long e = s_lkey[b0 + mid];
+        if (e > v || (e == v && L2 < L))
+          lo = mid + 1;
+        else
+          hi = mid;
       }
-    for (int i = threadIdx.x; i < p.M; i += kGrowTreeThreads)
-      if (s_id[i] >= 1 && s_id[i] < nnodes) s_new[s_id[i]] = 1;
+      g += lo;
+    }
+    if (g < p.M) s_new[i + 1] = 1;
   }
   __syncthreads();
   {
