@@ -25,8 +25,8 @@
 //   grow_tree_kernel    one CTA per tree, all layers: merge each frontier
 //                       row's chunk records, ln q of the K tokens (float64:
 //                       a few values per row), create the children, choose
-//                       the next frontier; then sort every node by (value
-//                       desc, creation asc), keep M, renumber
+//                       the next frontier; then keep the M best nodes by
+//                       (value desc, creation asc) and renumber them
 // Ranking tokens by raw logit is ranking them by probability, so the token
 // choices are exact; node values are float64.
 #pragma once
@@ -532,7 +532,7 @@ constexpr int kGrowMaxRows = 1 + (kGrowMaxD - 1) * kGrowMaxK;  // draft rows per
 // of the tree (ln q of the K best tokens, the tokens, the logits, the row
 // normaliser and its log2) stay for the whole layer loop; behind them
 // `nstage` warps stage one row's chunk lists each (values, tokens, head
-// pointers).  The node sort reuses the whole space afterwards.
+// pointers).  The selection of the M best nodes reuses that area afterwards.
 __host__ __device__ inline size_t grow_row_bytes(int rows, int K) {
   const size_t b = (size_t)rows * K * (sizeof(double) + sizeof(float) + sizeof(int)) +
                    (size_t)rows * (sizeof(double) + sizeof(int) + 2 * sizeof(float));
@@ -549,8 +549,7 @@ __device__ __forceinline__ void grow_cp4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 // The tree kernel's block: 32 warps, so a tree's 41 draft rows (6 layers of
-// 8) are staged and merged in two batches and a 512-node sort keeps one
-// element per thread.
+// 8) are staged and merged in two batches.
 constexpr int kGrowTreeThreads = 1024;
 constexpr int kGrowTreeWarps = kGrowTreeThreads / 32;
 constexpr int kGrowLayerThreads = 128;  // warps that run the frontier layers
@@ -560,14 +559,14 @@ __host__ __device__ inline int grow_nstage(int nchunks, int K) {
   return (int)(fit < (size_t)kGrowTreeWarps ? fit : (size_t)kGrowTreeWarps);
 }
 // The rows' results, then one area used first for staging the rows' chunk
-// records and then, once every row is reduced, for the final sort.
+// records and then, once every row is reduced, for the selection.
 __host__ __device__ inline size_t grow_tree_smem(int nchunks, int K, int rows, int nnodes) {
   const size_t stage = (size_t)grow_nstage(nchunks, K) * grow_stage_bytes(nchunks, K);
   // the selection: every non-root node's key by id and by layer rank, its
   // rank within its layer, and the kept flags / new ids
-  const size_t sort = (size_t)(nnodes - 1) * (2 * sizeof(unsigned long long) + sizeof(int)) +
-                      (size_t)nnodes * sizeof(int);
-  return grow_row_bytes(rows, K) + (stage > sort ? stage : sort);
+  const size_t select = (size_t)(nnodes - 1) * (2 * sizeof(unsigned long long) + sizeof(int)) +
+                        (size_t)nnodes * sizeof(int);
+  return grow_row_bytes(rows, K) + (stage > select ? stage : select);
 }
 constexpr size_t kGrowTreeSmem =
     ((size_t)kGrowMaxRows * kGrowMaxK * 16 + (size_t)kGrowMaxRows * 20 + 15) / 16 * 16 +
