@@ -721,9 +721,9 @@ spec_status_t spec_tree_grow(const void* draft_logits, int dtype, float temperat
   // the node bookkeeping of every layer and the final ranking, one CTA per tree
   st = ensure_smem<sv::grow_tree_kernel>(sv::kGrowTreeSmem);
   if (st != SPEC_OK) return st;
-  return launch(sv::grow_tree_kernel, B,
+  return launch(sv::grow_tree_kernel, B * sv::kGrowTreeCluster,
                 sv::grow_tree_smem(L.nchunks, K, prm.rows_per_tree, nnodes), prm, stream,
-                true, 1, sv::kGrowTreeThreads);
+                true, sv::kGrowTreeCluster, sv::kGrowTreeThreads);
 }
 
 spec_status_t spec_verify_read_flags(void* workspace, uint32_t* host_flags, int clear,

@@ -22,7 +22,7 @@
 //                       the chunk's softmax partial (integer reference,
 //                       double-float sum) and its K largest logits (lowest
 //                       index on ties), by a threshold filter and a ranking
-//   grow_tree_kernel    one CTA per tree, all layers: merge each frontier
+//   grow_tree_kernel    two CTAs per tree (a cluster), all layers: merge each frontier
 //                       row's chunk records, ln q of the K tokens (float64:
 //                       a few values per row), create the children, choose
 //                       the next frontier; then keep the M best nodes by
@@ -553,6 +553,7 @@ __device__ __forceinline__ void grow_cp4(void* dst, const void* src) {
 constexpr int kGrowTreeThreads = 1024;
 constexpr int kGrowTreeWarps = kGrowTreeThreads / 32;
 constexpr int kGrowLayerThreads = 128;  // warps that run the frontier layers
+constexpr int kGrowTreeCluster = 2;     // CTAs per tree: each reduces half of its rows
 
 __host__ __device__ inline int grow_nstage(int nchunks, int K) {
   const size_t fit = kGrowStageBudget / grow_stage_bytes(nchunks, K);
@@ -572,15 +573,17 @@ constexpr size_t kGrowTreeSmem =
     ((size_t)kGrowMaxRows * kGrowMaxK * 16 + (size_t)kGrowMaxRows * 20 + 15) / 16 * 16 +
     kGrowStageBudget;
 
-// One CTA per tree.  A draft row's K best tokens and their ln q do not
-// depend on which node the frontier put in the row's slot, so every row of
-// the tree is reduced first, nstage rows at a time: the CTA stages the rows'
-// chunk records in shared memory, then warp w takes row q0 + w, merges the
-// chunk normalisers and picks the K best tokens from the chunk lists (each
-// sorted best first) by a threshold and a shuffle ranking; then
-// a thread per row takes log2 of the row sum and a thread per (row, rank)
-// its ln q = (z s - R - log2 S) ln 2, in float64.  The layers then run on
-// four warps: a child's value is its parent's plus the row's ln q, and the
+// A cluster of two CTAs per tree.  A draft row's K best tokens and their
+// ln q do not depend on which node the frontier put in the row's slot, so
+// every row of the tree is reduced first, each CTA taking half of the rows,
+// nstage at a time: the CTA stages the rows' chunk records in shared memory,
+// then warp w takes row q0 + w, merges the chunk normalisers and picks the
+// K best tokens from the chunk lists (each sorted best first) by a threshold
+// and a shuffle ranking; then a thread per row takes log2 of the row sum and
+// a thread per (row, rank) its ln q = (z s - R - log2 S) ln 2, in float64.
+// The second CTA's results reach the first through distributed shared
+// memory and the second CTA exits.  The layers then run on four warps of the
+// first CTA: a child's value is its parent's plus the row's ln q, and the
 // next frontier is the K children ranked best among the layer's children.
 // Finally the M best non-root nodes by (value desc, creation asc) are kept:
 // each layer's children are ranked while the layer runs, and a node's rank
@@ -596,8 +599,11 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
   __shared__ int s_front[kGrowMaxK];              // frontier: node id
   __shared__ double s_fval[kGrowMaxK];            // ... and value
   __shared__ int s_wtot[kGrowTreeWarps];
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = (int)cluster.block_rank();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = blockIdx.x;
+  const int b = blockIdx.x / kGrowTreeCluster;
   const int K = p.K;
   const int rows = p.rows_per_tree;
   const int ncand = p.nchunks * K;
@@ -619,14 +625,16 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
   // the next call's first kernel may become resident; it waits for this grid
   asm volatile("griddepcontrol.launch_dependents;");
 
-  // 1. every row of the tree: normaliser and K best tokens (float
-  //    arithmetic), nstage rows at a time: the CTA stages the rows' chunk
-  //    records together, then warp w reduces row q0 + w
+  // 1. this CTA's half of the tree's rows, [qa, qb): normaliser and K best
+  //    tokens (float arithmetic), nstage rows at a time: the CTA stages the
+  //    rows' chunk records together, then warp w reduces row q0 + w
+  const int half = (rows + 1) / 2;
+  const int qa = crank == 0 ? 0 : half, qb = crank == 0 ? half : rows;
   {
     const size_t sb = grow_stage_bytes(p.nchunks, K);
     uint8_t* stage0 = grow_mem + grow_row_bytes(rows, K);
-    for (int q0 = 0; q0 < rows; q0 += nstage) {
-      const int nb = min(nstage, rows - q0);
+    for (int q0 = qa; q0 < qb; q0 += nstage) {
+      const int nb = min(nstage, qb - q0);
       const GrowRec* rec0 = p.rec + ((size_t)b * rows + q0) * p.nchunks;
       // asynchronous 4-byte copies: every load of the batch is in flight at once
       for (int i = threadIdx.x; i < nb * ncand; i += kGrowTreeThreads) {
@@ -768,14 +776,26 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
     }
   }
   // 2. float64, a thread per row, then a thread per (row, rank)
-  for (int q = threadIdx.x; q < rows; q += kGrowTreeThreads)
+  for (int q = qa + (int)threadIdx.x; q < qb; q += kGrowTreeThreads)
     r_l2[q] = log2((double)r_hi[q] + (double)r_lo[q]);
   __syncthreads();
-  for (int t = threadIdx.x; t < rows * K; t += kGrowTreeThreads) {
+  for (int t = qa * K + (int)threadIdx.x; t < qb * K; t += kGrowTreeThreads) {
     const int q = t / K;
     r_lnq[t] = ((double)r_z[t] * (double)p.scale - (double)r_R[q] - r_l2[q]) * 0.6931471805599453;
   }
-  __syncthreads();
+  // the second CTA's rows (ln q and tokens) into the first CTA's shared
+  // memory, at the same offsets; the second CTA is done after that
+  cluster.sync();
+  if (crank == 0) {
+    const double* peer_lnq = cluster.map_shared_rank(r_lnq, 1);
+    const int* peer_tok = cluster.map_shared_rank(r_tok, 1);
+    for (int t = half * K + (int)threadIdx.x; t < rows * K; t += kGrowTreeThreads) {
+      r_lnq[t] = peer_lnq[t];
+      r_tok[t] = peer_tok[t];
+    }
+  }
+  cluster.sync();  // the second CTA's shared memory is no longer read
+  if (crank != 0) return;
 
   // the selection's arrays, in the staging area (free now), written by the
   // layers: each non-root node's key by id (node id - 1), each layer's keys in
