@@ -5,6 +5,9 @@ One step = one pass of the whole verification path over one batch:
   1. spec_verify_sample      B=64 sequences, k=4 drafts, V=128256, bf16, T=1.0
   2. spec_verify_greedy      same logits shape, 70% of drafts forced to argmax
   3. spec_verify_tree_greedy 16 trees of 60 nodes, depth <= 6, V=128256, bf16
+The three calls verify independent batches: a step forks them onto three
+streams (one workspace each) and joins them before the next step begins
+(`serial_ms_per_step` times the same steps with the calls one after another).
 Metric: verified draft positions per second (B*k + B*k + B*(N-1) = 1456 per
 step) and the achieved HBM bandwidth on the logits the method must read.
 
