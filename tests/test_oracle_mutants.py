@@ -62,6 +62,8 @@ MUTANTS = {
                                "if (!used[x] && (best < 0 || q[x] >= q[best])) best = x;"),
     "grow_wrong_depth": ("par[n] = front[j]; tok[n] = best; dep[n] = l + 1;",
                          "par[n] = front[j]; tok[n] = best; dep[n] = l;"),
+    "grow_keep_by_creation": ("          int t = order[a]; order[a] = order[c]; order[c] = t;\n        }\n    if (nn > M && M > 0)",
+                              "          (void)0;\n        }\n    if (nn > M && M > 0)"),
     "mask_wrong_word": ("        row[cur / 32] |= 1u << (cur % 32);\n        ++d;",
                         "        row[cur % W] |= 1u << (cur % 32);\n        ++d;"),
 }

@@ -743,6 +743,13 @@ def test_tree_grow_structure(oracle_mod, seed):
         for p in set(par[1:].tolist()):
             kids = r["tokens"][b, 1:][par[1:] == p]
             assert len(set(kids.tolist())) == len(kids)
+    # the budget keeps the M best nodes by value: the tree grown with every
+    # node kept has the same M largest values
+    n_all = K + (D - 1) * K * K
+    r_all = oracle_mod.tree_grow(z, 0.8, n_all, dtype="f32")
+    for b in range(B):
+        best = np.sort(r_all["values"][b, 1:])[::-1][:M]
+        assert np.array_equal(np.sort(r["values"][b, 1:])[::-1], best)
 
 
 def _logp_rows(*rows, V=6):
