@@ -64,6 +64,8 @@ MUTANTS = {
                          "par[n] = front[j]; tok[n] = best; dep[n] = l;"),
     "grow_keep_by_creation": ("          int t = order[a]; order[a] = order[c]; order[c] = t;\n        }\n    if (nn > M && M > 0)",
                               "          (void)0;\n        }\n    if (nn > M && M > 0)"),
+    "pq_first_row_only": ("    for (int i = 0; i < k; ++i) {\n      int32_t x = tokens[(size_t)b * k + i];\n      double p = pt[(size_t)i * V + x];\n      double q = pd[(size_t)i * V + x];\n      if (p_out)",
+                          "    for (int i = 0; i < k && i < 1; ++i) {\n      int32_t x = tokens[(size_t)b * k + i];\n      double p = pt[(size_t)i * V + x];\n      double q = pd[(size_t)i * V + x];\n      if (p_out)"),
     "mask_wrong_word": ("        row[cur / 32] |= 1u << (cur % 32);\n        ++d;",
                         "        row[cur % W] |= 1u << (cur % 32);\n        ++d;"),
 }
@@ -111,6 +113,7 @@ def _pin_checks(o):
     yield lambda: pins.test_emission_law_equals_target_later_position(o, 4)
     yield lambda: pins.test_bonus_token_law_is_last_target_row(o, 3)
     yield lambda: pins.test_zero_probability_cases(o)
+    yield lambda: pins.test_p_q_reported_for_every_row(o)
     yield lambda: pins.test_greedy_equals_argmax_decoding(o, "f32", 5)
     yield lambda: pins.test_tree_bruteforce(o, 1)
     yield lambda: pins.test_star_tree(o)

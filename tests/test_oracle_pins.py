@@ -285,6 +285,22 @@ def test_zero_probability_cases(oracle_mod):
     assert r["accepted_len"][0] == 2 and r["q"][0, 1] == 0.0
 
 
+def test_p_q_reported_for_every_row(oracle_mod):
+    # uniform rows: p(x) = q(x) = 1/V exactly.  The draft favours token 1 at
+    # position 0 (q > p there), so u just below 1 rejects position 0; the rows
+    # after the rejection still report their p and q
+    V, k = 8, 4
+    zt = np.zeros((1, k + 1, V), np.float32)
+    zd = np.zeros((1, k, V), np.float32)
+    zd[0, 0, 1] = 3.0
+    ua = np.full((1, k), np.nextafter(np.float32(1), np.float32(0)), np.float32)
+    r = oracle_mod.verify_sample(zt, zd, np.array([[1, 2, 3, 4]]), ua, np.array([0.5], np.float32),
+                                 1.0)
+    assert r["accepted_len"][0] == 0
+    assert r["p"][0, 0] == 1.0 / V and r["q"][0, 0] > 1.0 / V
+    assert (r["p"][0, 1:] == 1.0 / V).all() and (r["q"][0, 1:] == 1.0 / V).all()
+
+
 def test_residual_zero_falls_back_to_target_row(oracle_mod):
     V = 5
     zt = np.zeros((1, 2, V), np.float32)
