@@ -496,11 +496,13 @@ def run_ours(args, rank, world, local_rank):
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded Zipf-biased Gaussian logits; random draft trees)",
         "config": {"workload": "sample+greedy B=64 k=4 V=128256 bf16 T=1.0; "
                                "tree greedy B=16 N=60 depth<=6 V=128256 bf16",
                    "positions_per_step": pos_step, "algorithmic_bytes_per_step": bytes_step,
+                   "logits": "bf16 in HBM; exponentials, sums and comparisons in f32 "
+                             "(double-float sums, float64 final probabilities)",
                    "l2": f"{NSETS} rotating input sets; every set is reused only after a "
                          "246 MB tree read (> 129 MB L2)",
                    "parallelism": f"replicas x{world} (sequences shard, no collective)",
