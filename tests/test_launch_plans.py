@@ -1,6 +1,7 @@
-"""Launch plans checked on the host: the tree-growth kernel's staging depth
-and shared-memory size for every shape the interface admits (the plan
-functions of sv_grow.cuh, compiled with nvcc into a host program)."""
+"""Host-side checks of the CUDA sources, no GPU needed: the tree-growth
+kernel's staging depth and shared-memory size for every shape the interface
+admits (the plan functions of sv_grow.cuh, compiled with nvcc into a host
+program), and the provenance of the FMA-pipe 2^x coefficients."""
 import os
 import subprocess
 
@@ -23,3 +24,23 @@ def test_grow_plan_fits_every_admitted_shape(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout[-2000:]
     assert "shapes checked" in r.stdout
+
+
+def test_exp2_polynomial_comes_from_the_committed_fit():
+    # the FMA-pipe 2^x in sv_device.cuh uses the coefficients that
+    # csrc/fit_exp2_poly.py (Cody-Waite reduction, Remez exchange) prints
+    import re
+    import sys
+    script = os.path.join(CSRC, "fit_exp2_poly.py")
+    r = subprocess.run([sys.executable, script], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    fitted = [float(m) for m in re.findall(r"c\d = ([0-9.eE+-]+)", r.stdout)]
+    assert len(fitted) == 6
+    src = open(os.path.join(CSRC, "sv_device.cuh")).read()
+    body = src[src.index("float exp2_fma(float x)"):]
+    body = body[:body.index("\n}\n")]
+    used = [float(m) for m in re.findall(r"([0-9][0-9.]*e?-?[0-9]*)f", body)
+            if "." in m]
+    # the Horner chain lists c5 first and c0 last
+    coeffs = [c for c in used if c not in (12582912.0, 126.0)]
+    assert coeffs[::-1] == fitted, (coeffs, fitted)
