@@ -297,8 +297,8 @@ SPEC_API spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void
  * (sized for up to 16 layers); requires ceil(V / chunk) * K <= 2048 (chunk =
  * 16384 bf16 / 8192 fp32 elements).  Two kernel launches: the K best tokens
  * and softmax normaliser of every draft row read (B (1 + (D-1) K) rows, one
- * streaming pass), then one CTA per tree for the layer-by-layer expansion
- * and the final re-ranking.
+ * streaming pass), then a cluster of two CTAs per tree for the rows' merge,
+ * the layer-by-layer expansion and the selection of the M best nodes.
  */
 SPEC_API spec_status_t spec_tree_grow(const void* draft_logits, int dtype, float temperature,
                                       int B, int D, int K, int V, int M, int32_t* tokens,
