@@ -10,8 +10,13 @@
  * Conventions shared by every entry point
  *   - All array arguments are DEVICE pointers (cudaMalloc / torch CUDA
  *     memory), row-major and contiguous.  The caller owns all memory; the
- *     library allocates nothing and keeps no state across calls except the
- *     launch counter read by spec_verify_launch_count().
+ *     library allocates nothing.  State kept across calls: the launch counter
+ *     read by spec_verify_launch_count(); per device context, the kernels'
+ *     shared-memory opt-ins and launch shapes; and the fixed scratch array of
+ *     spec_verify_greedy_noalloc (resident on every device that loads the
+ *     library) with its device address.  Each per-context entry records the
+ *     context's unique id and is redone when it changes (after
+ *     cudaDeviceReset, for example).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call only enqueues work on that stream and returns; it
  *     never synchronises.  Outputs are valid once the stream reaches them.
@@ -338,8 +343,9 @@ SPEC_API uint64_t spec_verify_launch_count(void);
  * cudaMalloc, cudaFree or other allocating routine on this path.
  *
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture begins on the device.
+ *     (cudaGetSymbolAddress, with that device current) and caches it for the
+ *     device's current context; make that first call before any stream
+ *     capture begins on the device, and again after a cudaDeviceReset.
  *   - Calls whose scratch would exceed SPEC_NOALLOC_SCRATCH_BYTES return
  *     SPEC_ERR_TOO_LARGE before anything is enqueued (B=64 sequences of k=4
  *     drafts over V=128256 bf16 need about 0.66 MB).

@@ -186,19 +186,59 @@ void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, dim3 grid, d
   cfg->numAttrs = 1;
 }
 
-// Per-device launch shape of a persistent streaming kernel: the shared-memory
-// opt-in is set once per device, the grid is SMs x resident CTAs per SM.
+// Per-device state the library caches (shared-memory opt-ins, launch shapes,
+// the no-allocation array's address) belongs to the device's current context:
+// each cache entry records the context's unique id and is redone when the id
+// changes (after cudaDeviceReset, for example).
 constexpr int kMaxDevices = 64;
 constexpr size_t kStreamSmem = (size_t)sv::kStages * sv::kChunkBytes;
 std::mutex g_shape_mu;
+std::mutex g_ctx_mu;
+CUresult (*g_ctx_current)(CUcontext*) = nullptr;
+CUresult (*g_ctx_id)(CUcontext, unsigned long long*) = nullptr;
 
+// The current device and the unique id of its (primary) context, creating
+// that context if the runtime has not yet done so.
+spec_status_t current_context(int* dev, unsigned long long* id) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_ctx_mu);
+    if (!g_ctx_current || !g_ctx_id) {
+      void* f1 = nullptr;
+      void* f2 = nullptr;
+      cudaDriverEntryPointQueryResult q1, q2;
+      if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault,
+                                           &q1) != cudaSuccess ||
+          q1 != cudaDriverEntryPointSuccess || !f1 ||
+          cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+              cudaSuccess ||
+          q2 != cudaDriverEntryPointSuccess || !f2)
+        return SPEC_ERR_CUDA;
+      g_ctx_current = reinterpret_cast<CUresult (*)(CUcontext*)>(f1);
+      g_ctx_id = reinterpret_cast<CUresult (*)(CUcontext, unsigned long long*)>(f2);
+    }
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return SPEC_ERR_CUDA;
+  if (ctx == nullptr) {  // the runtime has not made the device's context current yet
+    if (cudaSetDevice(*dev) != cudaSuccess || g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx)
+      return SPEC_ERR_CUDA;
+  }
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// Per-device launch shape of a persistent streaming kernel: the shared-memory
+// opt-in is set once per device context, the grid is SMs x resident CTAs per
+// SM.
 template <auto kernel>
 spec_status_t persistent_grid(int items, int* grid) {
   static int cached[kMaxDevices] = {0};  // one table per kernel instantiation
+  static unsigned long long cached_ctx[kMaxDevices] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  unsigned long long ctx = 0;
+  if (current_context(&dev, &ctx) != SPEC_OK) return SPEC_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_shape_mu);
-  if (cached[dev] == 0) {
+  if (cached[dev] == 0 || cached_ctx[dev] != ctx) {
     int sms = 0, per_sm = 0;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kStreamSmem) != cudaSuccess)
@@ -209,23 +249,27 @@ spec_status_t persistent_grid(int items, int* grid) {
                                                       kStreamSmem) != cudaSuccess)
       return SPEC_ERR_CUDA;
     cached[dev] = std::max(1, sms * std::max(1, per_sm));
+    cached_ctx[dev] = ctx;
   }
   *grid = std::min(items, cached[dev]);
   return SPEC_OK;
 }
 
-// Dynamic shared-memory opt-in for a kernel, once per device.
+// Dynamic shared-memory opt-in for a kernel, once per device context.
 template <auto kernel>
 spec_status_t ensure_smem(size_t bytes) {
   static bool done[kMaxDevices] = {false};
+  static unsigned long long done_ctx[kMaxDevices] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  unsigned long long ctx = 0;
+  if (current_context(&dev, &ctx) != SPEC_OK) return SPEC_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_shape_mu);
-  if (!done[dev]) {
+  if (!done[dev] || done_ctx[dev] != ctx) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
         cudaSuccess)
       return SPEC_ERR_CUDA;
     done[dev] = true;
+    done_ctx[dev] = ctx;
   }
   return SPEC_OK;
 }
@@ -318,21 +362,24 @@ spec_status_t run_argmax(sv::ArgmaxParams prm, int rows, bool vec, void* stream)
 
 // Scratch of spec_verify_greedy_noalloc: a fixed array in the library's own
 // device memory (one copy per device that loads the library).  Host code may
-// not use the symbol as an address; its device address is looked up once per
-// device with cudaGetSymbolAddress while that device is current.
+// not use the symbol as an address; its device address is looked up with
+// cudaGetSymbolAddress while the device is current, once per device context.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
 void* g_noalloc_addr[kMaxDevices] = {nullptr};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {0};
 std::mutex g_noalloc_mu;
 
 spec_status_t noalloc_scratch(void** addr) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  unsigned long long ctx = 0;
+  if (current_context(&dev, &ctx) != SPEC_OK) return SPEC_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  if (g_noalloc_addr[dev] == nullptr || g_noalloc_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return SPEC_ERR_CUDA;
     g_noalloc_addr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
   *addr = g_noalloc_addr[dev];
   return SPEC_OK;
@@ -581,9 +628,6 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  // one CTA per SM in clusters of kLmCluster: as many clusters as can be
-  // resident at once (measured for this launch shape)
-  int max_clusters = 0;
   // row groups of at most kLmMaxRows rows, split evenly, each a multiple of
   // the 64-row H box (so two MMAs of equal N stay multiples of 16)
   const int gy = (rows + sv::kLmMaxRows - 1) / sv::kLmMaxRows;
@@ -609,32 +653,13 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   lp.stage_bytes = stage_bytes;
   lp.part = reinterpret_cast<sv::ArgPartial*>(ws + L.off_part);
   lp.flags = reinterpret_cast<unsigned*>(ws);
+  // one CTA per SM (the kernel holds the SM's tensor memory and most of its
+  // shared memory), at most one per vocabulary tile
+  const int gx = std::max(1, std::min(std::min(sms, ntiles), kLmMaxGrid));
   cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof cfg);
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = sv::kLmCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(sv::kLmThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = (cudaStream_t)stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.gridDim = dim3((unsigned)(sms / sv::kLmCluster * sv::kLmCluster), (unsigned)gy, 1);
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, sv::lmhead_argmax_kernel, &cfg) !=
-          cudaSuccess ||
-      max_clusters < 1)
-    return SPEC_ERR_CUDA;
-  const int nclusters =
-      std::max(1, std::min(std::min(max_clusters, (ntiles + sv::kLmCluster - 1) / sv::kLmCluster),
-                           kLmMaxGrid / sv::kLmCluster));
-  const int gx = nclusters * sv::kLmCluster;
-  lp.nclusters = nclusters;
-  cfg.gridDim = dim3((unsigned)gx, (unsigned)gy, 1);
-  cfg.numAttrs = 2;  // the cluster shape (queried above) and the dependent launch
+  cudaLaunchAttribute attr[1];
+  pdl_config(&cfg, attr, dim3((unsigned)gx, (unsigned)gy, 1), dim3(sv::kLmThreads, 1, 1),
+             (size_t)smem, stream);
   if (cudaLaunchKernelEx(&cfg, sv::lmhead_argmax_kernel, map_h, map_w, lp) != cudaSuccess)
     return SPEC_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -13,7 +13,8 @@
 // The vocabulary is the MMA's M (128 tensor-memory lanes per tile) and the
 // rows are its N (up to 384 columns, one or two MMAs of N <= 256), so rows
 // are padded only to a multiple of 64.  One CTA per SM walks a contiguous
-// range of vocabulary tiles for a group of rows.  Warp roles (192 threads):
+// range of vocabulary tiles for a group of rows; every CTA loads its own
+// operands (no cluster, no multicast).  Warp roles (192 threads):
 //   warp 0     TMA producer: per 64-wide K step, the tile's W slice and the
 //              rows' H slice (128-byte swizzled) into a 3-stage ring
 //   warp 1     allocates tensor memory; lane 0 issues tcgen05.mma
@@ -45,12 +46,10 @@ constexpr int kLmABytes = kLmBV * kLmBK * 2;          // 16 KB: W slice
 constexpr int kLmBBytes = kLmMaxRows * kLmBK * 2;     // up to 48 KB: H slice
 constexpr int kLmHBox = 64;                           // rows per H box (TMA)
 constexpr int kLmTmemCols = 512;
-constexpr int kLmCluster = 2;      // CTAs sharing each H slice (TMA multicast)
 
 struct LmHeadParams {
   int rows, d, V;       // rows = B * (k+1)
   int ntiles;           // ceil(V / kLmBV)
-  int nclusters;        // gridDim.x / kLmCluster
   int grp_rows;         // rows per row group (multiple of kLmHBox, <= kLmMaxRows)
   int stage_bytes;      // kLmABytes + grp_rows * 128
   ArgPartial* part;     // [rows, gridDim.x] one record per CTA segment
@@ -87,17 +86,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// The same, landing at this offset in every CTA of `mask` (a cluster), each
-// copy completing on that CTA's barrier at the same offset.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -113,26 +101,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_addr(bar))
       : "memory");
-}
-
-// Arrive on the barrier at this offset in every CTA of `mask` once every
-// tcgen05 operation this thread issued completes.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_addr(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
 }
 
 __device__ __forceinline__ void tmem_fence_before() {
@@ -182,21 +150,14 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = blockIdx.y * p.grp_rows;  // first row of this CTA's row group
   const int R = p.grp_rows;                  // columns used (rows past p.rows read as 0)
-  // The cluster owns tiles [T0, T1); member `crank` takes T0 + crank, T0 +
-  // crank + kLmCluster, ...  Every member runs the same number of steps (the
-  // H slices are shared); a step past T1 loads and multiplies the range's
-  // last tile again and its result is ignored.
-  const int crank = (int)cluster_rank();
-  const uint16_t cmask = (uint16_t)((1u << kLmCluster) - 1);
+  // the CTA owns the vocabulary tiles [T0, T1)
   int T0, T1;
   {
-    const long long G = p.nclusters, g = blockIdx.x / kLmCluster;
+    const long long G = gridDim.x, g = blockIdx.x;
     T0 = (int)((long long)p.ntiles * g / G);
     T1 = (int)((long long)p.ntiles * (g + 1) / G);
   }
-  const int nsteps = (T1 - T0 + kLmCluster - 1) / kLmCluster;
-  auto tile_of = [&](int j) { return min(T0 + j * kLmCluster + crank, T1 - 1); };
-  auto tile_real = [&](int j) { return T0 + j * kLmCluster + crank < T1; };
+  const int nsteps = T1 - T0;
   const int nk = (p.d + kLmBK - 1) / kLmBK;
   const int nmma = (R + kLmMaxN - 1) / kLmMaxN;  // MMAs per K step of 16
   const int nper = R / nmma;                     // N of each (a multiple of 16)
@@ -204,7 +165,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLmStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kLmCluster);  // released by every member's MMAs
+      mbar_init(&empty[s], 1);  // released by the MMAs that read the stage
     }
     mbar_init(&acc_full, 1);
     mbar_init(&acc_empty, 4);
@@ -222,7 +183,6 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   }
   tmem_fence_before();
   __syncthreads();
-  cluster_sync_all();  // peers' barriers are initialised before any multicast
   tmem_fence_after();
   const uint32_t tmem_base = tmem_base_holder;
   // a programmatic dependent of the kernel before it in the stream: the set-up
@@ -236,9 +196,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     unsigned phase = 0;
     const unsigned bytes = (unsigned)p.stage_bytes;
     for (int j = 0; j < nsteps && !*(volatile int*)&s_abort; ++j) {
-      const int t = tile_of(j);
+      const int t = T0 + j;
       for (int kb = 0; kb < nk; ++kb) {
-        // every member has released this stage (its H part lands in all of them)
+        // the MMAs that read this stage's previous contents have completed
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) {
           s_abort = 1;
           set_flag(p.flags, kFlagTimeout);
@@ -248,9 +208,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         uint8_t* st = ring + (size_t)stage * p.stage_bytes;
         mbar_expect_tx(&full[stage], bytes);
         tma_load_2d(st, &map_w, kb * kLmBK, t * kLmBV, &full[stage]);
-        for (int r = crank * kLmHBox; r < R; r += kLmCluster * kLmHBox)
-          tma_load_2d_mc(st + kLmABytes + r * 128, &map_h, kb * kLmBK, row0 + r, &full[stage],
-                         cmask);
+        for (int r = 0; r < R; r += kLmHBox)
+          tma_load_2d(st + kLmABytes + r * 128, &map_h, kb * kLmBK, row0 + r, &full[stage]);
         if (++stage == kLmStages) {
           stage = 0;
           phase ^= 1u;
@@ -287,7 +246,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             umma_bf16(tmem_base + m * nper, umma_desc_sw128(ast + kk * 32),
                       umma_desc_sw128(bst + m * nper * 128 + kk * 32), idesc,
                       (kb > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_mc(&empty[stage], cmask);  // free in every member once these finish
+        umma_commit(&empty[stage]);  // the stage is free once these finish
         if (++stage == kLmStages) {
           stage = 0;
           phase ^= 1u;
@@ -333,8 +292,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         break;
       }
       tmem_fence_after();
-      const int vocab = tile_of(j) * kLmBV + 32 * q + lane;
-      const bool valid = tile_real(j) && vocab < p.V;
+      const int vocab = (T0 + j) * kLmBV + 32 * q + lane;
+      const bool valid = vocab < p.V;
       for (int cb = 0; cb < R / 32; ++cb) {
         uint32_t r[32];
         tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + cb * 32, r);
@@ -389,12 +348,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       const int row = row0 + e + 128 * j;
       if (e + 128 * j < R && row < p.rows)
         p.part[(size_t)row * C + blockIdx.x] =
-            ArgPartial{best[j], bidx[j], tile_real(0) ? 1 : 0, 0};
+            ArgPartial{best[j], bidx[j], nsteps > 0 ? 1 : 0, 0};
     }
   }
   tmem_fence_before();
   __syncthreads();
-  cluster_sync_all();  // no peer still writes into this CTA or arrives on its barriers
   if (warp == 1) {
     tmem_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
