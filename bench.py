@@ -369,7 +369,6 @@ def run_ours(args, rank, world, local_rank):
             g_tail.replay()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
-    t_wall1 = time.time()
     launches = int(round(launches_per_step * K))
     if world > 1:
         torch.distributed.barrier()
@@ -404,31 +403,24 @@ def run_ours(args, rank, world, local_rank):
     stream.synchronize()
     step_samples = np.array([sev[i].elapsed_time(sev[i + 1]) for i in range(NS)])
 
-    # ---- per-call durations: each call alone, K times, same rotation, from
-    # CUDA graphs of NSETS calls (events between calls chained by programmatic
-    # dependent launch distort the chain, so each call type gets its own
-    # timed loop) ----
-    mean_ms = []
+    # ---- per-call durations: each call type alone, in its own loop of at
+    # least max(K, 200) calls and 0.5 s, same rotation, from CUDA graphs of
+    # NSETS calls (events between calls chained by programmatic dependent
+    # launch distort the chain, so the mean comes from one event pair around
+    # the whole loop; the spread from a second loop with one event pair per
+    # graph replay of NSETS calls) ----
+    per_call = {}
     for name in ("sample", "greedy", "tree"):
         fn = calls[name]
-        g_call = capture_graph(lambda: [fn(sets[i]) for i in range(NSETS)], stream)
-        reps = max(1, K // NSETS)
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                g_call.replay()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
-                g_call.replay()
-            e1.record(stream)
-        stream.synchronize()
-        mean_ms.append(e0.elapsed_time(e1) / (reps * NSETS))
-    mean_ms = np.array(mean_ms)
+        per_call[name] = time_call_loop(
+            lambda fn=fn: [fn(sets[i]) for i in range(NSETS)], NSETS, stream,
+            min_calls=max(K, 200), min_seconds=0.5)
+    mean_ms = np.array([per_call[n]["mean_ms"] for n in ("sample", "greedy", "tree")])
+    t_wall1 = time.time()
     clk = clocks.stop(t_wall0, t_wall1) if clocks else None
     next_rows = measure_next_rows(dev, stream, tree, K) \
         if rank == 0 and not args.skip_next_rows else None
-    at_scale = measure_at_scale(dev, stream, min(K, 400), measured_peak()[0]) \
+    at_scale = measure_at_scale(dev, stream, max(K, 200), measured_peak()[0]) \
         if rank == 0 and not args.skip_large else None
     total_ms = max_over_ranks(total_ms, dev)
     ms_step = total_ms / K
@@ -486,15 +478,29 @@ def run_ours(args, rank, world, local_rank):
     traffic = recorded_traffic(["sample", "greedy", "tree"][dom])
     breakdown = {}
     for j, nm in enumerate(names):
+        key = ["sample", "greedy", "tree"][j]
+        pc = per_call[key]
         gbs = byts[j] / (mean_ms[j] / 1e3) / 1e9
-        breakdown[["sample", "greedy", "tree"][j]] = {
+        breakdown[key] = {
             "kernels": nm, "ms": round(float(mean_ms[j]), 5),
             "algorithmic_bytes": int(byts[j]), "gb_s": round(gbs, 1),
-            "frac_of_peak": round(gbs / peak, 4)}
+            "frac_of_peak": round(gbs / peak, 4),
+            "calls_timed": pc["calls"],
+            "ms_p10_p50_p90": [round(pc["p10_ms"], 5), round(pc["p50_ms"], 5),
+                               round(pc["p90_ms"], 5)],
+            "spread": f"{pc['spread_calls']} calls, one event pair per graph replay of "
+                      f"{NSETS} calls"}
     step_gbs = bytes_step / (ms_step / 1e3) / 1e9
 
+    headline_calls = {
+        name: {"us_per_call": round(float(mean_ms[j]) * 1e3, 2),
+               "positions_per_s": round(B * k / (mean_ms[j] / 1e3), 1),
+               "gb_s": breakdown[name]["gb_s"], "frac_of_peak": breakdown[name]["frac_of_peak"],
+               "calls_timed": per_call[name]["calls"]}
+        for j, name in ((0, "sample"), (1, "greedy"))}
     result = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "calls_B64_k4": headline_calls, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded Zipf-biased Gaussian logits; random draft trees)",
@@ -571,7 +577,8 @@ def measure_at_scale(dev, stream, K, peak):
 
     out = {"workload": f"sample and greedy B={B} k={k} V={V} bf16 T=0.7 (Zipf-biased Gaussian "
                        "target, draft = target + N(0, 1.5^2))",
-           "timed": f"each call type in its own loop of {K} calls"}
+           "timed": f"each call type in its own loop of at least {K} calls (CUDA-graph "
+                    "replays of 4 calls; spread from one event pair per replay)"}
     with torch.cuda.stream(stream):
         call_sample()
     stream.synchronize()
@@ -579,21 +586,16 @@ def measure_at_scale(dev, stream, K, peak):
     for name, fn, byts, pos in (
             ("sample", call_sample, (B * (2 * k + 1) + pass2) * V * 2, B * k),
             ("greedy", call_greedy, B * (k + 1) * V * 2, B * k)):
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                fn()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(K):
-                fn()
-            e1.record(stream)
-        stream.synchronize()
-        ms = e0.elapsed_time(e1) / K
+        pc = time_call_loop(lambda fn=fn: [fn() for _ in range(4)], 4, stream, min_calls=K,
+                            min_seconds=0.0)
+        ms = pc["mean_ms"]
         gbs = byts / (ms / 1e3) / 1e9
         out[name] = {"us_per_call": round(ms * 1e3, 2), "algorithmic_bytes": int(byts),
                      "gb_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                     "positions_per_s": round(pos / (ms / 1e3), 1)}
+                     "positions_per_s": round(pos / (ms / 1e3), 1), "calls_timed": pc["calls"],
+                     "us_p10_p50_p90": [round(pc["p10_ms"] * 1e3, 2),
+                                        round(pc["p50_ms"] * 1e3, 2),
+                                        round(pc["p90_ms"] * 1e3, 2)]}
     del t, d, ws, wg
     torch.cuda.empty_cache()
     return out
@@ -610,6 +612,49 @@ def capture_graph(body, stream):
     with torch.cuda.graph(g, stream=stream):
         body()
     return g
+
+
+def time_call_loop(body, calls_per_body, stream, min_calls=200, min_seconds=0.5):
+    """Per-call time of whatever `body` enqueues (`calls_per_body` calls) on
+    `stream`, replayed from one CUDA graph.
+
+    mean: one event pair around a continuous loop of replays covering at
+    least `min_calls` calls and `min_seconds` (after 3 untimed replays);
+    spread: a second loop of as many replays, each between its own pair of
+    events, whose per-call times give p10/p50/p90."""
+    import torch
+    g = capture_graph(body, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    est = e0.elapsed_time(e1) / 10 / 1e3               # seconds per replay
+    reps = max(-(-min_calls // calls_per_body), int(np.ceil(min_seconds / max(est, 1e-7))))
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    mean_ms = e0.elapsed_time(e1) / (reps * calls_per_body)
+    nrep = max(-(-min_calls // calls_per_body), 50)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nrep + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(nrep):
+            g.replay()
+            ev[i + 1].record(stream)
+    stream.synchronize()
+    per = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(nrep)]) / calls_per_body
+    return {"mean_ms": float(mean_ms), "calls": int(reps * calls_per_body),
+            "p10_ms": float(np.percentile(per, 10)), "p50_ms": float(np.percentile(per, 50)),
+            "p90_ms": float(np.percentile(per, 90)), "spread_calls": int(nrep * calls_per_body)}
 
 
 def _time_loop(fn, stream, K, per_graph=20):

@@ -330,6 +330,22 @@ SPEC_API spec_status_t spec_verify_selftest_exp2(const float* x, float* y_fma, f
 SPEC_API uint64_t spec_verify_launch_count(void);
 
 /*
+ * Diagnostic control of the bounded waits (no counterpart in the pages).
+ *
+ * Every wait of the verification kernels on their own bulk copies gives up
+ * after a limit (0.2 s by default): the CTA then sets SPEC_FLAG_TIMEOUT,
+ * stops copying, waits (with the default limit) for the copies it has in
+ * flight and finishes its control flow, so the call completes with
+ * unspecified outputs and the flag raised instead of hanging.  This sets the
+ * limit used by calls of spec_verify_sample, spec_verify_greedy,
+ * spec_verify_tree_greedy and spec_verify_greedy_noalloc enqueued afterwards,
+ * process-wide; limit_ns = 0 restores the default.  A limit shorter than a
+ * copy's latency (a few hundred ns) makes the waits give up, which is how a
+ * test exercises that path.  Not for production use.
+ */
+SPEC_API void spec_verify_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
  * Greedy verification without any allocation (no counterpart in the pages:
  * this is a deployment convenience, not part of the method).
  *

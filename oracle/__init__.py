@@ -60,8 +60,10 @@ def _bind(lib):
     I = ctypes.c_int
     D = ctypes.c_double
     lib.oracle_verify_sample.argtypes = [P, P, I, P, P, P, D, I, I, I,
-                                         P, P, P, P, P, P, P, P]
+                                         P, P, P, P, P, P, P, P, D, P]
     lib.oracle_verify_sample.restype = I
+    lib.oracle_sample_claim.argtypes = [P, P, I, P, P, P, D, I, I, I, P, P, P, P]
+    lib.oracle_sample_claim.restype = I
     lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P]
     lib.oracle_verify_greedy.restype = I
     lib.oracle_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P]
@@ -119,11 +121,19 @@ def _check(rc):
         raise OracleError(f"oracle error {rc}: {ERRORS.get(rc, '?')}")
 
 
-def verify_sample(target, draft, tokens, u_accept, u_sample, temperature, dtype="f32", lib=None):
+FLAG_WINDOW = 1e-6
+
+
+def verify_sample(target, draft, tokens, u_accept, u_sample, temperature, dtype="f32", lib=None,
+                  window=FLAG_WINDOW):
     """Sampling verification over a batch.  Returns a dict of numpy arrays.
 
     target [B, k+1, V], draft [B, k, V] (float32, or uint16 bf16 bits);
     tokens int32 [B, k]; u_accept float32 [B, k]; u_sample float32 [B].
+    Besides the outputs of the method, the dict holds the diagnostics
+    ``acc_margin``, ``cdf_margin`` (distance of the uniforms to the nearest
+    decision boundary), ``fallback`` (reading R6 applied) and ``flag_prob``
+    (chance that fresh uniforms put a margin below ``window``).
     """
     lib = lib or _load()
     target = _logits(target, dtype)
@@ -142,15 +152,44 @@ def verify_sample(target, draft, tokens, u_accept, u_sample, temperature, dtype=
         acc_margin=np.zeros(B, np.float64),
         cdf_margin=np.zeros(B, np.float64),
         fallback=np.zeros(B, np.int32),
+        flag_prob=np.zeros(B, np.float64),
     )
     rc = lib.oracle_verify_sample(
         _ptr(target), _ptr(draft), _dtype_code(dtype), _ptr(tokens), _ptr(u_accept),
         _ptr(u_sample), float(temperature), B, k, V,
         _ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out["p"]), _ptr(out["q"]),
         _ptr(out["resid_mass"]), _ptr(out["acc_margin"]), _ptr(out["cdf_margin"]),
-        _ptr(out["fallback"]))
+        _ptr(out["fallback"]), float(window), _ptr(out["flag_prob"]))
     _check(rc)
     return out
+
+
+def sample_claim(target, draft, tokens, u_accept, u_sample, temperature, claim_len, claim_tok,
+                 dtype="f32", lib=None):
+    """How far a claimed outcome (accepted length, token drawn at that
+    position) of sampling verification is from the exact float64 outcome:
+    returns ``(violation, claim_R)`` per sequence.  ``violation`` is 0 for the
+    exact outcome, +inf for an outcome no rounding can produce, else the
+    largest distance of a uniform to the boundary the claim puts it across
+    (acceptance scale, or CDF scale divided by R).  ``claim_R`` is the residual
+    mass of the claimed distribution (0 for the bonus draw)."""
+    lib = lib or _load()
+    target = _logits(target, dtype)
+    B, k1, V = target.shape
+    k = k1 - 1
+    draft = _logits(draft if draft is not None else np.zeros((B, 0, V)), dtype)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, k)
+    u_accept = np.ascontiguousarray(u_accept, dtype=np.float32).reshape(B, k)
+    u_sample = np.ascontiguousarray(u_sample, dtype=np.float32).reshape(B)
+    cl = np.ascontiguousarray(claim_len, dtype=np.int32).reshape(B)
+    ct = np.ascontiguousarray(claim_tok, dtype=np.int32).reshape(B)
+    viol = np.zeros(B, np.float64)
+    cR = np.zeros(B, np.float64)
+    rc = lib.oracle_sample_claim(
+        _ptr(target), _ptr(draft), _dtype_code(dtype), _ptr(tokens), _ptr(u_accept),
+        _ptr(u_sample), float(temperature), B, k, V, _ptr(cl), _ptr(ct), _ptr(viol), _ptr(cR))
+    _check(rc)
+    return viol, cR
 
 
 def verify_greedy(target, tokens, dtype="f32", lib=None):
@@ -256,7 +295,9 @@ def tree_grow(logits, temperature, M, dtype="bf16", lib=None):
     """EAGLE-2 tree growth (reading R12 of spec_oracle.c).  ``logits``
     [B, D, K, V] draft rows by layer and frontier slot.  Returns dict with
     tokens, parents, depth [B, M+1] int32, values [B, M+1] float64 and
-    min_gap [B] (smallest value gap at a selection boundary)."""
+    min_gap [B] (smallest gap between a kept and a dropped value that are not
+    equal, over every selection boundary; exact ties are decided by the tie
+    rule)."""
     lib = lib or _load()
     z = _logits(logits, dtype)
     B, D, K, V = z.shape

@@ -138,6 +138,53 @@ static int inverse_cdf(const double* w, int V, double u, double* total_out,
   return tok;
 }
 
+/* Measure of the set of u in [0, 1) within `window` of at least one point of
+ * b[0..n) (points sorted ascending): a union of intervals of half-width
+ * `window` around each point, clipped to [0, 1). */
+static double near_points_measure(const double* b, int n, double window) {
+  double total = 0.0, lo = 0.0, hi = -1.0;
+  for (int i = 0; i < n; ++i) {
+    double a = b[i] - window, c = b[i] + window;
+    if (a < 0.0) a = 0.0;
+    if (c > 1.0) c = 1.0;
+    if (c <= a) continue;
+    if (hi < 0.0 || a > hi) { /* a new interval starts */
+      if (hi > lo) total += hi - lo;
+      lo = a;
+      hi = c;
+    } else if (c > hi) {
+      hi = c;
+    }
+  }
+  if (hi > lo) total += hi - lo;
+  return total;
+}
+
+/* Chance, over a uniform u in [0, 1), that the inverse-CDF draw of R5 over
+ * the weights w[0..V) lands within window*R of a cumulative value (the
+ * boundary set C_{-1} = 0, C_0, ..., C_{V-1} = R, divided by R).  `scratch`
+ * holds V + 1 doubles. */
+static double cdf_flag_measure(const double* w, int V, double window, double* scratch) {
+  double R = 0.0;
+  for (int j = 0; j < V; ++j) R += w[j];
+  if (!(R > 0.0)) return 0.0;
+  double c = 0.0;
+  scratch[0] = 0.0;
+  for (int j = 0; j < V; ++j) {
+    c += w[j];
+    scratch[j + 1] = c / R;
+  }
+  return near_points_measure(scratch, V + 1, window);
+}
+
+/* Chance, over a uniform u in [0, 1), that u lies within `window` of the
+ * acceptance threshold p/q (0 where the decision cannot depend on u). */
+static double accept_flag_measure(double p, double q, double window) {
+  if (!(q > 0.0) || !(p > 0.0)) return 0.0;
+  double a = p / q;
+  return near_points_measure(&a, 1, window);
+}
+
 /*
  * Sampling verification, one call over B sequences.
  *
@@ -157,7 +204,11 @@ static int inverse_cdf(const double* w, int V, double u, double* total_out,
  * every position; resid_mass [B] (R of the rejected row, 0 when all accepted).
  * Diagnostics: acc_margin [B] = min over decided positions i <= n of
  * |u_i - p_i/q_i| (infinite where the decision is forced); cdf_margin [B];
- * fallback [B] = 1 where R6 applied.  Any diagnostic pointer may be NULL.
+ * fallback [B] = 1 where R6 applied; flag_prob [B] = the chance, over fresh
+ * uniforms and given the row's decided positions and drawn distribution,
+ * that one of the margins falls below `window` (the acceptance measures of
+ * the decided positions plus the CDF boundary measure, capped at 1).  Any
+ * diagnostic pointer may be NULL.
  */
 int oracle_verify_sample(const void* target, const void* draft, int dtype,
                          const int32_t* tokens, const float* u_accept,
@@ -165,14 +216,15 @@ int oracle_verify_sample(const void* target, const void* draft, int dtype,
                          int V, int32_t* accepted_len, int32_t* out_tokens,
                          double* p_out, double* q_out, double* resid_mass,
                          double* acc_margin, double* cdf_margin,
-                         int32_t* fallback) {
+                         int32_t* fallback, double window, double* flag_prob) {
   if (B < 0 || k < 0 || V < 1 || !(temperature > 0.0) || !isfinite(temperature))
     return OR_ERR_ARG;
   if (dtype != OR_F32 && dtype != OR_BF16) return OR_ERR_ARG;
   double* pt = (double*)malloc(sizeof(double) * (size_t)(k + 1) * (size_t)V);
   double* pd = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * (size_t)V);
   double* r = (double*)malloc(sizeof(double) * (size_t)V);
-  if (!pt || !pd || !r) { free(pt); free(pd); free(r); return OR_ERR_NOMEM; }
+  double* cb = (double*)malloc(sizeof(double) * ((size_t)V + 1));
+  if (!pt || !pd || !r || !cb) { free(pt); free(pd); free(r); free(cb); return OR_ERR_NOMEM; }
   int rc = OR_OK;
   for (int b = 0; b < B && rc == OR_OK; ++b) {
     /* probabilities of every row of this sequence */
@@ -191,7 +243,7 @@ int oracle_verify_sample(const void* target, const void* draft, int dtype,
 
     /* accept test left to right, stop at the first rejection */
     int n = k;
-    double amarg = INFINITY;
+    double amarg = INFINITY, fprob = 0.0;
     for (int i = 0; i < k; ++i) {
       int32_t x = tokens[(size_t)b * k + i];
       double p = pt[(size_t)i * V + x];
@@ -205,6 +257,7 @@ int oracle_verify_sample(const void* target, const void* draft, int dtype,
       double q = pd[(size_t)i * V + x];
       double u = (double)u_accept[(size_t)b * k + i];
       if (q > 0.0 && p > 0.0) amarg = fmin(amarg, fabs(u - p / q));
+      fprob += accept_flag_measure(p, q, window);
       if (!(u * q < p)) { n = i; break; }
     }
 
@@ -224,9 +277,11 @@ int oracle_verify_sample(const void* target, const void* draft, int dtype,
         memcpy(r, pt + (size_t)n * V, sizeof(double) * (size_t)V);
       }
       tok = inverse_cdf(r, V, (double)u_sample[b], &R, &cmarg);
+      fprob += cdf_flag_measure(r, V, window, cb);
       if (fb) R = 0.0;
     } else {
       tok = inverse_cdf(pt + (size_t)k * V, V, (double)u_sample[b], &R, &cmarg);
+      fprob += cdf_flag_measure(pt + (size_t)k * V, V, window, cb);
       R = 0.0;
     }
 
@@ -241,6 +296,111 @@ int oracle_verify_sample(const void* target, const void* draft, int dtype,
     if (acc_margin) acc_margin[b] = amarg;
     if (cdf_margin) cdf_margin[b] = cmarg;
     if (fallback) fallback[b] = fb;
+    if (flag_prob) flag_prob[b] = fprob < 1.0 ? fprob : 1.0;
+  }
+  free(pt);
+  free(pd);
+  free(r);
+  free(cb);
+  return rc;
+}
+
+/* Distance from x to the half-open interval [lo, hi) (0 inside). */
+static double dist_to_interval(double x, double lo, double hi) {
+  if (x < lo) return lo - x;
+  if (x >= hi) return x - hi;
+  return 0.0;
+}
+
+/*
+ * How far a claimed outcome of sampling verification is from the exact
+ * (float64) outcome of R3-R6, for every sequence.  Two correct
+ * implementations that round differently may only disagree where a uniform
+ * sits closer to a decision boundary than their rounding error; this
+ * measures how close the claim needs that to be.
+ *
+ * The claim is (claim_len[b], claim_tok[b]): the accepted length and the
+ * token drawn at that position.  violation[b] is 0 when the claim is the
+ * exact outcome; +inf when no rounding can produce it (a decision the
+ * uniform cannot reach, a length outside [0, k], a drawn token of zero
+ * weight); else the largest of
+ *   |u_i - p_i/q_i| over the positions whose claimed decision differs from
+ *   the exact one (claimed accepted at i < claim_len, rejected at claim_len),
+ *   and
+ *   the distance from u*R to [C_{t-1}, C_t), divided by R, for the claimed
+ *   token t and the claimed distribution (the residual of row claim_len
+ *   after a rejection, with R6's fallback; else p of the bonus row).
+ * claim_R[b] receives R of the claimed distribution as resid_mass reports it
+ * (0 for the bonus draw and for the fallback).
+ */
+int oracle_sample_claim(const void* target, const void* draft, int dtype, const int32_t* tokens,
+                        const float* u_accept, const float* u_sample, double temperature, int B,
+                        int k, int V, const int32_t* claim_len, const int32_t* claim_tok,
+                        double* violation, double* claim_R) {
+  if (B < 0 || k < 0 || V < 1 || !(temperature > 0.0) || !isfinite(temperature))
+    return OR_ERR_ARG;
+  if (dtype != OR_F32 && dtype != OR_BF16) return OR_ERR_ARG;
+  double* pt = (double*)malloc(sizeof(double) * (size_t)(k + 1) * (size_t)V);
+  double* pd = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * (size_t)V);
+  double* r = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!pt || !pd || !r) { free(pt); free(pd); free(r); return OR_ERR_NOMEM; }
+  int rc = OR_OK;
+  for (int b = 0; b < B && rc == OR_OK; ++b) {
+    for (int i = 0; i <= k && rc == OR_OK; ++i)
+      rc = softmax_row(target, dtype, ((size_t)b * (size_t)(k + 1) + (size_t)i) * (size_t)V,
+                       V, temperature, pt + (size_t)i * V);
+    for (int i = 0; i < k && rc == OR_OK; ++i)
+      rc = softmax_row(draft, dtype, ((size_t)b * (size_t)k + (size_t)i) * (size_t)V, V,
+                       temperature, pd + (size_t)i * V);
+    if (rc != OR_OK) break;
+    const int n = claim_len[b];
+    if (n < 0 || n > k) {
+      violation[b] = INFINITY;
+      claim_R[b] = 0.0;
+      continue;
+    }
+    /* the claim's decisions: accepted at i < n, rejected at n (when n < k) */
+    double viol = 0.0;
+    for (int i = 0; i < k && i <= n; ++i) {
+      const int32_t x = tokens[(size_t)b * k + i];
+      if (x < 0 || x >= V) { rc = OR_ERR_TOKEN; break; }
+      const double p = pt[(size_t)i * V + x];
+      const double q = pd[(size_t)i * V + x];
+      const double u = (double)u_accept[(size_t)b * k + i];
+      const int accepted = (u * q < p);
+      const int claimed = (i < n);
+      if (accepted == claimed) continue;
+      viol = fmax(viol, (q > 0.0 && p > 0.0) ? fabs(u - p / q) : INFINITY);
+    }
+    if (rc != OR_OK) break;
+    /* the claimed distribution, and where the claimed token's CDF interval is */
+    const double* w = pt + (size_t)k * V;
+    int fb = 0;
+    if (n < k) {
+      double tot = 0.0;
+      for (int j = 0; j < V; ++j) {
+        const double d = pt[(size_t)n * V + j] - pd[(size_t)n * V + j];
+        r[j] = d > 0.0 ? d : 0.0;
+        tot += r[j];
+      }
+      if (!(tot > 0.0)) { /* R6 */
+        fb = 1;
+        memcpy(r, pt + (size_t)n * V, sizeof(double) * (size_t)V);
+      }
+      w = r;
+    }
+    double tot = 0.0;
+    for (int j = 0; j < V; ++j) tot += w[j];
+    const int t = claim_tok[b];
+    if (t < 0 || t >= V || !(w[t] > 0.0) || !(tot > 0.0)) {
+      viol = INFINITY;
+    } else {
+      double c0 = 0.0;
+      for (int j = 0; j < t; ++j) c0 += w[j];
+      viol = fmax(viol, dist_to_interval((double)u_sample[b] * tot, c0, c0 + w[t]) / tot);
+    }
+    violation[b] = viol;
+    claim_R[b] = (n < k && !fb) ? tot : 0.0;
   }
   free(pt);
   free(pd);
@@ -517,11 +677,28 @@ int oracle_lm_head_greedy(const uint16_t* hidden, const uint16_t* w_lm, const in
  *
  * logits [B, D, K, V] (draft rows by layer and frontier slot), T, node
  * budget M.  Outputs [B, M+1]: tokens (root -1), parents (root -1), depth,
- * values (float64).  Also reports, per tree, the smallest value gap at any
- * selection boundary (frontier cut or final cut; +inf if none) in min_gap.
+ * values (float64).  Also reports, per tree, the smallest gap between a kept
+ * and a dropped value at any selection boundary (frontier cut or final cut),
+ * counting only unequal values (exact ties are decided by the tie rule), in
+ * min_gap (+inf if none).
  */
 static int cand_before(double va, int ca, double vb, int cb) {
   return va > vb || (va == vb && ca < cb); /* higher value, then earlier creation */
+}
+
+/* The smallest difference between a kept and a dropped value that are not
+ * equal, at a cut keeping the first `keep` of the n entries of `order`
+ * (sorted by value, highest first; 0 < keep < n); +inf if every such pair is
+ * equal.  Equal values are ordered by the tie rule, exactly; unequal ones
+ * this close could swap under a rounding of the values. */
+static double cut_gap(const double* val, const int32_t* order, int n, int keep) {
+  const double vk = val[order[keep - 1]], vd = val[order[keep]];
+  double g = INFINITY;
+  for (int j = keep; j < n; ++j) /* the highest dropped value below the lowest kept */
+    if (val[order[j]] < vk) { g = vk - val[order[j]]; break; }
+  for (int i = keep - 1; i >= 0; --i) /* the lowest kept value above the highest dropped */
+    if (val[order[i]] > vd) { if (val[order[i]] - vd < g) g = val[order[i]] - vd; break; }
+  return g;
 }
 
 int oracle_tree_grow(const void* logits, int dtype, int B, int D, int K, int V, double T, int M,
@@ -576,7 +753,7 @@ int oracle_tree_grow(const void* logits, int dtype, int B, int D, int K, int V, 
             }
         nfront = nc < K ? nc : K;
         for (int j = 0; j < nfront; ++j) front[j] = order[j];
-        if (nc > K) { double g = val[order[K - 1]] - val[order[K]]; if (g < gap) gap = g; }
+        if (nc > K) { double g = cut_gap(val, order, nc, K); if (g < gap) gap = g; }
       }
     }
     if (rc != OR_OK) break;
@@ -588,7 +765,7 @@ int oracle_tree_grow(const void* logits, int dtype, int B, int D, int K, int V, 
         if (cand_before(val[order[c]], order[c], val[order[a]], order[a])) {
           int t = order[a]; order[a] = order[c]; order[c] = t;
         }
-    if (nn > M && M > 0) { double g = val[order[M - 1]] - val[order[M]]; if (g < gap) gap = g; }
+    if (nn > M && M > 0) { double g = cut_gap(val, order, nn, M); if (g < gap) gap = g; }
     for (int c = 0; c < n; ++c) newid[c] = -1;
     newid[0] = 0;
     for (int c = 0; c < M; ++c) newid[order[c]] = 1; /* mark */

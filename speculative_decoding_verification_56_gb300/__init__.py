@@ -100,6 +100,8 @@ def load_library(path: str = LIB_PATH):
         lib.spec_verify_read_flags.restype = I
         lib.spec_verify_launch_count.argtypes = []
         lib.spec_verify_launch_count.restype = ctypes.c_uint64
+        lib.spec_verify_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.spec_verify_set_wait_limit_ns.restype = None
         lib.spec_status_string.argtypes = [I]
         lib.spec_status_string.restype = ctypes.c_char_p
         lib.spec_verify_abi_version.argtypes = []
@@ -175,6 +177,13 @@ def spec_verify_launch_count() -> int:
 
 def spec_verify_abi_version() -> int:
     return int(load_library().spec_verify_abi_version())
+
+
+def spec_verify_set_wait_limit_ns(limit_ns: int) -> None:
+    """Limit of the verification kernels' waits on their bulk copies for calls
+    enqueued afterwards (0 restores the default 0.2 s); a diagnostic control
+    for testing the timeout path."""
+    load_library().spec_verify_set_wait_limit_ns(int(limit_ns))
 
 
 def spec_verify_sample(target_logits, draft_logits, draft_tokens, u_accept, u_sample,

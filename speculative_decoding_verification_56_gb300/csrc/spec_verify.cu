@@ -28,6 +28,9 @@ static_assert(sv::kMaxDraft == SPEC_MAX_K, "finish kernel buffers are sized for 
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+// limit of the verification kernels' waits on their bulk copies
+// (spec_verify_set_wait_limit_ns)
+std::atomic<uint64_t> g_wait_limit_ns{sv::kWaitLimitNs};
 
 constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 256;
@@ -326,6 +329,7 @@ constexpr double kKeepBytes = 80.0 * (1 << 20);
 template <typename E>
 spec_status_t run_sample(sv::SampleParams prm, int rows, bool vec, void* stream) {
   prm.items = rows * prm.nchunks;
+  prm.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   {
     const double pair = 2.0 * prm.B * (double)prm.V * sizeof(typename E::storage);
     prm.keep_pos = pair > 0 ? std::min(prm.k + 1, (int)(kKeepBytes / pair)) : 0;
@@ -346,6 +350,7 @@ spec_status_t run_sample(sv::SampleParams prm, int rows, bool vec, void* stream)
 template <typename E>
 spec_status_t run_argmax(sv::ArgmaxParams prm, int rows, bool vec, void* stream) {
   prm.items = rows * prm.nchunks;
+  prm.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   if (vec) {
     int grid = 0;
     spec_status_t st = persistent_grid<sv::stream_argmax_kernel<E>>(prm.items, &grid);
@@ -677,6 +682,7 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   prm.flags = lp.flags;
   prm.part = lp.part;
   prm.rowarg = reinterpret_cast<int32_t*>(ws + L.off_arg);
+  prm.wait_ns = sv::kWaitLimitNs;
   return launch(sv::argmax_resolve_kernel, B, 0, prm, stream, true);
 }
 
@@ -800,6 +806,10 @@ spec_status_t spec_verify_selftest_exp2(const float* x, float* y_fma, float* y_s
 }
 
 uint64_t spec_verify_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void spec_verify_set_wait_limit_ns(uint64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns == 0 ? sv::kWaitLimitNs : limit_ns, std::memory_order_relaxed);
+}
 
 const char* spec_status_string(int status) {
   switch (status) {

@@ -21,6 +21,7 @@ constexpr int kChunkBytes = kVecPerChunk * 16;
 constexpr int kStages = 3;                              // bulk-copy ring depth per CTA
 constexpr int kRefEmpty = -(1 << 30);                   // reference of an empty slice
 constexpr uint64_t kWaitLimitNs = 200000000ull;         // 0.2 s per bulk-copy wait
+constexpr uint32_t kSuspendHintNs = 1000000u;           // longest sleep inside one try_wait
 
 // Flag bits (mirrors include/spec_verify.h).
 constexpr unsigned kFlagTokenRange = 1u;
@@ -341,16 +342,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Test a barrier phase; the thread may sleep up to ~1 ms in the instruction
-// while the phase is incomplete (woken when it completes), so waiting warps
-// do not spin through the issue slots.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+// Test a barrier phase; the thread may sleep up to `hint_ns` (at most ~1 ms)
+// in the instruction while the phase is incomplete (woken when it completes),
+// so waiting warps do not spin through the issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity,
+                                              uint32_t hint_ns = kSuspendHintNs) {
   uint32_t done;
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return done != 0;
 }
@@ -361,13 +363,17 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for a barrier phase; give up after kWaitLimitNs (returns false).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Wait for a barrier phase; give up after limit_ns (returns false).  With the
+// default limit a sleeping try_wait is woken by the phase's completion; a
+// shorter limit also shortens each sleep, so that the limit is observed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  const uint32_t hint = limit_ns < kSuspendHintNs ? (uint32_t)limit_ns : kSuspendHintNs;
+  if (mbar_try_wait(bar, parity, hint)) return true;
   const uint64_t t0 = global_ns();
   for (unsigned it = 0; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (mbar_try_wait(bar, parity, hint)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
   }
   return false;
 }

@@ -96,6 +96,9 @@ struct SampleParams {
   FSum* csum;      // [B*nchunks]
   FSum* csum_p;    // [B*nchunks]
   float* zx;  // [rows] logit of each row's draft token, captured while it streams
+  // limit of each wait on a bulk copy (kWaitLimitNs unless a test shortens
+  // it to exercise the timeout path); drains always use kWaitLimitNs
+  unsigned long long wait_ns;
 };
 
 struct ArgmaxParams {
@@ -111,6 +114,7 @@ struct ArgmaxParams {
   unsigned* flags;
   ArgPartial* part;   // [B*rows_per_seq * nchunks]
   int32_t* rowarg;    // [B*rows_per_seq]
+  unsigned long long wait_ns;  // as SampleParams::wait_ns
 };
 
 // Row r of sequence b: r in [0, k] is target row r, r in [k+1, 2k] is draft
@@ -714,7 +718,10 @@ __device__ __forceinline__ int ring_init(Ring& ring, int i0, int i1, IssueFn iss
   return issued;
 }
 
-// Thread 0, at the end: wait (bounded) for the copies issued into each slot.
+// Thread 0, at the end: wait (bounded, with the default limit whatever the
+// limit of the loop's waits) for the copies issued into each slot.  After an
+// abort no copy is issued into a slot whose previous copy a warp gave up on
+// (ring_refill), so only the last kStages issued copies can be in flight.
 __device__ __noinline__ void ring_drain(Ring& ring, int i0, int issued) {
   for (int j = max(i0, issued - kStages); j < issued; ++j)
     mbar_wait_bounded(&ring.full[(j - i0) % kStages], (unsigned)(((j - i0) / kStages) & 1));
@@ -726,9 +733,10 @@ __device__ __noinline__ void ring_drain(Ring& ring, int i0, int issued) {
 template <typename E>
 __device__ __forceinline__ bool ring_take(Ring& ring, const uint8_t* stage_mem, int slot,
                                           unsigned par, int nvec, unsigned* flags,
-                                          uint4 (&raw)[kVecPerThread]) {
+                                          uint4 (&raw)[kVecPerThread],
+                                          uint64_t limit_ns = kWaitLimitNs) {
   bool ok = *(volatile int*)&ring.abort == 0;
-  if (ok && !mbar_wait_bounded(&ring.full[slot], par)) {
+  if (ok && !mbar_wait_bounded(&ring.full[slot], par, limit_ns)) {
     ok = false;
     ring.abort = 1;
     set_flag(flags, kFlagTimeout);
@@ -746,16 +754,22 @@ __device__ __forceinline__ bool ring_take(Ring& ring, const uint8_t* stage_mem, 
 }
 
 // Thread 0: once every warp has released `slot` (phase parity `par`), reuse
-// it for item `nxt` (if any).  Returns the new count of issued items.
+// it for item `nxt` (if any).  Returns the new count of issued items.  A warp
+// that gives up on a copy sets ring.abort before it releases the slot, and
+// the release orders that write before this thread's wait returns, so the
+// second check below never lets a copy land on a slot whose previous copy may
+// still be in flight.
 template <typename IssueFn>
 __device__ __forceinline__ int ring_refill(Ring& ring, int slot, unsigned par, int nxt, int i1,
-                                           int issued, unsigned* flags, IssueFn issue) {
+                                           int issued, unsigned* flags, IssueFn issue,
+                                           uint64_t limit_ns = kWaitLimitNs) {
   if (nxt >= i1 || *(volatile int*)&ring.abort) return issued;
-  if (!mbar_wait_bounded(&ring.empty[slot], par)) {
+  if (!mbar_wait_bounded(&ring.empty[slot], par, limit_ns)) {
     ring.abort = 1;
     set_flag(flags, kFlagTimeout);
     return issued;
   }
+  if (*(volatile int*)&ring.abort) return issued;
   issue(nxt, slot);
   return nxt + 1;
 }
@@ -803,9 +817,10 @@ __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleP
   for (int it = i0; it < i1; ++it) {
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     uint4 raw[kVecPerThread];
-    const bool ok = ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw);
+    const bool ok =
+        ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw, p.wait_ns);
     if (threadIdx.x == 0)
-      issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
+      issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue, p.wait_ns);
     if (ok) {
       stats_chunk<E>(raw, p.scale, st);
       capture_token<E>(p, raw, tok, j0, j1, row);
@@ -867,9 +882,10 @@ __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const Argmax
   for (int it = i0; it < i1; ++it) {
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     uint4 raw[kVecPerThread];
-    const bool ok = ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw);
+    const bool ok =
+        ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw, p.wait_ns);
     if (threadIdx.x == 0)
-      issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
+      issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue, p.wait_ns);
     if (ok) argmax_chunk<E>(raw, j0, st);
     const bool row_end = (c + 1 == C);
     if (row_end || it + 1 == i1) {
@@ -1435,8 +1451,12 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
 
   // 3. prefix structure of this CTA's chunks: even local chunks through
   // registers, odd ones through the staging buffer (bulk async copies)
+  // thread 0 keeps at most one staging copy (pair) in flight; stage_pending
+  // is the barrier parity of the one it has not yet seen land (-1: none)
+  int stage_pending = -1;
   auto stage_issue = [&](int lc) {  // thread 0
     const int c = rank + kClusterCTAs * lc;
+    stage_pending = (lc >> 1) & 1;
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     const unsigned bytes = (unsigned)(j1 - j0) * (unsigned)sizeof(St);
     mbar_expect_tx(&s_bar, resid ? 2 * bytes : bytes);
@@ -1453,9 +1473,11 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
     const int nvec = (j1 - j0 + E::kEPV - 1) / E::kEPV;
     uint4 vt[kVecPerThread], vd[kVecPerThread];
     if (kVec && (lc & 1)) {
-      if (!mbar_wait_bounded(&s_bar, (unsigned)(lc >> 1) & 1u)) {
+      if (!mbar_wait_bounded(&s_bar, (unsigned)(lc >> 1) & 1u, p.wait_ns)) {
         stage_ok = false;
         if (threadIdx.x == 0) set_flag(p.flags, kFlagTimeout);
+      } else if (threadIdx.x == 0) {
+        stage_pending = -1;
       }
 #pragma unroll
       for (int q = 0; q < kVecPerThread; ++q) {
@@ -1545,10 +1567,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   }
   cluster.sync();  // no CTA reads a peer's shared memory after this point
 
-  // a staging copy whose wait ran out may still be in flight: wait again
-  // (bounded) before leaving
-  if (kVec && !stage_ok && threadIdx.x == 0)
-    for (int ph = 0; ph < 2; ++ph) mbar_wait_bounded(&s_bar, (unsigned)ph);
+  // a staging copy whose wait ran out may still be in flight: wait for it
+  // again (bounded, with the default limit) before leaving
+  if (kVec && threadIdx.x == 0 && stage_pending >= 0)
+    mbar_wait_bounded(&s_bar, (unsigned)stage_pending);
 
   // 5. the owner of the chosen chunk walks it
   const int cstar = s_c;

@@ -66,7 +66,7 @@ def oracle_sample(c, rows=None):
 def sample_parity(c, rows=None, allow_flags=None, ws=None):
     g = gpu_sample(c, ws=ws)
     o = oracle_sample(c, rows)
-    return ph.compare_sample(g, o, rows=rows, allow_flags=allow_flags, V=c.V), g, o
+    return ph.compare_sample(g, o, rows=rows, allow_flags=allow_flags, case=c), g, o
 
 
 # ---------------------------------------------------------------------------
@@ -92,11 +92,13 @@ def test_sample_zipf128k_full():
     assert 0 < (g["accepted_len"] < c.k).sum() < c.B
 
 
-def test_sample_zipf152k_sampled_rows():
+def test_sample_zipf152k_full():
+    # every one of the 256 sequences (3840 rows of 151936 logits) against the
+    # float64 oracle
     c = synth.zipf152k(seed=0)
-    rows = np.arange(0, c.B, 11)          # 24 sequences spread over the batch
-    s, g, _ = sample_parity(c, rows=rows)
-    # properties that hold at any size, checked on every row
+    s, g, _ = sample_parity(c)
+    assert s["rows"] == c.B
+    # properties that hold at any size
     n = g["accepted_len"]
     assert ((n >= 0) & (n <= c.k)).all()
     for b in range(c.B):
@@ -126,7 +128,9 @@ def test_sample_flag_rate_many_rows():
     c = synth.make_chain_case(B=20000, k=4, V=96, dtype="f32", temperature=1.0,
                               target_sigma=1.5, draft_noise=0.7, seed=11)
     s, _, _ = sample_parity(c)
-    assert s["flagged"] <= 2
+    # the flagged count stays within the Poisson bound of the exact law's
+    # own expectation (about 2.9 of these 20000 rows)
+    assert s["flagged"] <= s["flag_allowance"]
 
 
 # ---------------------------------------------------------------------------
@@ -203,7 +207,7 @@ def test_sample_zero_probabilities_and_fallback():
     flags = sv.spec_verify_read_flags(ws)
     g = {k: v.cpu().numpy() for k, v in out.items()}
     o = oracle_sample(c)
-    ph.compare_sample(g, o, allow_flags=0)
+    ph.compare_sample(g, o, allow_flags=0, case=c)
     assert g["accepted_len"][0] == 0 and g["accepted_len"][1] == 2
     assert o["fallback"][2] == 1 and flags & sv.SPEC_FLAG_RESIDUAL_FALLBACK
 
@@ -222,7 +226,8 @@ def test_sample_invalid_token_sets_flag():
     ok = np.array([0, 3])
     o = oracle.verify_sample(c.target[ok], c.draft[ok], c.tokens[ok], c.u_accept[ok],
                              c.u_sample[ok], 1.0)
-    ph.compare_sample({k: v.cpu().numpy() for k, v in out.items()}, o, rows=ok, allow_flags=0)
+    ph.compare_sample({k: v.cpu().numpy() for k, v in out.items()}, o, rows=ok, allow_flags=0,
+                      case=c)
 
 
 # ---------------------------------------------------------------------------
@@ -362,7 +367,7 @@ def test_inputs_written_by_the_kernel_just_before():
         torch.add(t_src, 0, out=t)             # the kernel right before the call
         out = sv.verify_sample(t, d, tok, x["ua"], x["us"], c.temperature, workspace=ws)
         g = {k: v.cpu().numpy() for k, v in out.items()}
-        ph.compare_sample(g, o, V=c.V)
+        ph.compare_sample(g, o, case=c)
         t.zero_()
         d.zero_()
         tok.zero_()
@@ -406,7 +411,7 @@ def test_three_calls_on_three_streams():
         gtr = sv.verify_tree_greedy(tt, ttok, tpar, t.max_depth,
                                     workspace=ws[sv.SPEC_MODE_TREE_GREEDY], stream=streams[2])
         torch.cuda.synchronize()
-        ph.compare_sample({k: v.cpu().numpy() for k, v in gs.items()}, o, V=c.V)
+        ph.compare_sample({k: v.cpu().numpy() for k, v in gs.items()}, o, case=c)
         ph.compare_exact({k: v.cpu().numpy() for k, v in gg.items()}, og,
                          ["accepted_len", "out_tokens"])
         ph.compare_exact({k: v.cpu().numpy() for k, v in gtr.items()}, ot,

@@ -206,6 +206,12 @@ def test_kv_commit_after_tree_verification():
 # EAGLE-2 tree growth
 # ---------------------------------------------------------------------------
 
+# Node values are sums of float64 logarithms that the GPU and the oracle round
+# differently (a few 1e-15 relative); two unequal values closer than this at a
+# selection cut may swap.
+GROW_GAP = 1e-9
+
+
 def _gpu_grow(z, dtype, T, M):
     t = sv.to_device_logits(z, dtype)
     out = sv.tree_grow(t, T, M)
@@ -225,8 +231,25 @@ def test_tree_grow_matches_oracle(B, D, K, V, M, T, dtype, seed):
     z = synth.make_grow_logits(B=B, D=D, K=K, V=V, dtype=dtype, seed=seed)
     ref = oracle.tree_grow(z, T, M, dtype=dtype)
     got = _gpu_grow(z, dtype, T, M)
-    ok = ref["min_gap"] > 1e-9          # trees with a near-tie at a cut may differ
-    assert ok.mean() >= 0.5
+    # a tree may differ only where two unequal values meet at a cut closer
+    # than GROW_GAP (exact ties are decided by the tie rule and compared)
+    ok = ref["min_gap"] > GROW_GAP
+    assert ok.mean() >= 0.9
+    for key in ("tokens", "parents", "depth"):
+        assert np.array_equal(got[key][ok], ref[key][ok]), key
+    assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)
+
+
+def test_tree_grow_full_workload():
+    # the benchmark's grow workload: 16 trees, 6 layers x 8 frontier rows over
+    # V = 128256 bf16, budget 59; exact ties between siblings (equal bf16
+    # logits) are compared, since the tie rule decides them
+    B, D, K, V, M = 16, 6, 8, 128256, 59
+    z = synth.make_grow_logits(B=B, D=D, K=K, V=V, seed=0)
+    ref = oracle.tree_grow(z, 1.0, M, dtype="bf16")
+    got = _gpu_grow(z, "bf16", 1.0, M)
+    ok = ref["min_gap"] > GROW_GAP
+    assert ok.mean() >= 0.9, ref["min_gap"]
     for key in ("tokens", "parents", "depth"):
         assert np.array_equal(got[key][ok], ref[key][ok]), key
     assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)
@@ -247,8 +270,8 @@ def test_tree_grow_tied_block(B, D, K, V, M, dtype):
     ref = oracle.tree_grow(z, 1.0, M, dtype=dtype)
     got = _gpu_grow(z, dtype, 1.0, M)
     assert set(np.unique(ref["tokens"][:, 1:])) <= set(range(K))
-    ok = ref["min_gap"] > 1e-9
-    assert ok.mean() >= 0.5
+    ok = ref["min_gap"] > GROW_GAP
+    assert ok.mean() >= 0.9
     for key in ("tokens", "parents", "depth"):
         assert np.array_equal(got[key][ok], ref[key][ok]), key
     assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)
@@ -265,8 +288,8 @@ def test_tree_grow_largest_tree_and_budgets():
         out = sv.tree_grow(t, 1.0, M)
         torch.cuda.synchronize()
         got = {key: v.cpu().numpy() for key, v in out.items()}
-        ok = ref["min_gap"] > 1e-9
-        assert ok.any()
+        ok = ref["min_gap"] > GROW_GAP
+        assert ok.mean() >= 0.9 or M == 0, (M, ref["min_gap"])
         for key in ("tokens", "parents", "depth"):
             assert np.array_equal(got[key][ok], ref[key][ok]), (M, key)
         assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)

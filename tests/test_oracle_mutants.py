@@ -17,14 +17,14 @@ import test_oracle_pins as pins
 SRC = os.path.join(os.path.dirname(oracle.__file__), "spec_oracle.c")
 
 MUTANTS = {
-    "residual_sign": ("double d = pt[(size_t)n * V + j] - pd[(size_t)n * V + j];",
-                      "double d = pd[(size_t)n * V + j] - pt[(size_t)n * V + j];"),
+    "residual_sign": ("        double d = pt[(size_t)n * V + j] - pd[(size_t)n * V + j];",
+                      "        double d = pd[(size_t)n * V + j] - pt[(size_t)n * V + j];"),
     "accept_transposed": ("if (!(u * q < p)) { n = i; break; }",
                           "if (!(u * p < q)) { n = i; break; }"),
     "accept_non_strict": ("if (!(u * q < p)) { n = i; break; }",
                           "if (!(u * q <= p)) { n = i; break; }"),
-    "residual_wrong_row": ("double d = pt[(size_t)n * V + j] - pd[(size_t)n * V + j];",
-                           "double d = pt[(size_t)(n + 1) * V + j] - pd[(size_t)n * V + j];"),
+    "residual_wrong_row": ("        double d = pt[(size_t)n * V + j] - pd[(size_t)n * V + j];",
+                           "        double d = pt[(size_t)(n + 1) * V + j] - pd[(size_t)n * V + j];"),
     "bonus_wrong_row": ("tok = inverse_cdf(pt + (size_t)k * V,",
                         "tok = inverse_cdf(pt + (size_t)(k > 0 ? k - 1 : 0) * V,"),
     "temperature_dropped": ("out[j] = exp(logit_at(base, dtype, off + (size_t)j) / T - m);",
@@ -66,6 +66,20 @@ MUTANTS = {
                               "          (void)0;\n        }\n    if (nn > M && M > 0)"),
     "pq_first_row_only": ("    for (int i = 0; i < k; ++i) {\n      int32_t x = tokens[(size_t)b * k + i];\n      double p = pt[(size_t)i * V + x];\n      double q = pd[(size_t)i * V + x];\n      if (p_out)",
                           "    for (int i = 0; i < k && i < 1; ++i) {\n      int32_t x = tokens[(size_t)b * k + i];\n      double p = pt[(size_t)i * V + x];\n      double q = pd[(size_t)i * V + x];\n      if (p_out)"),
+    "cdf_margin_not_over_R": ("*margin_out = (R > 0.0) ? fmin(m0, m1) / R : 0.0;",
+                              "*margin_out = (R > 0.0) ? fmin(m0, m1) : 0.0;"),
+    "acc_margin_past_n": ("      fprob += accept_flag_measure(p, q, window);\n      if (!(u * q < p)) { n = i; break; }",
+                          "      fprob += accept_flag_measure(p, q, window);\n      if (!(u * q < p) && n == k) n = i;"),
+    "flag_prob_without_cdf": ("      fprob += cdf_flag_measure(r, V, window, cb);\n",
+                              "\n"),
+    "claim_ignores_decisions": ("      if (accepted == claimed) continue;",
+                                "      if (1) continue;"),
+    "claim_interval_off_by_one": ("      for (int j = 0; j < t; ++j) c0 += w[j];",
+                                  "      for (int j = 0; j <= t; ++j) c0 += w[j];"),
+    "grow_gap_ignores_final_cut": ("    if (nn > M && M > 0) { double g = cut_gap(val, order, nn, M); if (g < gap) gap = g; }",
+                                   "    (void)cut_gap;"),
+    "grow_gap_counts_ties": ("  const double vk = val[order[keep - 1]], vd = val[order[keep]];\n  double g = INFINITY;",
+                             "  const double vk = val[order[keep - 1]], vd = val[order[keep]];\n  double g = vk - vd;"),
     "mask_wrong_word": ("        row[cur / 32] |= 1u << (cur % 32);\n        ++d;",
                         "        row[cur % W] |= 1u << (cur % 32);\n        ++d;"),
 }
@@ -100,6 +114,9 @@ class _Variant:
     def tree_grow(self, *a, **kw):
         return oracle.tree_grow(*a, lib=self.lib, **kw)
 
+    def sample_claim(self, *a, **kw):
+        return oracle.sample_claim(*a, lib=self.lib, **kw)
+
     def expected_tokens(self, *a, **kw):
         return oracle.expected_tokens(*a, lib=self.lib, **kw)
 
@@ -130,6 +147,9 @@ def _pin_checks(o):
     yield lambda: pins.test_tree_grow_two_layers_full_expansion(o)
     yield lambda: pins.test_tree_grow_k1_is_the_greedy_chain(o)
     yield lambda: pins.test_tree_grow_structure(o, 0)
+    yield lambda: pins.test_margins_and_flag_probability_worked_example(o)
+    yield lambda: pins.test_claim_violation_worked_example(o)
+    yield lambda: pins.test_tree_grow_min_gap_worked_example(o)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

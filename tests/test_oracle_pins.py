@@ -812,3 +812,106 @@ def test_tree_grow_ties_take_the_lower_token(oracle_mod):
     assert r["tokens"][0, 1] == 2
     r = oracle_mod.tree_grow(z, 1.0, 2, dtype="f32")
     assert r["tokens"][0, 1:].tolist() == [2, 5]
+
+
+# ---------------------------------------------------------------------------
+# diagnostics that decide which sampling rows may differ, and how
+# ---------------------------------------------------------------------------
+
+def _worked_margin_case():
+    """Two drafts over V = 4, T = 1, logits = ln(probability), worked by hand.
+
+    position 0: p = (.1 .2 .3 .4), q = (.4 .3 .2 .1), draft token 0: p/q = 1/4;
+                u = 0.3 rejects (0.3 * 0.4 >= 0.1), 0.05 from the threshold.
+    position 1: p = q = (.1 .2 .3 .4), u = 0.99: 0.01 from the threshold p/q = 1,
+                but never decided (position 0 rejects).
+    residual of row 0: max(0, p - q) = (0 0 .1 .3), R = 0.4; u_sample = 0.5
+                puts u*R = 0.2 between C_2 = 0.1 and C_3 = 0.4: token 3, 0.1 from
+                C_2, i.e. 0.25 of R.
+    bonus row 2: p = 1/4 each (C = .25 .5 .75 1; u*R = 0.5 exactly on C_1).
+    """
+    ln = lambda v: np.log(np.array(v, np.float64)).astype(np.float32)
+    zt = np.stack([ln([.1, .2, .3, .4]), ln([.1, .2, .3, .4]), np.zeros(4, np.float32)])[None]
+    zd = np.stack([ln([.4, .3, .2, .1]), ln([.1, .2, .3, .4])])[None]
+    toks = np.array([[0, 3]], np.int32)
+    ua = np.array([[0.3, 0.99]], np.float32)
+    us = np.array([0.5], np.float32)
+    return zt, zd, toks, ua, us
+
+
+def test_margins_and_flag_probability_worked_example(oracle_mod):
+    zt, zd, toks, ua, us = _worked_margin_case()
+    r = oracle_mod.verify_sample(zt, zd, toks, ua, us, 1.0, window=0.01)
+    assert r["accepted_len"][0] == 0 and r["out_tokens"][0].tolist() == [3, -1, -1]
+    assert r["resid_mass"][0] == pytest.approx(0.4, rel=1e-6)
+    # acceptance margin of the decided position only (not 0.01 of position 1)
+    assert r["acc_margin"][0] == pytest.approx(abs(0.3 - 0.25), rel=1e-5)
+    # CDF margin as a fraction of R: 0.1 / 0.4
+    assert r["cdf_margin"][0] == pytest.approx(0.25, rel=1e-5)
+    # flag chance at window 0.01: the acceptance window around 1/4 (0.02) and
+    # the CDF boundaries 0, 1/4, 1 of the residual (0.01 + 0.02 + 0.01)
+    assert r["flag_prob"][0] == pytest.approx(0.06, rel=1e-5)
+
+
+def test_claim_violation_worked_example(oracle_mod):
+    zt, zd, toks, ua, us = _worked_margin_case()
+
+    def claim(n, t):
+        v, R = oracle_mod.sample_claim(zt, zd, toks, ua, us, 1.0, np.array([n]), np.array([t]))
+        return v[0], R[0]
+
+    v, R = claim(0, 3)                 # the exact outcome
+    assert v == 0.0 and R == pytest.approx(0.4, rel=1e-6)
+    v, _ = claim(0, 2)                 # u*R = 0.2 lies 0.1 past [C_1, C_2) = [0, 0.1)
+    assert v == pytest.approx(0.25, rel=1e-5)
+    assert claim(0, 0)[0] == np.inf    # zero residual weight: never drawn
+    # n = 1: accepts position 0 (0.05 from its threshold) and rejects position
+    # 1 (0.01); row 1's residual is empty, so p of row 1 is drawn (reading R6):
+    # u = 0.5 gives token 2, token 3's interval [0.6, 1) is 0.1 away
+    v, R = claim(1, 3)
+    assert v == pytest.approx(0.1, rel=1e-5) and R == 0.0
+    v, _ = claim(1, 2)
+    assert v == pytest.approx(0.05, rel=1e-5)
+    # n = 2 (bonus): only position 0 is crossed; u*R = 0.5 is C_1 exactly, so
+    # both neighbouring tokens sit at distance 0 from their interval
+    assert claim(2, 2)[0] == pytest.approx(0.05, rel=1e-5)
+    assert claim(2, 1)[0] == pytest.approx(0.05, rel=1e-5)
+    assert claim(2, 0)[0] == pytest.approx(0.25, rel=1e-5)
+    assert claim(3, 0)[0] == np.inf and claim(-1, 0)[0] == np.inf
+
+
+def _gap_case():
+    """D = 3 layers, K = 2, V = 4, T = 1, rows given as probabilities.
+
+    layer 0 (root): (.6 .38 .01 .01) -> a = 0.6, b = 0.38
+    layer 1: a's row (.5 .4 .05 .05) -> .30, .24; b's row (.7 .2 .05 .05) ->
+             .266, .076; the frontier keeps .30 and .266 and drops .24: gap
+             ln(.266/.24)
+    layer 2: both frontier rows uniform -> .075, .075 (under .30) and .0665,
+             .0665 (under .266): exact ties between siblings
+    """
+    ln = lambda v: np.log(np.array(v, np.float64)).astype(np.float32)
+    z = np.zeros((1, 3, 2, 4), np.float32)
+    z[0, 0, 0] = z[0, 0, 1] = ln([.6, .38, .01, .01])
+    z[0, 1, 0] = ln([.5, .4, .05, .05])
+    z[0, 1, 1] = ln([.7, .2, .05, .05])
+    return z
+
+
+def test_tree_grow_min_gap_worked_example(oracle_mod):
+    z = _gap_case()
+    gap = lambda M: oracle_mod.tree_grow(z, 1.0, M, dtype="f32")["min_gap"][0]
+    frontier = np.log(.266 / .24)
+    # every node kept: only the frontier cut
+    assert gap(10) == pytest.approx(frontier, rel=1e-5)
+    # M = 6 keeps .076 and drops .075: the final cut is the closer one
+    assert gap(6) == pytest.approx(np.log(.076 / .075), rel=1e-5)
+    # M = 7 splits the exact tie .075 / .075: the tie rule decides it, and the
+    # nearest unequal pair across the cut is .076 (kept) and .075 (dropped)
+    assert gap(7) == pytest.approx(np.log(.076 / .075), rel=1e-5)
+    # M = 9 splits the tie .0665 / .0665: the nearest unequal pair is .075 / .0665
+    assert gap(9) == pytest.approx(min(frontier, np.log(.075 / .0665)), rel=1e-5)
+    # the cut between the tied siblings still follows creation order
+    r = oracle_mod.tree_grow(z, 1.0, 7, dtype="f32")
+    kept_l3 = [v for v in range(1, 8) if r["depth"][0, v] == 3]
+    assert len(kept_l3) == 1 and r["tokens"][0, kept_l3[0]] == 0
