@@ -339,9 +339,10 @@ SPEC_API uint64_t spec_verify_launch_count(void);
  * unspecified outputs and the flag raised instead of hanging.  This sets the
  * limit used by calls of spec_verify_sample, spec_verify_greedy,
  * spec_verify_tree_greedy and spec_verify_greedy_noalloc enqueued afterwards,
- * process-wide; limit_ns = 0 restores the default.  A limit shorter than a
- * copy's latency (a few hundred ns) makes the waits give up, which is how a
- * test exercises that path.  Not for production use.
+ * process-wide; limit_ns = 0 restores the default.  limit_ns = 1 gives up
+ * whenever a copy has not landed at the first look, which is how a test
+ * exercises that path (other limits below a microsecond are rounded up by
+ * the resolution of the GPU's global timer).  Not for production use.
  */
 SPEC_API void spec_verify_set_wait_limit_ns(uint64_t limit_ns);
 

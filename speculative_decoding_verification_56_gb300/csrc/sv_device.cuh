@@ -365,11 +365,14 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Wait for a barrier phase; give up after limit_ns (returns false).  With the
 // default limit a sleeping try_wait is woken by the phase's completion; a
-// shorter limit also shortens each sleep, so that the limit is observed.
+// shorter limit also shortens each sleep, so that the limit is observed.  A
+// limit of 1 ns gives up as soon as one test finds the phase incomplete
+// (shorter than the resolution of the global timer).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity,
                                                   uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t hint = limit_ns < kSuspendHintNs ? (uint32_t)limit_ns : kSuspendHintNs;
   if (mbar_try_wait(bar, parity, hint)) return true;
+  if (limit_ns <= 1) return false;
   const uint64_t t0 = global_ns();
   for (unsigned it = 0; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity, hint)) return true;

@@ -3,8 +3,9 @@
 Every wait of the verification kernels on their own bulk copies gives up
 after a limit; the CTA then raises SPEC_FLAG_TIMEOUT, stops copying, waits
 (with the default limit) for the copies it has in flight and finishes its
-control flow.  Here the limit is shortened to 100 ns, below the latency of
-any copy from HBM, so the waits give up: the call must return, raise the
+control flow.  Here the limit is set to 1 ns, which gives up whenever a copy
+has not landed at the first look (the first copies of every CTA have not:
+they were issued a few hundred ns earlier): the call must return, raise the
 flag, and leave the context usable, with the next call (default limit)
 matching the oracle again.  Nothing here faults or hangs the GPU: the copies
 still land, and only the waits on them are cut short.
@@ -20,7 +21,7 @@ from speculative_decoding_verification_56_gb300 import build, synth
 
 pytestmark = pytest.mark.gpu
 
-SHORT_NS = 100
+SHORT_NS = 1
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,6 +39,11 @@ def _inputs(c):
 
 
 def _with_short_limit(fn):
+    # evict the inputs from L2 first (a write larger than its 129 MB), so that
+    # the first copies of every CTA come from HBM and cannot have landed when
+    # the consumers first look
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush.fill_(1)
     sv.spec_verify_set_wait_limit_ns(SHORT_NS)
     try:
         out = fn()
