@@ -19,7 +19,6 @@
 
 #include "spec_verify.h"
 #include "sv_kernels.cuh"
-#include "sv_team.cuh"
 #include "sv_tree.cuh"
 #include "sv_lmhead.cuh"
 #include "sv_grow.cuh"
@@ -323,89 +322,6 @@ spec_status_t run_finish(const sv::SampleParams& prm, void* stream) {
   return launch(sv::draw_resolve_kernel<E, kVec>, prm.B, 0, prm, stream, true);
 }
 
-// Launch shape of the team kernel of sampling verification (one cluster of
-// CS CTAs per team, one CTA per SM): the ring depth that fits beside the
-// kernel's tables, and the largest number of teams resident at once, per
-// device context.  Returns false where the team kernel does not apply (the
-// drawn row's chunks do not fit CS x kTmLocalChunks, or no ring fits).
-constexpr int kSmemPerBlock = 227 * 1024;
-// sampling verification by the team kernel where it applies (else the
-// statistics kernel and the clustered finish)
-constexpr bool kTeamSample = true;
-
-template <typename E, int CS>
-spec_status_t team_shape(int rows_per_seq, int nchunks, int* nstages, int* smem, int* maxclus) {
-  *nstages = 0;
-  if (nchunks > CS * sv::kTmLocalChunks) return SPEC_OK;
-  static int cached_static[kMaxDevices] = {0};
-  static int cached_clus[kMaxDevices][sv::kTmMaxStages + 1] = {{0}};
-  static unsigned long long cached_ctx[kMaxDevices] = {0};
-  int dev = 0;
-  unsigned long long ctx = 0;
-  if (current_context(&dev, &ctx) != SPEC_OK) return SPEC_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_shape_mu);
-  auto kernel = sv::team_sample_kernel<E, CS>;
-  if (cached_ctx[dev] != ctx || cached_static[dev] == 0) {
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemPerBlock - (int)fa.sharedSizeBytes) != cudaSuccess)
-      return SPEC_ERR_CUDA;
-    cached_static[dev] = (int)fa.sharedSizeBytes + 1;
-    for (int st = 0; st <= sv::kTmMaxStages; ++st) cached_clus[dev][st] = 0;
-    cached_ctx[dev] = ctx;
-  }
-  const int avail = kSmemPerBlock - (cached_static[dev] - 1);
-  const int nloc = (nchunks + CS - 1) / CS;
-  int S = sv::kTmMaxStages;
-  while (S >= 2 && sv::TeamLayout::make(S, rows_per_seq, nloc).bytes > avail) --S;
-  if (S < 2) return SPEC_OK;
-  const int bytes = sv::TeamLayout::make(S, rows_per_seq, nloc).bytes;
-  if (cached_clus[dev][S] == 0) {
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(CS, 1, 1);
-    cfg.blockDim = dim3(sv::kTmThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)bytes;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1)
-      return SPEC_ERR_CUDA;
-    cached_clus[dev][S] = n;
-  }
-  *nstages = S;
-  *smem = bytes;
-  *maxclus = cached_clus[dev][S];
-  return SPEC_OK;
-}
-
-// Sampling verification by the team kernel: the teams split the sequences
-// into contiguous ranges, as few rounds as the resident teams allow, the
-// rounds spread evenly over the teams.  Returns SPEC_ERR_INVALID_ARG (nothing
-// launched) where the team kernel does not apply.
-template <typename E>
-spec_status_t run_team_sample(const sv::SampleParams& prm, void* stream) {
-  constexpr int CS = 4;
-  int S = 0, smem = 0, maxclus = 0;
-  const spec_status_t st = team_shape<E, CS>(2 * prm.k + 1, prm.nchunks, &S, &smem, &maxclus);
-  if (st != SPEC_OK) return st;
-  if (S == 0) return SPEC_ERR_INVALID_ARG;
-  const int rounds = (prm.B + maxclus - 1) / maxclus;
-  const int nclus = (prm.B + rounds - 1) / rounds;
-  sv::TeamParams tp;
-  tp.p = prm;
-  tp.nstages = S;
-  tp.seq_per_team = rounds;
-  return launch(sv::team_sample_kernel<E, CS>, nclus * CS, (size_t)smem, tp, stream, true, CS,
-                sv::kTmThreads);
-}
-
 // L2 budget for the rows streamed with a keep hint (well under the 129 MB L2
 // of a GB300, so that the rest of the stream does not evict them).
 constexpr double kKeepBytes = 80.0 * (1 << 20);
@@ -419,11 +335,6 @@ spec_status_t run_sample(sv::SampleParams prm, int rows, bool vec, void* stream)
     prm.keep_pos = pair > 0 ? std::min(prm.k + 1, (int)(kKeepBytes / pair)) : 0;
   }
   spec_status_t st;
-  if (vec && kTeamSample) {
-    prm.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-    st = run_team_sample<E>(prm, stream);
-    if (st != SPEC_ERR_INVALID_ARG) return st;  // else: the two-kernel path below
-  }
   if (vec) {
     int grid = 0;
     st = persistent_grid<sv::stream_stats_kernel<E>>(prm.items, &grid);

@@ -447,9 +447,9 @@ def test_exp2_fma_accuracy():
 
 
 def test_launch_count():
-    # sampling: one kernel on the bulk-copy path (rows of whole 16-byte
-    # vectors), statistics + finish on plain loads; greedy: argmax + resolve
-    for V, n_sample in ((100, 1), (101, 2)):
+    # statistics + clustered finish for sampling; argmax + resolve for greedy,
+    # on the bulk-copy path (rows of whole 16-byte vectors) and the other
+    for V, n_sample in ((100, 2), (101, 2)):
         c = synth.make_chain_case(B=2, k=2, V=V, dtype="f32", seed=0)
         n0 = sv.spec_verify_launch_count()
         gpu_sample(c)
