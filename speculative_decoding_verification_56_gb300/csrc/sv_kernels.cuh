@@ -537,29 +537,30 @@ __device__ void finalize_arg_rows4(const ArgmaxParams& p, int b, int r0, int str
   }
 }
 
-// Chain resolve: accept while the draft equals the target argmax (one warp).
-__device__ void resolve_chain(const ArgmaxParams& p, int b) {
+// Chain resolve: accept while the draft equals the target argmax (one warp),
+// from the sequence's draft tokens `tok` [k] and row argmaxes `g` [k+1]
+// (shared memory).
+__device__ void resolve_chain(const ArgmaxParams& p, int b, const int32_t* tok, const int32_t* g) {
   const int lane = threadIdx.x & 31;
   const int k = p.rows_per_seq - 1;
-  const int32_t* g = p.rowarg + (size_t)b * p.rows_per_seq;
   int n = k;
   bool bad = false;
   for (int i0 = 0; i0 < k; i0 += 32) {
     const int i = i0 + lane;
     bool miss = false;
     if (i < k) {
-      const int x = p.tokens[(size_t)b * k + i];
+      const int x = tok[i];
       bad |= (x < 0 || x >= p.V);
-      miss = x != __ldcg(&g[i]);
+      miss = x != g[i];
     }
     const unsigned m = __ballot_sync(0xffffffffu, miss);
     if (n == k && m) n = i0 + __ffs(m) - 1;
   }
-  if (bad) set_flag(p.flags, kFlagTokenRange);
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_flag(p.flags, kFlagTokenRange);
   for (int i = lane; i <= k; i += 32) {
     int v = -1;
-    if (i < n) v = p.tokens[(size_t)b * k + i];
-    else if (i == n) v = __ldcg(&g[n]);
+    if (i < n) v = tok[i];
+    else if (i == n) v = g[n];
     p.out_tokens[(size_t)b * (k + 1) + i] = v;
   }
   if (lane == 0) p.accepted_len[b] = n;
@@ -634,20 +635,31 @@ __device__ void resolve_tree(const ArgmaxParams& p, int b, const int32_t* par,
 // parents, tokens and row argmaxes; larger ones read global memory.
 constexpr int kTreeSmemNodes = 2048;
 
-// Merge the rows of sequence (tree) b and resolve it (whole CTA; the three
-// scratch arrays hold kTreeSmemNodes entries each, in shared memory).  T:
-// records per lane and row loaded at once.
-template <int T>
-__device__ void resolve_sequence(const ArgmaxParams& p, int b, int32_t* s_par, int32_t* s_tok,
-                                 int32_t* s_g) {
+// Load what the resolve needs of sequence (tree) b besides the argmax kernel's
+// records: the draft tokens of a chain, or the parents and tokens of a tree
+// of up to kTreeSmemNodes nodes (whole CTA, before the dependency wait: the
+// argmax kernel does not write them).
+__device__ void resolve_prefetch(const ArgmaxParams& p, int b, int32_t* s_par, int32_t* s_tok) {
   const int N = p.rows_per_seq;
-  const bool in_smem = p.tree && N <= kTreeSmemNodes;
-  if (in_smem) {  // independent loads, issued before the merges
-    for (int v = threadIdx.x; v < N; v += kThreads) {
+  if (!p.tree) {
+    for (int i = threadIdx.x; i < N - 1; i += blockDim.x)
+      s_tok[i] = p.tokens[(size_t)b * (N - 1) + i];
+  } else if (N <= kTreeSmemNodes) {
+    for (int v = threadIdx.x; v < N; v += blockDim.x) {
       s_par[v] = p.parents[(size_t)b * N + v];
       s_tok[v] = p.tokens[(size_t)b * N + v];
     }
   }
+}
+
+// Merge the rows of sequence (tree) b and resolve it (whole CTA; the three
+// scratch arrays hold kTreeSmemNodes entries each, in shared memory, with the
+// prefetched inputs).  T: records per lane and row loaded at once.
+template <int T>
+__device__ void resolve_sequence(const ArgmaxParams& p, int b, int32_t* s_par, int32_t* s_tok,
+                                 int32_t* s_g) {
+  const int N = p.rows_per_seq;
+  const bool in_smem = !p.tree || N <= kTreeSmemNodes;
   for (int r0 = threadIdx.x >> 5; r0 < N; r0 += 4 * kWarps) {
     int g[4];
     finalize_arg_rows4<T>(p, b, r0, kWarps, N, g);
@@ -660,7 +672,7 @@ __device__ void resolve_sequence(const ArgmaxParams& p, int b, int32_t* s_par, i
   __syncthreads();
   if (threadIdx.x < 32) {
     if (!p.tree)
-      resolve_chain(p, b);
+      resolve_chain(p, b, s_tok, s_g);
     else if (in_smem)
       resolve_tree(p, b, s_par, s_tok, s_g);
     else
@@ -671,10 +683,12 @@ __device__ void resolve_sequence(const ArgmaxParams& p, int b, int32_t* s_par, i
 
 __global__ void __launch_bounds__(kThreads) argmax_resolve_kernel(const ArgmaxParams p) {
   __shared__ int32_t s_par[kTreeSmemNodes], s_tok[kTreeSmemNodes], s_g[kTreeSmemNodes];
+  resolve_prefetch(p, blockIdx.x, s_par, s_tok);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the next call's streaming kernel may become resident now; it waits for
   // this grid before touching memory
   asm volatile("griddepcontrol.launch_dependents;");
+  __syncthreads();  // the prefetched inputs
   resolve_sequence<4>(p, blockIdx.x, s_par, s_tok, s_g);
 }
 
