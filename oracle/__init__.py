@@ -100,7 +100,7 @@ def load_variant(lib_path):
 
 
 def _dtype_code(dtype: str) -> int:
-    return {"f32": 0, "bf16": 1}[dtype]
+    return {"f32": 0, "bf16": 1, "f64": 2}[dtype]
 
 
 def _ptr(a: np.ndarray):
@@ -108,7 +108,7 @@ def _ptr(a: np.ndarray):
 
 
 def _logits(a, dtype):
-    want = np.uint16 if dtype == "bf16" else np.float32
+    want = {"bf16": np.uint16, "f32": np.float32, "f64": np.float64}[dtype]
     return np.ascontiguousarray(a, dtype=want)
 
 
@@ -289,6 +289,47 @@ def lm_head_greedy(hidden, w_lm, tokens, seqs=None, lib=None):
                                    _ptr(res["argmax"]), _ptr(res["gap"]), _ptr(res["mag"]))
     _check(rc)
     return res
+
+
+def _bf16_to_f64(bits):
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def lm_head_logits(hidden, w_lm):
+    """Exact logits z = W_LM h in float64 of bf16 hidden states [rows, d] and
+    a bf16 LM head [V, d] (raw 16-bit patterns): "EAGLE math", "EAGLE's move"
+    (p = softmax(LM_head(f))).  The products of two bf16 values are exact in
+    float64 and the sums are rounded in float64 (a library matrix product)."""
+    return _bf16_to_f64(hidden) @ _bf16_to_f64(w_lm).T
+
+
+def lm_head_sample(h_target, h_draft, w_lm, tokens, u_accept, u_sample, temperature, seqs=None,
+                   lib=None, window=FLAG_WINDOW):
+    """LM head fused with sampling verification (reading R13 of spec_oracle.c's
+    header): the target rows' logits W_LM h_t and the draft rows' logits
+    W_LM h_d, then sampling verification of them in float64
+    (:func:`verify_sample` on float64 logits).  h_target [B*(k+1), d] and
+    h_draft [B*k, d] bf16 bits, sequence-major; ``seqs`` selects the
+    sequences to evaluate (default all).  Returns the verify_sample dict for
+    those sequences, plus the float64 logits ``zt`` [S, k+1, V] and ``zd``
+    [S, k, V]."""
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    B, k = tok.shape
+    V = np.asarray(w_lm).shape[0]
+    sq = np.arange(B) if seqs is None else np.asarray(seqs, dtype=np.int64)
+    Ht = np.asarray(h_target).reshape(B, k + 1, -1)[sq].reshape(len(sq) * (k + 1), -1)
+    zt = lm_head_logits(Ht, w_lm).reshape(len(sq), k + 1, V)
+    if k > 0:
+        Hd = np.asarray(h_draft).reshape(B, k, -1)[sq].reshape(len(sq) * k, -1)
+        zd = lm_head_logits(Hd, w_lm).reshape(len(sq), k, V)
+    else:
+        zd = np.zeros((len(sq), 0, V))
+    out = verify_sample(zt, zd, tok[sq], np.asarray(u_accept)[sq], np.asarray(u_sample)[sq],
+                        temperature, dtype="f64", lib=lib, window=window)
+    out["zt"] = zt
+    out["zd"] = zd
+    return out
 
 
 def tree_grow(logits, temperature, M, dtype="bf16", lib=None):

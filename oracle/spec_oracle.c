@@ -52,6 +52,11 @@
  *      minus top-2) and the magnitude sum |W_j*| . |h| of the winner are
  *      reported so that a comparison can excuse rows whose argmax a float32
  *      accumulation could legitimately move.
+ *   R13 LM head fused with sampling verification: the target rows' logits
+ *      W_LM h_t and the draft rows' logits W_LM h_d (the drafted features go
+ *      through the target's own LM head), exact in float64 from the bf16
+ *      inputs (a float64 matrix product in the Python binding), then
+ *      sampling verification (R1-R6) of those float64 logits (OR_F64).
  *   R12 EAGLE-2 tree growth: node 0 is the root (value 0).  At layer l the
  *      frontier (slot j holds a node; layer 0: the root in slot 0) is
  *      expanded with draft row logits[b, l, j]: q = softmax(z / T); the
@@ -80,10 +85,13 @@
 
 #define OR_F32 0
 #define OR_BF16 1
+#define OR_F64 2 /* logits already in float64 (the LM head's exact products) */
 
-/* One stored logit as float64: fp32 as is, bf16 widened by a 16-bit shift. */
+/* One stored logit as float64: fp32 as is, bf16 widened by a 16-bit shift,
+ * float64 as is. */
 static double logit_at(const void* base, int dtype, size_t idx) {
   if (dtype == OR_F32) return (double)((const float*)base)[idx];
+  if (dtype == OR_F64) return ((const double*)base)[idx];
   uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
   float f;
   memcpy(&f, &bits, sizeof f);
@@ -219,7 +227,7 @@ int oracle_verify_sample(const void* target, const void* draft, int dtype,
                          int32_t* fallback, double window, double* flag_prob) {
   if (B < 0 || k < 0 || V < 1 || !(temperature > 0.0) || !isfinite(temperature))
     return OR_ERR_ARG;
-  if (dtype != OR_F32 && dtype != OR_BF16) return OR_ERR_ARG;
+  if (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_F64) return OR_ERR_ARG;
   double* pt = (double*)malloc(sizeof(double) * (size_t)(k + 1) * (size_t)V);
   double* pd = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * (size_t)V);
   double* r = (double*)malloc(sizeof(double) * (size_t)V);
@@ -339,7 +347,7 @@ int oracle_sample_claim(const void* target, const void* draft, int dtype, const 
                         double* violation, double* claim_R) {
   if (B < 0 || k < 0 || V < 1 || !(temperature > 0.0) || !isfinite(temperature))
     return OR_ERR_ARG;
-  if (dtype != OR_F32 && dtype != OR_BF16) return OR_ERR_ARG;
+  if (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_F64) return OR_ERR_ARG;
   double* pt = (double*)malloc(sizeof(double) * (size_t)(k + 1) * (size_t)V);
   double* pd = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * (size_t)V);
   double* r = (double*)malloc(sizeof(double) * (size_t)V);

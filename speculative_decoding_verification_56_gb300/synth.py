@@ -368,6 +368,39 @@ def make_lm_head_case(*, B, k, d, V, seed=0, peak=6.0, p_match=0.7, flat_frac=0.
     return H_bits, W_bits, tokens, intended.astype(np.int32)
 
 
+class LmSampleInputs:
+    """Inputs of the LM head fused with sampling verification: target hidden
+    states [B*(k+1), d], drafted features [B*k, d] and the LM head [V, d] as
+    bf16 bits; draft tokens, uniforms and the temperature."""
+
+    def __init__(self, B, k, d, V, temperature, h_target, h_draft, w_lm, tokens, u_accept,
+                 u_sample):
+        self.B, self.k, self.d, self.V = B, k, d, V
+        self.temperature = temperature
+        self.h_target, self.h_draft, self.w_lm = h_target, h_draft, w_lm
+        self.tokens, self.u_accept, self.u_sample = tokens, u_accept, u_sample
+
+
+def make_lm_head_sample_case(*, B, k, d, V, seed=0, peak=6.0, p_match=0.7, flat_frac=0.1,
+                             feature_noise=0.3, temperature=1.0):
+    """The LM-head recipe of make_lm_head_case for the target hidden states,
+    plus drafted features h_d = h_t + N(0, feature_noise^2) per element of the
+    k drafted positions (a drafter that predicts the target's features with
+    some error).  Draft tokens are the intended token of the position with
+    probability p_match, else uniform; uniforms from seed + 1."""
+    H_bits, W_bits, tokens, _ = make_lm_head_case(B=B, k=k, d=d, V=V, seed=seed, peak=peak,
+                                                  p_match=p_match, flat_frac=flat_frac)
+    rng = np.random.default_rng(seed + 7)
+    Ht = bf16_bits_to_f32(H_bits).reshape(B, k + 1, d)
+    Hd = Ht[:, :k] + feature_noise * rng.standard_normal((B, k, d)).astype(np.float32)
+    Hd_bits = f32_to_bf16_bits(Hd.reshape(B * k, d).astype(np.float32))
+    urng = np.random.default_rng(seed + 1)
+    u_accept = uniforms_f32(urng, (B, k))
+    u_sample = uniforms_f32(urng, (B,))
+    return LmSampleInputs(B, k, d, V, float(temperature), H_bits, Hd_bits, W_bits, tokens,
+                          u_accept, u_sample)
+
+
 # ---------------------------------------------------------------------------
 # Draft rows for tree growth
 # ---------------------------------------------------------------------------

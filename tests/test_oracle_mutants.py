@@ -80,6 +80,8 @@ MUTANTS = {
                                    "    (void)cut_gap;"),
     "grow_gap_counts_ties": ("  const double vk = val[order[keep - 1]], vd = val[order[keep]];\n  double g = INFINITY;",
                              "  const double vk = val[order[keep - 1]], vd = val[order[keep]];\n  double g = vk - vd;"),
+    "f64_logits_read_as_f32": ("  if (dtype == OR_F64) return ((const double*)base)[idx];",
+                               "  if (dtype == OR_F64) return (double)((const float*)base)[idx];"),
     "mask_wrong_word": ("        row[cur / 32] |= 1u << (cur % 32);\n        ++d;",
                         "        row[cur % W] |= 1u << (cur % 32);\n        ++d;"),
 }
@@ -117,6 +119,9 @@ class _Variant:
     def sample_claim(self, *a, **kw):
         return oracle.sample_claim(*a, lib=self.lib, **kw)
 
+    def lm_head_sample(self, *a, **kw):
+        return oracle.lm_head_sample(*a, lib=self.lib, **kw)
+
     def expected_tokens(self, *a, **kw):
         return oracle.expected_tokens(*a, lib=self.lib, **kw)
 
@@ -150,6 +155,7 @@ def _pin_checks(o):
     yield lambda: pins.test_margins_and_flag_probability_worked_example(o)
     yield lambda: pins.test_claim_violation_worked_example(o)
     yield lambda: pins.test_tree_grow_min_gap_worked_example(o)
+    yield lambda: pins.test_lm_head_sample_equals_plain_sampling_on_exact_logits(o)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

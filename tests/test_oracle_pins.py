@@ -915,3 +915,39 @@ def test_tree_grow_min_gap_worked_example(oracle_mod):
     r = oracle_mod.tree_grow(z, 1.0, 7, dtype="f32")
     kept_l3 = [v for v in range(1, 8) if r["depth"][0, v] == 3]
     assert len(kept_l3) == 1 and r["tokens"][0, kept_l3[0]] == 0
+
+
+# ---------------------------------------------------------------------------
+# LM head fused with sampling verification
+# ---------------------------------------------------------------------------
+
+def _int_bf16(rng, shape, lo, hi):
+    """Small integers as bf16 bits (exactly representable)."""
+    return synth.f32_to_bf16_bits(rng.integers(lo, hi, size=shape).astype(np.float32))
+
+
+def test_lm_head_sample_equals_plain_sampling_on_exact_logits(oracle_mod):
+    # integer weights and features: every logit W h is a small integer, exact
+    # in float32, so the fused oracle must equal plain sampling verification
+    # of logits computed here by an integer matrix product
+    rng = np.random.default_rng(3)
+    B, k, d, V, T = 6, 3, 16, 40, 1.3
+    W = _int_bf16(rng, (V, d), -2, 3)
+    Ht = _int_bf16(rng, (B * (k + 1), d), -2, 3)
+    Hd = _int_bf16(rng, (B * k, d), -2, 3)
+    toks = rng.integers(0, V, (B, k)).astype(np.int32)
+    ua = synth.uniforms_f32(rng, (B, k))
+    us = synth.uniforms_f32(rng, (B,))
+    r = oracle_mod.lm_head_sample(Ht, Hd, W, toks, ua, us, T)
+    Wi = synth.bf16_bits_to_f32(W).astype(np.int64)
+    zt = (synth.bf16_bits_to_f32(Ht).astype(np.int64) @ Wi.T).astype(np.float32).reshape(B, k + 1, V)
+    zd = (synth.bf16_bits_to_f32(Hd).astype(np.int64) @ Wi.T).astype(np.float32).reshape(B, k, V)
+    ref = oracle_mod.verify_sample(zt, zd, toks, ua, us, T, dtype="f32")
+    for key in ("accepted_len", "out_tokens"):
+        assert np.array_equal(r[key], ref[key]), key
+    for key in ("p", "q", "resid_mass"):
+        assert np.allclose(r[key], ref[key], rtol=1e-12, atol=0), key
+    # a subset of sequences gives the same rows
+    sub = oracle_mod.lm_head_sample(Ht, Hd, W, toks, ua, us, T, seqs=[4, 1])
+    assert np.array_equal(sub["out_tokens"], ref["out_tokens"][[4, 1]])
+    assert 0 < (r["accepted_len"] < k).sum() < B
