@@ -817,7 +817,49 @@ def measure_next_rows(dev, stream, tree, K):
         "unfused": "torch.matmul (cuBLAS) writing bf16 logits, then spec_verify_greedy",
         "bound": "W_LM stream (1.05 GB) and tensor cores, about balanced at 320 rows",
         "timed": "CUDA-graph replay of 4 calls"}
-    del H, Wm, logits, lm
+
+    # LM head fused with sampling verification on the same shape: 320 target
+    # rows, 256 drafted features (the target's first k hidden states of each
+    # sequence plus N(0, 0.3^2) noise), T = 1; the unfused path writes both
+    # logits matrices with cuBLAS and runs spec_verify_sample
+    g = torch.Generator(device=dev).manual_seed(3)
+    Hd = (H.view(Bl, kl + 1, d)[:, :kl].float()
+          + 0.3 * torch.randn(Bl, kl, d, device=dev, generator=g)).to(torch.bfloat16)
+    Hd = Hd.reshape(Bl * kl, d).contiguous()
+    ua = torch.rand(Bl, kl, device=dev, generator=g)
+    us = torch.rand(Bl, device=dev, generator=g)
+    wss = sv.alloc_workspace(sv.SPEC_MODE_LM_HEAD_SAMPLE, Bl, kl, Vl, sv.SPEC_DTYPE_BF16, dev)
+    wsu = sv.alloc_workspace(sv.SPEC_MODE_SAMPLE, Bl, kl, Vl, sv.SPEC_DTYPE_BF16, dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    so = dict(n=torch.empty(Bl, **i32), tok=torch.empty(Bl, kl + 1, **i32),
+              p=torch.empty(Bl, kl, **f32), q=torch.empty(Bl, kl, **f32), R=torch.empty(Bl, **f32))
+    logits_d = torch.empty(Bl * kl, Vl, dtype=torch.bfloat16, device=dev)
+
+    def fused_sample():
+        sv.spec_lm_head_verify_sample(H, Hd, Wm, tk, ua, us, 1.0, so["n"], so["tok"], so["p"],
+                                      so["q"], so["R"], wss, stream)
+
+    def unfused_sample():
+        torch.matmul(H, Wm.t(), out=logits)
+        torch.matmul(Hd, Wm.t(), out=logits_d)
+        sv.spec_verify_sample(logits.view(Bl, kl + 1, Vl), logits_d.view(Bl, kl, Vl), tk, ua, us,
+                              1.0, so["n"], so["tok"], so["p"], so["q"], so["R"], wsu, stream)
+    ms_fs = _time_loop(fused_sample, stream, max(20, K // 20), per_graph=2)
+    ms_us = _time_loop(unfused_sample, stream, max(20, K // 20), per_graph=2)
+    flops_s = 2.0 * (rows + Bl * kl) * d * Vl
+    out["lm_head_sample"] = {
+        "workload": f"B={Bl} k={kl}: {rows} target rows and {Bl * kl} drafted features, hidden {d}, "
+                    f"V={Vl}, bf16 in, fp32 accumulate, T=1",
+        "us_per_call": round(ms_fs * 1e3, 2),
+        "tflops_statistics_gemm_equivalent": round(flops_s / (ms_fs / 1e3) / 1e12, 1),
+        "unfused_us_per_call": round(ms_us * 1e3, 2),
+        "unfused": "torch.matmul (cuBLAS) writing bf16 target and draft logits, then "
+                   "spec_verify_sample",
+        "launches": 4,
+        "bound": "the statistics GEMM (576 rows) and a second pass over W_LM for the 2B drawn rows",
+        "timed": "CUDA-graph replay of 2 calls"}
+    del H, Wm, logits, lm, Hd, logits_d, wss, wsu
 
     # EAGLE-2 tree growth producing the tree workload's shape (16 trees of 60
     # nodes): 6 layers of 8 frontier rows over V=128256 bf16 draft rows

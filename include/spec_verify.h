@@ -85,7 +85,8 @@ typedef enum {
   SPEC_MODE_TREE_MASK = 3, /* spec_tree_attention_mask: the flag header only */
   SPEC_MODE_KV_COMMIT = 4, /* spec_kv_commit_path: the flag header only */
   SPEC_MODE_LM_HEAD_GREEDY = 5, /* spec_lm_head_verify_greedy (k_or_N = k) */
-  SPEC_MODE_TREE_GROW = 6       /* spec_tree_grow (k_or_N = K children per node) */
+  SPEC_MODE_TREE_GROW = 6,      /* spec_tree_grow (k_or_N = K children per node) */
+  SPEC_MODE_LM_HEAD_SAMPLE = 7  /* spec_lm_head_verify_sample (k_or_N = k, d <= SPEC_LM_MAX_D) */
 } spec_mode_t;
 
 /* Bits of the workspace flag word (sticky until read with clear != 0). */
@@ -277,6 +278,40 @@ SPEC_API spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void
                                                   int d, int V, int32_t* accepted_len,
                                                   int32_t* out_tokens, void* workspace,
                                                   size_t workspace_bytes, void* stream);
+
+/*
+ * The target's LM head fused with sampling verification ("EAGLE math",
+ * "EAGLE's move": p = softmax(LM_head(f)), the drafted features going through
+ * the target's own LM head; "EAGLE-3 speculative decoding review", "Does
+ * Using a Small Model's Answer Reduce Quality?" eqs. A(x), p_residual).
+ * The target rows' logits W_LM h_t and the draft rows' logits W_LM h_d are
+ * reduced on the tensor cores to their softmax statistics and draft-token
+ * logits without being written; the accept test follows, and only the rows
+ * a sequence draws from (the target and draft rows of its first rejection,
+ * or its bonus row) are recomputed as fp32 logits in the workspace for the
+ * residual or bonus draw.  Same decisions and outputs as spec_verify_sample
+ * on the float32-accumulated logits.
+ *   hidden_target bf16 [B*(k+1), d]  row b*(k+1)+i: the target's hidden state
+ *                                    at position i of sequence b
+ *   hidden_draft  bf16 [B*k, d]      row b*k+i: the drafted feature of
+ *                                    position i (NULL when k = 0)
+ *   w_lm          bf16 [V, d]        the LM head, row j = vocabulary entry j
+ *   draft_tokens, u_accept, u_sample, temperature, outputs: as
+ *                 spec_verify_sample
+ *   d             multiple of 8, at most SPEC_LM_MAX_D; the matrices 16-byte
+ *                 aligned
+ * Four kernel launches: the statistics GEMM (tcgen05, softmax epilogue), the
+ * accept test with the gather of the drawn rows' hidden states, the GEMM
+ * that writes those rows' logits, and the draw (as spec_verify_sample's).
+ * Workspace: spec_verify_workspace_bytes(SPEC_MODE_LM_HEAD_SAMPLE, B, k, V,
+ * SPEC_DTYPE_BF16).
+ */
+#define SPEC_LM_MAX_D 8192
+SPEC_API spec_status_t spec_lm_head_verify_sample(
+    const void* hidden_target, const void* hidden_draft, const void* w_lm,
+    const int32_t* draft_tokens, const float* u_accept, const float* u_sample, float temperature,
+    int B, int k, int d, int V, int32_t* accepted_len, int32_t* out_tokens, float* p_out,
+    float* q_out, float* resid_mass, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * EAGLE-2 dynamic draft-tree growth ("EAGLE math", "EAGLE-2: dynamic draft

@@ -13,6 +13,7 @@ Entry points (same names as the C ABI):
 * :func:`spec_tree_attention_mask` -- ancestor bitmask + depth of draft trees
 * :func:`spec_kv_commit_path`     -- move the accepted path's KV entries into place
 * :func:`spec_lm_head_verify_greedy` -- LM head (tcgen05 GEMM) fused with greedy verification
+* :func:`spec_lm_head_verify_sample` -- LM head (tcgen05 GEMM) fused with sampling verification
 * :func:`spec_tree_grow`          -- EAGLE-2 dynamic draft-tree growth
 * :func:`spec_verify_workspace_bytes`, :func:`spec_verify_read_flags`,
   :func:`spec_verify_launch_count`, :func:`spec_status_string`
@@ -46,6 +47,8 @@ SPEC_MODE_TREE_MASK = 3
 SPEC_MODE_KV_COMMIT = 4
 SPEC_MODE_LM_HEAD_GREEDY = 5
 SPEC_MODE_TREE_GROW = 6
+SPEC_MODE_LM_HEAD_SAMPLE = 7
+SPEC_LM_MAX_D = 8192
 SPEC_FLAG_TOKEN_RANGE = 1
 SPEC_FLAG_BAD_PARENT = 2
 SPEC_FLAG_DEPTH = 4
@@ -94,6 +97,9 @@ def load_library(path: str = LIB_PATH):
         lib.spec_kv_commit_path.restype = I
         lib.spec_lm_head_verify_greedy.argtypes = [P, P, P, I, I, I, I, P, P, P, Z, P]
         lib.spec_lm_head_verify_greedy.restype = I
+        lib.spec_lm_head_verify_sample.argtypes = [P, P, P, P, P, P, F, I, I, I, I, P, P, P, P, P,
+                                                   P, Z, P]
+        lib.spec_lm_head_verify_sample.restype = I
         lib.spec_tree_grow.argtypes = [P, I, F, I, I, I, I, I, P, P, P, P, P, Z, P]
         lib.spec_tree_grow.restype = I
         lib.spec_verify_read_flags.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I, P]
@@ -322,6 +328,38 @@ def spec_lm_head_verify_greedy(hidden, w_lm, draft_tokens, accepted_len, out_tok
     _check(st, "spec_lm_head_verify_greedy")
 
 
+def spec_lm_head_verify_sample(h_target, h_draft, w_lm, draft_tokens, u_accept, u_sample,
+                               temperature, accepted_len, out_tokens, p_out, q_out, resid_mass,
+                               workspace, stream=None):
+    """LM head fused with sampling verification (C ABI
+    ``spec_lm_head_verify_sample``): ``h_target`` bf16 [B*(k+1), d],
+    ``h_draft`` bf16 [B*k, d], ``w_lm`` bf16 [V, d], the rest as
+    :func:`spec_verify_sample`."""
+    torch = _torch()
+    B, k = draft_tokens.shape
+    rows, d = h_target.shape
+    V = w_lm.shape[0]
+    if rows != B * (k + 1) or w_lm.shape[1] != d:
+        raise ValueError("h_target must be [B*(k+1), d] and w_lm [V, d]")
+    if k > 0 and tuple(h_draft.shape) != (B * k, d):
+        raise ValueError("h_draft must be [B*k, d]")
+    st = load_library().spec_lm_head_verify_sample(
+        _dev(h_target, "h_target", torch.bfloat16),
+        _dev(h_draft, "h_draft", torch.bfloat16, optional=k == 0),
+        _dev(w_lm, "w_lm", torch.bfloat16),
+        _dev(draft_tokens, "draft_tokens", torch.int32, optional=k == 0),
+        _dev(u_accept, "u_accept", torch.float32, optional=k == 0),
+        _dev(u_sample, "u_sample", torch.float32), float(temperature), B, k, d, V,
+        _dev(accepted_len, "accepted_len", torch.int32),
+        _dev(out_tokens, "out_tokens", torch.int32),
+        _dev(p_out, "p_out", torch.float32, optional=k == 0),
+        _dev(q_out, "q_out", torch.float32, optional=k == 0),
+        _dev(resid_mass, "resid_mass", torch.float32),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream))
+    _check(st, "spec_lm_head_verify_sample")
+
+
 def spec_tree_grow(draft_logits, temperature, M, tokens, parents, depth, values, workspace,
                    stream=None):
     """EAGLE-2 tree growth (C ABI ``spec_tree_grow``): ``draft_logits``
@@ -437,6 +475,27 @@ def lm_head_verify_greedy(hidden, w_lm, draft_tokens, workspace=None, stream=Non
                out_tokens=torch.empty(B, k + 1, dtype=torch.int32, device=dev))
     spec_lm_head_verify_greedy(hidden, w_lm, draft_tokens, out["accepted_len"],
                                out["out_tokens"], workspace, stream)
+    return out
+
+
+def lm_head_verify_sample(h_target, h_draft, w_lm, draft_tokens, u_accept, u_sample, temperature,
+                          workspace=None, stream=None):
+    """Sampling verification straight from hidden states, drafted features
+    and the LM head; returns the outputs of :func:`verify_sample`."""
+    torch = _torch()
+    B, k = draft_tokens.shape
+    dev = h_target.device
+    if workspace is None:
+        workspace = alloc_workspace(SPEC_MODE_LM_HEAD_SAMPLE, B, k, w_lm.shape[0],
+                                    SPEC_DTYPE_BF16, dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(accepted_len=torch.empty(B, **i32), out_tokens=torch.empty(B, k + 1, **i32),
+               p=torch.empty(B, k, **f32), q=torch.empty(B, k, **f32),
+               resid_mass=torch.empty(B, **f32))
+    spec_lm_head_verify_sample(h_target, h_draft, w_lm, draft_tokens, u_accept, u_sample,
+                               temperature, out["accepted_len"], out["out_tokens"], out["p"],
+                               out["q"], out["resid_mass"], workspace, stream)
     return out
 
 

@@ -50,6 +50,7 @@ struct Layout {
   size_t off_part = 0, off_desc = 0, off_csum = 0, off_csum_p = 0, off_zx = 0;  // sample
   size_t off_gsum = 0, off_gsum_p = 0;
   size_t off_arg = 0;                                            // greedy / tree
+  size_t off_log = 0;  // LM head + sampling: the drawn rows' logits
 };
 
 // Returns false for arguments outside the documented limits.
@@ -73,6 +74,40 @@ bool make_layout(int mode, int B, int kN, int V, int dtype, Layout* L) {
     off = align_up(off + (size_t)B * sv::kGrowMaxNodes * sizeof(double));
     L->off_gsum = off;  // parent, token, depth [3][B, kGrowMaxNodes]
     off = align_up(off + 3 * (size_t)B * sv::kGrowMaxNodes * sizeof(int32_t));
+    L->bytes = off;
+    return true;
+  }
+  if (mode == SPEC_MODE_LM_HEAD_SAMPLE) {
+    // statistics records of up to kLmMaxGrid CTAs per row, captured token
+    // logits, the draw's structures over fp32 rows, the drawn rows' hidden
+    // states [2B, d <= SPEC_LM_MAX_D] and their logits [2B, V] fp32
+    if (B < 0 || kN < 0 || kN > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return false;
+    const long long rows = (long long)B * (2LL * kN + 1);
+    if (rows * kLmMaxGrid > 0x7FFFFFFFLL) return false;
+    const int C = (V + sv::F32::kChunk - 1) / sv::F32::kChunk;
+    if ((long long)B * C * sv::kVecPerChunk > 0x7FFFFFFFLL) return false;
+    L->rows = (int)rows;
+    L->nchunks = C;
+    size_t off = kDataOffset;
+    L->off_part = off;
+    off = align_up(off + (size_t)rows * kLmMaxGrid * sizeof(sv::SoftmaxPartial));
+    L->off_zx = off;
+    off = align_up(off + (size_t)rows * sizeof(float));
+    L->off_desc = off;
+    off = align_up(off + (size_t)B * sizeof(sv::DrawDesc));
+    const size_t bc = (size_t)B * C;
+    L->off_csum = off;
+    off = align_up(off + bc * sizeof(sv::FSum));
+    L->off_csum_p = off;
+    off = align_up(off + bc * sizeof(sv::FSum));
+    L->off_gsum = off;
+    off = align_up(off + bc * sv::kVecPerChunk * sizeof(float));
+    L->off_gsum_p = off;
+    off = align_up(off + bc * sv::kVecPerChunk * sizeof(float));
+    L->off_arg = off;
+    off = align_up(off + (size_t)2 * B * SPEC_LM_MAX_D * sizeof(uint16_t));
+    L->off_log = off;
+    off = align_up(off + (size_t)2 * B * V * sizeof(float));
     L->bytes = off;
     return true;
   }
@@ -308,6 +343,50 @@ spec_status_t encode_bf16_kmajor(CUtensorMap* map, const void* base, int inner, 
   return r == CUDA_SUCCESS ? SPEC_OK : SPEC_ERR_INVALID_ARG;
 }
 
+// Row groups of an LM-head GEMM: at most kLmMaxRows rows each, split evenly,
+// each a multiple of the 64-row H box (so two MMAs of equal N stay multiples
+// of 16).  Returns false when the rows need more groups than a grid allows.
+bool lm_row_groups(int rows, int* ngroups, int* grp) {
+  if (rows <= 0) {
+    *ngroups = 0;
+    *grp = sv::kLmHBox;
+    return true;
+  }
+  const int gy = (rows + sv::kLmMaxRows - 1) / sv::kLmMaxRows;
+  if (gy > 32768) return false;
+  *ngroups = gy;
+  *grp = ((rows + gy - 1) / gy + sv::kLmHBox - 1) / sv::kLmHBox * sv::kLmHBox;
+  return true;
+}
+
+// One CTA per SM (the kernel holds the SM's tensor memory and most of its
+// shared memory), at most one per vocabulary tile.
+spec_status_t lm_grid_x(int ntiles, int* gx) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  *gx = std::max(1, std::min(std::min(sms, ntiles), kLmMaxGrid));
+  return SPEC_OK;
+}
+
+template <int Mode>
+spec_status_t launch_lmhead(const CUtensorMap& map_h, const CUtensorMap& map_h1,
+                            const CUtensorMap& map_w, const sv::LmHeadParams& lp, int gx, int gy,
+                            void* stream) {
+  const spec_status_t st = ensure_smem<sv::lmhead_kernel<Mode>>(
+      (size_t)sv::kLmStages * (sv::kLmABytes + sv::kLmBBytes) + 1024);
+  if (st != SPEC_OK) return st;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(&cfg, attr, dim3((unsigned)gx, (unsigned)gy, 1), dim3(sv::kLmThreads, 1, 1),
+             (size_t)sv::kLmStages * lp.stage_bytes + 1024, stream);
+  if (cudaLaunchKernelEx(&cfg, sv::lmhead_kernel<Mode>, map_h, map_h1, map_w, lp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return SPEC_OK;
+}
+
 template <typename E, bool kVec>
 spec_status_t run_finish(const sv::SampleParams& prm, void* stream) {
   if (prm.nchunks <= sv::kClusterMaxChunks) {
@@ -452,6 +531,8 @@ spec_status_t spec_verify_sample(const void* target_logits, const void* draft_lo
   prm.gsum = reinterpret_cast<float*>(ws + L.off_gsum);
   prm.gsum_p = reinterpret_cast<float*>(ws + L.off_gsum_p);
   prm.zx = reinterpret_cast<float*>(ws + L.off_zx);
+  prm.nrec = L.nchunks;
+  prm.drawn = nullptr;
 
   const bool vec = vec_ok(target_logits, V, dtype) && (k == 0 || vec_ok(draft_logits, V, dtype));
   if (dtype == SPEC_DTYPE_BF16) return run_sample<sv::BF16>(prm, L.rows, vec, stream);
@@ -629,19 +710,9 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
   const int rows = L.rows;
   const int ntiles = (V + sv::kLmBV - 1) / sv::kLmBV;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  // row groups of at most kLmMaxRows rows, split evenly, each a multiple of
-  // the 64-row H box (so two MMAs of equal N stay multiples of 16)
-  const int gy = (rows + sv::kLmMaxRows - 1) / sv::kLmMaxRows;
-  if (gy > 65535) return SPEC_ERR_INVALID_ARG;
-  const int grp = ((rows + gy - 1) / gy + sv::kLmHBox - 1) / sv::kLmHBox * sv::kLmHBox;
-  const int stage_bytes = sv::kLmABytes + grp * 128;
-  const int smem = sv::kLmStages * stage_bytes + 1024;
-  spec_status_t st = ensure_smem<sv::lmhead_argmax_kernel>(
-      (size_t)sv::kLmStages * (sv::kLmABytes + sv::kLmBBytes) + 1024);
+  int gy = 0, grp = 0, gx = 0;
+  if (!lm_row_groups(rows, &gy, &grp)) return SPEC_ERR_INVALID_ARG;
+  spec_status_t st = lm_grid_x(ntiles, &gx);
   if (st != SPEC_OK) return st;
   CUtensorMap map_h, map_w;
   st = encode_bf16_kmajor(&map_h, hidden, d, rows, sv::kLmHBox);
@@ -650,24 +721,19 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   if (st != SPEC_OK) return st;
   char* ws = static_cast<char*>(workspace);
   sv::LmHeadParams lp;
+  std::memset(&lp, 0, sizeof lp);
   lp.rows = rows;
   lp.d = d;
   lp.V = V;
   lp.ntiles = ntiles;
   lp.grp_rows = grp;
-  lp.stage_bytes = stage_bytes;
+  lp.stage_bytes = sv::kLmABytes + grp * 128;
   lp.part = reinterpret_cast<sv::ArgPartial*>(ws + L.off_part);
   lp.flags = reinterpret_cast<unsigned*>(ws);
-  // one CTA per SM (the kernel holds the SM's tensor memory and most of its
-  // shared memory), at most one per vocabulary tile
-  const int gx = std::max(1, std::min(std::min(sms, ntiles), kLmMaxGrid));
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  pdl_config(&cfg, attr, dim3((unsigned)gx, (unsigned)gy, 1), dim3(sv::kLmThreads, 1, 1),
-             (size_t)smem, stream);
-  if (cudaLaunchKernelEx(&cfg, sv::lmhead_argmax_kernel, map_h, map_w, lp) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  g_launches.fetch_add(1, std::memory_order_relaxed);
+  lp.ngroups0 = gy;
+  lp.grp_rows1 = sv::kLmHBox;
+  st = launch_lmhead<sv::kLmArgmax>(map_h, map_h, map_w, lp, gx, gy, stream);
+  if (st != SPEC_OK) return st;
   // merge the per-CTA records and resolve the chains (the greedy resolve)
   sv::ArgmaxParams prm;
   std::memset(&prm, 0, sizeof prm);
@@ -684,6 +750,134 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   prm.rowarg = reinterpret_cast<int32_t*>(ws + L.off_arg);
   prm.wait_ns = sv::kWaitLimitNs;
   return launch(sv::argmax_resolve_kernel, B, 0, prm, stream, true);
+}
+
+spec_status_t spec_lm_head_verify_sample(
+    const void* hidden_target, const void* hidden_draft, const void* w_lm,
+    const int32_t* draft_tokens, const float* u_accept, const float* u_sample, float temperature,
+    int B, int k, int d, int V, int32_t* accepted_len, int32_t* out_tokens, float* p_out,
+    float* q_out, float* resid_mass, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || k < 0 || k > SPEC_MAX_K || d < 8 || d > SPEC_LM_MAX_D || d % 8 || V < 1 ||
+      V > SPEC_MAX_V)
+    return SPEC_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(SPEC_MODE_LM_HEAD_SAMPLE, B, k, V, SPEC_DTYPE_BF16, &L))
+    return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!hidden_target || !w_lm || !u_sample || !accepted_len || !out_tokens || !resid_mass)
+    return SPEC_ERR_INVALID_ARG;
+  if (k > 0 && (!hidden_draft || !draft_tokens || !u_accept || !p_out || !q_out))
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned(hidden_target, 16) || !aligned(w_lm, 16) || (k > 0 && !aligned(hidden_draft, 16)))
+    return SPEC_ERR_ALIGNMENT;
+  if (!aligned(accepted_len, 4) || !aligned(out_tokens, 4) || !aligned(u_sample, 4) ||
+      !aligned(resid_mass, 4) ||
+      (k > 0 && (!aligned(draft_tokens, 4) || !aligned(u_accept, 4) || !aligned(p_out, 4) ||
+                 !aligned(q_out, 4))))
+    return SPEC_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
+  const int rows_t = B * (k + 1), rows_d = B * k, rows_2 = 2 * B;
+  const int ntiles = (V + sv::kLmBV - 1) / sv::kLmBV;
+  int gy0 = 0, grp0 = 0, gy1 = 0, grp1 = 0, gy2 = 0, grp2 = 0, gx = 0;
+  if (!lm_row_groups(rows_t, &gy0, &grp0) || !lm_row_groups(rows_d, &gy1, &grp1) ||
+      !lm_row_groups(rows_2, &gy2, &grp2) || gy0 + gy1 > 65535)
+    return SPEC_ERR_INVALID_ARG;
+  spec_status_t st = lm_grid_x(ntiles, &gx);
+  if (st != SPEC_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + L.off_arg);
+  float* lbuf = reinterpret_cast<float*>(ws + L.off_log);
+  CUtensorMap map_ht, map_hd, map_w, map_hb;
+  st = encode_bf16_kmajor(&map_ht, hidden_target, d, rows_t, sv::kLmHBox);
+  if (st != SPEC_OK) return st;
+  st = k > 0 ? encode_bf16_kmajor(&map_hd, hidden_draft, d, rows_d, sv::kLmHBox) : SPEC_OK;
+  if (k == 0) map_hd = map_ht;  // no draft rows: never read
+  if (st != SPEC_OK) return st;
+  st = encode_bf16_kmajor(&map_w, w_lm, d, V, sv::kLmBV);
+  if (st != SPEC_OK) return st;
+  st = encode_bf16_kmajor(&map_hb, hbuf, d, rows_2, sv::kLmHBox);
+  if (st != SPEC_OK) return st;
+
+  // 1. softmax statistics of every target and draft row, and the draft
+  // tokens' logits, from the tensor cores' accumulators
+  sv::LmHeadParams lp;
+  std::memset(&lp, 0, sizeof lp);
+  lp.rows = rows_t;
+  lp.d = d;
+  lp.V = V;
+  lp.ntiles = ntiles;
+  lp.grp_rows = grp0;
+  lp.stage_bytes = sv::kLmABytes + std::max(grp0, grp1) * 128;
+  lp.flags = reinterpret_cast<unsigned*>(ws);
+  lp.ngroups0 = gy0;
+  lp.rows1 = rows_d;
+  lp.grp_rows1 = grp1;
+  lp.k = k;
+  lp.scale = (float)(1.4426950408889634 / (double)temperature);
+  lp.tokens = draft_tokens;
+  lp.spart = reinterpret_cast<sv::SoftmaxPartial*>(ws + L.off_part);
+  lp.zx = reinterpret_cast<float*>(ws + L.off_zx);
+  st = launch_lmhead<sv::kLmStats>(map_ht, map_hd, map_w, lp, gx, gy0 + gy1, stream);
+  if (st != SPEC_OK) return st;
+
+  // 2. accept test; hidden states of the rows each sequence draws from
+  sv::SampleParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  prm.target = lbuf;
+  prm.draft = lbuf;
+  prm.tokens = draft_tokens;
+  prm.u_accept = u_accept;
+  prm.u_sample = u_sample;
+  prm.scale = lp.scale;
+  prm.B = B;
+  prm.k = k;
+  prm.V = V;
+  prm.nchunks = L.nchunks;
+  prm.nrec = gx;
+  prm.accepted_len = accepted_len;
+  prm.out_tokens = out_tokens;
+  prm.p_out = p_out;
+  prm.q_out = q_out;
+  prm.resid_mass = resid_mass;
+  prm.flags = lp.flags;
+  prm.part = lp.spart;
+  prm.desc = reinterpret_cast<sv::DrawDesc*>(ws + L.off_desc);
+  prm.csum = reinterpret_cast<sv::FSum*>(ws + L.off_csum);
+  prm.csum_p = reinterpret_cast<sv::FSum*>(ws + L.off_csum_p);
+  prm.gsum = reinterpret_cast<float*>(ws + L.off_gsum);
+  prm.gsum_p = reinterpret_cast<float*>(ws + L.off_gsum_p);
+  prm.zx = lp.zx;
+  prm.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  prm.drawn = lbuf;
+  {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    pdl_config(&cfg, attr, dim3((unsigned)B, 1, 1), dim3(sv::kThreads, 1, 1), 0, stream);
+    if (cudaLaunchKernelEx(&cfg, sv::lm_sample_gather_kernel, prm,
+                           static_cast<const uint16_t*>(hidden_target),
+                           static_cast<const uint16_t*>(hidden_draft), hbuf, d) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+
+  // 3. those rows' logits, fp32
+  sv::LmHeadParams lq = lp;
+  lq.rows = rows_2;
+  lq.grp_rows = grp2;
+  lq.stage_bytes = sv::kLmABytes + grp2 * 128;
+  lq.ngroups0 = gy2;
+  lq.rows1 = 0;
+  lq.grp_rows1 = sv::kLmHBox;
+  lq.logits = lbuf;
+  st = launch_lmhead<sv::kLmLogits>(map_hb, map_hb, map_w, lq, gx, gy2, stream);
+  if (st != SPEC_OK) return st;
+
+  // 4. the residual or bonus draw (the accept test again, then the draw over
+  // the recomputed rows), as spec_verify_sample's
+  if (vec_ok(lbuf, V, SPEC_DTYPE_F32)) return run_finish<sv::F32, true>(prm, stream);
+  return run_finish<sv::F32, false>(prm, stream);
 }
 
 spec_status_t spec_tree_grow(const void* draft_logits, int dtype, float temperature, int B,

@@ -99,6 +99,11 @@ struct SampleParams {
   // limit of each wait on a bulk copy (kWaitLimitNs unless a test shortens
   // it to exercise the timeout path); drains always use kWaitLimitNs
   unsigned long long wait_ns;
+  int nrec;   // statistics records per row (nchunks, or the LM head's CTAs)
+  // the rows the draw re-reads, when they are not the logits inputs: fp32
+  // [2B, V], row 2b the target row of sequence b's drawn position, 2b + 1 its
+  // draft row (the LM head fused with sampling recomputes them); else null
+  const float* drawn;
 };
 
 struct ArgmaxParams {
@@ -387,8 +392,8 @@ __device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out
   const int lane = threadIdx.x & 31;
   const int rows_per_seq = 2 * p.k + 1;
   const int b = row / rows_per_seq, r = row - b * rows_per_seq;
-  const SoftmaxPartial* pr = p.part + (size_t)row * p.nchunks;
-  const int nrec = p.nchunks;
+  const SoftmaxPartial* pr = p.part + (size_t)row * p.nrec;
+  const int nrec = p.nrec;
   float zx = 0.0f;
   int x = -1;
   if (r != p.k && lane == 0) {  // rows with a draft token: target r < k, draft r > k
@@ -997,10 +1002,15 @@ template <typename E>
 __device__ __forceinline__ DrawRows draw_rows(const SampleParams& p, int b, const DrawDesc& d) {
   using S = typename E::storage;
   DrawRows w;
-  w.t = reinterpret_cast<const S*>(p.target) + ((size_t)b * (p.k + 1) + d.n) * (size_t)p.V;
-  w.d = d.n < p.k
-            ? reinterpret_cast<const S*>(p.draft) + ((size_t)b * p.k + d.n) * (size_t)p.V
-            : nullptr;
+  if (p.drawn) {  // recomputed rows (fp32)
+    w.t = p.drawn + (size_t)(2 * b) * p.V;
+    w.d = d.n < p.k ? p.drawn + (size_t)(2 * b + 1) * p.V : nullptr;
+  } else {
+    w.t = reinterpret_cast<const S*>(p.target) + ((size_t)b * (p.k + 1) + d.n) * (size_t)p.V;
+    w.d = d.n < p.k
+              ? reinterpret_cast<const S*>(p.draft) + ((size_t)b * p.k + d.n) * (size_t)p.V
+              : nullptr;
+  }
   w.nref_t = d.nref_t;
   w.inv_t = d.inv_t;
   w.nref_d = d.nref_d;

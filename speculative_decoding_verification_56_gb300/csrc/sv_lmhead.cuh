@@ -47,13 +47,31 @@ constexpr int kLmBBytes = kLmMaxRows * kLmBK * 2;     // up to 48 KB: H slice
 constexpr int kLmHBox = 64;                           // rows per H box (TMA)
 constexpr int kLmTmemCols = 512;
 
+// What the epilogue makes of each accumulator tile.
+enum LmMode : int {
+  kLmArgmax = 0,  // running (max, lowest index) per row: greedy verification
+  kLmStats = 1,   // running softmax partial per row and the draft token's logit: sampling
+  kLmLogits = 2,  // the logits themselves, fp32 (the rows a sampling draw re-reads)
+};
+
 struct LmHeadParams {
-  int rows, d, V;       // rows = B * (k+1)
+  int rows, d, V;       // rows of the first matrix (argmax: B * (k+1))
   int ntiles;           // ceil(V / kLmBV)
-  int grp_rows;         // rows per row group (multiple of kLmHBox, <= kLmMaxRows)
-  int stage_bytes;      // kLmABytes + grp_rows * 128
-  ArgPartial* part;     // [rows, gridDim.x] one record per CTA segment
+  int grp_rows;         // rows per row group of the first matrix (multiple of kLmHBox)
+  int stage_bytes;      // kLmABytes + grp_rows * 128 (the largest group)
+  ArgPartial* part;     // argmax: [rows, gridDim.x] one record per CTA segment
   unsigned* flags;
+  // sampling (kLmStats): the first matrix holds the target rows [B(k+1), d],
+  // the second the drafted features [Bk, d]; records use the sampling row
+  // numbering b(2k+1) + r (r <= k target, r > k draft)
+  int ngroups0;         // row groups of the first matrix (blockIdx.y below it)
+  int rows1, grp_rows1; // rows and rows per group of the second matrix
+  int k;
+  float scale;          // log2(e) / T
+  const int32_t* tokens;    // [B, k]
+  SoftmaxPartial* spart;    // [B(2k+1), gridDim.x]
+  float* zx;                // [B(2k+1)]: the draft token's logit
+  float* logits;            // kLmLogits: [rows, V] fp32
 };
 
 // --- tcgen05 / TMA helpers (inline PTX) ------------------------------------
@@ -133,23 +151,58 @@ __device__ __forceinline__ bool lm_better(float v1, int i1, float v2, int i2) {
   return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
+// Sampling row number (b(2k+1) + r) of local row `lr` of the CTA's matrix.
+__device__ __forceinline__ int lm_sample_row(const LmHeadParams& p, bool draft, int lr) {
+  if (!draft) {
+    const int b = lr / (p.k + 1), i = lr - b * (p.k + 1);
+    return b * (2 * p.k + 1) + i;
+  }
+  const int b = lr / p.k, i = lr - b * p.k;
+  return b * (2 * p.k + 1) + p.k + 1 + i;
+}
+
+// Butterfly over the 32 lanes of a warp for 32 columns at once: afterwards
+// lane c holds the reduction of column c over all lanes in v[0].
+template <typename Op>
+__device__ __forceinline__ void lane_butterfly(float (&v)[32], Op op) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < off; ++j) {
+      const float send = upper ? v[j] : v[j + off];
+      const float keep = upper ? v[j + off] : v[j];
+      v[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+  }
+}
+
+template <int Mode>
 __global__ void __launch_bounds__(kLmThreads, 1)
-    lmhead_argmax_kernel(const __grid_constant__ CUtensorMap map_h,
-                         const __grid_constant__ CUtensorMap map_w, const LmHeadParams p) {
+    lmhead_kernel(const __grid_constant__ CUtensorMap map_h,
+                  const __grid_constant__ CUtensorMap map_h1,
+                  const __grid_constant__ CUtensorMap map_w, const LmHeadParams p) {
   extern __shared__ uint8_t lm_raw[];
   __shared__ uint64_t full[kLmStages], empty[kLmStages];
   __shared__ uint64_t acc_full, acc_empty, drain;
   __shared__ uint32_t tmem_base_holder;
   __shared__ int s_abort;
-  __shared__ float red_v[4][kLmMaxRows];  // per-quadrant column maxima of one tile
+  __shared__ float red_v[4][kLmMaxRows];  // per-quadrant column results of one tile
   __shared__ int red_i[4][kLmMaxRows];
+  __shared__ int s_tok[kLmMaxRows];       // kLmStats: the draft token of each column (row)
 
   // 1024-byte aligned operand ring (128-byte swizzle atoms)
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(lm_raw) + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = blockIdx.y * p.grp_rows;  // first row of this CTA's row group
-  const int R = p.grp_rows;                  // columns used (rows past p.rows read as 0)
+  // the CTA's row group: of the first matrix, or (sampling) of the second
+  const bool second = (int)blockIdx.y >= p.ngroups0;
+  const int R = second ? p.grp_rows1 : p.grp_rows;  // columns used (rows past the end read as 0)
+  const int row0 = second ? ((int)blockIdx.y - p.ngroups0) * p.grp_rows1 : blockIdx.y * p.grp_rows;
+  const int nrows = second ? p.rows1 : p.rows;
+  const CUtensorMap* hmap = second ? &map_h1 : &map_h;
+  const int stage_bytes = kLmABytes + R * 128;
   // the CTA owns the vocabulary tiles [T0, T1)
   int T0, T1;
   {
@@ -189,12 +242,29 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   // above overlaps that kernel's end; no global memory is touched before it
   // has finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if constexpr (Mode == kLmStats) {
+    // the draft token of each row of the group (-1: the bonus row, padding)
+    for (int c = threadIdx.x; c < R; c += kLmThreads) {
+      const int lr = row0 + c;
+      int t = -1;
+      if (lr < nrows) {
+        if (!second) {
+          const int b = lr / (p.k + 1), i = lr - b * (p.k + 1);
+          if (i < p.k) t = p.tokens[(size_t)b * p.k + i];
+        } else {
+          t = p.tokens[lr];  // draft row b*k + i carries token [b, i]
+        }
+      }
+      s_tok[c] = t;
+    }
+    __syncthreads();
+  }
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     int stage = 0, issued = 0;
     unsigned phase = 0;
-    const unsigned bytes = (unsigned)p.stage_bytes;
+    const unsigned bytes = (unsigned)stage_bytes;
     for (int j = 0; j < nsteps && !*(volatile int*)&s_abort; ++j) {
       const int t = T0 + j;
       for (int kb = 0; kb < nk; ++kb) {
@@ -209,7 +279,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         mbar_expect_tx(&full[stage], bytes);
         tma_load_2d(st, &map_w, kb * kLmBK, t * kLmBV, &full[stage]);
         for (int r = 0; r < R; r += kLmHBox)
-          tma_load_2d(st + kLmABytes + r * 128, &map_h, kb * kLmBK, row0 + r, &full[stage]);
+          tma_load_2d(st + kLmABytes + r * 128, hmap, kb * kLmBK, row0 + r, &full[stage]);
         if (++stage == kLmStages) {
           stage = 0;
           phase ^= 1u;
@@ -260,15 +330,16 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     mbar_wait_bounded(&drain, 0);
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
-    // Accumulator lane = vocabulary entry of the tile, column = row.  Each
-    // warp reduces its 32 lanes per column with a butterfly that leaves
-    // column c's (max, lowest index) in lane c; the four quadrants' results
-    // meet in shared memory and each epilogue thread keeps the running best
-    // of rows e, e + 128, ... over the CTA's tiles.
+    // Accumulator lane = vocabulary entry of the tile, column = row.  Argmax
+    // and statistics reduce each warp's 32 lanes per column with a butterfly
+    // that leaves column c's result in lane c; the four quadrants' results
+    // meet in shared memory and each epilogue thread keeps the running
+    // result of rows e, e + 128, ... over the CTA's tiles.
     const int q = warp & 3;   // tensor-memory lane quadrant of this warp
     const int e = threadIdx.x - 64;  // 0..127 among the epilogue threads
     float best[kLmMaxRows / 128];
     int bidx[kLmMaxRows / 128];
+    StatsState run[kLmMaxRows / 128];
 #pragma unroll
     for (int j = 0; j < kLmMaxRows / 128; ++j) {
       best[j] = -INFINITY;
@@ -297,58 +368,122 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       for (int cb = 0; cb < R / 32; ++cb) {
         uint32_t r[32];
         tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + cb * 32, r);
-        float v[32];
-        int ix[32];
+        if constexpr (Mode == kLmArgmax) {
+          float v[32];
+          int ix[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          v[c] = valid ? __uint_as_float(r[c]) : -INFINITY;
-          ix[c] = valid ? vocab : 0x7FFFFFFF;
-        }
+          for (int c = 0; c < 32; ++c) {
+            v[c] = valid ? __uint_as_float(r[c]) : -INFINITY;
+            ix[c] = valid ? vocab : 0x7FFFFFFF;
+          }
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-          const bool upper = (lane & off) != 0;
+          for (int off = 16; off >= 1; off >>= 1) {
+            const bool upper = (lane & off) != 0;
 #pragma unroll
-          for (int j = 0; j < off; ++j) {
-            const float send_v = upper ? v[j] : v[j + off];
-            const int send_i = upper ? ix[j] : ix[j + off];
-            const float keep_v = upper ? v[j + off] : v[j];
-            const int keep_i = upper ? ix[j + off] : ix[j];
-            const float got_v = __shfl_xor_sync(0xffffffffu, send_v, off);
-            const int got_i = __shfl_xor_sync(0xffffffffu, send_i, off);
-            const bool take = lm_better(got_v, got_i, keep_v, keep_i);
-            v[j] = take ? got_v : keep_v;
-            ix[j] = take ? got_i : keep_i;
+            for (int jj = 0; jj < off; ++jj) {
+              const float send_v = upper ? v[jj] : v[jj + off];
+              const int send_i = upper ? ix[jj] : ix[jj + off];
+              const float keep_v = upper ? v[jj + off] : v[jj];
+              const int keep_i = upper ? ix[jj + off] : ix[jj];
+              const float got_v = __shfl_xor_sync(0xffffffffu, send_v, off);
+              const int got_i = __shfl_xor_sync(0xffffffffu, send_i, off);
+              const bool take = lm_better(got_v, got_i, keep_v, keep_i);
+              v[jj] = take ? got_v : keep_v;
+              ix[jj] = take ? got_i : keep_i;
+            }
+          }
+          red_v[q][cb * 32 + lane] = v[0];
+          red_i[q][cb * 32 + lane] = ix[0];
+        } else if constexpr (Mode == kLmStats) {
+          float z[32], v[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            z[c] = valid ? __uint_as_float(r[c]) : -INFINITY;
+            v[c] = z[c];
+          }
+          // the draft token's logit, from the lane that holds it
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int col = cb * 32 + c;
+            if (valid && s_tok[col] == vocab && row0 + col < nrows)
+              p.zx[lm_sample_row(p, second, row0 + col)] = z[c];
+          }
+          // per column: the quadrant's integer reference, then its sum
+          lane_butterfly(v, [](float a, float b) { return fmaxf(a, b); });
+          const int ref = exp_ref(v[0], p.scale);  // column (cb*32 + lane)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float nref = -(float)__shfl_sync(0xffffffffu, ref, c);
+            v[c] = ex2(__fmaf_rn(z[c], p.scale, nref));  // 2^-inf = 0 past the vocabulary
+          }
+          lane_butterfly(v, [](float a, float b) { return __fadd_rn(a, b); });
+          red_v[q][cb * 32 + lane] = v[0];
+          red_i[q][cb * 32 + lane] = ref;
+        } else {
+          // the logits: for each column (row) the warp's 32 lanes store 32
+          // consecutive vocabulary entries
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int lr = row0 + cb * 32 + c;
+            if (valid && lr < nrows)
+              p.logits[(size_t)lr * p.V + vocab] = __uint_as_float(r[c]);
           }
         }
-        red_v[q][cb * 32 + lane] = v[0];
-        red_i[q][cb * 32 + lane] = ix[0];
       }
       tmem_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty);  // tensor memory read: next tile may start
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four quadrants' maxima are in
+      if constexpr (Mode != kLmLogits) {
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four quadrants' results are in
 #pragma unroll
-      for (int j = 0; j < kLmMaxRows / 128; ++j) {
-        const int c = e + 128 * j;
-        if (c < R) {
+        for (int jj = 0; jj < kLmMaxRows / 128; ++jj) {
+          const int c = e + 128 * jj;
+          if (c < R) {
+            if constexpr (Mode == kLmArgmax) {
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq)
-            if (lm_better(red_v[qq][c], red_i[qq][c], best[j], bidx[j])) {
-              best[j] = red_v[qq][c];
-              bidx[j] = red_i[qq][c];
+              for (int qq = 0; qq < 4; ++qq)
+                if (lm_better(red_v[qq][c], red_i[qq][c], best[jj], bidx[jj])) {
+                  best[jj] = red_v[qq][c];
+                  bidx[jj] = red_i[qq][c];
+                }
+            } else {
+              // the tile's partial of this row: the four quadrants rescaled
+              // (exactly, powers of two) to their largest reference
+              int tref = kRefEmpty;
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) tref = max(tref, red_i[qq][c]);
+              float tsum = 0.0f;
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq)
+                tsum = __fadd_rn(tsum, red_v[qq][c] * pow2i_f(red_i[qq][c] - tref));
+              if (tref > run[jj].ref) {
+                run[jj].acc.scale(pow2i_f(run[jj].ref - tref));
+                run[jj].ref = tref;
+              }
+              run[jj].acc.add(tsum * pow2i_f(tref - run[jj].ref));
             }
+          }
         }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the scratch may be reused
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // the scratch may be reused
       acc_phase ^= 1u;
     }
     const int C = gridDim.x;
 #pragma unroll
-    for (int j = 0; j < kLmMaxRows / 128; ++j) {
-      const int row = row0 + e + 128 * j;
-      if (e + 128 * j < R && row < p.rows)
-        p.part[(size_t)row * C + blockIdx.x] =
-            ArgPartial{best[j], bidx[j], nsteps > 0 ? 1 : 0, 0};
+    for (int jj = 0; jj < kLmMaxRows / 128; ++jj) {
+      const int lr = row0 + e + 128 * jj;
+      if (e + 128 * jj < R && lr < nrows) {
+        if constexpr (Mode == kLmArgmax) {
+          p.part[(size_t)lr * C + blockIdx.x] = ArgPartial{best[jj], bidx[jj], nsteps > 0 ? 1 : 0, 0};
+        } else if constexpr (Mode == kLmStats) {
+          SoftmaxPartial sp;
+          sp.ref = run[jj].ref;
+          sp.nch = nsteps > 0 ? 1 : 0;
+          sp.hi = run[jj].acc.hi;
+          sp.lo = run[jj].acc.lo;
+          p.spart[(size_t)lm_sample_row(p, second, lr) * C + blockIdx.x] = sp;
+        }
+      }
     }
   }
   tmem_fence_before();
@@ -358,6 +493,43 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kLmTmemCols)
                  : "memory");
+  }
+}
+
+// LM head fused with sampling verification, between the statistics GEMM and
+// the recomputation of the drawn rows: one CTA per sequence merges its rows'
+// records, runs the accept test, and copies the hidden states of the rows
+// the draw needs into hbuf [2B, d] (row 2b: the target row of the drawn
+// position, 2b + 1: its draft row, zero for the bonus draw).
+__global__ void __launch_bounds__(kThreads) lm_sample_gather_kernel(const SampleParams p,
+                                                                    const uint16_t* h_target,
+                                                                    const uint16_t* h_draft,
+                                                                    uint16_t* hbuf, int d) {
+  __shared__ RowStats s_rows[kMaxSeqRows];
+  __shared__ int s_n;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the statistics records
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int b = blockIdx.x, warp = threadIdx.x >> 5;
+  const int rows_per_seq = 2 * p.k + 1;
+  for (int r = warp; r < rows_per_seq; r += kWarps)
+    finalize_stats_row<F32>(p, b * rows_per_seq + r, &s_rows[r]);
+  __syncthreads();
+  if (warp == 0) {
+    const DrawDesc dd = resolve_sample_seq(p, b, [&](int r) { return s_rows[r]; }, false);
+    if ((threadIdx.x & 31) == 0) s_n = dd.n;
+  }
+  __syncthreads();
+  const int n = s_n;
+  const uint4* src_t =
+      reinterpret_cast<const uint4*>(h_target + ((size_t)b * (p.k + 1) + n) * (size_t)d);
+  const uint4* src_d =
+      n < p.k ? reinterpret_cast<const uint4*>(h_draft + ((size_t)b * p.k + n) * (size_t)d)
+              : nullptr;
+  uint4* dst_t = reinterpret_cast<uint4*>(hbuf + (size_t)(2 * b) * d);
+  uint4* dst_d = reinterpret_cast<uint4*>(hbuf + (size_t)(2 * b + 1) * d);
+  for (int i = threadIdx.x; i < d / 8; i += kThreads) {
+    dst_t[i] = src_t[i];
+    dst_d[i] = src_d ? src_d[i] : make_uint4(0, 0, 0, 0);
   }
 }
 

@@ -44,8 +44,8 @@ def flag_allowance(mu: float) -> int:
     return int(np.floor(mu + 4.0 * np.sqrt(mu) + 1.0))
 
 
-def flagged_rows(orc: dict) -> np.ndarray:
-    return (orc["acc_margin"] < FLAG_WINDOW) | (orc["cdf_margin"] < FLAG_WINDOW)
+def flagged_rows(orc: dict, window: float = FLAG_WINDOW) -> np.ndarray:
+    return (orc["acc_margin"] < window) | (orc["cdf_margin"] < window)
 
 
 def _check_structure(n, tok, drafts, rows_idx):
@@ -57,12 +57,13 @@ def _check_structure(n, tok, drafts, rows_idx):
         assert (tok[i, n[i] + 1:] == -1).all(), f"row {i}: slots after the draw are not -1"
 
 
-def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None, case=None):
+def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None, case=None,
+                   window=FLAG_WINDOW, pq_rtol=PQ_RTOL):
     """Assert sampling parity.  ``gpu`` holds numpy copies of the CUDA outputs
     (accepted_len, out_tokens, p, q, resid_mass); ``orc`` the oracle's result
-    for the same rows; ``case`` the inputs (needed to validate rows that
-    differ).  ``rows`` selects which GPU rows ``orc`` covers.  Returns a
-    summary dict."""
+    for the same rows (computed with the same flag ``window``); ``case`` the
+    inputs (needed to validate rows that differ).  ``rows`` selects which GPU
+    rows ``orc`` covers.  Returns a summary dict."""
     sel = slice(None) if rows is None else rows
     g_n = np.asarray(gpu["accepted_len"])[sel]
     g_tok = np.asarray(gpu["out_tokens"])[sel]
@@ -70,7 +71,7 @@ def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None, case=None)
     g_q = np.asarray(gpu["q"], dtype=np.float64)[sel]
     g_R = np.asarray(gpu["resid_mass"], dtype=np.float64)[sel]
     n_rows = g_n.shape[0]
-    flags = flagged_rows(orc)
+    flags = flagged_rows(orc, window)
     nflag = int(flags.sum())
     mu = float(np.sum(orc["flag_prob"]))
     if allow_flags is None:
@@ -80,7 +81,7 @@ def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None, case=None)
     # p and q on every row and position
     for name, gv, ov in (("p", g_p, orc["p"]), ("q", g_q, orc["q"])):
         err = np.abs(gv - ov)
-        lim = PQ_RTOL * np.abs(ov) + PQ_ATOL
+        lim = pq_rtol * np.abs(ov) + PQ_ATOL
         worst = np.unravel_index(np.argmax(err - lim), err.shape) if err.size else None
         assert (err <= lim).all(), f"{name} out of tolerance at {worst}: gpu {gv[worst]} " \
             f"oracle {ov[worst]}"
@@ -108,12 +109,12 @@ def compare_sample(gpu: dict, orc: dict, rows=None, allow_flags=None, case=None)
             drafts, case.u_accept[case_rows], case.u_sample[case_rows], case.temperature,
             g_n[idx], g_tok[idx, g_n[idx]], dtype=case.dtype)
         max_violation = float(viol.max())
-        assert (viol < FLAG_WINDOW).all(), \
-            f"rows {idx[viol >= FLAG_WINDOW]} hold outcomes outside the window: " \
-            f"violations {viol[viol >= FLAG_WINDOW]}"
+        assert (viol < window).all(), \
+            f"rows {idx[viol >= window]} hold outcomes outside the window: " \
+            f"violations {viol[viol >= window]}"
         ref_R[idx] = claim_R
     errR = np.abs(g_R - ref_R)
-    limR = np.maximum(R_RTOL * np.abs(ref_R), R_ATOL)
+    limR = np.maximum(max(R_RTOL, pq_rtol) * np.abs(ref_R), R_ATOL)
     badR = np.nonzero(errR > limR)[0]
     assert badR.size == 0, f"resid_mass out of tolerance rows {badR[:10]}: " \
         f"gpu {g_R[badR[:5]]} oracle {ref_R[badR[:5]]}"
