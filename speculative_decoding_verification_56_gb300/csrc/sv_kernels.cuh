@@ -56,7 +56,8 @@ struct ArgPartial {
 struct RowStats {  // one row after the merge
   int ref;         // integer reference R of the row
   float inv_sum;   // 1 / S rounded to float
-  double prob;     // p (or q) of the row's draft token, float64
+  float pm;        // p (or q) of the row's draft token is pm 2^pe exactly,
+  int pe;          // and zero when pe < -1022 (the float64 range)
 };
 
 // What the draw needs of sequence b: the selected position n and the
@@ -373,13 +374,36 @@ __device__ __forceinline__ void emit_arg_seg(const ArgmaxParams& p, const ArgSta
 // ---------------------------------------------------------------------------
 // Row and sequence finalisation (one warp per row / sequence / tree)
 // ---------------------------------------------------------------------------
-// 2^x / S as float64 for x <= 1 and S >= 1/2: the float mantissa
-// 2^frac(x) / S times the exact power of two 2^floor(x), so probabilities far
-// below the float range keep their value (float-pipe arithmetic except the
-// final exact scaling).
-__device__ __forceinline__ double exp2_over(float x, float S) {
+// p = 2^x / S for x <= 1 and S >= 1/2, as a float mantissa 2^frac(x) / S
+// and the exact power of two 2^floor(x), so probabilities far below the float
+// range keep their value; zero (pe below -1022, as in float64) for x = -inf.
+__device__ __forceinline__ void exp2_over(float x, float S, float* pm, int* pe) {
   const float n = floorf(x);
-  return pow2i_d((int)n) * (double)__fdiv_rn(ex2(__fsub_rn(x, n)), S);
+  *pe = n < -2000.0f ? -2000 : (int)n;
+  *pm = __fdiv_rn(ex2(__fsub_rn(x, n)), S);
+}
+
+// The row's token probability rounded to float (the call's p and q outputs).
+__device__ __forceinline__ float prob_float(const RowStats& r) {
+  return r.pe < -1022 ? 0.0f : ldexpf(r.pm, r.pe);
+}
+
+// The accept test u q < p with p = pm 2^pe, q = qm 2^qe, decided exactly as
+// float64 arithmetic decides it (u qm has at most 48 significant bits, so
+// the float64 product is exact).  u qm is formed exactly as a float pair
+// (product and fma remainder) and compared with pm 2^(pe - qe); uniforms
+// below 2^-60 or exponent gaps beyond 60 take the float64 product.
+__device__ __forceinline__ bool accept_test(float u, float pm, int pe, float qm, int qe) {
+  if (pe < -1022) return false;  // u q < 0 never holds
+  if (qe < -1022 || u == 0.0f) return true;
+  const int e = pe - qe;
+  if (u >= 0x1p-60f && e >= -60 && e <= 60) {
+    const float a = __fmul_rn(u, qm);
+    const float r = __fmaf_rn(u, qm, -a);
+    const float t = __fmul_rn(pm, __int_as_float((e + 127) << 23));
+    return a < t || (a == t && r < 0.0f);
+  }
+  return (double)u * ((double)qm * pow2i_d(qe)) < (double)pm * pow2i_d(pe);
 }
 
 // Merge one row's segment records (one warp).  Loads are issued four per
@@ -430,17 +454,17 @@ __device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out
   acc.scale(pow2i_f(lref - R));
   const FSum S = df_norm(warp_sum_df(acc));
   if (lane == 0) {
-    double prob = 0.0;
-    if (r != p.k) {
-      if (x >= 0 && x < p.V)
-        prob = exp2_over(__fmaf_rn(zx, p.scale, -(float)R), S.hi);
-      else
-        set_flag(p.flags, kFlagTokenRange);
-    }
     RowStats rs;
     rs.ref = R;
     rs.inv_sum = __frcp_rn(S.hi);
-    rs.prob = prob;
+    rs.pm = 0.0f;
+    rs.pe = -2000;  // probability zero
+    if (r != p.k) {
+      if (x >= 0 && x < p.V)
+        exp2_over(__fmaf_rn(zx, p.scale, -(float)R), S.hi, &rs.pm, &rs.pe);
+      else
+        set_flag(p.flags, kFlagTokenRange);
+    }
     *out = rs;
   }
 }
@@ -448,11 +472,13 @@ __device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out
 // Accept test left to right and first rejection of sequence b (one warp),
 // from the sequence's merged rows `rs` (index r of rows_per_seq).  Returns the
 // draw descriptor; with `write`, also stores the call's outputs for b (all
-// but the drawn token) and the descriptor.
+// but the drawn token) and the descriptor.  `ua` and `tok`, when given, hold
+// the sequence's uniforms and draft tokens (prefetched).
 template <typename RowFn>
 __device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, RowFn rs, bool write,
-                                       const float* ua = nullptr) {
+                                       const float* ua = nullptr, const int* tok = nullptr) {
   if (!ua) ua = p.u_accept + (size_t)b * p.k;
+  if (!tok) tok = p.tokens + (size_t)b * p.k;
   const int lane = threadIdx.x & 31;
   const int k = p.k;
   int n = k;
@@ -460,14 +486,12 @@ __device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, RowFn rs, b
     const int i = i0 + lane;
     bool rej = false;
     if (i < k) {
-      const double pi = rs(i).prob;
-      const double qi = rs(k + 1 + i).prob;
+      const RowStats ri = rs(i), rq = rs(k + 1 + i);
       if (write) {
-        p.p_out[(size_t)b * k + i] = (float)pi;
-        p.q_out[(size_t)b * k + i] = (float)qi;
+        p.p_out[(size_t)b * k + i] = prob_float(ri);
+        p.q_out[(size_t)b * k + i] = prob_float(rq);
       }
-      const double u = (double)ua[i];
-      rej = !(u * qi < pi);
+      rej = !accept_test(ua[i], ri.pm, ri.pe, rq.pm, rq.pe);
     }
     const unsigned m = __ballot_sync(0xffffffffu, rej);
     if (n == k && m) n = i0 + __ffs(m) - 1;
@@ -487,7 +511,7 @@ __device__ DrawDesc resolve_sample_seq(const SampleParams& p, int b, RowFn rs, b
   d.pad[0] = d.pad[1] = d.pad[2] = 0;
   if (write) {
     for (int i = lane; i <= k; i += 32)
-      p.out_tokens[(size_t)b * (k + 1) + i] = (i < n) ? p.tokens[(size_t)b * k + i] : -1;
+      p.out_tokens[(size_t)b * (k + 1) + i] = (i < n) ? tok[i] : -1;
     if (lane == 0) {
       p.accepted_len[b] = n;
       p.desc[b] = d;
@@ -1372,29 +1396,68 @@ constexpr int kClusterMaxChunks = kClusterCTAs * kLocalChunks;
 constexpr size_t kFinishGroupBytes = (size_t)kLocalChunks * kVecPerChunk * sizeof(float);
 constexpr size_t kFinishSmem = kFinishGroupBytes + 2 * (size_t)kChunkBytes;
 
-// Exclusive/inclusive double-float scan of lane values (n <= 32 lanes) with
-// the first lane whose inclusive prefix exceeds `target` (else the last lane
-// with positive value).  Returns the total; *sel, *excl for the chosen lane.
-__device__ __forceinline__ FSum lane_prefix_select(const FSum& v, int n, const FSum* target,
-                                                   int* sel, FSum* excl_sel) {
+// Quad sums of one chunk's group array (thread t: vectors 4t..4t+3) and
+// their inclusive scan within each warp; lane 31 leaves the warp's total in
+// wt[warp].  Every evaluation over the same group array gives the same
+// values, so the walk can repeat it for one warp.
+__device__ __forceinline__ FSum quad_scan(const float* s_g, FSum* wt, FSum* my_quad) {
+  const FSum q = quad_sum(*reinterpret_cast<const float4*>(s_g + 4 * threadIdx.x));
+  const FSum inc = warp_scan_df(q);
+  if (wt && (threadIdx.x & 31) == 31) wt[threadIdx.x >> 5] = inc;
+  *my_quad = q;
+  return inc;
+}
+
+// Prefixes of the warp totals of up to two local chunks at once (one warp,
+// a 16-lane scan per chunk): wp[lc][i] = wt[lc][0] + ... + wt[lc][i], and
+// ctot[lc] = wp[lc][kWarps - 1], the chunk total.  The walk compares the
+// target against these same prefixes to pick the warp block.
+static_assert(kWarps == 16, "two chunks of warp totals per warp scan");
+__device__ __forceinline__ void warp_prefixes(const FSum (*wt)[kWarps], FSum (*wp)[kWarps],
+                                              FSum* ctot, int nl) {
+  const int lane = threadIdx.x & 31;
+  for (int lc0 = 0; lc0 < nl; lc0 += 2) {
+    const int lc = lc0 + (lane >> 4), i = lane & 15;
+    FSum v = lc < nl ? wt[lc][i] : FSum::zero();
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      FSum y;
+      y.hi = __shfl_up_sync(0xffffffffu, v.hi, o);
+      y.lo = __shfl_up_sync(0xffffffffu, v.lo, o);
+      if (i >= o) v = df_add(y, v);
+    }
+    if (lc < nl) {
+      wp[lc][i] = v;
+      if (i == 15) ctot[lc] = v;
+    }
+  }
+}
+
+// Chunk choice of the draw (one warp, n <= 32 chunk totals v in lane order):
+// the normalised inclusive scan gives the total; the target is u * total;
+// the chosen chunk is the first whose inclusive prefix exceeds the target
+// (else the last with positive mass), with its exclusive prefix.
+struct ChunkChoice {
+  FSum total, target, base;
+  int c;
+};
+__device__ __forceinline__ ChunkChoice choose_chunk(const FSum& v, int n, float u) {
   const int lane = threadIdx.x & 31;
   const FSum inc = df_norm(warp_scan_df(v));
+  ChunkChoice ch;
+  ch.total.hi = __shfl_sync(0xffffffffu, inc.hi, 31);
+  ch.total.lo = __shfl_sync(0xffffffffu, inc.lo, 31);
+  ch.target = df_mul_f(u, ch.total);
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < n && df_less(ch.target, inc));
+  const unsigned pos = __ballot_sync(0xffffffffu, lane < n && v.hi > 0.0f);
+  ch.c = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
   FSum excl;
   excl.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
   excl.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
   if (lane == 0) excl = FSum::zero();
-  FSum tot;
-  tot.hi = __shfl_sync(0xffffffffu, inc.hi, 31);
-  tot.lo = __shfl_sync(0xffffffffu, inc.lo, 31);
-  if (target) {
-    const unsigned hit = __ballot_sync(0xffffffffu, lane < n && df_less(*target, inc));
-    const unsigned pos = __ballot_sync(0xffffffffu, lane < n && v.hi > 0.0f);
-    const int L = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
-    *sel = L;
-    excl_sel->hi = __shfl_sync(0xffffffffu, excl.hi, L);
-    excl_sel->lo = __shfl_sync(0xffffffffu, excl.lo, L);
-  }
-  return tot;
+  ch.base.hi = __shfl_sync(0xffffffffu, excl.hi, ch.c);
+  ch.base.lo = __shfl_sync(0xffffffffu, excl.lo, ch.c);
+  return ch;
 }
 
 // Group sums of one chunk's draw weights from 16-byte vectors already in
@@ -1419,6 +1482,130 @@ __device__ __forceinline__ void draw_groups_from(const SampleParams& p, const Dr
   }
 }
 
+// Walk of the chosen chunk by its owner CTA, from what the chunk pass left:
+// the group sums (s_g), the warp totals (wt) and their sequential prefixes
+// (wp).
+// Warp 0 picks the warp block from the prefixes; that block's warp scans its
+// quads, loads its block's vectors (coalesced, while it scans), and finds
+// the vector and element all at once: lane l takes element l % E of the
+// quad's vector l / E, recomputes that vector's weights and adds them in the
+// order of the group sums, so each lane holds exactly the running sum a
+// sequential walk reaches at its element.  Rounding that leaves the target
+// just past a level's end takes the last position with positive weight, as
+// in walk_chunk.
+struct QuadWalk {
+  FSum wbase;
+  int wb, exact, tok;
+};
+
+template <typename E, bool kVec>
+__device__ int walk_chunk_quads(const SampleParams& p, const DrawRows& w, bool resid,
+                                const float* s_g, const FSum* wt, const FSum* wp, int cstar,
+                                const FSum& target, const FSum& base, QuadWalk& qw) {
+  using St = typename E::storage;
+  constexpr int kE = E::kEPV;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int j0 = cstar * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
+  const int nvec = (j1 - j0 + kE - 1) / kE;
+  if (warp == 0) {
+    const FSum pre = lane < kWarps ? df_add(base, wp[lane]) : FSum::zero();
+    const float wv = lane < kWarps ? wt[lane].hi : 0.0f;
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < kWarps && df_less(target, df_norm(pre)));
+    const unsigned pos = __ballot_sync(0xffffffffu, lane < kWarps && wv > 0.0f);
+    const int wb = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+    FSum prev;
+    prev.hi = __shfl_sync(0xffffffffu, pre.hi, wb > 0 ? wb - 1 : 0);
+    prev.lo = __shfl_sync(0xffffffffu, pre.lo, wb > 0 ? wb - 1 : 0);
+    if (lane == 0) {
+      qw.wb = wb;
+      qw.exact = hit != 0;
+      qw.wbase = wb > 0 ? prev : base;
+      qw.tok = -1;
+    }
+  }
+  __syncthreads();
+  if (warp == qw.wb) {
+    // this warp block's vectors, coalesced: lane l holds vectors 32 i + l
+    const uint4 ninf = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+    uint4 xt[4], xd[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int vi = 128 * warp + 32 * i + lane;
+      const int j = j0 + vi * kE;
+      xt[i] = vi < nvec ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.t), j, j1) : ninf;
+      xd[i] = (resid && vi < nvec)
+                  ? fetch_vec<E, kVec>(reinterpret_cast<const St*>(w.d), j, j1)
+                  : ninf;
+    }
+    FSum q;
+    const FSum inc = quad_scan(s_g, nullptr, &q);
+    FSum exc;
+    exc.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
+    exc.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
+    if (lane == 0) exc = FSum::zero();
+    const FSum wbase = qw.wbase;
+    const unsigned qhit =
+        __ballot_sync(0xffffffffu, qw.exact && df_less(target, df_norm(df_add(wbase, inc))));
+    const unsigned qpos = __ballot_sync(0xffffffffu, q.hi > 0.0f);
+    const int L = qhit ? (__ffs(qhit) - 1) : (qpos ? (31 - __clz(qpos)) : 0);
+    FSum run;
+    run.hi = __shfl_sync(0xffffffffu, exc.hi, L);
+    run.lo = __shfl_sync(0xffffffffu, exc.lo, L);
+    run = df_add(wbase, run);
+    const bool act = lane < 4 * kE;
+    const int v = act ? lane / kE : 3, e = lane % kE;
+    // vector v of quad L is vector 4L + v of the block: lane (4L + v) % 32,
+    // register L / 8 (the same for every lane)
+    const int r = L >> 3, srcl = (4 * L + v) & 31;
+    const uint4 st = r == 0 ? xt[0] : r == 1 ? xt[1] : r == 2 ? xt[2] : xt[3];
+    const uint4 sd = r == 0 ? xd[0] : r == 1 ? xd[1] : r == 2 ? xd[2] : xd[3];
+    uint4 at, ad;
+    at.x = __shfl_sync(0xffffffffu, st.x, srcl);
+    at.y = __shfl_sync(0xffffffffu, st.y, srcl);
+    at.z = __shfl_sync(0xffffffffu, st.z, srcl);
+    at.w = __shfl_sync(0xffffffffu, st.w, srcl);
+    ad.x = __shfl_sync(0xffffffffu, sd.x, srcl);
+    ad.y = __shfl_sync(0xffffffffu, sd.y, srcl);
+    ad.z = __shfl_sync(0xffffffffu, sd.z, srcl);
+    ad.w = __shfl_sync(0xffffffffu, sd.w, srcl);
+    const int quad = warp * 32 + L;
+    const float4 g4 = *reinterpret_cast<const float4*>(s_g + 4 * quad);
+    const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+    // running sum before vector v, as a walk over the quad's vectors adds it
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+      if (i < v && gv[i] > 0.0f) run = df_add(run, df_from(gv[i]));
+    const float gme = v == 0 ? gv[0] : v == 1 ? gv[1] : v == 2 ? gv[2] : gv[3];
+    const bool vhit =
+        act && qhit != 0 && gme > 0.0f && df_less(target, df_norm(df_add(run, df_from(gme))));
+    float part = 0.0f, we = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kE; ++i) {
+      const float wi =
+          draw_weight(E::elem(at, i), resid ? E::elem(ad, i) : 0.0f, p.scale, w, resid, i);
+      if (i <= e) part = __fadd_rn(part, wi);
+      if (i == e) we = wi;
+    }
+    const int jj = j0 + (4 * quad + v) * kE + e;
+    const unsigned vh = __ballot_sync(0xffffffffu, vhit && e == 0);
+    const unsigned vp = __ballot_sync(0xffffffffu, act && e == 0 && gme > 0.0f);
+    // the first vector whose end passes the target, else the last positive one
+    const int vsel = vh ? (__ffs(vh) - 1) / kE : (vp ? (31 - __clz(vp)) / kE : -1);
+    const bool mine = act && v == vsel;
+    const unsigned eh = __ballot_sync(
+        0xffffffffu,
+        vh != 0 && mine && we > 0.0f && df_less(target, df_norm(df_add(run, df_from(part)))));
+    const unsigned lp = __ballot_sync(0xffffffffu, mine && we > 0.0f && jj < j1);
+    const int src = eh ? (__ffs(eh) - 1) : (lp ? (31 - __clz(lp)) : 0);
+    const int tj = __shfl_sync(0xffffffffu, jj, src);
+    if (lane == 0) qw.tok = (eh | lp) ? tj : -1;
+  }
+  __syncthreads();
+  int tok = qw.tok;
+  if (tok < 0 || tok >= p.V) tok = min(j0, p.V - 1);  // unreachable with finite inputs
+  return tok;
+}
+
 template <typename E, bool kVec>
 __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const SampleParams p) {
   using St = typename E::storage;
@@ -1430,7 +1617,8 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   __shared__ int s_tok[kMaxDraft];
   __shared__ float s_ua[kMaxDraft];
   __shared__ FSum s_ctot[kLocalChunks];
-  __shared__ WalkScratch ws;
+  __shared__ FSum s_wt[kLocalChunks][kWarps], s_wp[kLocalChunks][kWarps];
+  __shared__ QuadWalk s_walk;
   __shared__ DrawDesc s_desc;
   __shared__ FSum s_target, s_base, s_total;
   __shared__ uint64_t s_bar;
@@ -1465,7 +1653,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   // 2. accept test over the whole sequence
   if (warp == 0) {
     const DrawDesc dd =
-        resolve_sample_seq(p, b, [&](int r) { return s_rows[r]; }, rank == 0, s_ua);
+        resolve_sample_seq(p, b, [&](int r) { return s_rows[r]; }, rank == 0, s_ua, s_tok);
     if (lane == 0) s_desc = dd;
   }
   __syncthreads();
@@ -1474,7 +1662,8 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   const DrawRows w = draw_rows<E>(p, b, d);
 
   // 3. prefix structure of this CTA's chunks: even local chunks through
-  // registers, odd ones through the staging buffer (bulk async copies)
+  // registers, odd ones through the staging buffer (bulk async copies);
+  // each chunk leaves its group sums (s_g) and its warp totals (s_wt)
   // thread 0 keeps at most one staging copy (pair) in flight; stage_pending
   // is the barrier parity of the one it has not yet seen land (-1: none)
   int stage_pending = -1;
@@ -1525,23 +1714,29 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
       }
     }
     draw_groups_from<E>(p, w, resid, nvec, vt, vd, g);
-    __syncthreads();
-    FSum inc, qd;
-    const FSum t = chunk_scan_cta(g, ws.w, &inc, &qd);
-    if (threadIdx.x == 0) s_ctot[lc] = t;
-    __syncthreads();
+    __syncthreads();  // the chunk's group sums are complete
+    FSum q;
+    quad_scan(g, s_wt[lc], &q);
   }
+  const int nl = (C - rank + kClusterCTAs - 1) / kClusterCTAs;  // local chunks
+  __syncthreads();  // warp totals of every local chunk
+  if (warp == 0) warp_prefixes(s_wt, s_wp, s_ctot, nl);
   cluster.sync();
 
-  // 4. chunk totals from their owners; every CTA computes the same total, so
-  // the rare fallback below is taken by the whole cluster or by none of it
+  // 4. chunk totals from their owners (one read of the peers' shared
+  // memory); every CTA computes the same total, so the rare fallback below
+  // is taken by the whole cluster or by none of it
   if (warp == 0) {
     FSum v = FSum::zero();
     if (lane < C) v = *cluster.map_shared_rank(&s_ctot[lane / kClusterCTAs], lane % kClusterCTAs);
-    int sel = 0;
-    FSum excl;
-    const FSum total = lane_prefix_select(v, C, nullptr, &sel, &excl);
-    if (lane == 0) s_fallback = resid && !(total.hi > 0.0f);
+    const ChunkChoice ch = choose_chunk(v, C, u_sample);
+    if (lane == 0) {
+      s_fallback = resid && !(ch.total.hi > 0.0f);
+      s_c = ch.c;
+      s_base = ch.base;
+      s_target = ch.target;
+      s_total = ch.total;
+    }
   }
   __syncthreads();
   const bool fallback = s_fallback != 0;
@@ -1566,28 +1761,24 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
       }
       draw_groups_from<E>(p, w, false, nvec, vt, vd, g);
       __syncthreads();
-      FSum inc, qd;
-      const FSum t = chunk_scan_cta(g, ws.w, &inc, &qd);
-      if (threadIdx.x == 0) s_ctot[lc] = t;
-      __syncthreads();
+      FSum q;
+      quad_scan(g, s_wt[lc], &q);
     }
+    __syncthreads();
+    if (warp == 0) warp_prefixes(s_wt, s_wp, s_ctot, nl);
     cluster.sync();
-    if (rank == 0 && threadIdx.x == 0) set_flag(p.flags, kFlagResidualFallback);
-  }
-  if (warp == 0) {
-    FSum v = FSum::zero();
-    if (lane < C) v = *cluster.map_shared_rank(&s_ctot[lane / kClusterCTAs], lane % kClusterCTAs);
-    int sel = 0;
-    FSum excl;
-    const FSum total = lane_prefix_select(v, C, nullptr, &sel, &excl);
-    const FSum target = df_mul_f(u_sample, total);
-    lane_prefix_select(v, C, &target, &sel, &excl);
-    if (lane == 0) {
-      s_c = sel;
-      s_base = excl;
-      s_target = target;
-      s_total = total;
+    if (warp == 0) {
+      FSum v = FSum::zero();
+      if (lane < C) v = *cluster.map_shared_rank(&s_ctot[lane / kClusterCTAs], lane % kClusterCTAs);
+      const ChunkChoice ch = choose_chunk(v, C, u_sample);
+      if (lane == 0) {
+        s_c = ch.c;
+        s_base = ch.base;
+        s_target = ch.target;
+        s_total = ch.total;
+      }
     }
+    if (rank == 0 && threadIdx.x == 0) set_flag(p.flags, kFlagResidualFallback);
   }
   cluster.sync();  // no CTA reads a peer's shared memory after this point
 
@@ -1599,9 +1790,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   // 5. the owner of the chosen chunk walks it
   const int cstar = s_c;
   if (cstar % kClusterCTAs != rank) return;
-  const float* gsel = s_g + (cstar / kClusterCTAs) * kVecPerChunk;
-  const int tok =
-      walk_chunk<E, kVec>(p, w, resid && !fallback, gsel, cstar, s_target, s_base, ws);
+  const int lcs = cstar / kClusterCTAs;
+  const int tok = walk_chunk_quads<E, kVec>(p, w, resid && !fallback, s_g + lcs * kVecPerChunk,
+                                            s_wt[lcs], s_wp[lcs], cstar, s_target, s_base,
+                                            s_walk);
   if (threadIdx.x == 0) {
     p.out_tokens[(size_t)b * (p.k + 1) + d.n] = tok;
     p.resid_mass[b] = (d.n < p.k && !fallback) ? __fadd_rn(s_total.hi, s_total.lo) : 0.0f;
