@@ -61,7 +61,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU baseline (0 disables it)")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--profile-case", choices=["lm_head_greedy", "tree_grow"], default=None,
+    ap.add_argument("--profile-case", choices=["lm_head_greedy", "tree_grow", "sample"],
+                    default=None,
                     help="only run that kernel --calls times, untimed (for ncu)")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--skip-next-rows", action="store_true",
@@ -724,12 +725,36 @@ def grow_case(dev):
     return c
 
 
+def sample_case(dev):
+    """Sampling verification on the headline workload (B=64, k=4, V=128256,
+    bf16) over four device copies of the logits used in turn, as in the
+    per-call loops: each call reads logits that the previous three did not."""
+    import torch
+    import speculative_decoding_verification_56_gb300 as sv
+    from speculative_decoding_verification_56_gb300 import synth
+    cs = synth.zipf128k(seed=0)
+    c = {"sets": [(sv.to_device_logits(cs.target, cs.dtype, dev),
+                   sv.to_device_logits(cs.draft, cs.dtype, dev)) for _ in range(NSETS)],
+         "i": 0}
+    tok = torch.from_numpy(cs.tokens).to(dev)
+    ua = torch.from_numpy(cs.u_accept).to(dev)
+    us = torch.from_numpy(cs.u_sample).to(dev)
+    ws = sv.alloc_workspace(sv.SPEC_MODE_SAMPLE, cs.B, cs.k, cs.V, sv.SPEC_DTYPE_BF16, dev)
+
+    def call(stream):
+        t, d = c["sets"][c["i"] % NSETS]
+        c["i"] += 1
+        sv.verify_sample(t, d, tok, ua, us, cs.temperature, workspace=ws, stream=stream)
+    c["call"] = call
+    return c
+
+
 def profile_case(name, calls):
-    """Run one of the kernels around the draft tree `calls` times, untimed:
-    the program ncu profiles (`--profile-case`)."""
+    """Run one call type `calls` times, untimed: the program ncu profiles
+    (`--profile-case`)."""
     import torch
     dev = torch.device("cuda", 0)
-    c = {"lm_head_greedy": lm_head_case, "tree_grow": grow_case}[name](dev)
+    c = {"lm_head_greedy": lm_head_case, "tree_grow": grow_case, "sample": sample_case}[name](dev)
     for _ in range(calls):
         c["call"](None)
     torch.cuda.synchronize()

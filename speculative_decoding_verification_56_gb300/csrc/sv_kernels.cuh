@@ -450,9 +450,22 @@ __device__ void finalize_stats_row(const SampleParams& p, int row, RowStats* out
       }
     }
   }
-  const int R = warp_max_i(lref);
-  acc.scale(pow2i_f(lref - R));
-  const FSum S = df_norm(warp_sum_df(acc));
+  // butterfly over the lanes that hold records: the larger reference, and
+  // the other partial rescaled to it exactly (powers of two), at each step
+  const int width = nrec >= 32 ? 32 : (nrec <= 1 ? 1 : 1 << (32 - __clz(nrec - 1)));
+  for (int o = width >> 1; o > 0; o >>= 1) {
+    const int r2 = __shfl_xor_sync(0xffffffffu, lref, o);
+    FSum y;
+    y.hi = __shfl_xor_sync(0xffffffffu, acc.hi, o);
+    y.lo = __shfl_xor_sync(0xffffffffu, acc.lo, o);
+    const int m = max(lref, r2);
+    acc.scale(pow2i_f(lref - m));
+    y.scale(pow2i_f(r2 - m));
+    acc = df_add(acc, y);
+    lref = m;
+  }
+  const int R = lref;
+  const FSum S = df_norm(acc);
   if (lane == 0) {
     RowStats rs;
     rs.ref = R;
@@ -1386,10 +1399,10 @@ __global__ void __launch_bounds__(kThreads) draw_resolve_kernel(const SamplePara
 // itself (rank 0 writes the outputs).  CTA `rank` then builds the prefix
 // structure of chunks c = rank (mod kClusterCTAs) in its shared memory: its
 // first chunk through registers while a bulk async copy brings the second
-// (target and draft) into a staging buffer, and so on alternately.  After a
-// cluster barrier every CTA reads the chunk totals (distributed shared
-// memory), picks the chunk, and after a second barrier (no peer reads
-// afterwards) the chunk's owner walks it.
+// (target and draft) into a staging buffer, and so on alternately.  Each CTA
+// writes its chunk totals into every CTA's shared memory (distributed shared
+// memory); after one cluster barrier every CTA picks the chunk from its own
+// copy, the others leave, and the chunk's owner walks it.
 constexpr int kClusterCTAs = 4;
 constexpr int kLocalChunks = 4;
 constexpr int kClusterMaxChunks = kClusterCTAs * kLocalChunks;
@@ -1616,7 +1629,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   __shared__ RowStats s_rows[kMaxSeqRows];
   __shared__ int s_tok[kMaxDraft];
   __shared__ float s_ua[kMaxDraft];
-  __shared__ FSum s_ctot[kLocalChunks];
+  __shared__ FSum s_ctot[kLocalChunks], s_call[kClusterMaxChunks];
   __shared__ FSum s_wt[kLocalChunks][kWarps], s_wp[kLocalChunks][kWarps];
   __shared__ QuadWalk s_walk;
   __shared__ DrawDesc s_desc;
@@ -1719,16 +1732,23 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
     quad_scan(g, s_wt[lc], &q);
   }
   const int nl = (C - rank + kClusterCTAs - 1) / kClusterCTAs;  // local chunks
+  // warp 0: this CTA's chunk totals, written into every CTA's s_call
+  // (distributed shared memory), so that after the cluster barrier each CTA
+  // reads only its own shared memory and may leave without a second barrier
+  auto totals_to_cluster = [&]() {
+    warp_prefixes(s_wt, s_wp, s_ctot, nl);
+    __syncwarp();
+    const int lc = lane / kClusterCTAs, peer = lane % kClusterCTAs;
+    if (lc < nl) *cluster.map_shared_rank(&s_call[rank + kClusterCTAs * lc], peer) = s_ctot[lc];
+  };
   __syncthreads();  // warp totals of every local chunk
-  if (warp == 0) warp_prefixes(s_wt, s_wp, s_ctot, nl);
+  if (warp == 0) totals_to_cluster();
   cluster.sync();
 
-  // 4. chunk totals from their owners (one read of the peers' shared
-  // memory); every CTA computes the same total, so the rare fallback below
-  // is taken by the whole cluster or by none of it
+  // 4. the chunk choice; every CTA computes the same total, so the rare
+  // fallback below is taken by the whole cluster or by none of it
   if (warp == 0) {
-    FSum v = FSum::zero();
-    if (lane < C) v = *cluster.map_shared_rank(&s_ctot[lane / kClusterCTAs], lane % kClusterCTAs);
+    const FSum v = lane < C ? s_call[lane] : FSum::zero();
     const ChunkChoice ch = choose_chunk(v, C, u_sample);
     if (lane == 0) {
       s_fallback = resid && !(ch.total.hi > 0.0f);
@@ -1743,7 +1763,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
   if (fallback) {
     // the residual mass vanished in rounding: sample p of the rejected row;
     // its group sums and chunk totals replace the residual ones
-    cluster.sync();  // every CTA has read the residual totals
+    cluster.sync();  // every CTA has read the residual totals from its s_call
     for (int lc = 0; lc < kLocalChunks; ++lc) {
       const int c = rank + kClusterCTAs * lc;
       if (c >= C) break;
@@ -1765,11 +1785,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
       quad_scan(g, s_wt[lc], &q);
     }
     __syncthreads();
-    if (warp == 0) warp_prefixes(s_wt, s_wp, s_ctot, nl);
+    if (warp == 0) totals_to_cluster();
     cluster.sync();
     if (warp == 0) {
-      FSum v = FSum::zero();
-      if (lane < C) v = *cluster.map_shared_rank(&s_ctot[lane / kClusterCTAs], lane % kClusterCTAs);
+      const FSum v = lane < C ? s_call[lane] : FSum::zero();
       const ChunkChoice ch = choose_chunk(v, C, u_sample);
       if (lane == 0) {
         s_c = ch.c;
@@ -1779,8 +1798,9 @@ __global__ void __launch_bounds__(kThreads, 2) sample_finish_kernel(const Sample
       }
     }
     if (rank == 0 && threadIdx.x == 0) set_flag(p.flags, kFlagResidualFallback);
+    __syncthreads();
   }
-  cluster.sync();  // no CTA reads a peer's shared memory after this point
+  // no CTA touches a peer's shared memory after this point
 
   // a staging copy whose wait ran out may still be in flight: wait for it
   // again (bounded, with the default limit) before leaving
