@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU baseline (0 disables it)")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--profile-case", choices=["lm_head_greedy", "tree_grow", "sample"],
+    ap.add_argument("--profile-case", choices=["lm_head_greedy", "tree_grow", "sample", "step"],
                     default=None,
                     help="only run that kernel --calls times, untimed (for ncu)")
     ap.add_argument("--calls", type=int, default=3)
@@ -749,12 +749,44 @@ def sample_case(dev):
     return c
 
 
+def step_case(dev):
+    """One verification step per call, its three calls one after another on
+    one stream: sampling and greedy (B=64, k=4, V=128256) and tree greedy
+    (16 trees of 60 nodes), bf16, over four device copies of the inputs."""
+    import torch
+    import speculative_decoding_verification_56_gb300 as sv
+    samp, greedy, tree = workload(0)
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    sets = [dict(t=sv.to_device_logits(samp.target, samp.dtype, dev),
+                 d=sv.to_device_logits(samp.draft, samp.dtype, dev),
+                 tt=sv.to_device_logits(tree.target, tree.dtype, dev)) for _ in range(NSETS)]
+    tok, ua, us, gtok = up(samp.tokens), up(samp.u_accept), up(samp.u_sample), up(greedy.tokens)
+    ttok, tpar = up(tree.tokens), up(tree.parents)
+    ws = sv.alloc_workspace(sv.SPEC_MODE_SAMPLE, samp.B, samp.k, samp.V, sv.SPEC_DTYPE_BF16, dev)
+    wg = sv.alloc_workspace(sv.SPEC_MODE_GREEDY, greedy.B, greedy.k, greedy.V, sv.SPEC_DTYPE_BF16,
+                            dev)
+    wt = sv.alloc_workspace(sv.SPEC_MODE_TREE_GREEDY, tree.B, tree.N, tree.V, sv.SPEC_DTYPE_BF16,
+                            dev)
+    c = {"i": 0}
+
+    def call(stream):
+        x = sets[c["i"] % NSETS]
+        c["i"] += 1
+        sv.verify_sample(x["t"], x["d"], tok, ua, us, samp.temperature, workspace=ws,
+                         stream=stream)
+        sv.verify_greedy(x["t"], gtok, workspace=wg, stream=stream)
+        sv.verify_tree_greedy(x["tt"], ttok, tpar, tree.max_depth, workspace=wt, stream=stream)
+    c["call"] = call
+    return c
+
+
 def profile_case(name, calls):
     """Run one call type `calls` times, untimed: the program ncu profiles
     (`--profile-case`)."""
     import torch
     dev = torch.device("cuda", 0)
-    c = {"lm_head_greedy": lm_head_case, "tree_grow": grow_case, "sample": sample_case}[name](dev)
+    c = {"lm_head_greedy": lm_head_case, "tree_grow": grow_case, "sample": sample_case,
+         "step": step_case}[name](dev)
     for _ in range(calls):
         c["call"](None)
     torch.cuda.synchronize()
