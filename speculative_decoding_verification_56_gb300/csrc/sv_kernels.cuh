@@ -775,9 +775,9 @@ __device__ __forceinline__ int ring_init(Ring& ring, int i0, int i1, IssueFn iss
 }
 
 // Thread 0, at the end: wait (bounded, with the default limit whatever the
-// limit of the loop's waits) for the copies issued into each slot.  After an
-// abort no copy is issued into a slot whose previous copy a warp gave up on
-// (ring_refill), so only the last kStages issued copies can be in flight.
+// limit of the loop's waits) for the copies issued into each slot.  A slot
+// is reissued only after its previous copy landed (ring_take), so only the
+// last kStages issued copies can be in flight.
 __device__ __noinline__ void ring_drain(Ring& ring, int i0, int issued) {
   for (int j = max(i0, issued - kStages); j < issued; ++j)
     mbar_wait_bounded(&ring.full[(j - i0) % kStages], (unsigned)(((j - i0) / kStages) & 1));
@@ -785,7 +785,10 @@ __device__ __noinline__ void ring_drain(Ring& ring, int i0, int issued) {
 
 // Wait for the item in `slot` (phase parity `par`), copy this thread's
 // vectors to registers (past-the-end vectors read as -inf) and release the
-// slot.  Returns false once the CTA has aborted.
+// slot.  A warp releases the slot only when its lane 0 has seen the copy
+// land, so a slot is never reissued while its previous copy may still be in
+// flight (a warp that gives up, or finds the CTA aborted, does not release
+// it).  Returns false once the CTA has aborted.
 template <typename E>
 __device__ __forceinline__ bool ring_take(Ring& ring, const uint8_t* stage_mem, int slot,
                                           unsigned par, int nvec, unsigned* flags,
@@ -805,16 +808,15 @@ __device__ __forceinline__ bool ring_take(Ring& ring, const uint8_t* stage_mem, 
     raw[q] = (ok && vi < nvec) ? lds128(sm + q * kThreads * 16) : ninf;
   }
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&ring.empty[slot]);
+  if ((threadIdx.x & 31) == 0 && ok) mbar_arrive(&ring.empty[slot]);
   return ok;
 }
 
 // Thread 0: once every warp has released `slot` (phase parity `par`), reuse
-// it for item `nxt` (if any).  Returns the new count of issued items.  A warp
-// that gives up on a copy sets ring.abort before it releases the slot, and
-// the release orders that write before this thread's wait returns, so the
-// second check below never lets a copy land on a slot whose previous copy may
-// still be in flight.
+// it for item `nxt` (if any).  Returns the new count of issued items.  Every
+// release follows the landing of the slot's previous copy (ring_take), so a
+// completed wait makes the reissue safe even if the CTA has aborted since;
+// after an abort the missing releases let the wait run out instead.
 template <typename IssueFn>
 __device__ __forceinline__ int ring_refill(Ring& ring, int slot, unsigned par, int nxt, int i1,
                                            int issued, unsigned* flags, IssueFn issue,
@@ -825,7 +827,6 @@ __device__ __forceinline__ int ring_refill(Ring& ring, int slot, unsigned par, i
     set_flag(flags, kFlagTimeout);
     return issued;
   }
-  if (*(volatile int*)&ring.abort) return issued;
   issue(nxt, slot);
   return nxt + 1;
 }
