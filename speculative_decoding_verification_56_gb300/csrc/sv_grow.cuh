@@ -114,19 +114,24 @@ __device__ __forceinline__ size_t grow_row_offset(const GrowParams& p, int rowi)
 // (one CTA barrier); a full buffer is compacted to its K best, whose K-th
 // value raises thr.  Elements are tested against thr eight at a time
 // (packed compares) and only vectors whose maximum reaches thr are looked at.
-// Only at a segment end do the warps meet (CTA barriers):
-// the 16 warp lists are merged into the record of the segment's last item,
-// with the segment's softmax partial; the segment's other records carry an
-// empty list and an empty partial.
+// At a segment end each warp leaves its sorted K best and its softmax
+// partial in the segment's slot; the last warp to arrive merges them into
+// the record of the segment's last item, with no CTA barrier; the segment's
+// other records carry an empty list and an empty partial.
 constexpr int kGrowBuf = 32;  // candidates per warp buffer
+// Row segments open at once in a CTA: no warp runs more than kStages items
+// ahead of the slowest (the ring), and an item opens at most one segment.
+constexpr int kGrowSlots = 4;
+static_assert(kStages + 1 <= kGrowSlots, "segment slots cover the ring's spread");
 struct GrowSegSmem {
   uint2 buf[kWarps][kGrowBuf];        // (value bits, index) of the warp's candidates
   int n[kWarps];                      // entries appended (more than kGrowBuf: overflow)
-  uint2 lists[kWarps * kGrowMaxK];    // warp w's [w kGrowMaxK, +kGrowMaxK): compaction
-                                      // scratch, and its K best at a segment end
-  StatsSlot st[kWarps];
-  float wm[kWarps];                   // warp maxima of a segment's first item
-  unsigned thr_key;                   // largest published warp threshold (grow_fkey)
+  uint2 tmp[kWarps][kGrowMaxK];       // each warp's compaction scratch
+  uint2 lists[kGrowSlots][kWarps * kGrowMaxK];  // each warp's K best at a segment end
+  StatsSlot st[kGrowSlots][kWarps];   // each warp's softmax partial at a segment end
+  unsigned thr_key[kGrowSlots];       // largest published threshold (grow_fkey) of the segment
+  int cnt[kGrowSlots];                // warps done with the segment
+  float wm[kGrowSlots][kWarps];       // warp maxima of the segment's first item
 };
 
 // Order-preserving unsigned key of a non-NaN float and back, for atomicMax.
@@ -139,7 +144,10 @@ __device__ __forceinline__ float grow_funkey(unsigned k) {
 }
 __device__ __forceinline__ void grow_seg_smem_init(GrowSegSmem& sh) {
   if (threadIdx.x < kWarps) sh.n[threadIdx.x] = 0;
-  if (threadIdx.x == 0) sh.thr_key = grow_fkey(-INFINITY);
+  if (threadIdx.x < kGrowSlots) {
+    sh.thr_key[threadIdx.x] = grow_fkey(-INFINITY);
+    sh.cnt[threadIdx.x] = 0;
+  }
 }
 
 __device__ __forceinline__ uint2 grow_pack(float v, int i) {
@@ -193,7 +201,7 @@ __device__ __forceinline__ unsigned grow_ge_mask<BF16>(const uint4& v, float thr
 __device__ __forceinline__ int grow_warp_compact(GrowSegSmem& sh, int m, int K) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint2* buf = sh.buf[warp];
-  uint2* tmp = sh.lists + warp * kGrowMaxK;
+  uint2* tmp = sh.tmp[warp];
   __syncwarp();
   if (lane < m) {
     const uint2 me = buf[lane];
@@ -219,10 +227,10 @@ __device__ __forceinline__ int grow_warp_compact(GrowSegSmem& sh, int m, int K) 
 template <typename E>
 __device__ __forceinline__ int grow_warp_append(GrowSegSmem& sh, const uint4 (&raw)[kVecPerThread],
                                                 const float (&vm)[kVecPerThread], int j0, int j1,
-                                                int K, int nb, float& thr) {
+                                                int K, int nb, float& thr, unsigned* thr_key) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint2* buf = sh.buf[warp];
-  thr = fmaxf(thr, grow_funkey(*(volatile unsigned*)&sh.thr_key));
+  thr = fmaxf(thr, grow_funkey(*(volatile unsigned*)thr_key));
   const float seen = thr;  // published already, or this warp's own segment threshold
   unsigned mx = 0;  // 1 + the highest slot this lane took
 #pragma unroll
@@ -281,23 +289,74 @@ __device__ __forceinline__ int grow_warp_append(GrowSegSmem& sh, const uint4 (&r
   __syncwarp();
   if (lane == 0) {
     sh.n[warp] = n;
-    if (thr > seen) atomicMax(&sh.thr_key, grow_fkey(thr));  // only a raised threshold
+    if (thr > seen) atomicMax(thr_key, grow_fkey(thr));  // only a raised threshold
   }
   __syncwarp();
   return n;
 }
 
+// The merge of a closed row segment (one warp, the last to close it): K
+// rounds of a head merge over the 16 sorted warp lists of its slot (token
+// indices are distinct across warps, so the winner's list is the one whose
+// head it is; placeholders fill short lists) and the 16 softmax partials,
+// into the record of the segment's last item; then the slot is freed.
+__device__ __noinline__ void grow_seg_merge(const GrowParams& p, GrowSegSmem& sh, int slot,
+                                            int item) {
+  const int lane = threadIdx.x & 31;
+  const int K = p.K;
+  GrowRec* out = p.rec + item;
+  const uint2* L = sh.lists[slot];
+  int h = 0;
+  uint2 cur = lane < kWarps ? L[lane * kGrowMaxK] : grow_pack(-INFINITY, 0x7FFFFFFF);
+  for (int r = 0; r < K; ++r) {
+    float v = __uint_as_float(cur.x);
+    int i = (int)cur.y;
+    grow_warp_best(v, i);
+    if (lane == 0) {
+      out->val[r] = v;
+      out->idx[r] = i;
+    }
+    if (lane < kWarps && i != 0x7FFFFFFF && (int)cur.y == i) {
+      ++h;
+      cur = h < K ? L[lane * kGrowMaxK + h] : grow_pack(-INFINITY, 0x7FFFFFFF);
+    }
+  }
+  StatsSlot v = lane < kWarps ? sh.st[slot][lane] : StatsSlot{kRefEmpty, 0.0f, 0.0f, 0};
+  const int R = warp_max_i(v.ref);
+  FSum f;
+  f.hi = v.hi;
+  f.lo = v.lo;
+  f.scale(pow2i_f(v.ref - R));
+  const FSum tot = warp_sum_df(f);
+  __syncwarp();
+  if (lane == 0) {
+    out->ref = R;
+    out->hi = tot.hi;
+    out->lo = tot.lo;
+    out->nk = K;
+    sh.thr_key[slot] = grow_fkey(-INFINITY);  // the slot is free
+    sh.cnt[slot] = 0;
+  }
+}
+
 // One item for the whole CTA (every thread calls it with the same flags):
-// the softmax partial runs on in st; the warp appends its candidates; at a
-// segment end (last) the 16 warp lists and partials are merged into the
-// item's record (two CTA barriers), otherwise one warp writes the item's
-// empty record.  first: the item opens a segment (thr is set here).
+// the softmax partial runs on in st; the warp appends its candidates.  A
+// segment's state lives in slot seg % kGrowSlots.  first: the item opens a
+// segment; thr = the K-th largest of the 16 warp maxima (at least K of the
+// chunk's elements reach it), after the segment's one CTA barrier.  last:
+// the item closes it; each warp leaves its K best (sorted) and its partial
+// in the slot, and the last warp to arrive merges them (grow_seg_merge)
+// while the other warps move on; the merge is done before its warp reaches
+// the next segment's barrier, and no warp runs more than kStages items
+// ahead of the slowest, so kGrowSlots slots cover every segment in use.
+// Otherwise one warp writes the item's empty record.
 template <typename E>
 __device__ __forceinline__ void grow_seg_item(const GrowParams& p,
                                               const uint4 (&raw)[kVecPerThread], int item,
                                               bool first, bool last, StatsState& st, float& thr,
-                                              GrowSegSmem& sh) {
+                                              GrowSegSmem& sh, int& seg) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int slot = seg & (kGrowSlots - 1);
   const int c = item % p.nchunks;
   const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
   const int K = p.K;
@@ -305,15 +364,13 @@ __device__ __forceinline__ void grow_seg_item(const GrowParams& p,
 #pragma unroll
   for (int q = 0; q < kVecPerThread; ++q) vm[q] = grow_vec_max<E>(raw[q]);
   const float tmax = fmaxf(fmaxf(vm[0], vm[1]), fmaxf(vm[2], vm[3]));
-  stats_chunk<E>(raw, p.scale, st, tmax);
   if (first) {
-    // thr = the K-th largest of the 16 warp maxima (at least K of the
-    // chunk's elements reach it); every warp sorts them (bitonic over lanes
-    // 0..15, largest first) after one CTA barrier
+    // every warp sorts the 16 warp maxima (bitonic over lanes 0..15,
+    // largest first) after the barrier
     const float wmax = warp_max_f(tmax);
-    if (lane == 0) sh.wm[warp] = wmax;
+    if (lane == 0) sh.wm[slot][warp] = wmax;
     __syncthreads();
-    float v = lane < kWarps ? sh.wm[lane] : -INFINITY;
+    float v = lane < kWarps ? sh.wm[slot][lane] : -INFINITY;
 #pragma unroll
     for (int k = 2; k <= kWarps; k <<= 1)
 #pragma unroll
@@ -324,7 +381,10 @@ __device__ __forceinline__ void grow_seg_item(const GrowParams& p,
     thr = __shfl_sync(0xffffffffu, v, K - 1);
   }
   const int nb = sh.n[warp];  // 0 when the segment opens
-  int n = grow_warp_append<E>(sh, raw, vm, j0, j1, K, nb, thr);
+  int n = grow_warp_append<E>(sh, raw, vm, j0, j1, K, nb, thr, &sh.thr_key[slot]);
+  // the softmax partial after the candidates, so that the vector maxima are
+  // no longer live across its arithmetic
+  stats_chunk<E>(raw, p.scale, st, tmax);
   GrowRec* out = p.rec + item;  // item = row * nchunks + chunk
   if (!last) {
     if (warp == item % kWarps) {
@@ -341,117 +401,29 @@ __device__ __forceinline__ void grow_seg_item(const GrowParams& p,
     }
     return;
   }
-  // segment end: the warp's K best, best first, at lists[warp kGrowMaxK ..]
-  // (the compaction leaves them there); placeholders fill a short list
+  // segment end: this warp's K best, best first (placeholders fill a short
+  // list), and its softmax partial, into the slot
   n = grow_warp_compact(sh, n, K);
-  uint2* lw = sh.lists + warp * kGrowMaxK;
-  for (int r = n + lane; r < K; r += 32) lw[r] = grow_pack(-INFINITY, 0x7FFFFFFF);
+  uint2* lw = sh.lists[slot] + warp * kGrowMaxK;
+  for (int r = lane; r < K; r += 32) lw[r] = r < n ? sh.buf[warp][r] : grow_pack(-INFINITY, 0x7FFFFFFF);
   {
     const int wref = warp_max_i(st.ref);
     FSum mine = st.acc;
     mine.scale(pow2i_f(st.ref - wref));
     const FSum wsum = warp_sum_df(mine);
-    if (lane == 0) sh.st[warp] = StatsSlot{wref, wsum.hi, wsum.lo, 0};
+    if (lane == 0) sh.st[slot][warp] = StatsSlot{wref, wsum.hi, wsum.lo, 0};
     st = StatsState();
   }
-  __syncthreads();
-  // the K best of the 16 sorted lists, by warp 0: lane l samples entry l % 2
-  // of list l / 2; theta, the K-th best sample, is reached by at least K
-  // entries, so the K best are among the entries >= theta (a prefix of every
-  // list), ranked against one another in the warp's scratch when they fit;
-  // otherwise every entry is ranked by the whole CTA
-  int gather = 0;  // warp 0: candidates gathered (0: use the fallback)
-  if (warp == 0) {
-    uint2* g = sh.buf[0];  // warp 0's buffer is free at a segment end
-    const int sw = lane >> 1, sp = lane & 1;
-    const uint2 smp = sp < K ? sh.lists[sw * kGrowMaxK + sp] : grow_pack(-INFINITY, 0x7FFFFFFF);
-    const float sv = __uint_as_float(smp.x);
-    const int sx = (int)smp.y;
-    g[lane] = smp;
-    __syncwarp();
-    int srank = 0;
-    if (sx != 0x7FFFFFFF)
-      for (int u = 0; u < 32; ++u) srank += grow_before(g[u], sv, sx) ? 1 : 0;
-    const unsigned sel = __ballot_sync(0xffffffffu, sx != 0x7FFFFFFF && srank == K - 1);
-    const float theta = sel ? __shfl_sync(0xffffffffu, sv, __ffs(sel) - 1) : -INFINITY;
-    int cnt = 0;
-    if (lane < kWarps)
-      for (int h = 0; h < K; ++h) {
-        const uint2 e = sh.lists[lane * kGrowMaxK + h];
-        cnt += (e.y != 0x7FFFFFFFu && __uint_as_float(e.x) >= theta) ? 1 : 0;
-      }
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    __syncwarp();  // the samples are read before the candidates replace them
-    if (total <= 32) {
-      for (int h = 0; h < cnt; ++h) g[incl - cnt + h] = sh.lists[lane * kGrowMaxK + h];
-      __syncwarp();
-      if (lane < total) {
-        const uint2 me = g[lane];
-        const float v = __uint_as_float(me.x);
-        const int x = (int)me.y;
-        int rank = 0;
-        for (int u = 0; u < total; ++u) rank += grow_before(g[u], v, x) ? 1 : 0;
-        if (rank < K) {
-          out->val[rank] = v;
-          out->idx[rank] = x;
-        }
-      }
-      for (int r = total + lane; r < K; r += 32) {  // fewer than K elements in the segment
-        out->val[r] = -INFINITY;
-        out->idx[r] = 0x7FFFFFFF;
-      }
-      gather = total;
-    }
-    if (lane == 0) sh.n[0] = gather;  // tells the other warps whether to fall back
+  ++seg;
+  __syncwarp();  // the warp's list and partial are written; its buffer is free
+  int lastw = 0;
+  if (lane == 0) {
+    sh.n[warp] = 0;
+    __threadfence_block();
+    lastw = atomicAdd(&sh.cnt[slot], 1) == kWarps - 1;
+    if (lastw) __threadfence_block();
   }
-  __syncthreads();
-  if (sh.n[0] == 0) {
-    // each real entry's rank among all of them, by the CTA
-    const int T = kWarps * K;
-    const int t = threadIdx.x;
-    const int tw = t / K;
-    const uint2 me = t < T ? sh.lists[tw * kGrowMaxK + (t - tw * K)] : grow_pack(-INFINITY, 0x7FFFFFFF);
-    const bool real = t < T && me.y != 0x7FFFFFFFu;
-    int rank = 0;
-    if (real)
-      for (int w = 0; w < kWarps; ++w)
-        for (int r = 0; r < K; ++r)
-          rank += grow_before(sh.lists[w * kGrowMaxK + r], __uint_as_float(me.x), (int)me.y) ? 1 : 0;
-    const int nreal = __syncthreads_count(real);
-    if (real && rank < K) {
-      out->val[rank] = __uint_as_float(me.x);
-      out->idx[rank] = (int)me.y;
-    }
-    if (t >= nreal && t < K) {
-      out->val[t] = -INFINITY;
-      out->idx[t] = 0x7FFFFFFF;
-    }
-  }
-  if (threadIdx.x == 0) sh.thr_key = grow_fkey(-INFINITY);  // every warp is done with the segment
-  if (warp == kWarps - 1) {
-    StatsSlot v = lane < kWarps ? sh.st[lane] : StatsSlot{kRefEmpty, 0.0f, 0.0f, 0};
-    const int R = warp_max_i(v.ref);
-    FSum f;
-    f.hi = v.hi;
-    f.lo = v.lo;
-    f.scale(pow2i_f(v.ref - R));
-    const FSum tot = warp_sum_df(f);
-    if (lane == 0) {
-      out->ref = R;
-      out->hi = tot.hi;
-      out->lo = tot.lo;
-      out->nk = K;
-    }
-  }
-  __syncthreads();  // the lists and partials are read before the next segment
-  if (lane == 0) sh.n[warp] = 0;
-  __syncwarp();
+  if (__shfl_sync(0xffffffffu, lastw, 0)) grow_seg_merge(p, sh, slot, item);
 }
 
 // One CTA per item, plain loads (any row size and alignment).
@@ -473,7 +445,8 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_kernel(const GrowParams
   __syncthreads();
   StatsState st;
   float thr = -INFINITY;
-  grow_seg_item<E>(p, raw, item, true, true, st, thr, sh);
+  int seg = 0;
+  grow_seg_item<E>(p, raw, item, true, true, st, thr, sh, seg);
 }
 
 // Persistent CTAs over contiguous item ranges, the chunks streamed through
@@ -507,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_stream_kernel(const Gro
   unsigned par = 0;
   StatsState st;  // this thread's partial over the current row segment
   float thr = -INFINITY;
+  int seg = 0;  // row segments this CTA has closed
   for (int it = i0; it < i1; ++it) {
     const int c = it % C;
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
@@ -515,7 +489,8 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_stream_kernel(const Gro
     if (threadIdx.x == 0)
       issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
     // an aborted CTA ranks -inf: its flag is set
-    grow_seg_item<E>(p, raw, it, it == i0 || c == 0, c + 1 == C || it + 1 == i1, st, thr, sh);
+    grow_seg_item<E>(p, raw, it, it == i0 || c == 0, c + 1 == C || it + 1 == i1, st, thr, sh,
+                     seg);
     if (++slot == kStages) {
       slot = 0;
       par ^= 1u;
