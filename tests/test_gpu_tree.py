@@ -240,6 +240,22 @@ def test_tree_grow_matches_oracle(B, D, K, V, M, T, dtype, seed):
     assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)
 
 
+@pytest.mark.parametrize("V", [2048, 20000])
+def test_tree_grow_many_segments_per_cta(V):
+    # 8 trees of 16 layers x 16 frontier rows over short rows (one or two
+    # chunks each): every CTA of the streaming top-k closes several row
+    # segments, so its four segment slots are reused within the CTA
+    B, D, K, M = 8, 16, 16, 200
+    z = synth.make_grow_logits(B=B, D=D, K=K, V=V, seed=31)
+    ref = oracle.tree_grow(z, 1.0, M, dtype="bf16")
+    got = _gpu_grow(z, "bf16", 1.0, M)
+    ok = ref["min_gap"] > GROW_GAP
+    assert ok.mean() >= 0.9, ref["min_gap"]
+    for key in ("tokens", "parents", "depth"):
+        assert np.array_equal(got[key][ok], ref[key][ok]), key
+    assert np.allclose(got["values"][ok], ref["values"][ok], rtol=1e-6, atol=1e-6)
+
+
 def test_tree_grow_full_workload():
     # the benchmark's grow workload: 16 trees, 6 layers x 8 frontier rows over
     # V = 128256 bf16, budget 59; exact ties between siblings (equal bf16
