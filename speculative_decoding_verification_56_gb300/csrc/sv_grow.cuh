@@ -550,11 +550,12 @@ constexpr size_t kGrowTreeSmem =
 
 // A cluster of two CTAs per tree.  A draft row's K best tokens and their
 // ln q do not depend on which node the frontier put in the row's slot, so
-// every row of the tree is reduced first, each CTA taking half of the rows,
-// nstage at a time: the CTA stages the rows' chunk records in shared memory,
-// then warp w takes row q0 + w, merges the chunk normalisers and picks the
-// K best tokens from the chunk lists (each sorted best first) by a threshold
-// and a shuffle ranking; then a thread per row takes log2 of the row sum and
+// every row of the tree is reduced first, each CTA taking half of the rows:
+// a warp per row merges the chunk normalisers and ranks the candidates of
+// the row's live records (one per row segment) a lane each; rows with more
+// candidates than lanes are staged in shared memory, nstage at a time, and
+// warp w picks the K best from the chunk lists (each sorted best first) by
+// a threshold and a shuffle ranking; then a thread per row takes log2 of the row sum and
 // a thread per (row, rank) its ln q = (z s - R - log2 S) ln 2, in float64.
 // The second CTA's results reach the first through distributed shared
 // memory and the second CTA exits.  The layers then run on four warps of the
@@ -601,28 +602,108 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
   asm volatile("griddepcontrol.launch_dependents;");
 
   // 1. this CTA's half of the tree's rows, [qa, qb): normaliser and K best
-  //    tokens (float arithmetic), nstage rows at a time: the CTA stages the
-  //    rows' chunk records together, then warp w reduces row q0 + w
+  //    tokens (float arithmetic).  The streaming top-k leaves a row's
+  //    result in one record per row segment (the segment's last chunk) and
+  //    empty records (reference kRefEmpty, no candidates) elsewhere, so a
+  //    row usually has one live record, two when it is split between CTAs.
+  //    First a warp per row reads the records' headers, merges the
+  //    normaliser and, when the live records hold at most 32 candidates,
+  //    ranks them a lane each.  Rows with more go to the staged merge
+  //    below, nstage rows at a time: the CTA stages their chunk records
+  //    together, then warp w reduces the w-th of them.
   const int half = (rows + 1) / 2;
   const int qa = crank == 0 ? 0 : half, qb = crank == 0 ? half : rows;
+  __shared__ int s_fb[kGrowMaxRows];  // rows left to the staged merge
+  __shared__ int s_nfb;
+  if (threadIdx.x == 0) s_nfb = 0;
+  __syncthreads();
+  for (int q = qa + warp; q < qb; q += kGrowTreeWarps) {
+    const GrowRec* rec = p.rec + ((size_t)b * rows + q) * p.nchunks;
+    int lref = kRefEmpty;
+    FSum acc = FSum::zero();
+    unsigned live = 0;
+    for (int c0 = 0; c0 < p.nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      int gref = kRefEmpty;
+      FSum v = FSum::zero();
+      if (c < p.nchunks) {
+        gref = __ldcg(&rec[c].ref);
+        v.hi = __ldcg(&rec[c].hi);
+        v.lo = __ldcg(&rec[c].lo);
+      }
+      if (c0 == 0) live = __ballot_sync(0xffffffffu, gref != kRefEmpty);
+      if (gref > lref) {
+        acc.scale(pow2i_f(lref - gref));
+        lref = gref;
+      }
+      v.scale(pow2i_f(gref - lref));
+      acc = df_add(acc, v);
+    }
+    const int R = warp_max_i(lref);
+    acc.scale(pow2i_f(lref - R));
+    const FSum S = df_norm(warp_sum_df(acc));
+    if (lane == 0) {
+      r_R[q] = R;
+      r_hi[q] = S.hi;
+      r_lo[q] = S.lo;
+    }
+    const int nl = __popc(live);
+    if (p.nchunks > 32 || nl * K > 32) {  // the staged merge takes this row
+      if (lane == 0) s_fb[atomicAdd(&s_nfb, 1)] = q;
+      continue;
+    }
+    // candidate e of the j-th live record, a lane each (placeholders: index
+    // >= V), ranked against one another by shuffles
+    const int j = lane / K, e = lane - j * K;
+    float v = -INFINITY;
+    int x = 0x7FFFFFFF;
+    if (j < nl) {
+      unsigned m = live;  // drop the j live records before this lane's
+      for (int t = 0; t < j; ++t) m &= m - 1;
+      const int c = __ffs(m) - 1;
+      const int xi = __ldcg(&rec[c].idx[e]);
+      if (xi < p.V) {
+        v = __ldcg(&rec[c].val[e]);
+        x = xi;
+      }
+    }
+    int rank = 0;
+#pragma unroll 8
+    for (int u = 0; u < 32; ++u) {
+      const float vu = __shfl_sync(0xffffffffu, v, u);
+      const int xu = __shfl_sync(0xffffffffu, x, u);
+      rank += (xu != 0x7FFFFFFF && grow_better(vu, xu, v, x)) ? 1 : 0;
+    }
+    // fewer than K candidates (a row whose finite logits are fewer than K
+    // keeps -inf candidates in records marked empty): the staged merge
+    if (__popc(__ballot_sync(0xffffffffu, x != 0x7FFFFFFF)) < K) {
+      if (lane == 0) s_fb[atomicAdd(&s_nfb, 1)] = q;
+      continue;
+    }
+    if (x != 0x7FFFFFFF && rank < K) {
+      r_z[q * K + rank] = v;
+      r_tok[q * K + rank] = x;
+    }
+  }
+  __syncthreads();
+  const int nfb = s_nfb;
   {
     const size_t sb = grow_stage_bytes(p.nchunks, K);
     uint8_t* stage0 = grow_mem + grow_row_bytes(rows, K);
-    for (int q0 = qa; q0 < qb; q0 += nstage) {
-      const int nb = min(nstage, qb - q0);
-      const GrowRec* rec0 = p.rec + ((size_t)b * rows + q0) * p.nchunks;
+    for (int q0 = 0; q0 < nfb; q0 += nstage) {
+      const int nb = min(nstage, nfb - q0);
       // asynchronous 4-byte copies: every load of the batch is in flight at once
       for (int i = threadIdx.x; i < nb * ncand; i += kGrowTreeThreads) {
         const int w = i / ncand, k = i - w * ncand;
         const int c = k / K, r = k - c * K;
-        const GrowRec& g = rec0[(size_t)w * p.nchunks + c];
+        const GrowRec& g = p.rec[((size_t)b * rows + s_fb[q0 + w]) * p.nchunks + c];
         float* cv = reinterpret_cast<float*>(stage0 + (size_t)w * sb);
         grow_cp4(cv + k, &g.val[r]);
         grow_cp4(reinterpret_cast<int*>(cv + ncand) + k, &g.idx[r]);
       }
       for (int i = threadIdx.x; i < nb * p.nchunks; i += kGrowTreeThreads) {
         const int w = i / p.nchunks, c = i - w * p.nchunks;
-        const GrowRec& g = rec0[i];
+        const GrowRec& g = p.rec[((size_t)b * rows + s_fb[q0 + w]) * p.nchunks + c];
         int* hp = reinterpret_cast<int*>(stage0 + (size_t)w * sb) + 2 * (size_t)ncand;
         hp[c] = 0;
         grow_cp4(hp + p.nchunks + c, &g.ref);
@@ -632,7 +713,7 @@ __global__ void __launch_bounds__(kGrowTreeThreads, 1) grow_tree_kernel(const Gr
       asm volatile("cp.async.commit_group;\ncp.async.wait_all;" ::: "memory");
       __syncthreads();
       if (warp < nb) {
-        const int q = q0 + warp;
+        const int q = s_fb[q0 + warp];
         float* cv = reinterpret_cast<float*>(stage0 + (size_t)warp * sb);
         const int* ci = reinterpret_cast<const int*>(cv + ncand);
         int* hp = const_cast<int*>(ci) + ncand;  // list c's head; list c belongs to lane c mod 32
