@@ -737,7 +737,7 @@ __global__ void __launch_bounds__(kThreads) argmax_resolve_kernel(const ArgmaxPa
 // ---------------------------------------------------------------------------
 // Loader 1: persistent CTAs streaming chunk ranges through bulk async copies
 // ---------------------------------------------------------------------------
-// CTA g owns items [items*g/G, items*(g+1)/G) (item = row * nchunks + chunk).
+// CTA g owns a contiguous range of items (item = row * nchunks + chunk; item_range).
 // Thread 0 keeps kStages chunk copies in flight.  A slot is released (its
 // "empty" barrier, one arrival per warp) as soon as every warp has copied it
 // into registers, and thread 0 refills it before computing on its own copy.
@@ -750,10 +750,22 @@ struct Ring {
   int abort;
 };
 
+// CTA g's items.  CTAs start in index order (the second CTA of each SM a few
+// microseconds after the first), and in a short range that start decides
+// when the CTA ends: there the items left over by an even split go to the
+// first CTAs.  In long ranges they are spread evenly (front-loading measured
+// 2.5% slower on 67-item ranges).
+constexpr int kFrontLoadItems = 48;  // ranges shorter than this: remainder first
 __device__ __forceinline__ void item_range(int items, int& i0, int& i1) {
-  const long long G = gridDim.x, g = blockIdx.x;
-  i0 = (int)((long long)items * g / G);
-  i1 = (int)((long long)items * (g + 1) / G);
+  const int G = gridDim.x, g = blockIdx.x;
+  const int q = items / G, rem = items - q * G;
+  if (q < kFrontLoadItems) {
+    i0 = g * q + min(g, rem);
+    i1 = i0 + q + (g < rem ? 1 : 0);
+  } else {
+    i0 = (int)((long long)items * g / G);
+    i1 = (int)((long long)items * (g + 1) / G);
+  }
 }
 
 // Thread 0 initialises the barriers and issues the first kStages copies
