@@ -352,12 +352,11 @@ __device__ __noinline__ void grow_seg_merge(const GrowParams& p, GrowSegSmem& sh
 // Otherwise one warp writes the item's empty record.
 template <typename E>
 __device__ __forceinline__ void grow_seg_item(const GrowParams& p,
-                                              const uint4 (&raw)[kVecPerThread], int item,
+                                              const uint4 (&raw)[kVecPerThread], int item, int c,
                                               bool first, bool last, StatsState& st, float& thr,
                                               GrowSegSmem& sh, int& seg) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int slot = seg & (kGrowSlots - 1);
-  const int c = item % p.nchunks;
   const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
   const int K = p.K;
   float vm[kVecPerThread];
@@ -446,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_kernel(const GrowParams
   StatsState st;
   float thr = -INFINITY;
   int seg = 0;
-  grow_seg_item<E>(p, raw, item, true, true, st, thr, sh, seg);
+  grow_seg_item<E>(p, raw, item, c, true, true, st, thr, sh, seg);
 }
 
 // Persistent CTAs over contiguous item ranges, the chunks streamed through
@@ -481,16 +480,17 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_stream_kernel(const Gro
   StatsState st;  // this thread's partial over the current row segment
   float thr = -INFINITY;
   int seg = 0;  // row segments this CTA has closed
+  int c = i0 % C;  // the item's chunk, counted along (no division per item)
   for (int it = i0; it < i1; ++it) {
-    const int c = it % C;
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     uint4 raw[kVecPerThread];
     ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw);
     if (threadIdx.x == 0)
       issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
     // an aborted CTA ranks -inf: its flag is set
-    grow_seg_item<E>(p, raw, it, it == i0 || c == 0, c + 1 == C || it + 1 == i1, st, thr, sh,
-                     seg);
+    grow_seg_item<E>(p, raw, it, c, it == i0 || c == 0, c + 1 == C || it + 1 == i1, st, thr,
+                     sh, seg);
+    if (++c == C) c = 0;
     if (++slot == kStages) {
       slot = 0;
       par ^= 1u;
