@@ -464,8 +464,13 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_stream_kernel(const Gro
   asm volatile("griddepcontrol.launch_dependents;");
   if (i0 >= i1) return;
   const int C = p.nchunks;
-  auto issue = [&](int item, int slot) {
-    const int rowi = item / C, c = item - (item / C) * C;
+  int nrow = i0 / C, nc = i0 % C;  // the next item thread 0 issues (in order)
+  auto issue = [&](int /*item: the next in order*/, int slot) {
+    const int rowi = nrow, c = nc;
+    if (++nc == C) {
+      nc = 0;
+      ++nrow;
+    }
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     const unsigned bytes = (unsigned)(j1 - j0) * (unsigned)sizeof(St);
     mbar_expect_tx(&ring.full[slot], bytes);

@@ -862,9 +862,18 @@ __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleP
   const int rows_per_seq = 2 * p.k + 1;
 
   const uint64_t pol_keep = l2_policy_keep(), pol_stream = l2_policy_stream();
-  auto issue = [&](int item, int slot) {
-    const int row = item / C, c = item - (item / C) * C;
-    const int b = row / rows_per_seq, r = row - b * rows_per_seq;
+  // thread 0 issues the range's items in order (ring_init, then one refill
+  // per item), so the next one's sequence, row and chunk are counted along
+  int nb = (i0 / C) / rows_per_seq, nr = i0 / C - nb * rows_per_seq, nc = i0 % C;
+  auto issue = [&](int /*item: the next in order*/, int slot) {
+    const int b = nb, r = nr, c = nc;
+    if (++nc == C) {
+      nc = 0;
+      if (++nr == rows_per_seq) {
+        nr = 0;
+        ++nb;
+      }
+    }
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     const unsigned bytes = (unsigned)(j1 - j0) * (unsigned)sizeof(S);
     const int pos = r <= p.k ? r : r - p.k - 1;  // draft position of the row
@@ -930,8 +939,13 @@ __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const Argmax
   if (i0 >= i1) return;
   const int C = p.nchunks;
 
-  auto issue = [&](int item, int slot) {
-    const int row = item / C, c = item - (item / C) * C;
+  int nrow = i0 / C, nc = i0 % C;  // the next item thread 0 issues (in order)
+  auto issue = [&](int /*item: the next in order*/, int slot) {
+    const int row = nrow, c = nc;
+    if (++nc == C) {
+      nc = 0;
+      ++nrow;
+    }
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     const unsigned bytes = (unsigned)(j1 - j0) * (unsigned)sizeof(S);
     mbar_expect_tx(&ring.full[slot], bytes);
