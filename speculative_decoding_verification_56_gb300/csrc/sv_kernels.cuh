@@ -939,13 +939,10 @@ __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const Argmax
   if (i0 >= i1) return;
   const int C = p.nchunks;
 
-  int nrow = i0 / C, nc = i0 % C;  // the next item thread 0 issues (in order)
-  auto issue = [&](int /*item: the next in order*/, int slot) {
-    const int row = nrow, c = nc;
-    if (++nc == C) {
-      nc = 0;
-      ++nrow;
-    }
+  // (the item's row and chunk by division: counting them along, as the
+  // statistics kernel does, measured 0.2-0.6 us slower here)
+  auto issue = [&](int item, int slot) {
+    const int row = item / C, c = item - (item / C) * C;
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     const unsigned bytes = (unsigned)(j1 - j0) * (unsigned)sizeof(S);
     mbar_expect_tx(&ring.full[slot], bytes);
