@@ -490,11 +490,13 @@ __global__ void __launch_bounds__(kThreads, 2) grow_topk_stream_kernel(const Gro
     const int j0 = c * E::kChunk, j1 = min(p.V, j0 + E::kChunk);
     uint4 raw[kVecPerThread];
     ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw);
-    if (threadIdx.x == 0)
-      issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
     // an aborted CTA ranks -inf: its flag is set
     grow_seg_item<E>(p, raw, it, c, it == i0 || c == 0, c + 1 == C || it + 1 == i1, st, thr,
                      sh, seg);
+    // the refill after the item's work, when the other warps have usually
+    // released the slot (before it, warp 0 waits for them: 0.7 us slower)
+    if (threadIdx.x == 0)
+      issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue);
     if (++c == C) c = 0;
     if (++slot == kStages) {
       slot = 0;

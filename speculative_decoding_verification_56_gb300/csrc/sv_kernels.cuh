@@ -740,7 +740,9 @@ __global__ void __launch_bounds__(kThreads) argmax_resolve_kernel(const ArgmaxPa
 // CTA g owns a contiguous range of items (item = row * nchunks + chunk; item_range).
 // Thread 0 keeps kStages chunk copies in flight.  A slot is released (its
 // "empty" barrier, one arrival per warp) as soon as every warp has copied it
-// into registers, and thread 0 refills it before computing on its own copy.
+// into registers, and thread 0 refills it with the item kStages ahead: before
+// its own work on the item in the statistics kernel (heavy arithmetic), after
+// it in the argmax and growth kernels.
 // The loop has no CTA-wide barrier.  Every wait is bounded: a wait that runs
 // out sets kFlagTimeout, the CTA keeps its control flow but stops copying and
 // computing, and it drains the copies still in flight before it exits.
@@ -897,6 +899,8 @@ __global__ void __launch_bounds__(kThreads, 2) stream_stats_kernel(const SampleP
     uint4 raw[kVecPerThread];
     const bool ok =
         ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw, p.wait_ns);
+    // the refill before this thread's (heavy) work on the item, so the copy
+    // three items ahead goes out at once (after the work: 0.5-6 us slower)
     if (threadIdx.x == 0)
       issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue, p.wait_ns);
     if (ok) {
@@ -964,9 +968,12 @@ __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const Argmax
     uint4 raw[kVecPerThread];
     const bool ok =
         ring_take<E>(ring, stage_mem, slot, par, (j1 - j0) / E::kEPV, p.flags, raw, p.wait_ns);
+    if (ok) argmax_chunk<E>(raw, j0, st);
+    // the refill after this thread's own (light) work on the item: by then
+    // the other warps have usually released the slot, so warp 0 is not held
+    // (before the work, as in the statistics kernel, measured 0.2-2 us slower)
     if (threadIdx.x == 0)
       issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue, p.wait_ns);
-    if (ok) argmax_chunk<E>(raw, j0, st);
     const bool row_end = (c + 1 == C);
     if (row_end || it + 1 == i1) {
       emit_arg_seg(p, st, row, c_first, c, ss, seg);
