@@ -43,10 +43,16 @@
  *   - B = 0 is a no-op that returns SPEC_OK.
  *   - Every call's kernels are programmatic dependent launches:
  *     the first kernel of a call waits for the kernel before it in the
- *     stream to finish (and its writes to be visible) before it reads or
- *     writes memory, and the last kernel of a call lets the next kernel in
- *     the stream be scheduled early.  Consecutive calls on one stream thus
- *     overlap their launches, never their memory accesses.
+ *     stream to finish (and its writes to be visible) before it writes
+ *     memory or reads anything but its logits, and the last kernel of a call
+ *     lets the next kernel in the stream be scheduled early.  The streaming
+ *     kernels of spec_verify_greedy and spec_verify_tree_greedy start reading
+ *     their logits before that wait, while the call before them on the
+ *     stream is finishing.  So the logits of a call must not be written by
+ *     the library call issued just before it on the same stream (no call of
+ *     this library writes a caller's logits; a kernel of the caller's own,
+ *     issued between two calls, has always finished before the next call's
+ *     kernels start).
  */
 #ifndef SPEC_VERIFY_H_
 #define SPEC_VERIFY_H_

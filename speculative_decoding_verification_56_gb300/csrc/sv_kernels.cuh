@@ -936,12 +936,22 @@ __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const Argmax
   __shared__ SegSlots ss;
   using S = typename E::storage;
 
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in stream_stats_kernel
+  // launched as a programmatic dependent of whatever kernel precedes it in
+  // the stream.  It reads only the logits before its first write (a segment
+  // record), and waits for that grid only there: so its copies start while
+  // the call before it is finishing.  The logits must therefore not be
+  // written by the call before it on the stream (no call of this library
+  // writes a caller's logits; a caller's kernel never triggers early, so it
+  // has finished before this one starts).
   int i0, i1;
   item_range(p.items, i0, i1);
   asm volatile("griddepcontrol.launch_dependents;");
-  if (i0 >= i1) return;
+  if (i0 >= i1) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
   const int C = p.nchunks;
+  bool waited = false;
 
   // (the item's row and chunk by division: counting them along, as the
   // statistics kernel does, measured 0.2-0.6 us slower here)
@@ -976,6 +986,10 @@ __global__ void __launch_bounds__(kThreads, 2) stream_argmax_kernel(const Argmax
       issued = ring_refill(ring, slot, par, it + kStages, i1, issued, p.flags, issue, p.wait_ns);
     const bool row_end = (c + 1 == C);
     if (row_end || it + 1 == i1) {
+      if (!waited) {  // the first write of this grid: the grid before it has finished
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        waited = true;
+      }
       emit_arg_seg(p, st, row, c_first, c, ss, seg);
       st = ArgState();
       c_first = 0;
