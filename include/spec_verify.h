@@ -46,13 +46,13 @@
  *     stream to finish (and its writes to be visible) before it writes
  *     memory or reads anything but its logits, and the last kernel of a call
  *     lets the next kernel in the stream be scheduled early.  The streaming
- *     kernels of spec_verify_greedy and spec_verify_tree_greedy start reading
- *     their logits before that wait, while the call before them on the
- *     stream is finishing.  So the logits of a call must not be written by
- *     the library call issued just before it on the same stream (no call of
- *     this library writes a caller's logits; a kernel of the caller's own,
- *     issued between two calls, has always finished before the next call's
- *     kernels start).
+ *     kernels of spec_verify_greedy, spec_verify_tree_greedy and (for short
+ *     per-CTA ranges) spec_verify_sample start reading their logits (and
+ *     sampling its draft tokens) before that wait, while the call before
+ *     them on the stream is finishing.  So the inputs of a call must not be
+ *     written by the library call issued just before it on the same stream
+ *     (a kernel of the caller's own, issued between two calls, has always
+ *     finished before the next call's kernels start).
  */
 #ifndef SPEC_VERIFY_H_
 #define SPEC_VERIFY_H_

@@ -416,9 +416,15 @@ spec_status_t run_sample(sv::SampleParams prm, int rows, bool vec, void* stream)
   spec_status_t st;
   if (vec) {
     int grid = 0;
-    st = persistent_grid<sv::stream_stats_kernel<E>>(prm.items, &grid);
+    st = persistent_grid<sv::stream_stats_kernel<E, false>>(prm.items, &grid);
     if (st != SPEC_OK) return st;
-    st = launch(sv::stream_stats_kernel<E>, grid, kStreamSmem, prm, stream, true);
+    if (prm.items / grid < sv::kFrontLoadItems) {  // short ranges: start before the wait
+      st = persistent_grid<sv::stream_stats_kernel<E, true>>(prm.items, &grid);
+      if (st != SPEC_OK) return st;
+      st = launch(sv::stream_stats_kernel<E, true>, grid, kStreamSmem, prm, stream, true);
+    } else {
+      st = launch(sv::stream_stats_kernel<E, false>, grid, kStreamSmem, prm, stream, true);
+    }
   } else {
     st = launch(sv::chunk_stats_kernel<E, false>, prm.items, 0, prm, stream, false);
   }

@@ -382,6 +382,38 @@ def test_inputs_written_by_the_kernel_just_before():
                          ["accepted_len", "out_tokens"])
 
 
+def test_back_to_back_calls_share_a_workspace():
+    # The argmax streaming kernel reads its logits before waiting for the
+    # call before it on the stream (the previous call's resolve kernel, which
+    # reads the same workspace's records); its first record write must still
+    # come after that kernel.  Greedy and tree calls on alternating inputs,
+    # one workspace, one stream, no synchronisation until the end.
+    c1 = synth.greedy_variant(synth.zipf128k(seed=7, B=16), 0.7)
+    c2 = synth.greedy_variant(synth.zipf128k(seed=8, B=16), 0.5)
+    t = synth.make_tree_case(B=8, N=40, V=128256, dtype="bf16", seed=9)
+    nbytes = max(sv.spec_verify_workspace_bytes(sv.SPEC_MODE_GREEDY, 16, 4, 128256, sv.SPEC_DTYPE_BF16),
+                 sv.spec_verify_workspace_bytes(sv.SPEC_MODE_TREE_GREEDY, 8, 40, 128256,
+                                                sv.SPEC_DTYPE_BF16))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    xs = [(sv.to_device_logits(c.target, c.dtype), torch.from_numpy(c.tokens).cuda()) for c in (c1, c2)]
+    tt = sv.to_device_logits(t.target, t.dtype)
+    ttok, tpar = torch.from_numpy(t.tokens).cuda(), torch.from_numpy(t.parents).cuda()
+    torch.cuda.synchronize()
+    outs = []
+    for i in range(6):
+        outs.append(("g", i % 2, sv.verify_greedy(xs[i % 2][0], xs[i % 2][1], workspace=ws)))
+        outs.append(("t", 0, sv.verify_tree_greedy(tt, ttok, tpar, t.max_depth, workspace=ws)))
+    torch.cuda.synchronize()
+    og = [oracle.verify_greedy(c.target, c.tokens, dtype=c.dtype) for c in (c1, c2)]
+    ot = oracle.verify_tree_greedy(t.target, t.tokens, t.parents, t.max_depth, dtype="bf16")
+    for kind, j, out in outs:
+        g = {k: v.cpu().numpy() for k, v in out.items()}
+        if kind == "g":
+            ph.compare_exact(g, og[j], ["accepted_len", "out_tokens"])
+        else:
+            ph.compare_exact(g, ot, ["accepted_len", "path_nodes", "out_tokens"])
+
+
 def test_three_calls_on_three_streams():
     # the benchmark step's layout: sampling, greedy and tree calls forked onto
     # three streams, one workspace each, running at the same time
