@@ -360,13 +360,42 @@ bool lm_row_groups(int rows, int* ngroups, int* grp) {
 }
 
 // One CTA per SM (the kernel holds the SM's tensor memory and most of its
-// shared memory), at most one per vocabulary tile.
+// shared memory), in pairs: as many pairs as can be resident at once, at most
+// one per 256-entry vocabulary tile.  The number of co-resident pairs is
+// asked of the runtime once per device and context.
+template <int Mode>
 spec_status_t lm_grid_x(int ntiles, int* gx) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  *gx = std::max(1, std::min(std::min(sms, ntiles), kLmMaxGrid));
+  static int pairs_cached[kMaxDevices] = {0};
+  static unsigned long long pairs_ctx[kMaxDevices] = {0};
+  int dev = 0;
+  unsigned long long ctx = 0;
+  if (current_context(&dev, &ctx) != SPEC_OK) return SPEC_ERR_CUDA;
+  int pairs = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_shape_mu);
+    if (pairs_ctx[dev] == ctx && pairs_cached[dev] > 0) pairs = pairs_cached[dev];
+  }
+  if (pairs == 0) {
+    // the occupancy query sees the kernel's shared-memory opt-in
+    const spec_status_t st = ensure_smem<sv::lmhead_kernel<Mode>>((size_t)sv::kLmRingBytes + 1024);
+    if (st != SPEC_OK) return st;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(2 * std::max(1, sms / 2)), 1, 1);
+    cfg.blockDim = dim3(sv::kLmThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)sv::kLmRingBytes + 1024;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, sv::lmhead_kernel<Mode>, &cfg) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    pairs = std::max(1, std::min(clusters, sms / 2));
+    std::lock_guard<std::mutex> lock(g_shape_mu);
+    pairs_cached[dev] = pairs;
+    pairs_ctx[dev] = ctx;
+  }
+  *gx = 2 * std::max(1, std::min(std::min(pairs, ntiles), kLmMaxGrid / 2));
   return SPEC_OK;
 }
 
@@ -374,13 +403,13 @@ template <int Mode>
 spec_status_t launch_lmhead(const CUtensorMap& map_h, const CUtensorMap& map_h1,
                             const CUtensorMap& map_w, const sv::LmHeadParams& lp, int gx, int gy,
                             void* stream) {
-  const spec_status_t st = ensure_smem<sv::lmhead_kernel<Mode>>(
-      (size_t)sv::kLmStages * (sv::kLmABytes + sv::kLmBBytes) + 1024);
+  const spec_status_t st =
+      ensure_smem<sv::lmhead_kernel<Mode>>((size_t)sv::kLmRingBytes + 1024);
   if (st != SPEC_OK) return st;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   pdl_config(&cfg, attr, dim3((unsigned)gx, (unsigned)gy, 1), dim3(sv::kLmThreads, 1, 1),
-             (size_t)sv::kLmStages * lp.stage_bytes + 1024, stream);
+             (size_t)lp.nstages * lp.stage_bytes + 1024, stream);
   if (cudaLaunchKernelEx(&cfg, sv::lmhead_kernel<Mode>, map_h, map_h1, map_w, lp) != cudaSuccess)
     return SPEC_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -715,13 +744,13 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   if (!workspace || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
   if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
   const int rows = L.rows;
-  const int ntiles = (V + sv::kLmBV - 1) / sv::kLmBV;
+  const int ntiles = (V + sv::kLmPairBV - 1) / sv::kLmPairBV;
   int gy = 0, grp = 0, gx = 0;
   if (!lm_row_groups(rows, &gy, &grp)) return SPEC_ERR_INVALID_ARG;
-  spec_status_t st = lm_grid_x(ntiles, &gx);
+  spec_status_t st = lm_grid_x<sv::kLmArgmax>(ntiles, &gx);
   if (st != SPEC_OK) return st;
   CUtensorMap map_h, map_w;
-  st = encode_bf16_kmajor(&map_h, hidden, d, rows, sv::kLmHBox);
+  st = encode_bf16_kmajor(&map_h, hidden, d, rows, sv::lm_half_rows(grp));
   if (st != SPEC_OK) return st;
   st = encode_bf16_kmajor(&map_w, w_lm, d, V, sv::kLmBV);
   if (st != SPEC_OK) return st;
@@ -733,7 +762,8 @@ spec_status_t spec_lm_head_verify_greedy(const void* hidden, const void* w_lm,
   lp.V = V;
   lp.ntiles = ntiles;
   lp.grp_rows = grp;
-  lp.stage_bytes = sv::kLmABytes + grp * 128;
+  lp.stage_bytes = sv::lm_stage_bytes(grp);
+  lp.nstages = sv::lm_stages(lp.stage_bytes);
   lp.part = reinterpret_cast<sv::ArgPartial*>(ws + L.off_part);
   lp.flags = reinterpret_cast<unsigned*>(ws);
   lp.ngroups0 = gy;
@@ -785,25 +815,26 @@ spec_status_t spec_lm_head_verify_sample(
   if (!workspace || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
   if (!aligned(workspace, kAlign)) return SPEC_ERR_ALIGNMENT;
   const int rows_t = B * (k + 1), rows_d = B * k, rows_2 = 2 * B;
-  const int ntiles = (V + sv::kLmBV - 1) / sv::kLmBV;
+  const int ntiles = (V + sv::kLmPairBV - 1) / sv::kLmPairBV;
   int gy0 = 0, grp0 = 0, gy1 = 0, grp1 = 0, gy2 = 0, grp2 = 0, gx = 0;
   if (!lm_row_groups(rows_t, &gy0, &grp0) || !lm_row_groups(rows_d, &gy1, &grp1) ||
       !lm_row_groups(rows_2, &gy2, &grp2) || gy0 + gy1 > 65535)
     return SPEC_ERR_INVALID_ARG;
-  spec_status_t st = lm_grid_x(ntiles, &gx);
+  spec_status_t st = lm_grid_x<sv::kLmStats>(ntiles, &gx);
   if (st != SPEC_OK) return st;
   char* ws = static_cast<char*>(workspace);
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws + L.off_arg);
   float* lbuf = reinterpret_cast<float*>(ws + L.off_log);
   CUtensorMap map_ht, map_hd, map_w, map_hb;
-  st = encode_bf16_kmajor(&map_ht, hidden_target, d, rows_t, sv::kLmHBox);
+  st = encode_bf16_kmajor(&map_ht, hidden_target, d, rows_t, sv::lm_half_rows(grp0));
   if (st != SPEC_OK) return st;
-  st = k > 0 ? encode_bf16_kmajor(&map_hd, hidden_draft, d, rows_d, sv::kLmHBox) : SPEC_OK;
+  st = k > 0 ? encode_bf16_kmajor(&map_hd, hidden_draft, d, rows_d, sv::lm_half_rows(grp1))
+             : SPEC_OK;
   if (k == 0) map_hd = map_ht;  // no draft rows: never read
   if (st != SPEC_OK) return st;
   st = encode_bf16_kmajor(&map_w, w_lm, d, V, sv::kLmBV);
   if (st != SPEC_OK) return st;
-  st = encode_bf16_kmajor(&map_hb, hbuf, d, rows_2, sv::kLmHBox);
+  st = encode_bf16_kmajor(&map_hb, hbuf, d, rows_2, sv::lm_half_rows(grp2));
   if (st != SPEC_OK) return st;
 
   // 1. softmax statistics of every target and draft row, and the draft
@@ -815,7 +846,8 @@ spec_status_t spec_lm_head_verify_sample(
   lp.V = V;
   lp.ntiles = ntiles;
   lp.grp_rows = grp0;
-  lp.stage_bytes = sv::kLmABytes + std::max(grp0, grp1) * 128;
+  lp.stage_bytes = sv::lm_stage_bytes(std::max(grp0, grp1));
+  lp.nstages = sv::lm_stages(lp.stage_bytes);
   lp.flags = reinterpret_cast<unsigned*>(ws);
   lp.ngroups0 = gy0;
   lp.rows1 = rows_d;
@@ -872,7 +904,8 @@ spec_status_t spec_lm_head_verify_sample(
   sv::LmHeadParams lq = lp;
   lq.rows = rows_2;
   lq.grp_rows = grp2;
-  lq.stage_bytes = sv::kLmABytes + grp2 * 128;
+  lq.stage_bytes = sv::lm_stage_bytes(grp2);
+  lq.nstages = sv::lm_stages(lq.stage_bytes);
   lq.ngroups0 = gy2;
   lq.rows1 = 0;
   lq.grp_rows1 = sv::kLmHBox;

@@ -8,25 +8,37 @@
 // target row's argmax, so the GEMM's epilogue keeps a running (max, lowest
 // index) per row and the [rows, V] logits are never written.
 //
-//   Z tile^T = W_LM[v0 : v0+128, :] x H[rows, :]^T   (both K-major, bf16)
+//   Z tile^T = W_LM[v0 : v0+256, :] x H[rows, :]^T   (both K-major, bf16)
 //
-// The vocabulary is the MMA's M (128 tensor-memory lanes per tile) and the
-// rows are its N (up to 384 columns, one or two MMAs of N <= 256), so rows
-// are padded only to a multiple of 64.  One CTA per SM walks a contiguous
-// range of vocabulary tiles for a group of rows; every CTA loads its own
-// operands (no cluster, no multicast).  Warp roles (192 threads):
-//   warp 0     TMA producer: per 64-wide K step, the tile's W slice and the
-//              rows' H slice (128-byte swizzled) into a 3-stage ring
-//   warp 1     allocates tensor memory; lane 0 issues tcgen05.mma
-//              (M=128, N=rows/2 or rows, K=16) into a 128 x rows fp32
-//              accumulator and commits stage releases and tile completion
-//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quadrant, a butterfly
-//              reduction across lanes per column (row), a merge of the four
-//              quadrants in shared memory and a running argmax per row
-//              (lowest index wins ties); the accumulator is released as
-//              soon as it has been read
-// Each CTA writes one argmax record per row for its vocabulary segment, in
-// the layout the greedy resolve kernel merges.  Every wait is bounded.
+// The vocabulary is the MMA's M and the rows are its N (up to 384 columns,
+// one or two MMAs of N <= 256), so rows are padded only to a multiple of 64.
+// Two CTAs of a cluster, on two SMs, share each tile through the two-CTA
+// form of the MMA (cta_group::2, M = 256): each CTA loads its own 128
+// vocabulary rows of W and half of each MMA's rows of H into its shared
+// memory, and each holds the 128 x rows accumulator of its vocabulary rows
+// (fp32) in its own tensor memory.  Per SM and K
+// step this moves 16 KB of W and half of H, against all of H for a CTA that
+// computes 128 x rows alone, so the same shared memory keeps more of the W
+// stream in flight.  Each pair walks a contiguous range of 256-entry
+// vocabulary tiles for a group of rows.  Warp roles (320 threads per CTA):
+//   warp 0     TMA producer (both CTAs): per 64-wide K step, the CTA's W
+//              slice and H halves (128-byte swizzled) into a ring of up to
+//              eight stages; both CTAs' bytes complete on the leader's
+//              `full` barrier of the stage
+//   warp 1     allocates tensor memory (both CTAs); in the leader (cluster
+//              rank 0) lane 0 issues tcgen05.mma (M=256, N=rows/2 or rows,
+//              K=16) and commits stage releases and tile completion to the
+//              barriers of both CTAs
+//   warps 2-9  epilogue (both CTAs), two warps per 32-lane quadrant of
+//              tensor memory, each taking half of the tile's columns: tcgen05.ld,
+//              a butterfly reduction across lanes per column (row), a merge
+//              of the four quadrants in shared memory and a running argmax
+//              per row (lowest index wins ties); the accumulator is released
+//              to the leader as soon as it has been read
+// Each CTA writes one argmax record per row for its vocabulary lanes, in the
+// layout the greedy resolve kernel merges.  Every wait is bounded, and both
+// CTAs meet at cluster barriers after set-up and before tensor memory is
+// freed, so no CTA leaves while its peer can still touch its memory.
 #pragma once
 
 #include <cuda.h>
@@ -35,17 +47,29 @@
 
 namespace sv {
 
-constexpr int kLmBV = 128;         // vocabulary per tile (UMMA M, tensor-memory lanes)
-constexpr int kLmMaxRows = 384;    // rows per row group (UMMA N total, tensor-memory columns;
-                                   // three stages of 16 KB + 48 KB fit in shared memory)
-constexpr int kLmMaxN = 256;       // N of one MMA instruction
-constexpr int kLmBK = 64;          // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kLmStages = 3;
-constexpr int kLmThreads = 192;
-constexpr int kLmABytes = kLmBV * kLmBK * 2;          // 16 KB: W slice
-constexpr int kLmBBytes = kLmMaxRows * kLmBK * 2;     // up to 48 KB: H slice
-constexpr int kLmHBox = 64;                           // rows per H box (TMA)
+constexpr int kLmBV = 128;           // vocabulary rows per CTA and tile (tensor-memory lanes)
+constexpr int kLmPairBV = 2 * kLmBV;  // vocabulary per tile of a CTA pair (UMMA M)
+constexpr int kLmMaxRows = 384;       // rows per row group (UMMA N total, tensor-memory columns)
+constexpr int kLmMaxN = 256;          // N of one MMA instruction
+constexpr int kLmBK = 64;             // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kLmMaxStages = 8;
+constexpr int kLmRingBytes = 192 * 1024;  // operand ring per CTA (dynamic shared memory)
+constexpr int kLmThreads = 320;
+constexpr int kLmEpiThreads = kLmThreads - 64;  // warps 2-9
+constexpr int kLmABytes = kLmBV * kLmBK * 2;  // 16 KB: the CTA's W slice
+constexpr int kLmHBox = 64;                   // row groups are multiples of this
 constexpr int kLmTmemCols = 512;
+constexpr int kLmMaxSlots = 4;  // accumulator slots of nper columns in tensor memory
+
+// MMAs per K step of 16 for a row group of R rows (a multiple of kLmHBox),
+// the rows of each MMA that one CTA of the pair holds, a CTA's bytes per
+// stage, and the ring depth that fits kLmRingBytes.
+__host__ __device__ constexpr int lm_nmma(int R) { return (R + kLmMaxN - 1) / kLmMaxN; }
+__host__ __device__ constexpr int lm_half_rows(int R) { return R / lm_nmma(R) / 2; }
+__host__ __device__ constexpr int lm_stage_bytes(int R) { return kLmABytes + R * 64; }
+__host__ __device__ constexpr int lm_stages(int stage_bytes) {
+  return kLmRingBytes / stage_bytes < kLmMaxStages ? kLmRingBytes / stage_bytes : kLmMaxStages;
+}
 
 // What the epilogue makes of each accumulator tile.
 enum LmMode : int {
@@ -56,9 +80,10 @@ enum LmMode : int {
 
 struct LmHeadParams {
   int rows, d, V;       // rows of the first matrix (argmax: B * (k+1))
-  int ntiles;           // ceil(V / kLmBV)
+  int ntiles;           // ceil(V / kLmPairBV): tiles of a CTA pair
   int grp_rows;         // rows per row group of the first matrix (multiple of kLmHBox)
-  int stage_bytes;      // kLmABytes + grp_rows * 128 (the largest group)
+  int stage_bytes;      // ring stride: lm_stage_bytes of the larger row group
+  int nstages;          // lm_stages(stage_bytes)
   ArgPartial* part;     // argmax: [rows, gridDim.x] one record per CTA segment
   unsigned* flags;
   // sampling (kLmStats): the first matrix holds the target rows [B(k+1), d],
@@ -95,28 +120,88 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
+// This CTA's rank in its cluster, and the shared::cluster address of a
+// shared-memory variable in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+  return a;
+}
+
+// Every thread of both CTAs; memory before it is visible to the cluster after.
+__device__ __forceinline__ void cluster_sync_all() {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on an mbarrier of either CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+// mbar_wait_bounded for a barrier that the peer CTA also arrives on: the
+// phase test acquires at cluster scope.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, unsigned parity) {
+  const uint64_t t0 = global_ns();
+  for (unsigned it = 0; it < (1u << 30); ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, "
+        "%3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    if (done) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return false;
+}
+
+// 2-D tile load into this CTA's shared memory whose bytes complete on an
+// mbarrier of either CTA of the pair (bar_cluster: shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// One MMA of the CTA pair (issued by the leader): A's 256 rows are the two
+// CTAs' 128-row operands at the same shared-memory address, B's N rows the
+// two CTAs' N/2-row operands (the leader's first), and each CTA's tensor
+// memory receives the accumulator rows of its own A rows.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive on `bar` once every tcgen05 operation this thread issued completes.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+// Arrive once on the barrier at `bar`'s offset in both CTAs of the pair when
+// every tcgen05 operation this thread issued completes.
+__device__ __forceinline__ void umma_commit_both(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"((unsigned short)3)
+      : "memory");
+}
+
+// The same, on this CTA's barrier only.
+__device__ __forceinline__ void umma_commit_own(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_addr(bar))
       : "memory");
 }
@@ -179,13 +264,13 @@ __device__ __forceinline__ void lane_butterfly(float (&v)[32], Op op) {
 }
 
 template <int Mode>
-__global__ void __launch_bounds__(kLmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap map_h,
                   const __grid_constant__ CUtensorMap map_h1,
                   const __grid_constant__ CUtensorMap map_w, const LmHeadParams p) {
   extern __shared__ uint8_t lm_raw[];
-  __shared__ uint64_t full[kLmStages], empty[kLmStages];
-  __shared__ uint64_t acc_full, acc_empty, drain;
+  __shared__ uint64_t full[kLmMaxStages], empty[kLmMaxStages];
+  __shared__ uint64_t acc_full[2], slot_empty[kLmMaxSlots], drain;
   __shared__ uint32_t tmem_base_holder;
   __shared__ int s_abort;
   __shared__ float red_v[4][kLmMaxRows];  // per-quadrant column results of one tile
@@ -196,46 +281,61 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(lm_raw) + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the CTA's row group: of the first matrix, or (sampling) of the second
+  const uint32_t rank = cluster_rank();  // 0: the pair's leader, which issues the MMAs
+  const bool leader = rank == 0;
+  // the pair's row group: of the first matrix, or (sampling) of the second
   const bool second = (int)blockIdx.y >= p.ngroups0;
   const int R = second ? p.grp_rows1 : p.grp_rows;  // columns used (rows past the end read as 0)
   const int row0 = second ? ((int)blockIdx.y - p.ngroups0) * p.grp_rows1 : blockIdx.y * p.grp_rows;
   const int nrows = second ? p.rows1 : p.rows;
   const CUtensorMap* hmap = second ? &map_h1 : &map_h;
-  const int stage_bytes = kLmABytes + R * 128;
-  // the CTA owns the vocabulary tiles [T0, T1)
+  const int nmma = lm_nmma(R);          // MMAs per K step of 16
+  const int half = lm_half_rows(R);     // rows of each MMA held by one CTA
+  const int nper = 2 * half;            // N of each MMA (a multiple of 32)
+  // Tensor memory holds nslots accumulator slots of nper columns; tile j's
+  // MMA m accumulates in slot (j * nmma + m) mod nslots.  With three slots of
+  // 160 columns (320 rows) the next tile's first MMA writes the free slot
+  // and its second the slot the epilogue reads first; with one MMA per tile
+  // the two slots alternate.  nslots <= 2 * nmma keeps the MMAs at most one
+  // tile ahead of the epilogue (a slot is reused by the tile after next at
+  // the latest), which the two alternating acc_full barriers rely on.
+  const int nslots = min(kLmTmemCols / nper, 2 * nmma);
+  const int S = p.nstages;
+  // the pair owns the vocabulary tiles [T0, T1)
   int T0, T1;
   {
-    const long long G = gridDim.x, g = blockIdx.x;
+    const long long G = gridDim.x / 2, g = blockIdx.x / 2;
     T0 = (int)((long long)p.ntiles * g / G);
     T1 = (int)((long long)p.ntiles * (g + 1) / G);
   }
   const int nsteps = T1 - T0;
   const int nk = (p.d + kLmBK - 1) / kLmBK;
-  const int nmma = (R + kLmMaxN - 1) / kLmMaxN;  // MMAs per K step of 16
-  const int nper = R / nmma;                     // N of each (a multiple of 16)
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kLmStages; ++s) {
-      mbar_init(&full[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);   // the leader's producer; both CTAs' bytes (leader only)
       mbar_init(&empty[s], 1);  // released by the MMAs that read the stage
     }
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, 4);
+    mbar_init(&acc_full[0], 1);
+    mbar_init(&acc_full[1], 1);
+    // the eight epilogue warps of both CTAs read every slot (leader only)
+    for (int s = 0; s < kLmMaxSlots; ++s) mbar_init(&slot_empty[s], 16);
     mbar_init(&drain, 1);
     s_abort = 0;
     mbar_init_fence();
   }
-  if (warp == 1) {  // tensor memory for the accumulators (whole warp)
+  if (warp == 1) {  // tensor memory for the accumulators (a warp of each CTA, together)
     asm volatile(
-        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+        "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
             smem_addr(&tmem_base_holder)),
         "r"(kLmTmemCols)
         : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
+  // both CTAs' barriers and tensor memory exist before either CTA's copies,
+  // MMAs or commits can reach them
   tmem_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tmem_fence_after();
   const uint32_t tmem_base = tmem_base_holder;
   // a programmatic dependent of the kernel before it in the stream: the set-up
@@ -261,10 +361,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   }
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (both CTAs) ----------------
+    const uint32_t full0 = cluster_addr(&full[0], 0);  // the leader's barriers
+    const unsigned pair_bytes = 2u * (unsigned)lm_stage_bytes(R);
     int stage = 0, issued = 0;
     unsigned phase = 0;
-    const unsigned bytes = (unsigned)stage_bytes;
     for (int j = 0; j < nsteps && !*(volatile int*)&s_abort; ++j) {
       const int t = T0 + j;
       for (int kb = 0; kb < nk; ++kb) {
@@ -276,31 +377,62 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
         ++issued;
         uint8_t* st = ring + (size_t)stage * p.stage_bytes;
-        mbar_expect_tx(&full[stage], bytes);
-        tma_load_2d(st, &map_w, kb * kLmBK, t * kLmBV, &full[stage]);
-        for (int r = 0; r < R; r += kLmHBox)
-          tma_load_2d(st + kLmABytes + r * 128, hmap, kb * kLmBK, row0 + r, &full[stage]);
-        if (++stage == kLmStages) {
+        const uint32_t fb = full0 + 8u * (uint32_t)stage;
+        if (leader) mbar_expect_tx(&full[stage], pair_bytes);
+        tma_load_2d_pair(st, &map_w, kb * kLmBK, t * kLmPairBV + (int)rank * kLmBV, fb);
+        for (int m = 0; m < nmma; ++m)
+          tma_load_2d_pair(st + kLmABytes + m * half * 128, hmap, kb * kLmBK,
+                           row0 + m * nper + (int)rank * half, fb);
+        if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    // every copy this thread issued has landed before the CTA can leave
-    for (int j = max(0, issued - kLmStages); j < issued; ++j)
-      mbar_wait_bounded(&full[j % kLmStages], (unsigned)((j / kLmStages) & 1));
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    const uint32_t idesc = umma_idesc_bf16_f32(kLmBV, nper);
-    int stage = 0;
-    unsigned phase = 0, acc_phase = 0;
+    // every copy this thread issued has landed before the CTA can leave: the
+    // leader sees its stages fill; the follower's copies complete on the
+    // leader's barriers, so it waits for the MMAs that read them to release
+    // the stages
+    for (int j = max(0, issued - S); j < issued; ++j) {
+      const unsigned par = (unsigned)((j / S) & 1);
+      if (leader)
+        mbar_wait_bounded(&full[j % S], par);
+      else
+        mbar_wait_bounded(&empty[j % S], par);
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ---------------- MMA issuer (the leader) ----------------
+    const uint32_t idesc = umma_idesc_bf16_f32(kLmPairBV, nper);
+    // The issue loop is what paces the tensor cores here (one thread issues
+    // every MMA of the pair), so descriptors are built once: the start
+    // address field (16-byte units, bits 0-13) advances by 2 per K step of
+    // 16 and by stage_bytes / 16 per stage.  Shared-memory offsets stay below
+    // 2^18 bytes, so the additions never carry out of the field.
+    const uint64_t adesc0 = umma_desc_sw128(smem_addr(ring));
+    const uint64_t sstep = (uint64_t)(p.stage_bytes >> 4);
+    const uint64_t bofs = (uint64_t)(kLmABytes >> 4);
+    const uint64_t mofs = (uint64_t)((half * 128) >> 4);
+    const bool two = nmma > 1;
+    int stage = 0, sbase = 0;
+    unsigned phase = 0, spar = 0;  // spar: bit s = uses of slot s so far, mod 2
     for (int j = 0; j < nsteps && !*(volatile int*)&s_abort; ++j) {
-      if (!mbar_wait_bounded(&acc_empty, acc_phase ^ 1u)) {
+      // both CTAs' epilogues have read the slots this tile accumulates in
+      const int sl0 = sbase, sl1 = sbase + 1 < nslots ? sbase + 1 : 0;
+      bool ok = mbar_wait_cluster_bounded(&slot_empty[sl0], ((spar >> sl0) & 1u) ^ 1u);
+      spar ^= 1u << sl0;
+      if (ok && two) {
+        ok = mbar_wait_cluster_bounded(&slot_empty[sl1], ((spar >> sl1) & 1u) ^ 1u);
+        spar ^= 1u << sl1;
+      }
+      if (!ok) {
         s_abort = 1;
         set_flag(p.flags, kFlagTimeout);
         break;
       }
       tmem_fence_after();
+      const uint32_t tm0 = tmem_base + (uint32_t)(sl0 * nper);
+      const uint32_t tm1 = tmem_base + (uint32_t)(sl1 * nper);
+      sbase = (sbase + nmma) % nslots;
       for (int kb = 0; kb < nk; ++kb) {
         if (!mbar_wait_bounded(&full[stage], phase)) {
           s_abort = 1;
@@ -308,25 +440,33 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           break;
         }
         tmem_fence_after();
-        const uint32_t ast = smem_addr(ring + (size_t)stage * p.stage_bytes);
-        const uint32_t bst = ast + kLmABytes;
+        const uint64_t ad = adesc0 + (uint64_t)stage * sstep;
+        const uint64_t bd = ad + bofs;
+        const uint32_t acc = kb > 0 ? 1u : 0u;
+        if (two) {
+          umma_bf16_pair(tm0, ad, bd, idesc, acc);
+          umma_bf16_pair(tm1, ad, bd + mofs, idesc, acc);
 #pragma unroll
-        for (int kk = 0; kk < kLmBK / 16; ++kk)
-          for (int m = 0; m < nmma; ++m)
-            umma_bf16(tmem_base + m * nper, umma_desc_sw128(ast + kk * 32),
-                      umma_desc_sw128(bst + m * nper * 128 + kk * 32), idesc,
-                      (kb > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&empty[stage]);  // the stage is free once these finish
-        if (++stage == kLmStages) {
+          for (int kk = 1; kk < kLmBK / 16; ++kk) {
+            umma_bf16_pair(tm0, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
+            umma_bf16_pair(tm1, ad + 2 * kk, bd + mofs + 2 * kk, idesc, 1u);
+          }
+        } else {
+          umma_bf16_pair(tm0, ad, bd, idesc, acc);
+#pragma unroll
+          for (int kk = 1; kk < kLmBK / 16; ++kk)
+            umma_bf16_pair(tm0, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
+        }
+        umma_commit_both(&empty[stage]);  // the stage is free in both CTAs once these finish
+        if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      umma_commit(&acc_full);  // the tile's accumulators are complete
-      acc_phase ^= 1u;
+      umma_commit_both(&acc_full[j & 1]);  // the tile's accumulators are complete in both CTAs
     }
     // every MMA this thread issued has completed before tensor memory is freed
-    umma_commit(&drain);
+    umma_commit_own(&drain);
     mbar_wait_bounded(&drain, 0);
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
@@ -334,25 +474,32 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     // and statistics reduce each warp's 32 lanes per column with a butterfly
     // that leaves column c's result in lane c; the four quadrants' results
     // meet in shared memory and each epilogue thread keeps the running
-    // result of rows e, e + 128, ... over the CTA's tiles.
-    const int q = warp & 3;   // tensor-memory lane quadrant of this warp
-    const int e = threadIdx.x - 64;  // 0..127 among the epilogue threads
-    float best[kLmMaxRows / 128];
-    int bidx[kLmMaxRows / 128];
-    StatsState run[kLmMaxRows / 128];
+    // result of rows e, e + 256 over the CTA's tiles.
+    const int q = warp & 3;          // tensor-memory lane quadrant of this warp
+    const int e = threadIdx.x - 64;  // 0..255 among the epilogue threads
+    constexpr int kPer = (kLmMaxRows + kLmEpiThreads - 1) / kLmEpiThreads;  // rows per thread
+    float best[kPer];
+    int bidx[kPer];
+    StatsState run[kPer];
 #pragma unroll
-    for (int j = 0; j < kLmMaxRows / 128; ++j) {
+    for (int j = 0; j < kPer; ++j) {
       best[j] = -INFINITY;
       bidx[j] = 0x7FFFFFFF;
     }
-    unsigned acc_phase = 0;
+    const uint32_t slot_empty0 = cluster_addr(&slot_empty[0], 0);  // the leader's barriers
+    const int nblk = nper / 32;  // column blocks of one slot
+    // The two warps of a quadrant take alternate column blocks, so that the
+    // slot of the tile's first MMA -- the one the next tile's second MMA
+    // reuses -- is read after about half of the epilogue.
+    const int cb0 = warp >= 6 ? 1 : 0;
+    const int ncb = R / 32;
     for (int j = 0; j < nsteps; ++j) {
       // every epilogue thread takes the same decision, so none is left at a
       // named barrier the others no longer reach
-      const unsigned ok = mbar_wait_bounded(&acc_full, acc_phase) ? 1u : 0u;
+      const unsigned ok = mbar_wait_bounded(&acc_full[j & 1], (unsigned)((j >> 1) & 1)) ? 1u : 0u;
       unsigned all_ok;
       asm volatile(
-          "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n bar.red.and.pred b, 1, 128, a;\n"
+          "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n bar.red.and.pred b, 1, 256, a;\n"
           " selp.u32 %0, 1, 0, b;\n}"
           : "=r"(all_ok)
           : "r"(ok)
@@ -363,11 +510,19 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         break;
       }
       tmem_fence_after();
-      const int vocab = (T0 + j) * kLmBV + 32 * q + lane;
+      const int vocab = (T0 + j) * kLmPairBV + (int)rank * kLmBV + 32 * q + lane;
       const bool valid = vocab < p.V;
-      for (int cb = 0; cb < R / 32; ++cb) {
+      for (int cb = cb0; cb < ncb; cb += 2) {
+        const int m = cb / nblk, cbl = cb - m * nblk;
+        const int slot = (j * nmma + m) % nslots;
         uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + cb * 32, r);
+        tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(slot * nper + cbl * 32), r);
+        if (cbl >= nblk - 2) {  // this warp's last block of the slot
+          // the slot is read (the load has completed): its next tile may start
+          tmem_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(slot_empty0 + 8u * (uint32_t)slot);
+        }
         if constexpr (Mode == kLmArgmax) {
           float v[32];
           int ix[32];
@@ -430,14 +585,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           }
         }
       }
-      tmem_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty);  // tensor memory read: next tile may start
       if constexpr (Mode != kLmLogits) {
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four quadrants' results are in
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // the four quadrants' results are in
 #pragma unroll
-        for (int jj = 0; jj < kLmMaxRows / 128; ++jj) {
-          const int c = e + 128 * jj;
+        for (int jj = 0; jj < kPer; ++jj) {
+          const int c = e + kLmEpiThreads * jj;
           if (c < R) {
             if constexpr (Mode == kLmArgmax) {
 #pragma unroll
@@ -464,15 +616,14 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             }
           }
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the scratch may be reused
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // the scratch may be reused
       }
-      acc_phase ^= 1u;
     }
     const int C = gridDim.x;
 #pragma unroll
-    for (int jj = 0; jj < kLmMaxRows / 128; ++jj) {
-      const int lr = row0 + e + 128 * jj;
-      if (e + 128 * jj < R && lr < nrows) {
+    for (int jj = 0; jj < kPer; ++jj) {
+      const int lr = row0 + e + kLmEpiThreads * jj;
+      if (e + kLmEpiThreads * jj < R && lr < nrows) {
         if constexpr (Mode == kLmArgmax) {
           p.part[(size_t)lr * C + blockIdx.x] = ArgPartial{best[jj], bidx[jj], nsteps > 0 ? 1 : 0, 0};
         } else if constexpr (Mode == kLmStats) {
@@ -486,11 +637,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       }
     }
   }
+  // neither CTA frees its tensor memory or leaves while the leader's MMAs
+  // or the peer's epilogue may still use it
   tmem_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tmem_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kLmTmemCols)
                  : "memory");
   }
