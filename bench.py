@@ -872,7 +872,8 @@ def measure_next_rows(dev, stream, tree, K):
         "w_lm_gb_s": round(w_bytes / (ms_f / 1e3) / 1e9, 1),
         "unfused_us_per_call": round(ms_u * 1e3, 2),
         "unfused": "torch.matmul (cuBLAS) writing bf16 logits, then spec_verify_greedy",
-        "bound": "W_LM stream (1.05 GB) and tensor cores, about balanced at 320 rows",
+        "bound": "tensor cores on SM pairs (M=256 x N=160 MMAs from one issuing thread per pair), "
+                 "W_LM streamed once",
         "timed": "CUDA-graph replay of 4 calls"}
 
     # LM head fused with sampling verification on the same shape: 320 target

@@ -53,6 +53,11 @@ def _rows_argmax(H, W):
     (2, 2, 200, 5000, 4), (100, 4, 64, 700, 5),        # 500 rows: two halves of 256
     (1, 0, 8, 257, 6), (130, 4, 64, 700, 7),           # 650 rows: two row groups
     (41, 0, 96, 20000, 8),                             # 41 rows: halves of 32, one partly empty
+    # three or more 256-entry vocabulary tiles per CTA pair, so the
+    # accumulator slots rotate: 320 rows (two MMAs, three slots), 384 rows
+    # (two MMAs, two slots), 256 and 64 rows (one MMA, two slots)
+    (64, 4, 64, 60001, 10), (96, 3, 64, 60001, 11), (64, 3, 64, 60001, 12),
+    (32, 1, 64, 60001, 13),
 ])
 def test_lm_head_rows_and_chains(B, k, d, V, seed):
     H, W, tok, _ = synth.make_lm_head_case(B=B, k=k, d=d, V=V, seed=seed)
@@ -146,6 +151,7 @@ def _lm_sample_parity(c, seqs=None):
     (5, 2, 200, 5000, 1.2, 4), (100, 4, 64, 700, 1.0, 5),   # 500 target rows: two row groups
     (2, 1, 72, 129, 1.0, 6),                                # odd V: the draw's plain loads
     (6, 3, 96, 20000, 0.7, 7),
+    (64, 4, 64, 60001, 1.0, 8),   # 320 target, 256 draft, 128 drawn rows; rotating slots
 ])
 def test_lm_head_sample_matches_oracle(B, k, d, V, T, seed):
     c = synth.make_lm_head_sample_case(B=B, k=k, d=d, V=V, seed=seed, temperature=T,
