@@ -685,6 +685,47 @@ def _time_loop(fn, stream, K, per_graph=20):
     return e0.elapsed_time(e1) / (reps * per_graph)
 
 
+def _time_pair(fa, fb, stream, K, per_graph=4, rounds=8):
+    """Mean ms of one fa() call and of one fb() call, timed in alternating
+    rounds (each a CUDA-graph replay of about K / rounds calls) so that both
+    see the same clock and thermal state; the median round of each is
+    returned.  Used where a fused call is compared with its unfused
+    equivalent: under the power cap the clock drifts over seconds."""
+    import torch
+    graphs = []
+    for fn in (fa, fb):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(per_graph):
+                fn()
+        graphs.append(g)
+    reps = max(1, K // (per_graph * rounds))
+    out = [[], []]
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            for _ in range(2):
+                g.replay()
+        for _ in range(rounds):
+            for i, g in enumerate(graphs):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+                out[i].append((e0, e1))
+    stream.synchronize()
+    med = []
+    for pairs in out:
+        ms = sorted(a.elapsed_time(b) / (reps * per_graph) for a, b in pairs)
+        med.append(ms[len(ms) // 2])
+    return med[0], med[1]
+
+
 def lm_head_case(dev):
     """LM head fused with greedy verification on the greedy workload's shape:
     B=64, k=4 (320 target rows), hidden 4096, V=128256, bf16."""
@@ -853,13 +894,12 @@ def measure_next_rows(dev, stream, tree, K):
     H, Wm, tk, acc_l, out_l, wsl = lm["H"], lm["W"], lm["tokens"], lm["acc"], lm["out"], lm["ws"]
     wsg = sv.alloc_workspace(sv.SPEC_MODE_GREEDY, Bl, kl, Vl, sv.SPEC_DTYPE_BF16, dev)
     logits = torch.empty(rows, Vl, dtype=torch.bfloat16, device=dev)
-    ms_f = _time_loop(lambda: sv.spec_lm_head_verify_greedy(H, Wm, tk, acc_l, out_l, wsl, stream),
-                      stream, max(40, K // 10), per_graph=4)
-
     def unfused():
         torch.matmul(H, Wm.t(), out=logits)
         sv.spec_verify_greedy(logits.view(Bl, kl + 1, Vl), tk, acc_l, out_l, wsg, stream)
-    ms_u = _time_loop(unfused, stream, max(40, K // 10), per_graph=4)
+    ms_f, ms_u = _time_pair(
+        lambda: sv.spec_lm_head_verify_greedy(H, Wm, tk, acc_l, out_l, wsl, stream), unfused,
+        stream, max(64, K // 10), per_graph=4)
     flops = 2.0 * rows * d * Vl
     w_bytes = Vl * d * 2
     peak_tf, peak_kind_tf = measured_tflops()
@@ -874,7 +914,8 @@ def measure_next_rows(dev, stream, tree, K):
         "unfused": "torch.matmul (cuBLAS) writing bf16 logits, then spec_verify_greedy",
         "bound": "tensor cores on SM pairs (M=256 x N=160 MMAs from one issuing thread per pair), "
                  "W_LM streamed once",
-        "timed": "CUDA-graph replay of 4 calls"}
+        "timed": "fused and unfused in 8 alternating rounds of CUDA-graph replays (4 calls "
+                 "per graph); median round of each"}
 
     # LM head fused with sampling verification on the same shape: 320 target
     # rows, 256 drafted features (the target's first k hidden states of each
@@ -903,8 +944,7 @@ def measure_next_rows(dev, stream, tree, K):
         torch.matmul(Hd, Wm.t(), out=logits_d)
         sv.spec_verify_sample(logits.view(Bl, kl + 1, Vl), logits_d.view(Bl, kl, Vl), tk, ua, us,
                               1.0, so["n"], so["tok"], so["p"], so["q"], so["R"], wsu, stream)
-    ms_fs = _time_loop(fused_sample, stream, max(20, K // 20), per_graph=2)
-    ms_us = _time_loop(unfused_sample, stream, max(20, K // 20), per_graph=2)
+    ms_fs, ms_us = _time_pair(fused_sample, unfused_sample, stream, max(32, K // 20), per_graph=2)
     flops_s = 2.0 * (rows + Bl * kl) * d * Vl
     out["lm_head_sample"] = {
         "workload": f"B={Bl} k={kl}: {rows} target rows and {Bl * kl} drafted features, hidden {d}, "
@@ -916,7 +956,8 @@ def measure_next_rows(dev, stream, tree, K):
                    "spec_verify_sample",
         "launches": 4,
         "bound": "the statistics GEMM (576 rows) and a second pass over W_LM for the 2B drawn rows",
-        "timed": "CUDA-graph replay of 2 calls"}
+        "timed": "fused and unfused in 8 alternating rounds of CUDA-graph replays (2 calls "
+                 "per graph); median round of each"}
     del H, Wm, logits, lm, Hd, logits_d, wss, wsu
 
     # EAGLE-2 tree growth producing the tree workload's shape (16 trees of 60

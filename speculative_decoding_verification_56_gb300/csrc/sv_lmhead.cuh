@@ -229,6 +229,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// The same load without its wait, and the wait: tmem_wait_ld ties the
+// registers of one earlier load, so that nothing reads them before the
+// loads have completed (the first wait covers every load issued before it).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 
 // (value, index) comparison: larger value, then lower index.
@@ -512,17 +539,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
       tmem_fence_after();
       const int vocab = (T0 + j) * kLmPairBV + (int)rank * kLmBV + 32 * q + lane;
       const bool valid = vocab < p.V;
-      for (int cb = cb0; cb < ncb; cb += 2) {
-        const int m = cb / nblk, cbl = cb - m * nblk;
-        const int slot = (j * nmma + m) % nslots;
-        uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(slot * nper + cbl * 32), r);
-        if (cbl >= nblk - 2) {  // this warp's last block of the slot
-          // the slot is read (the load has completed): its next tile may start
-          tmem_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote(slot_empty0 + 8u * (uint32_t)slot);
-        }
+      // one 32-column block's reduction (or, for the logits, its stores)
+      auto block = [&](const int cb, const uint32_t (&r)[32]) {
         if constexpr (Mode == kLmArgmax) {
           float v[32];
           int ix[32];
@@ -583,6 +601,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
             if (valid && lr < nrows)
               p.logits[(size_t)lr * p.V + vocab] = __uint_as_float(r[c]);
           }
+        }
+      };
+      const uint32_t qbase = tmem_base + ((uint32_t)(32 * q) << 16);
+      if (Mode == kLmArgmax && nmma == 2) {
+        // Each warp loads all its blocks of a slot (at most three), waits
+        // once and frees the slot before reducing them: the slot of the
+        // first MMA is the one the next tile's second MMA waits for.  (The
+        // statistics epilogue, with its larger register state, keeps the
+        // per-block order below, which measured faster there.)
+        for (int m = 0; m < 2; ++m) {
+          const int slot = (j * 2 + m) % nslots;
+          const int lo = m * nblk, hi = lo + nblk;
+          const int c0 = lo + ((lo & 1) != cb0 ? 1 : 0), c1 = c0 + 2, c2 = c0 + 4;
+          const uint32_t sbase = qbase + (uint32_t)(slot * nper - lo * 32);
+          uint32_t r0[32], r1[32], r2[32];
+          tmem_ld32_async(sbase + (uint32_t)(c0 * 32), r0);
+          if (c1 < hi) tmem_ld32_async(sbase + (uint32_t)(c1 * 32), r1);
+          if (c2 < hi) tmem_ld32_async(sbase + (uint32_t)(c2 * 32), r2);
+          tmem_wait_ld(r0);
+          if (c1 < hi) tmem_wait_ld(r1);
+          if (c2 < hi) tmem_wait_ld(r2);
+          tmem_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(slot_empty0 + 8u * (uint32_t)slot);
+          block(c0, r0);
+          if (c1 < hi) block(c1, r1);
+          if (c2 < hi) block(c2, r2);
+        }
+      } else {
+        for (int cb = cb0; cb < ncb; cb += 2) {
+          const int m = cb / nblk, cbl = cb - m * nblk;
+          const int slot = (j * nmma + m) % nslots;
+          uint32_t r[32];
+          tmem_ld32(qbase + (uint32_t)(slot * nper + cbl * 32), r);
+          if (cbl >= nblk - 2) {  // this warp's last block of the slot
+            // the slot is read (the load has completed): its next tile may start
+            tmem_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(slot_empty0 + 8u * (uint32_t)slot);
+          }
+          block(cb, r);
         }
       }
       if constexpr (Mode != kLmLogits) {
