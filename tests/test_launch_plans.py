@@ -1,7 +1,8 @@
 """Host-side checks of the CUDA sources, no GPU needed: the tree-growth
 kernel's staging depth and shared-memory size for every shape the interface
 admits (the plan functions of sv_grow.cuh, compiled with nvcc into a host
-program), and the provenance of the FMA-pipe 2^x coefficients."""
+program), the fused LM head's plan for every row-group size (sv_lmhead.cuh,
+likewise), and the provenance of the FMA-pipe 2^x coefficients."""
 import os
 import subprocess
 
@@ -24,6 +25,21 @@ def test_grow_plan_fits_every_admitted_shape(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout[-2000:]
     assert "shapes checked" in r.stdout
+
+
+def test_lmhead_plan_fits_every_row_group(tmp_path):
+    from speculative_decoding_verification_56_gb300 import build
+    try:
+        nvcc = build._nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    exe = tmp_path / "lmhead_plan_check"
+    cmd = [nvcc, *build.ARCH_FLAGS, "-std=c++17", "-O1", "-I", build.INCLUDE, "-I", CSRC,
+           os.path.join(ROOT, "tests", "lmhead_plan_check.cu"), "-o", str(exe)]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout[-2000:]
+    assert "6 row-group sizes checked" in r.stdout
 
 
 def test_exp2_polynomial_comes_from_the_committed_fit():
