@@ -16,11 +16,10 @@
 // form of the MMA (cta_group::2, M = 256): each CTA loads its own 128
 // vocabulary rows of W and half of each MMA's rows of H into its shared
 // memory, and each holds the 128 x rows accumulator of its vocabulary rows
-// (fp32) in its own tensor memory.  Per SM and K
-// step this moves 16 KB of W and half of H, against all of H for a CTA that
-// computes 128 x rows alone, so the same shared memory keeps more of the W
-// stream in flight.  Each pair walks a contiguous range of 256-entry
-// vocabulary tiles for a group of rows.  Warp roles (320 threads per CTA):
+// (fp32) in its own tensor memory.  Per SM and K step this moves 16 KB of W
+// and half of H, against all of H for a CTA that computes 128 x rows alone.
+// Each pair walks a contiguous range of 256-entry vocabulary tiles for a
+// group of rows.  Warp roles (320 threads per CTA):
 //   warp 0     TMA producer (both CTAs): per 64-wide K step, the CTA's W
 //              slice and H halves (128-byte swizzled) into a ring of up to
 //              eight stages; both CTAs' bytes complete on the leader's
@@ -30,11 +29,14 @@
 //              K=16) and commits stage releases and tile completion to the
 //              barriers of both CTAs
 //   warps 2-9  epilogue (both CTAs), two warps per 32-lane quadrant of
-//              tensor memory, each taking half of the tile's columns: tcgen05.ld,
+//              tensor memory taking alternate 32-column blocks: tcgen05.ld,
 //              a butterfly reduction across lanes per column (row), a merge
 //              of the four quadrants in shared memory and a running argmax
-//              per row (lowest index wins ties); the accumulator is released
-//              to the leader as soon as it has been read
+//              per row (lowest index wins ties)
+// Tensor memory holds two to four accumulator slots (three of 160 columns
+// for 320 rows), used in rotation: the next tile's MMAs start in the free
+// slot while the epilogue still reads the previous tile, and each slot is
+// released to the leader as soon as both CTAs' epilogues have read it.
 // Each CTA writes one argmax record per row for its vocabulary lanes, in the
 // layout the greedy resolve kernel merges.  Every wait is bounded, and both
 // CTAs meet at cluster barriers after set-up and before tensor memory is
