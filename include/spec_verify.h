@@ -275,7 +275,10 @@ SPEC_API spec_status_t spec_kv_commit_path(void* cache, int B, int planes, long 
  * Outputs as spec_verify_greedy.  The argmax is of the float32-accumulated
  * products (lowest index among equal values); rows whose top two logits lie
  * closer than the accumulation error may pick either.  Two kernel launches
- * (tcgen05 GEMM with an argmax epilogue; record merge + chain resolve).
+ * (tcgen05 GEMM with an argmax epilogue; record merge + chain resolve).  The
+ * GEMM runs on clusters of two CTAs, one per SM, that share each 256-entry
+ * vocabulary tile through two-CTA MMAs; it occupies every SM it can hold a
+ * pair on (most of each SM's shared and tensor memory) until it ends.
  * Workspace: spec_verify_workspace_bytes(SPEC_MODE_LM_HEAD_GREEDY, B, k, V,
  * SPEC_DTYPE_BF16).
  */
