@@ -181,8 +181,7 @@ bool vec_ok(const void* p, int V, int dtype) {
 template <typename KernelT, typename ParamT>
 spec_status_t launch(KernelT kernel, int grid, size_t smem, const ParamT& prm, void* stream,
                      bool pdl, int cluster = 1, int threads = sv::kThreads) {
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof cfg);
+  cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
@@ -213,7 +212,7 @@ spec_status_t launch(KernelT kernel, int grid, size_t smem, const ParamT& prm, v
 // for the preceding kernel in the stream with griddepcontrol.wait).
 void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, dim3 grid, dim3 block,
                 size_t smem, void* stream) {
-  std::memset(cfg, 0, sizeof *cfg);
+  *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = grid;
   cfg->blockDim = block;
   cfg->dynamicSmemBytes = smem;
@@ -382,8 +381,7 @@ spec_status_t lm_grid_x(int ntiles, int* gx) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return SPEC_ERR_CUDA;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(2 * std::max(1, sms / 2)), 1, 1);
     cfg.blockDim = dim3(sv::kLmThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)sv::kLmRingBytes + 1024;
